@@ -1,0 +1,521 @@
+#!/usr/bin/env python
+"""Benchmark of the MoL ("virtual experts") LoRA layer on GB300.
+
+One step = one MoE layer's MoL LoRA path over one batch: remap + align once,
+then the gate_up stage (shrink, expand) and the down stage (shrink, expand)
+reusing the routing. The workload is the bs=23 decode configuration (23
+tokens, 128 experts x 8 adapters = 1024 virtual experts, top-8, rank 32,
+gate_up 2048 -> 2x32 -> 2x768, down 768 -> 32 -> 2048), synthetic seeded data.
+
+Each step replays one CUDA graph of a whole layer. Steps rotate over
+--layers distinct layers (own weights, routing and activations) so that a
+step never finds its weights in L2: 8 decode layers touch ~0.7 GB per cycle,
+over 5x the 129 MB L2.
+
+Prints one JSON line (rank 0). Under torchrun every rank runs an independent
+replica (the path has no exchange step): weak scaling, value summed over ranks
+against the slowest rank's time.
+
+--impl reference times the CPU oracle on the same workload and metric.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "MoL LoRA layer (token,vexpert) pairs/s at 1 GB300"
+UNIT = "pairs/s"
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20000)
+    p.add_argument("--warmup", type=int, default=500)
+    p.add_argument("--impl", choices=["mol", "reference"], default="mol")
+    p.add_argument("--config", default="decode")
+    p.add_argument("--layers", type=int, default=8, help="distinct layers rotated across steps")
+    p.add_argument("--seed", type=int, default=0)
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--no-kernels", action="store_true", help="skip the per-kernel timing phase")
+    p.add_argument("--cpu-worker", action="store_true", help=argparse.SUPPRESS)
+    p.add_argument("--cpu-budget", type=float, default=15.0, help=argparse.SUPPRESS)
+    return p.parse_args(argv)
+
+
+# --------------------------------------------------------------------------- helpers
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]),
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples, kept with host timestamps."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.samples = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50", "-i", gpu_id], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [f.strip() for f in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        win = [s for t, s in self.samples if t0 - 0.1 <= t <= t1 + 0.1]
+        if not win and self.samples:  # a very short region: the samples around it
+            near = sorted(self.samples, key=lambda ts: min(abs(ts[0] - t0), abs(ts[0] - t1)))[:2]
+            win = [s for _, s in near]
+        if not win:
+            return dict(sm_mhz=None, sm_max_mhz=None, reasons=[], samples=0)
+        sm = [float(s[1]) for s in win if s[1].replace(".", "").isdigit()]
+        mx = [float(s[2]) for s in win if s[2].replace(".", "").isdigit()]
+        reasons = set()
+        for s in win:
+            for name, val in zip(self.NAMES, s[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return dict(sm_mhz=statistics.median(sm) if sm else None, sm_max_mhz=max(mx) if mx else None,
+                    reasons=sorted(reasons), samples=len(win))
+
+
+# --------------------------------------------------------------------------- GPU arm
+
+class LayerState:
+    """Device tensors of one layer: routing, workspace, per-stage inputs and outputs."""
+
+    def __init__(self, wl, li, dev, mol, torch):
+        self.wl, self.li = wl, li
+        self.topk = torch.from_numpy(li.topk_ids).to(dev)
+        self.lora = torch.from_numpy(li.lora_ids).to(dev)
+        self.routing = mol.alloc_routing(wl.numel, wl.V, wl.BM, dev)
+        self.ws = mol.alloc_workspace(wl.numel, wl.V, wl.BM, dev)
+        self.stages = []
+        for st in li.stages:
+            self.stages.append(dict(
+                st=st, x=st.x.to_device(dev), A=st.A.to_device(dev), B=st.B.to_device(dev),
+                out=st.out0.to_device(dev),
+                inter=torch.zeros((wl.numel, st.stage.R), dtype=torch.float32, device=dev)))
+
+    def forward(self, mol):
+        wl = self.wl
+        for si, d in enumerate(self.stages):
+            mol.mol_lora_forward(d["x"], d["st"].x_row_div, self.topk, self.lora, wl.E, wl.L,
+                                 d["A"], d["B"], d["st"].stage.S, wl.scale, d["out"], self.routing,
+                                 d["inter"], compute_routing=(si == 0), workspace=self.ws)
+
+    def counts(self):
+        """Valid pairs, touched virtual experts and distinct token rows, from the routing output."""
+        vt = self.routing.vtopk_ids.cpu().numpy().reshape(-1)
+        valid = vt >= 0
+        touched = np.unique(vt[valid])
+        rows = np.unique(np.nonzero(valid)[0] // self.wl.topk)
+        return int(valid.sum()), int(touched.size), int(rows.size)
+
+    def stage_bytes(self, si, pairs, touched, token_rows):
+        """Algorithmic HBM bytes of one stage's shrink and expand."""
+        st = self.stages[si]["st"].stage
+        x_rows = token_rows if self.stages[si]["st"].x_row_div > 1 else pairs
+        shrink = touched * st.R * st.K * 2 + x_rows * st.K * 2 + pairs * st.R * 4
+        expand = touched * st.N * st.r * 2 + pairs * st.R * 4 + pairs * st.N * 2 * 2
+        return shrink, expand
+
+    def align_bytes(self):
+        wl = self.wl
+        return wl.numel * (4 + 4) + wl.T * 4 + self.routing.capacity * 4 + self.routing.expert_ids.numel() * 4 + 4
+
+
+def time_graphs(torch, graphs, steps, warmup):
+    """Replay graphs round-robin; return ms per replay from CUDA events on the current stream."""
+    n = len(graphs)
+    for i in range(warmup):
+        graphs[i % n].replay()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for i in range(steps):
+        graphs[i % n].replay()
+    e.record()
+    torch.cuda.synchronize()
+    return s.elapsed_time(e) / steps
+
+
+def capture(torch, fn):
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        fn()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    import moe_lora_virtual_gb300 as mol
+    from moe_lora_virtual_gb300.build import build_library
+    from synth import WORKLOADS, make_layer
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    if rank == 0:
+        build_library()
+    if world > 1:
+        dist.barrier()
+    mol.library()
+
+    wl = WORKLOADS[args.config]
+    layers = [LayerState(wl, make_layer(wl, args.seed + 1000 * rank, layer=i), dev, mol, torch)
+              for i in range(args.layers)]
+    for L_ in layers:
+        L_.forward(mol)
+    torch.cuda.synchronize()
+    cnt = [L_.counts() for L_ in layers]
+    pairs_per_step = float(np.mean([c[0] for c in cnt]))
+    plan_tiles = 1 if mol.workspace_bytes(wl.numel, wl.V, wl.BM) == 0 else 3
+    launches_per_step = plan_tiles + 2 * len(wl.stages)
+
+    graphs = [capture(torch, lambda L_=L_: L_.forward(mol)) for L_ in layers]
+
+    props = torch.cuda.get_device_properties(dev)
+    gpu_id = str(local)
+    try:
+        gpu_id = "GPU-" + str(props.uuid)
+    except Exception:
+        pass
+    clocks = ClockSampler(gpu_id)
+    time.sleep(0.3)
+
+    # ---- timed region: exactly K steps -----------------------------------------------
+    for i in range(args.warmup):
+        graphs[i % len(graphs)].replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    ev0.record()
+    for i in range(args.steps):
+        graphs[i % len(graphs)].replay()
+    ev1.record()
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if world > 1:
+        dist.barrier()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    time.sleep(0.15)
+    clk = clocks.summary(t0, t1)
+    clocks.stop()
+
+    if world > 1:
+        tmax = torch.tensor([ms], device=dev)
+        dist.all_reduce(tmax, op=dist.ReduceOp.MAX)
+        ms = float(tmax.item())
+        ptot = torch.tensor([pairs_per_step], device=dev, dtype=torch.float64)
+        dist.all_reduce(ptot)
+        pairs_all = float(ptot.item())
+    else:
+        pairs_all = pairs_per_step
+    value = pairs_all / (ms * 1e-3)
+
+    # ---- per-kernel timing (each kernel alone in its own graphs, same rotation) -------
+    peaks = measured_peaks()
+    kern = {}
+    roof = None
+    if not args.no_kernels:
+        def stage_call(L_, si, which):
+            d = L_.stages[si]
+            st = d["st"]
+            if which == "shrink":
+                return lambda: mol.mol_lora_shrink(d["x"], st.x_row_div, d["A"], st.stage.S,
+                                                   L_.routing, d["inter"])
+            return lambda: mol.mol_lora_expand(d["inter"], d["B"], st.stage.S, wl.scale,
+                                               L_.routing, d["out"])
+
+        def align_call(L_):
+            return lambda: mol.mol_align_block_size(L_.routing.vtopk_ids, wl.V, wl.BM,
+                                                    routing=L_.routing, workspace=L_.ws)
+
+        ksteps = max(200, min(args.steps, 5000))
+        kern["align"] = time_graphs(torch, [capture(torch, align_call(L_)) for L_ in layers],
+                                    ksteps, 20) * 1e3
+        for si, st in enumerate(wl.stages):
+            for which in ("shrink", "expand"):
+                gs = [capture(torch, stage_call(L_, si, which)) for L_ in layers]
+                kern[f"{which}_{st.name}"] = time_graphs(torch, gs, ksteps, 20) * 1e3
+        # dominant kernel: the stage kernel with the most algorithmic bytes
+        best = None
+        for si, st in enumerate(wl.stages):
+            sb = [L_.stage_bytes(si, *c) for L_, c in zip(layers, cnt)]
+            for j, which in enumerate(("shrink", "expand")):
+                b = float(np.mean([x[j] for x in sb]))
+                if best is None or b > best[1]:
+                    best = (f"{which}_{st.name}", b)
+        name, nbytes = best
+        us = kern[name]
+        achieved = nbytes / (us * 1e-6) / 1e9
+        roof = dict(kernel=name, bound="hbm", achieved=round(achieved, 1), peak=peaks["hbm_gbs"],
+                    unit="GB/s", frac=round(achieved / peaks["hbm_gbs"], 4),
+                    traffic=TRAFFIC.get((args.config, name)), bytes_per_launch=int(nbytes),
+                    us_per_launch=round(us, 3), peak_source=peaks["source"])
+
+    layer_bytes = float(np.mean([sum(sum(L_.stage_bytes(si, *c)) for si in range(len(wl.stages)))
+                                 + L_.align_bytes() for L_, c in zip(layers, cnt)]))
+
+    # ---- end to end through the public API with host buffers -------------------------
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, torch, mol, wl, layers, pairs_per_step, world, dev)
+
+    out = dict(metric=METRIC, value=round(value, 1), unit=UNIT, n_gpus=world, steps=args.steps,
+               warmup=args.warmup, ms_per_step=round(ms, 6), us_per_layer=round(ms * 1e3, 3),
+               higher_is_better=True, scaling="weak", vs_baseline=None, dtype="bf16",
+               data="synthetic",
+               config=dict(workload=f"{args.config}: {wl.note}", T=wl.T, E=wl.E, topk=wl.topk,
+                           max_loras=wl.L, num_vexperts=wl.V, block_m=wl.BM,
+                           stages=[f"{s.name} K={s.K} R={s.R} N={s.N}" for s in wl.stages],
+                           pairs_per_layer=pairs_per_step, layers_rotated=args.layers,
+                           l2="inputs larger than L2: steps rotate over distinct layers",
+                           parallelism=f"replicas{world}"),
+               layer_hbm=dict(bytes=int(layer_bytes),
+                              achieved_gbs=round(layer_bytes / (ms * 1e-3) / 1e9, 1),
+                              frac=round(layer_bytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)),
+               kernels_us={k: round(v, 3) for k, v in kern.items()},
+               roofline=roof, e2e=e2e, gpu_launches=launches_per_step * args.steps,
+               clocks=dict(sm_mhz=clk["sm_mhz"], sm_max_mhz=clk["sm_max_mhz"],
+                           reasons=clk["reasons"], samples=clk["samples"]))
+    if rank == 0 and not args.no_cpu:
+        out["cpu_baseline"] = cpu_baseline(args)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(out))
+
+
+def run_e2e(args, torch, mol, wl, layers, pairs_per_step, world, dev):
+    """Per step: pinned host -> device copies of the step's inputs, the layer, device -> host copy
+    of the outputs; captured (copies included) in one graph per layer."""
+    host = []
+    for L_ in layers:
+        h = dict(topk=torch.from_numpy(L_.li.topk_ids).pin_memory(),
+                 lora=torch.from_numpy(L_.li.lora_ids).pin_memory(), x=[], out_in=[], out_back=[])
+        for d in L_.stages:
+            h["x"].append(d["x"].cpu().pin_memory())
+            h["out_in"].append(d["out"].cpu().pin_memory())
+            h["out_back"].append(torch.empty_like(h["out_in"][-1]).pin_memory())
+        host.append(h)
+
+    def step(L_, h):
+        L_.topk.copy_(h["topk"], non_blocking=True)
+        L_.lora.copy_(h["lora"], non_blocking=True)
+        for d, x, o in zip(L_.stages, h["x"], h["out_in"]):
+            d["x"].copy_(x, non_blocking=True)
+            d["out"].copy_(o, non_blocking=True)
+        L_.forward(mol)
+        for d, ob in zip(L_.stages, h["out_back"]):
+            ob.copy_(d["out"], non_blocking=True)
+
+    graphs = [capture(torch, lambda L_=L_, h=h: step(L_, h)) for L_, h in zip(layers, host)]
+    steps = min(args.steps, 5000)
+    ms = time_graphs(torch, graphs, steps, min(args.warmup, 50))
+    h0 = host[0]
+    bi = h0["topk"].nbytes + h0["lora"].nbytes + sum(t.nbytes for t in h0["x"] + h0["out_in"])
+    bo = sum(t.nbytes for t in h0["out_back"])
+    # eager calls (no graph) for reference
+    n_e = min(steps, 500)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(n_e):
+        step(layers[i % len(layers)], host[i % len(host)])
+    torch.cuda.synchronize()
+    ms_eager = (time.perf_counter() - t0) * 1e3 / n_e
+    return dict(value=round(pairs_per_step * world / (ms * 1e-3), 1), unit=UNIT,
+                h2d_bytes_per_step=int(bi), d2h_bytes_per_step=int(bo), ms_per_step=round(ms, 6),
+                mode="graph replay of pinned-host copies + mol_lora_forward calls",
+                eager_value=round(pairs_per_step * world / (ms_eager * 1e-3), 1),
+                eager_ms_per_step=round(ms_eager, 6), steps=steps)
+
+
+# traffic (dram bytes read + written) per launch from ncu captures, keyed by
+# (workload, kernel); None until the current kernel has been captured.
+TRAFFIC = {}
+
+
+# --------------------------------------------------------------------------- CPU (oracle)
+
+def oracle_layer_sample(wl, li, blocks_per_step, step_idx, routing_cache):
+    """Oracle on one step's sample of the layer: the routing, then both stages on a rotating
+    window of routed blocks. Returns the number of (token, vexpert) pairs processed."""
+    import oracle
+
+    key = id(li)
+    if key not in routing_cache:
+        vt = oracle.virtual_topk(li.topk_ids, li.lora_ids, wl.E, wl.L).reshape(-1)
+        s, e, n = oracle.align_block_size(vt, wl.V, wl.BM)
+        real = np.nonzero(e[: n // wl.BM] >= 0)[0]
+        routing_cache[key] = (s, e, n, real)
+    s, e, n, real = routing_cache[key]
+    if blocks_per_step >= real.size:
+        pick = real
+    else:
+        start = (step_idx * blocks_per_step) % real.size
+        pick = np.take(real, np.arange(start, start + blocks_per_step), mode="wrap")
+    e_s = np.full_like(e, -1)
+    e_s[pick] = e[pick]
+    pairs = 0
+    for t in pick:
+        ids = s[t * wl.BM:(t + 1) * wl.BM]
+        pairs += int(np.sum(ids < wl.numel))
+    for st in li.stages:
+        if not hasattr(st, "_host_out0"):
+            st._host_out0 = st.out0.host_all()
+        inter = oracle.lora_shrink(st.x, st.x_row_div, st.A, s, e_s, n, wl.BM, wl.numel,
+                                   np.zeros((wl.numel, st.stage.R), np.float32))
+        oracle.lora_expand(inter, st.B, st.stage.S, st.stage.r, st.stage.Ns, wl.scale, None, s,
+                           e_s, n, wl.BM, wl.numel, st._host_out0)
+    return pairs
+
+
+def cpu_worker(args):
+    """Runs in a child process with one BLAS thread: the oracle on a bounded sample."""
+    from synth import WORKLOADS, make_layer
+
+    wl = WORKLOADS[args.config]
+    li = make_layer(wl, args.seed, layer=0)
+    cache = {}
+    oracle_layer_sample(wl, li, 4, 0, cache)          # warm: routing + conversions
+    t0 = time.perf_counter()
+    pairs = 0
+    k = 0
+    while time.perf_counter() - t0 < args.cpu_budget:
+        pairs += oracle_layer_sample(wl, li, 1 << 30, k, cache)
+        k += 1
+    dt = time.perf_counter() - t0
+    print(json.dumps(dict(pairs=pairs, seconds=dt, layers=k)))
+
+
+def cpu_baseline(args):
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT"):
+        env.pop(k, None)
+    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-worker", "--config", args.config,
+           "--seed", str(args.seed), "--cpu-budget", "15"]
+    try:
+        res = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=600)
+        d = json.loads(res.stdout.strip().splitlines()[-1])
+    except Exception as exc:  # report, never fail the GPU line
+        return dict(value=None, unit=UNIT, cores=1, kind="oracle", sample=f"failed: {exc}")
+    return dict(value=round(d["pairs"] / d["seconds"], 1), unit=UNIT, cores=1, kind="oracle",
+                sample=f"{d['layers']} whole {args.config} layers (all routed blocks, both stages) "
+                       f"in {d['seconds']:.1f} s, numpy float64, 1 BLAS thread")
+
+
+def run_reference(args):
+    """The CPU oracle timed on the same workload and metric (the reference arm)."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1 and rank != 0:
+        return
+    from synth import WORKLOADS, make_layer
+
+    wl = WORKLOADS[args.config]
+    li = make_layer(wl, args.seed, layer=0)
+    cache = {}
+    # calibrate: blocks per step so that warmup + steps stay within ~120 s
+    t0 = time.perf_counter()
+    oracle_layer_sample(wl, li, 1, 0, cache)
+    t_first = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    oracle_layer_sample(wl, li, 4, 1, cache)
+    per_block = max((time.perf_counter() - t0) / 4, 1e-5)
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    bps = int(max(1, min(1 << 20, budget / per_block)))
+    for i in range(args.warmup):
+        oracle_layer_sample(wl, li, bps, i, cache)
+    t0 = time.perf_counter()
+    pairs = 0
+    for i in range(args.steps):
+        pairs += oracle_layer_sample(wl, li, bps, args.warmup + i, cache)
+    dt = time.perf_counter() - t0
+    value = pairs / dt
+    nthreads = os.environ.get("OPENBLAS_NUM_THREADS") or os.environ.get("OMP_NUM_THREADS") or str(os.cpu_count())
+    out = dict(impl="reference", metric=METRIC, value=round(value, 1), unit=UNIT, n_gpus=world,
+               steps=args.steps, warmup=args.warmup, ms_per_step=round(dt * 1e3 / args.steps, 4),
+               higher_is_better=True, scaling="weak", vs_baseline=None, dtype="f64",
+               data="synthetic",
+               config=dict(workload=f"{args.config}: {wl.note}", blocks_per_step=bps,
+                           routing_s=round(t_first, 4)),
+               cpu_baseline=dict(value=round(value, 1), unit=UNIT, cores=int(nthreads),
+                                 kind="oracle",
+                                 sample=f"{bps} routed blocks of one {args.config} layer per step"),
+               e2e=dict(value=round(value, 1), unit=UNIT, h2d_bytes_per_step=0, d2h_bytes_per_step=0))
+    print(json.dumps(out))
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.cpu_worker:
+        cpu_worker(args)
+    elif args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,203 @@
+/*
+ * mol.h -- C ABI of the MoL ("virtual experts") LoRA hot path on GB300 (sm_103a).
+ *
+ * Each (routed expert, LoRA adapter) pair is one virtual expert of a larger
+ * MoE: V = num_experts * max_loras (fork PR #24 "feat(mol):
+ * SGLANG_OPT_MOL_LORA_STAGE_CFG", the "...and grid blowup / Root cause"
+ * commit). One LoRA stage of a MoE layer runs four steps:
+ *
+ *   1. mol_virtual_topk      remap top-k expert ids to virtual ids;
+ *   2. mol_align_block_size  group pairs by virtual expert into BLOCK_M-padded
+ *                            blocks, invalid ids in a trailing sentinel bucket;
+ *   3. mol_lora_shrink       inter = x . lora_a^T per block (fp32 out);
+ *   4. mol_lora_expand       out += scale * inter . lora_b^T per block (bf16 RMW).
+ *
+ * mol_lora_forward runs 1-4 (or 3-4 on an existing routing) in one call.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Data pointers are DEVICE pointers, owned by the caller, on the current
+ *   CUDA device; the library never allocates, frees or keeps them.
+ * - bf16 tensors are passed as raw 16-bit storage (const void* / void*).
+ * - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *   Every call only enqueues work on `stream` and returns: it does not
+ *   synchronize, allocate, or read device memory on the host, so a sequence of
+ *   calls can be captured into a CUDA graph.
+ * - Arguments are validated on the host before anything is enqueued. On an
+ *   error status nothing is launched and no output is touched.
+ * - Bad device *data* never faults: ids outside [0, V) go to the sentinel
+ *   bucket; sorted_token_ids entries outside [0, numel) are skipped.
+ * - Return value: MOL_OK (0) or a negative MOL_ERR_* status;
+ *   mol_status_string() names it, mol_last_cuda_error() gives the cudaError_t
+ *   behind MOL_ERR_CUDA (per host thread).
+ * - Scalars and pointers only; no struct is passed by value.
+ * - Routing layout (all int32):
+ *     vtopk_ids         [num_tokens * topk]  virtual ids, negative = sentinel
+ *     sorted_token_ids  [capacity]           flat pair ids grouped by bucket,
+ *                                            ascending inside a bucket, pads = numel
+ *     expert_ids        [capacity / block_m] virtual expert of each block, -1 for
+ *                                            sentinel blocks and blocks past the end
+ *     num_tokens_post_padded [1]             number of filled slots (multiple of block_m)
+ *   capacity must be >= mol_align_capacity(numel, V, block_m).
+ */
+#ifndef MOL_H_
+#define MOL_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOL_OK 0
+#define MOL_ERR_INVALID_ARG (-1)  /* null pointer, negative size, inconsistent sizes */
+#define MOL_ERR_CAPACITY (-2)     /* routing buffer or workspace smaller than required */
+#define MOL_ERR_UNSUPPORTED (-3)  /* shape/alignment outside the kernels' contract, or not sm_103 */
+#define MOL_ERR_CUDA (-4)         /* a CUDA call failed; see mol_last_cuda_error() */
+
+/* Bucket cap of align: V + 1 (sentinel) <= 8192 (sglang PR 24262 prhub summary,
+ * "Implementation breakdown" item 2 and "Risks" item 2: at most 8191 virtual experts). */
+#define MOL_MAX_BUCKETS 8192
+/* Largest number of (token, slot) pairs one call accepts. */
+#define MOL_MAX_NUMEL (1 << 22)
+
+/* Library ABI version (major * 100 + minor). */
+int32_t mol_version(void);
+
+/* Text for a status code; never NULL. */
+const char* mol_status_string(int32_t status);
+
+/* cudaError_t of the last MOL_ERR_CUDA returned on this host thread (0 if none). */
+int32_t mol_last_cuda_error(void);
+
+/*
+ * Slots of sorted_token_ids needed for any routing of `numel` pairs:
+ * ceil_BM(numel + min(numel, V + 1) * (block_m - 1)). The fork PR #24
+ * code-review commit calls this the worst-case untrimmed routing buffer; the
+ * bound is tight (one pair per bucket reaches it). Pure host arithmetic.
+ * Returns -1 on invalid arguments.
+ */
+int64_t mol_align_capacity(int64_t numel, int32_t num_vexperts, int32_t block_m);
+
+/*
+ * Bytes of device workspace mol_align_block_size / mol_lora_forward need for
+ * these sizes (0 when one thread block does the whole align). Pure host
+ * arithmetic. Returns 0 on invalid arguments (the call itself then fails).
+ */
+size_t mol_workspace_bytes(int64_t numel, int32_t num_vexperts, int32_t block_m);
+
+/*
+ * Step 1: virtual top-k remap (sglang PR 24171 prhub summary, "Key source
+ * snippets", _fused_virtual_topk_ids_kernel; fork PR #24 "fix(lora): -1 = no
+ * adapter" commit).
+ *   vtopk[i] = base                       if base < 0 (sentinel kept verbatim)
+ *            = -1                         if lora < 0, lora >= max_loras or base >= num_experts
+ *            = base + lora * num_experts  otherwise
+ * with base = topk_ids[i], lora = lora_ids[i / topk].
+ *   topk_ids  int32 [num_tokens, topk], row-major, device
+ *   lora_ids  int32 [num_tokens], device (per-token adapter slot, -1 = none)
+ *   vtopk_ids int32 [num_tokens, topk], device, written (may not alias inputs)
+ * num_tokens >= 0, topk >= 1, num_experts >= 1, max_loras >= 1,
+ * num_tokens * topk <= MOL_MAX_NUMEL. num_tokens == 0 enqueues nothing.
+ */
+int32_t mol_virtual_topk(const int32_t* topk_ids, const int32_t* lora_ids, int64_t num_tokens,
+                         int32_t topk, int32_t num_experts, int32_t max_loras,
+                         int32_t* vtopk_ids, void* stream);
+
+/*
+ * Step 2: align_block_size with a sentinel bucket (sglang PR 24171 prhub
+ * summary, "Key source snippets", _align_block_size_torch; sglang PR 24262
+ * prhub summary, "Implementation breakdown": histogram, prefix sum, expert_ids,
+ * scatter, no host synchronisation).
+ * bucket(i) = vtopk[i] if 0 <= vtopk[i] < V else V. Bucket b holds c_b pairs
+ * and p_b = ceil(c_b / block_m) * block_m slots at offset o_b = sum_{b'<b} p_b'.
+ *   sorted_token_ids[o_b + j] = j-th smallest i with bucket(i) == b (j < c_b),
+ *                               numel in [o_b + c_b, o_b + p_b) and [ntpp, capacity)
+ *   expert_ids[t]             = b for t in [o_b, o_b + p_b) / block_m when b < V, else -1
+ *   *num_tokens_post_padded   = ntpp = sum_b p_b (the sentinel bucket is counted)
+ * All three outputs are written in full. Deterministic and bit-reproducible.
+ *   vtopk_ids    int32 [numel], device
+ *   num_vexperts V >= 1, V + 1 <= MOL_MAX_BUCKETS
+ *   block_m      one of 16, 32, 64, 128
+ *   capacity     >= mol_align_capacity(numel, V, block_m), multiple of block_m
+ *   workspace    device, >= mol_workspace_bytes(numel, V, block_m) bytes, 16-byte
+ *                aligned (may be NULL when that is 0); contents are scratch
+ */
+int32_t mol_align_block_size(const int32_t* vtopk_ids, int64_t numel, int32_t num_vexperts,
+                             int32_t block_m, int32_t* sorted_token_ids, int64_t capacity,
+                             int32_t* expert_ids, int32_t* num_tokens_post_padded,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Step 3: LoRA shrink per block (fork PR #24 "Root cause" commit: the MoL
+ * shrink stage is a fused-MoE GEMM over virtual experts with N = S*r, K = the
+ * input width; code-review commit: weight layout [E, N, K]).
+ * For every block t with t * block_m < ntpp and v = expert_ids[t] >= 0, and
+ * every slot whose pair id i = sorted_token_ids[t*block_m + m] is in [0, numel):
+ *   inter[i, j] = sum_k x[i / x_row_div, k] * lora_a[v, j, k],  j < R = num_slices*rank
+ * accumulated in fp32. Rows of pairs in no such block are not written.
+ *   x          bf16, row q at x + q * x_row_stride (elements), K valid columns
+ *   x_row_div  topk for token-row input (gate_up), 1 for per-pair input (down)
+ *   lora_a     bf16 [num_vexperts, R, K], contiguous
+ *   inter      fp32 [numel, R], contiguous
+ * Contract: K % 8 == 0, R % 16 == 0, R <= 256, x_row_stride % 8 == 0,
+ * x, lora_a, inter 16-byte aligned, capacity % block_m == 0.
+ */
+int32_t mol_lora_shrink(const void* x, int64_t x_row_stride, int32_t x_row_div, int32_t K,
+                        const void* lora_a, int32_t num_slices, int32_t rank,
+                        const int32_t* sorted_token_ids, const int32_t* expert_ids,
+                        const int32_t* num_tokens_post_padded, int64_t capacity,
+                        int32_t block_m, int64_t numel, int32_t num_vexperts, float* inter,
+                        void* stream);
+
+/*
+ * Step 4: LoRA expand per block, added into the MoE output (fork PR #24 PR
+ * body "Background (measured attribution)": M x N output from a K = rank
+ * contraction; "Fix": weight view [E, N, K]).
+ * For the same blocks and pairs as the shrink, for slice s < num_slices and
+ * n < slice_n:
+ *   out[i, s*slice_n + n] = bf16_rn( out + scale * w_i *
+ *                           sum_j inter[i, s*rank + j] * lora_b[v, s*slice_n + n, j] )
+ * with w_i = topk_weights[i] (or 1 when topk_weights is NULL); accumulation,
+ * scale and add in fp32, one round-to-nearest-even to bf16. Rows of pairs in
+ * no processed block are bit-unchanged ("-1 = no adapter": no delta).
+ *   inter        fp32 [numel, num_slices*rank]
+ *   lora_b       bf16 [num_vexperts, num_slices*slice_n, rank], contiguous
+ *   topk_weights fp32 [numel] or NULL
+ *   out          bf16, row i at out + i * out_row_stride (elements), updated in place
+ * Contract: rank in {16, 32, 64, 128}, slice_n % 8 == 0, out_row_stride % 8 == 0,
+ * out_row_stride >= num_slices * slice_n, inter/lora_b/out 16-byte aligned.
+ */
+int32_t mol_lora_expand(const float* inter, const void* lora_b, int32_t num_slices, int32_t rank,
+                        int32_t slice_n, float scale, const float* topk_weights,
+                        const int32_t* sorted_token_ids, const int32_t* expert_ids,
+                        const int32_t* num_tokens_post_padded, int64_t capacity, int32_t block_m,
+                        int64_t numel, int32_t num_vexperts, void* out, int64_t out_row_stride,
+                        void* stream);
+
+/*
+ * One MoL LoRA stage end to end (fork PR #24 PR body "Background": per layer
+ * one routing feeds every MoL stage). With compute_routing = 1 the call runs
+ * steps 1-2 into the given routing buffers (vtopk_ids, sorted_token_ids,
+ * expert_ids, num_tokens_post_padded), then 3-4; with 0 it reads those
+ * buffers as they are (the down stage reusing the gate_up routing) and
+ * topk_ids / lora_ids / workspace may be NULL. Arguments are those of the
+ * four calls above; numel = num_tokens * topk; V = num_experts * max_loras.
+ */
+int32_t mol_lora_forward(const void* x, int64_t x_row_stride, int32_t x_row_div, int32_t K,
+                         const int32_t* topk_ids, const int32_t* lora_ids, int64_t num_tokens,
+                         int32_t topk, int32_t num_experts, int32_t max_loras,
+                         const void* lora_a, const void* lora_b, int32_t num_slices,
+                         int32_t rank, int32_t slice_n, float scale,
+                         const float* topk_weights, void* out, int64_t out_row_stride,
+                         int32_t block_m, int32_t compute_routing, int32_t* vtopk_ids,
+                         int32_t* sorted_token_ids, int64_t capacity, int32_t* expert_ids,
+                         int32_t* num_tokens_post_padded, float* inter,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOL_H_ */

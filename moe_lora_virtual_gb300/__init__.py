@@ -1,0 +1,237 @@
+"""Python binding of the MoL ("virtual experts") LoRA library for GB300.
+
+Argument marshalling only: every step runs in the CUDA kernels of
+``libmol.so`` through its C ABI (``include/mol.h``). PyTorch supplies device
+memory and the current stream. The functions keep the C names; each raises
+``MolError`` on a non-zero status. There is no CPU fallback: if the library
+is missing, the first call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import NamedTuple, Optional
+
+import torch
+
+from .build import LIB_PATH
+
+MOL_OK = 0
+MOL_ERR_INVALID_ARG = -1
+MOL_ERR_CAPACITY = -2
+MOL_ERR_UNSUPPORTED = -3
+MOL_ERR_CUDA = -4
+MOL_MAX_BUCKETS = 8192
+MOL_MAX_NUMEL = 1 << 22
+
+EXPORTS = (
+    "mol_version", "mol_status_string", "mol_last_cuda_error", "mol_align_capacity",
+    "mol_workspace_bytes", "mol_virtual_topk", "mol_align_block_size", "mol_lora_shrink",
+    "mol_lora_expand", "mol_lora_forward",
+)
+
+_lib = None
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_I64 = ctypes.c_int64
+_F32 = ctypes.c_float
+_SZ = ctypes.c_size_t
+
+_SIGS = {
+    "mol_version": (_I32, []),
+    "mol_status_string": (ctypes.c_char_p, [_I32]),
+    "mol_last_cuda_error": (_I32, []),
+    "mol_align_capacity": (_I64, [_I64, _I32, _I32]),
+    "mol_workspace_bytes": (_SZ, [_I64, _I32, _I32]),
+    "mol_virtual_topk": (_I32, [_P, _P, _I64, _I32, _I32, _I32, _P, _P]),
+    "mol_align_block_size": (_I32, [_P, _I64, _I32, _I32, _P, _I64, _P, _P, _P, _SZ, _P]),
+    "mol_lora_shrink": (_I32, [_P, _I64, _I32, _I32, _P, _I32, _I32, _P, _P, _P, _I64, _I32, _I64,
+                               _I32, _P, _P]),
+    "mol_lora_expand": (_I32, [_P, _P, _I32, _I32, _I32, _F32, _P, _P, _P, _P, _I64, _I32, _I64,
+                               _I32, _P, _I64, _P]),
+    "mol_lora_forward": (_I32, [_P, _I64, _I32, _I32, _P, _P, _I64, _I32, _I32, _I32, _P, _P, _I32,
+                                _I32, _I32, _F32, _P, _P, _I64, _I32, _I32, _P, _P, _I64, _P, _P,
+                                _P, _P, _SZ, _P]),
+}
+
+
+class MolError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        lib = library()
+        msg = lib.mol_status_string(status).decode()
+        cuda = lib.mol_last_cuda_error() if status == MOL_ERR_CUDA else 0
+        super().__init__(f"{fn}: status {status} ({msg})" + (f", cudaError {cuda}" if cuda else ""))
+        self.status = status
+        self.cuda_error = cuda
+
+
+def library(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load libmol.so once and declare every export's signature."""
+    global _lib
+    if _lib is None:
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"MoL CUDA library not built ({p} missing): run "
+                               "moe_lora_virtual_gb300.build.build_library() first")
+        lib = ctypes.CDLL(p)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def _check(fn: str, status: int) -> None:
+    if status != MOL_OK:
+        raise MolError(fn, status)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _need(t: torch.Tensor, dtype: torch.dtype, name: str) -> None:
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise TypeError(f"{name}: expected a CUDA tensor")
+
+
+def _row_stride(t: torch.Tensor, name: str) -> int:
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError(f"{name}: expected a 2-D tensor with unit column stride")
+    return t.stride(0)
+
+
+def align_capacity(numel: int, num_vexperts: int, block_m: int) -> int:
+    return int(library().mol_align_capacity(numel, num_vexperts, block_m))
+
+
+def workspace_bytes(numel: int, num_vexperts: int, block_m: int) -> int:
+    return int(library().mol_workspace_bytes(numel, num_vexperts, block_m))
+
+
+class Routing(NamedTuple):
+    vtopk_ids: torch.Tensor            # int32 [numel]
+    sorted_token_ids: torch.Tensor     # int32 [capacity]
+    expert_ids: torch.Tensor           # int32 [capacity // block_m]
+    num_tokens_post_padded: torch.Tensor  # int32 [1]
+    block_m: int
+    numel: int
+    num_vexperts: int
+
+    @property
+    def capacity(self) -> int:
+        return self.sorted_token_ids.numel()
+
+
+def alloc_routing(numel: int, num_vexperts: int, block_m: int, device) -> Routing:
+    cap = align_capacity(numel, num_vexperts, block_m)
+    i32 = dict(dtype=torch.int32, device=device)
+    return Routing(torch.empty(numel, **i32), torch.empty(cap, **i32),
+                   torch.empty(cap // block_m, **i32), torch.empty(1, **i32),
+                   block_m, numel, num_vexperts)
+
+
+def alloc_workspace(numel: int, num_vexperts: int, block_m: int, device) -> Optional[torch.Tensor]:
+    n = workspace_bytes(numel, num_vexperts, block_m)
+    return torch.empty(n, dtype=torch.uint8, device=device) if n else None
+
+
+def mol_virtual_topk(topk_ids: torch.Tensor, lora_ids: torch.Tensor, num_experts: int,
+                     max_loras: int, vtopk_ids: Optional[torch.Tensor] = None, stream=None):
+    _need(topk_ids, torch.int32, "topk_ids")
+    _need(lora_ids, torch.int32, "lora_ids")
+    T, k = topk_ids.shape
+    if vtopk_ids is None:
+        vtopk_ids = torch.empty_like(topk_ids)
+    _check("mol_virtual_topk", library().mol_virtual_topk(
+        _ptr(topk_ids.contiguous()), _ptr(lora_ids.contiguous()), T, k, num_experts, max_loras,
+        _ptr(vtopk_ids), _stream(stream)))
+    return vtopk_ids
+
+
+def mol_align_block_size(vtopk_ids: torch.Tensor, num_vexperts: int, block_m: int,
+                         routing: Optional[Routing] = None,
+                         workspace: Optional[torch.Tensor] = None, stream=None) -> Routing:
+    _need(vtopk_ids, torch.int32, "vtopk_ids")
+    v = vtopk_ids.reshape(-1)
+    numel = v.numel()
+    if routing is None:
+        routing = alloc_routing(numel, num_vexperts, block_m, v.device)
+        routing = routing._replace(vtopk_ids=v)
+    if workspace is None:
+        workspace = alloc_workspace(numel, num_vexperts, block_m, v.device)
+    wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("mol_align_block_size", library().mol_align_block_size(
+        _ptr(v), numel, num_vexperts, block_m, _ptr(routing.sorted_token_ids), routing.capacity,
+        _ptr(routing.expert_ids), _ptr(routing.num_tokens_post_padded), _ptr(workspace), wsb,
+        _stream(stream)))
+    return routing
+
+
+def mol_lora_shrink(x: torch.Tensor, x_row_div: int, lora_a: torch.Tensor, num_slices: int,
+                    routing: Routing, inter: Optional[torch.Tensor] = None, stream=None):
+    _need(x, torch.bfloat16, "x")
+    _need(lora_a, torch.bfloat16, "lora_a")
+    V, R, K = lora_a.shape
+    if inter is None:
+        inter = torch.empty(routing.numel, R, dtype=torch.float32, device=x.device)
+    _need(inter, torch.float32, "inter")
+    _check("mol_lora_shrink", library().mol_lora_shrink(
+        _ptr(x), _row_stride(x, "x"), x_row_div, K, _ptr(lora_a), num_slices, R // num_slices,
+        _ptr(routing.sorted_token_ids), _ptr(routing.expert_ids),
+        _ptr(routing.num_tokens_post_padded), routing.capacity, routing.block_m, routing.numel,
+        routing.num_vexperts, _ptr(inter), _stream(stream)))
+    return inter
+
+
+def mol_lora_expand(inter: torch.Tensor, lora_b: torch.Tensor, num_slices: int, scale: float,
+                    routing: Routing, out: torch.Tensor,
+                    topk_weights: Optional[torch.Tensor] = None, stream=None):
+    _need(inter, torch.float32, "inter")
+    _need(lora_b, torch.bfloat16, "lora_b")
+    _need(out, torch.bfloat16, "out")
+    if topk_weights is not None:
+        _need(topk_weights, torch.float32, "topk_weights")
+    V, N, r = lora_b.shape
+    _check("mol_lora_expand", library().mol_lora_expand(
+        _ptr(inter), _ptr(lora_b), num_slices, r, N // num_slices, float(scale), _ptr(topk_weights),
+        _ptr(routing.sorted_token_ids), _ptr(routing.expert_ids),
+        _ptr(routing.num_tokens_post_padded), routing.capacity, routing.block_m, routing.numel,
+        routing.num_vexperts, _ptr(out), _row_stride(out, "out"), _stream(stream)))
+    return out
+
+
+def mol_lora_forward(x: torch.Tensor, x_row_div: int, topk_ids: Optional[torch.Tensor],
+                     lora_ids: Optional[torch.Tensor], num_experts: int, max_loras: int,
+                     lora_a: torch.Tensor, lora_b: torch.Tensor, num_slices: int, scale: float,
+                     out: torch.Tensor, routing: Routing, inter: torch.Tensor,
+                     compute_routing: bool = True, topk_weights: Optional[torch.Tensor] = None,
+                     workspace: Optional[torch.Tensor] = None, num_tokens: Optional[int] = None,
+                     topk: Optional[int] = None, stream=None) -> None:
+    """One MoL LoRA stage; with compute_routing the routing buffers are (re)computed."""
+    _need(x, torch.bfloat16, "x")
+    if topk_ids is not None:
+        _need(topk_ids, torch.int32, "topk_ids")
+        num_tokens, topk = topk_ids.shape
+    if lora_ids is not None:
+        _need(lora_ids, torch.int32, "lora_ids")
+    V, R, K = lora_a.shape
+    _, N, r = lora_b.shape
+    wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("mol_lora_forward", library().mol_lora_forward(
+        _ptr(x), _row_stride(x, "x"), x_row_div, K, _ptr(topk_ids), _ptr(lora_ids), num_tokens,
+        topk, num_experts, max_loras, _ptr(lora_a), _ptr(lora_b), num_slices, r,
+        N // num_slices, float(scale), _ptr(topk_weights), _ptr(out), _row_stride(out, "out"),
+        routing.block_m, int(bool(compute_routing)), _ptr(routing.vtopk_ids),
+        _ptr(routing.sorted_token_ids), routing.capacity, _ptr(routing.expert_ids),
+        _ptr(routing.num_tokens_post_padded), _ptr(inter), _ptr(workspace), wsb, _stream(stream)))

@@ -1,0 +1,371 @@
+// Virtual top-k remap and align_block_size with a sentinel bucket (sm_103a).
+//
+// Remap: sglang PR 24171 prhub summary, "Key source snippets"
+// (_fused_virtual_topk_ids_kernel: keep negative ids, else base + lora * E);
+// fork PR #24 "fix(lora): -1 = no adapter" commit (no-adapter tokens get no
+// delta, so they are remapped to -1).
+// Align: sglang PR 24171 prhub summary, "Key source snippets"
+// (_align_block_size_torch: sentinel bucket V, bucket_count = V + 1, sentinel
+// blocks keep -1); sglang PR 24262 prhub summary, "Implementation breakdown"
+// (histogram, prefix sum, expert_ids, scatter in a few launches, no host
+// synchronisation; up to 8192 buckets).
+//
+// Design. The order inside a bucket is ascending flat index, so the scatter
+// is a stable counting sort. Pairs are cut into tiles (one thread block each);
+// a tile is cut into 8 contiguous warp segments; a warp walks its segment in
+// rounds of 32 pairs in order. Inside a round, __match_any_sync gives each
+// lane the lanes holding the same bucket; a per-warp shared-memory table of
+// 16-bit counters (one per bucket) carries the running count across rounds.
+// Pass 1 counts, a column scan over the 8 warp tables turns counts into
+// per-warp bases, pass 2 recomputes each pair's stable rank inside the tile.
+// Everything is ordered by construction (tile < warp < round < lane), so the
+// result is bit-reproducible with no atomics. With one tile the same block
+// finishes the job (bucket scan, expert_ids, scatter): one launch. With more
+// tiles, per-tile histograms go to the workspace, one block scans them, and a
+// third launch scatters.
+
+#include <algorithm>
+
+#include "mol_device.cuh"
+#include "mol_internal.h"
+
+namespace mol {
+
+constexpr int kAlignThreads = 256;
+constexpr int kAlignWarps = kAlignThreads / 32;
+constexpr int kScanThreads = 1024;
+constexpr int kTileMin = 4096;
+constexpr int kMaxTiles = 128;
+constexpr int kAlignSmemMax = 200 * 1024;
+
+MOL_DEV int remap_one(int base, int lora, int num_experts, int max_loras) {
+  if (base < 0) return base;
+  if (lora < 0 || lora >= max_loras || base >= num_experts) return -1;
+  return base + lora * num_experts;
+}
+
+MOL_DEV int bucket_of(int vid, int num_vexperts) {
+  return (vid >= 0 && vid < num_vexperts) ? vid : num_vexperts;
+}
+
+__global__ void virtual_topk_kernel(const int* __restrict__ topk_ids, const int* __restrict__ lora_ids,
+                                    int64_t numel, int topk, int num_experts, int max_loras,
+                                    int* __restrict__ vtopk) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < numel;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    vtopk[i] = remap_one(topk_ids[i], lora_ids[i / topk], num_experts, max_loras);
+  }
+}
+
+// Exclusive scan of one int per thread over the block; `total` = sum of all.
+template <int THREADS>
+MOL_DEV int block_exclusive_scan(int v, int* sh, int& total) {
+  constexpr int NW = THREADS / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) sh[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int w = lane < NW ? sh[lane] : 0;
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += n;
+    }
+    if (lane < NW) sh[lane] = wi - w;
+    if (lane == NW - 1) sh[NW] = wi;
+  }
+  __syncthreads();
+  const int res = sh[warp] + incl - v;
+  total = sh[NW];
+  __syncthreads();
+  return res;
+}
+
+// counts[b] -> exclusive offsets of the BM-padded buckets (in place), then
+// expert_ids of every block and num_tokens_post_padded.
+template <int THREADS>
+MOL_DEV void bucket_offsets(int* counts, int nb, int num_vexperts, int block_m, int64_t capacity,
+                            int* __restrict__ expert_ids, int* __restrict__ ntpp_out, int* sh) {
+  const int per = (nb + THREADS - 1) / THREADS;
+  const int b0 = min((int)threadIdx.x * per, nb), b1 = min(b0 + per, nb);
+  int local = 0;
+  for (int b = b0; b < b1; ++b) local += (counts[b] + block_m - 1) / block_m * block_m;
+  int total;
+  int run = block_exclusive_scan<THREADS>(local, sh, total);
+  for (int b = b0; b < b1; ++b) {
+    const int pb = (counts[b] + block_m - 1) / block_m * block_m;
+    counts[b] = run;
+    if (b < num_vexperts) {
+      const int t0 = run / block_m;
+      for (int k = 0; k < pb / block_m; ++k) expert_ids[t0 + k] = b;
+    }
+    run += pb;
+  }
+  __syncthreads();
+  const int64_t nblk = capacity / block_m;
+  for (int64_t t = counts[num_vexperts] / block_m + threadIdx.x; t < nblk; t += THREADS)
+    expert_ids[t] = -1;
+  if (threadIdx.x == 0) *ntpp_out = total;
+}
+
+template <bool REMAP>
+__global__ void __launch_bounds__(kAlignThreads, 1)
+align_tile_kernel(const int* __restrict__ src, const int* __restrict__ lora_ids, int topk,
+                  int num_experts, int max_loras, int* __restrict__ vtopk_out, int64_t numel,
+                  int num_vexperts, int block_m, int64_t capacity, int tile, int tiles, int nb_pad,
+                  int* __restrict__ sorted_ids, int* __restrict__ expert_ids,
+                  int* __restrict__ ntpp_out, int* __restrict__ ws_hist,
+                  int* __restrict__ ws_rank) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  __shared__ int sh_scan[kAlignWarps + 1];
+  const int nb = num_vexperts + 1;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint16_t* tbl = reinterpret_cast<uint16_t*>(smem);   // [kAlignWarps][nb_pad]
+  uint16_t* keys = tbl + kAlignWarps * nb_pad;         // [tile]
+  int* offs = reinterpret_cast<int*>(keys + tile);     // [nb], single-tile only
+  const bool fused = (tiles == 1);
+
+  // Every slot starts as padding (value numel); real pairs overwrite theirs.
+  for (int64_t q = (int64_t)blockIdx.x * kAlignThreads + tid; q < capacity;
+       q += (int64_t)gridDim.x * kAlignThreads)
+    sorted_ids[q] = (int)numel;
+  if ((int)blockIdx.x >= tiles) return;  // fill-only block
+
+  const int64_t t0 = (int64_t)blockIdx.x * tile;
+  const int tlen = (int)min((int64_t)tile, numel - t0);
+  for (int q = tid; q < tlen; q += kAlignThreads) {
+    const int64_t i = t0 + q;
+    int vid;
+    if (REMAP) {
+      vid = remap_one(src[i], lora_ids[i / topk], num_experts, max_loras);
+      vtopk_out[i] = vid;
+    } else {
+      vid = src[i];
+    }
+    keys[q] = (uint16_t)bucket_of(vid, num_vexperts);
+  }
+  {
+    uint4* t4 = reinterpret_cast<uint4*>(tbl);
+    const int n4 = kAlignWarps * nb_pad / 8;
+    for (int q = tid; q < n4; q += kAlignThreads) t4[q] = make_uint4(0, 0, 0, 0);
+  }
+  __syncthreads();
+
+  // Pass 1: per-warp bucket counts over the warp's contiguous segment.
+  const int seg = tile / kAlignWarps;
+  const int s0 = warp * seg, s1 = min(s0 + seg, tlen);
+  uint16_t* mine = tbl + warp * nb_pad;
+  for (int r = s0; r < s1; r += 32) {
+    const int q = r + lane;
+    const bool valid = q < s1;
+    const unsigned key = valid ? keys[q] : 0xFFFFu;
+    const unsigned peers = __match_any_sync(0xffffffffu, key);
+    if (valid && lane == __ffs(peers) - 1) mine[key] = (uint16_t)(mine[key] + __popc(peers));
+    __syncwarp();
+  }
+  __syncthreads();
+
+  // Column scan: warp tables become exclusive bases; the tile total per bucket
+  // goes to shared memory (one tile) or to the workspace histogram.
+  for (int b = tid; b < nb; b += kAlignThreads) {
+    int run = 0;
+#pragma unroll
+    for (int w = 0; w < kAlignWarps; ++w) {
+      uint16_t* p = tbl + w * nb_pad + b;
+      const int c = *p;
+      *p = (uint16_t)run;
+      run += c;
+    }
+    if (fused)
+      offs[b] = run;
+    else
+      ws_hist[(int64_t)blockIdx.x * nb + b] = run;
+  }
+  __syncthreads();
+  if (fused)
+    bucket_offsets<kAlignThreads>(offs, nb, num_vexperts, block_m, capacity, expert_ids, ntpp_out,
+                                  sh_scan);
+
+  // Pass 2: stable rank of every pair inside the tile.
+  for (int r = s0; r < s1; r += 32) {
+    const int q = r + lane;
+    const bool valid = q < s1;
+    const unsigned key = valid ? keys[q] : 0xFFFFu;
+    const unsigned peers = __match_any_sync(0xffffffffu, key);
+    const int base = valid ? (int)mine[key] : 0;
+    __syncwarp();
+    if (valid && lane == __ffs(peers) - 1) mine[key] = (uint16_t)(base + __popc(peers));
+    __syncwarp();
+    if (valid) {
+      const int lr = base + __popc(peers & lanemask_lt());
+      const int64_t i = t0 + q;
+      if (fused)
+        sorted_ids[offs[key] + lr] = (int)i;
+      else
+        ws_rank[i] = lr;
+    }
+  }
+}
+
+// Multi-tile: per-bucket prefix over tiles, bucket offsets, expert_ids, ntpp.
+__global__ void __launch_bounds__(kScanThreads, 1)
+align_scan_kernel(int* __restrict__ ws_hist, int* __restrict__ ws_offs, int tiles,
+                  int num_vexperts, int block_m, int64_t capacity, int* __restrict__ expert_ids,
+                  int* __restrict__ ntpp_out) {
+  extern __shared__ __align__(16) int counts[];
+  __shared__ int sh_scan[kScanThreads / 32 + 1];
+  const int nb = num_vexperts + 1;
+  for (int b = threadIdx.x; b < nb; b += kScanThreads) {
+    int run = 0;
+    int p = 0;
+    for (; p + 8 <= tiles; p += 8) {
+      int c[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) c[u] = ws_hist[(int64_t)(p + u) * nb + b];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        ws_hist[(int64_t)(p + u) * nb + b] = run;
+        run += c[u];
+      }
+    }
+    for (; p < tiles; ++p) {
+      const int c = ws_hist[(int64_t)p * nb + b];
+      ws_hist[(int64_t)p * nb + b] = run;
+      run += c;
+    }
+    counts[b] = run;
+  }
+  __syncthreads();
+  bucket_offsets<kScanThreads>(counts, nb, num_vexperts, block_m, capacity, expert_ids, ntpp_out,
+                               sh_scan);
+  __syncthreads();
+  for (int b = threadIdx.x; b < nb; b += kScanThreads) ws_offs[b] = counts[b];
+}
+
+__global__ void align_scatter_kernel(const int* __restrict__ vtopk, int64_t numel, int num_vexperts,
+                                     int tile, const int* __restrict__ ws_hist,
+                                     const int* __restrict__ ws_offs,
+                                     const int* __restrict__ ws_rank, int* __restrict__ sorted_ids) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= numel) return;
+  const int key = bucket_of(vtopk[i], num_vexperts);
+  const int64_t p = i / tile;
+  sorted_ids[ws_offs[key] + ws_hist[p * (num_vexperts + 1) + key] + ws_rank[i]] = (int)i;
+}
+
+// ---------------------------------------------------------------------------
+
+AlignPlan make_align_plan(int64_t numel, int num_vexperts, int block_m) {
+  AlignPlan p{};
+  p.numel = numel;
+  p.nb = num_vexperts + 1;
+  p.nb_pad = (p.nb + 7) & ~7;
+  p.block_m = block_m;
+  const int64_t nonempty = std::min<int64_t>(numel, p.nb);
+  p.capacity = (numel + nonempty * (block_m - 1) + block_m - 1) / block_m * block_m;
+  if (numel <= kTileMin) {
+    p.tile = (int)std::max<int64_t>(256, (numel + 255) / 256 * 256);
+    p.tiles = 1;
+  } else {
+    const int64_t want = (numel + kMaxTiles - 1) / kMaxTiles;
+    p.tile = (int)std::max<int64_t>(kTileMin, (want + 255) / 256 * 256);
+    p.tiles = (int)((numel + p.tile - 1) / p.tile);
+  }
+  size_t smem = (size_t)kAlignWarps * p.nb_pad * 2 + (size_t)p.tile * 2;
+  if (p.tiles == 1) smem += (size_t)p.nb * 4;
+  p.smem_tile = (smem + 15) / 16 * 16;
+  if (p.tiles == 1) {
+    p.ws_bytes = 0;
+  } else {
+    const size_t ints = (size_t)p.tiles * p.nb + p.nb + (size_t)numel;
+    p.ws_bytes = (ints * 4 + 255) / 256 * 256;
+  }
+  return p;
+}
+
+static int sm_count(int device) {
+  static int cache[64] = {0};
+  if (device < 0 || device >= 64) return 148;
+  if (cache[device] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || n <= 0)
+      n = 148;
+    cache[device] = n;
+  }
+  return cache[device];
+}
+
+cudaError_t prepare_align_kernels() {
+  cudaError_t e = cudaFuncSetAttribute(align_tile_kernel<true>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kAlignSmemMax);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(align_tile_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kAlignSmemMax);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(align_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kAlignSmemMax);
+}
+
+cudaError_t launch_virtual_topk(const int32_t* topk_ids, const int32_t* lora_ids, int64_t numel,
+                                int topk, int num_experts, int max_loras, int32_t* vtopk,
+                                cudaStream_t stream) {
+  if (numel == 0) return cudaSuccess;
+  const int threads = 256;
+  const int64_t blocks = std::min<int64_t>((numel + threads - 1) / threads, 4096);
+  virtual_topk_kernel<<<(unsigned)blocks, threads, 0, stream>>>(topk_ids, lora_ids, numel, topk,
+                                                                num_experts, max_loras, vtopk);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_align(const AlignPlan& plan, bool remap, const int32_t* src,
+                         const int32_t* lora_ids, int topk, int num_experts, int max_loras,
+                         int32_t* vtopk_out, int num_vexperts, int32_t* sorted_ids,
+                         int32_t* expert_ids, int32_t* ntpp, void* workspace,
+                         cudaStream_t stream) {
+  if (plan.numel == 0) return cudaMemsetAsync(ntpp, 0, sizeof(int32_t), stream);
+  int device = 0;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return e;
+  int* ws_hist = nullptr;
+  int* ws_offs = nullptr;
+  int* ws_rank = nullptr;
+  unsigned grid = 1;
+  if (plan.tiles > 1) {
+    ws_hist = static_cast<int*>(workspace);
+    ws_offs = ws_hist + (size_t)plan.tiles * plan.nb;
+    ws_rank = ws_offs + plan.nb;
+    const int64_t fill_blocks = (plan.capacity + 16383) / 16384;
+    grid = (unsigned)std::max<int64_t>(plan.tiles, std::min<int64_t>(sm_count(device), fill_blocks));
+  }
+  if (remap) {
+    align_tile_kernel<true><<<grid, kAlignThreads, plan.smem_tile, stream>>>(
+        src, lora_ids, topk, num_experts, max_loras, vtopk_out, plan.numel, num_vexperts,
+        plan.block_m, plan.capacity, plan.tile, plan.tiles, plan.nb_pad, sorted_ids, expert_ids,
+        ntpp, ws_hist, ws_rank);
+  } else {
+    align_tile_kernel<false><<<grid, kAlignThreads, plan.smem_tile, stream>>>(
+        src, nullptr, 1, 1, 1, nullptr, plan.numel, num_vexperts, plan.block_m, plan.capacity,
+        plan.tile, plan.tiles, plan.nb_pad, sorted_ids, expert_ids, ntpp, ws_hist, ws_rank);
+  }
+  e = cudaGetLastError();
+  if (e != cudaSuccess || plan.tiles == 1) return e;
+  align_scan_kernel<<<1, kScanThreads, (size_t)plan.nb * 4, stream>>>(
+      ws_hist, ws_offs, plan.tiles, num_vexperts, plan.block_m, plan.capacity, expert_ids, ntpp);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int64_t sblocks = (plan.numel + 255) / 256;
+  const int32_t* vt = remap ? vtopk_out : src;
+  align_scatter_kernel<<<(unsigned)sblocks, 256, 0, stream>>>(vt, plan.numel, num_vexperts,
+                                                              plan.tile, ws_hist, ws_offs, ws_rank,
+                                                              sorted_ids);
+  return cudaGetLastError();
+}
+
+}  // namespace mol

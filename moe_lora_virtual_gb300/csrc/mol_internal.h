@@ -1,0 +1,49 @@
+// Host-side launchers behind the C ABI (not exported).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace mol {
+
+// Geometry of the align step for given sizes (host arithmetic).
+struct AlignPlan {
+  int64_t numel;
+  int nb;          // buckets = V + 1
+  int nb_pad;      // nb rounded up to 8
+  int block_m;
+  int64_t capacity;
+  int tile;        // pairs per tile block
+  int tiles;       // number of tile blocks (1 = single fused block)
+  size_t smem_tile;
+  size_t ws_bytes;  // workspace needed (0 when tiles == 1)
+};
+
+AlignPlan make_align_plan(int64_t numel, int num_vexperts, int block_m);
+
+cudaError_t prepare_kernels(int device);
+
+cudaError_t launch_virtual_topk(const int32_t* topk_ids, const int32_t* lora_ids, int64_t numel,
+                                int topk, int num_experts, int max_loras, int32_t* vtopk,
+                                cudaStream_t stream);
+
+// remap != 0: `src` is topk_ids and the remap is fused (vtopk written);
+// remap == 0: `src` is vtopk_ids.
+cudaError_t launch_align(const AlignPlan& plan, bool remap, const int32_t* src,
+                         const int32_t* lora_ids, int topk, int num_experts, int max_loras,
+                         int32_t* vtopk_out, int num_vexperts, int32_t* sorted_ids,
+                         int32_t* expert_ids, int32_t* ntpp, void* workspace, cudaStream_t stream);
+
+cudaError_t launch_shrink(const void* x, int64_t x_stride, int x_div, int K, const void* lora_a,
+                          int R, const int32_t* sorted_ids, const int32_t* expert_ids,
+                          const int32_t* ntpp, int64_t capacity, int block_m, int64_t numel,
+                          int num_vexperts, float* inter, cudaStream_t stream);
+
+cudaError_t launch_expand(const float* inter, const void* lora_b, int S, int r, int Ns, float scale,
+                          const float* topk_weights, const int32_t* sorted_ids,
+                          const int32_t* expert_ids, const int32_t* ntpp, int64_t capacity,
+                          int block_m, int64_t numel, int num_vexperts, void* out,
+                          int64_t out_stride, cudaStream_t stream);
+
+}  // namespace mol

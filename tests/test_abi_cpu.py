@@ -1,0 +1,118 @@
+"""CPU checks of the C-ABI library: it builds, loads, exports every declared symbol,
+and its host-side arithmetic and argument validation behave as declared.
+
+No call here reaches a kernel: validation rejects the arguments first, or the
+entry point is pure host arithmetic.
+"""
+
+import ctypes
+import os
+import re
+import shutil
+
+import numpy as np
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mol.h")
+
+needs_nvcc = pytest.mark.skipif(not (shutil.which("nvcc") or os.path.exists("/usr/local/cuda/bin/nvcc")),
+                                reason="nvcc not available")
+
+
+@pytest.fixture(scope="module")
+def mol():
+    from moe_lora_virtual_gb300.build import build_library
+
+    build_library()
+    import moe_lora_virtual_gb300 as m
+
+    m.library()
+    return m
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(mol_\w+)\s*\(", src)))
+
+
+@needs_nvcc
+def test_exports_every_declared_symbol(mol):
+    lib = mol.library()
+    names = declared_functions()
+    assert len(names) == 10
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(mol.EXPORTS)
+
+
+@needs_nvcc
+def test_status_strings_and_version(mol):
+    lib = mol.library()
+    assert lib.mol_version() == 100
+    for code in (0, -1, -2, -3, -4, 7):
+        assert isinstance(lib.mol_status_string(code), bytes)
+    assert lib.mol_last_cuda_error() == 0
+
+
+@needs_nvcc
+@pytest.mark.parametrize("numel,V,BM", [(0, 1, 16), (1, 1, 16), (184, 1024, 16), (32768, 8064, 64),
+                                        (65536, 4096, 64), (10, 3, 4), (7, 100, 128)])
+def test_capacity_matches_oracle(mol, numel, V, BM):
+    assert mol.align_capacity(numel, V, BM) == oracle.align_capacity(numel, V, BM)
+
+
+@needs_nvcc
+def test_workspace_sizes(mol):
+    assert mol.workspace_bytes(184, 1024, 16) == 0          # one block does the whole align
+    assert mol.workspace_bytes(4096, 8191, 16) == 0
+    w = mol.workspace_bytes(65536, 4096, 64)
+    assert w >= 4 * (65536 + 4097) and w % 256 == 0
+    assert mol.workspace_bytes(1 << 22, 8191, 16) <= 4 * (128 * 8192 + 8192 + (1 << 22)) + 256
+    assert mol.workspace_bytes(-1, 16, 16) == 0
+    assert mol.workspace_bytes(16, 8192, 16) == 0           # rejected sizes report 0
+
+
+@needs_nvcc
+def test_validation_rejects_before_any_launch(mol):
+    lib = mol.library()
+    P = ctypes.c_void_p
+    # align: bad block_m, bucket cap, negative sizes, capacity, missing workspace
+    assert lib.mol_align_block_size(P(16), 64, 16, 48, P(16), 4096, P(16), P(16), None, 0, None) == -3
+    assert lib.mol_align_block_size(P(16), 64, 8192, 16, P(16), 4096, P(16), P(16), None, 0, None) == -3
+    assert lib.mol_align_block_size(P(16), -5, 16, 16, P(16), 4096, P(16), P(16), None, 0, None) == -1
+    assert lib.mol_align_block_size(P(16), 64, 16, 16, P(16), 64, P(16), P(16), None, 0, None) == -2
+    assert lib.mol_align_block_size(P(16), 70000, 16, 16, P(16), 1 << 20, P(16), P(16), None, 0, None) == -2
+    assert lib.mol_align_block_size(P(16), (1 << 22) + 1, 16, 16, P(16), 1 << 30, P(16), P(16), None, 0, None) == -3
+    # shrink / expand contracts
+    assert lib.mol_lora_shrink(P(16), 64, 1, 60, P(16), 1, 16, P(16), P(16), P(16), 64, 16, 8, 4, P(16), None) == -3
+    assert lib.mol_lora_shrink(P(16), 64, 1, 64, P(16), 1, 8, P(16), P(16), P(16), 64, 16, 8, 4, P(16), None) == -3
+    assert lib.mol_lora_shrink(P(18), 64, 1, 64, P(16), 1, 16, P(16), P(16), P(16), 64, 16, 8, 4, P(16), None) == -3
+    assert lib.mol_lora_shrink(P(16), 64, 0, 64, P(16), 1, 16, P(16), P(16), P(16), 64, 16, 8, 4, P(16), None) == -1
+    assert lib.mol_lora_shrink(P(16), 64, 1, 64, P(16), 1, 16, P(16), P(16), P(16), 65, 16, 8, 4, P(16), None) == -1
+    assert lib.mol_lora_expand(P(16), P(16), 1, 24, 16, 1.0, None, P(16), P(16), P(16), 64, 16, 8, 4, P(16), 16, None) == -3
+    assert lib.mol_lora_expand(P(16), P(16), 1, 16, 12, 1.0, None, P(16), P(16), P(16), 64, 16, 8, 4, P(16), 16, None) == -3
+    assert lib.mol_lora_expand(P(16), P(16), 2, 16, 64, 1.0, None, P(16), P(16), P(16), 64, 16, 8, 4, P(16), 64, None) == -1
+    assert lib.mol_lora_expand(P(16), P(16), 1, 16, 64, 1.0, None, P(16), P(16), P(16), 64, 16, 8, 4, P(24), 64, None) == -3
+    # remap
+    assert lib.mol_virtual_topk(P(16), P(16), -1, 8, 4, 4, P(16), None) == -1
+    assert lib.mol_virtual_topk(P(16), P(16), 1 << 20, 8, 4, 4, P(16), None) == -3
+    # forward: V + 1 over the bucket cap
+    assert lib.mol_lora_forward(P(16), 64, 1, 64, P(16), P(16), 4, 2, 4096, 2, P(16), P(16), 1, 16, 16,
+                                1.0, None, P(16), 16, 16, 1, P(16), P(16), 4096, P(16), P(16), P(16),
+                                None, 0, None) == -3
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    import moe_lora_virtual_gb300 as m
+
+    saved = m._lib
+    try:
+        m._lib = None
+        with pytest.raises(RuntimeError, match="not built"):
+            m.library(str(tmp_path / "missing.so"))
+    finally:
+        m._lib = saved
