@@ -119,6 +119,29 @@ class ClockSampler:
                     reasons=sorted(reasons), samples=len(win))
 
 
+# --------------------------------------------------------------------------- ranks
+
+def combine_ranks(ms: float, pairs: float, device=None):
+    """Weak scaling over independent replicas: slowest rank's time, sum of every rank's pairs."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return ms, pairs
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    p = torch.tensor([pairs], dtype=torch.float64, device=device)
+    dist.all_reduce(p, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(p.item())
+
+
+def shard_tokens(num_tokens: int, world: int, rank: int):
+    """Contiguous token range of `rank` when one batch is split over `world` replicas."""
+    base, extra = divmod(num_tokens, world)
+    start = rank * base + min(rank, extra)
+    return start, start + base + (1 if rank < extra else 0)
+
+
 # --------------------------------------------------------------------------- GPU arm
 
 class LayerState:
@@ -260,15 +283,7 @@ def run_gpu(args):
     clk = clocks.summary(t0, t1)
     clocks.stop()
 
-    if world > 1:
-        tmax = torch.tensor([ms], device=dev)
-        dist.all_reduce(tmax, op=dist.ReduceOp.MAX)
-        ms = float(tmax.item())
-        ptot = torch.tensor([pairs_per_step], device=dev, dtype=torch.float64)
-        dist.all_reduce(ptot)
-        pairs_all = float(ptot.item())
-    else:
-        pairs_all = pairs_per_step
+    ms, pairs_all = combine_ranks(ms, pairs_per_step, dev if world > 1 else None)
     value = pairs_all / (ms * 1e-3)
 
     # ---- per-kernel timing (each kernel alone in its own graphs, same rotation) -------

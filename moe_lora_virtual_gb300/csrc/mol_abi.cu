@@ -151,7 +151,8 @@ int32_t mol_align_block_size(const int32_t* vtopk_ids, int64_t numel, int32_t nu
                              void* workspace, size_t workspace_bytes, void* stream) {
   int32_t st = check_align_args(numel, num_vexperts, block_m);
   if (st != MOL_OK) return st;
-  if (!num_tokens_post_padded || (numel > 0 && (!vtopk_ids || !sorted_token_ids || !expert_ids)))
+  if (!num_tokens_post_padded || (numel > 0 && !vtopk_ids) ||
+      (capacity > 0 && (!sorted_token_ids || !expert_ids)))
     return MOL_ERR_INVALID_ARG;
   const mol::AlignPlan plan = mol::make_align_plan(numel, num_vexperts, block_m);
   if (capacity < plan.capacity || capacity % block_m != 0) return MOL_ERR_CAPACITY;
@@ -237,8 +238,8 @@ int32_t mol_lora_forward(const void* x, int64_t x_row_stride, int32_t x_row_div,
   const mol::AlignPlan plan = mol::make_align_plan(numel, V, block_m);
   if (compute_routing) {
     if (!num_tokens_post_padded) return MOL_ERR_INVALID_ARG;
-    if (numel > 0 && (!topk_ids || !lora_ids || !vtopk_ids || !sorted_token_ids || !expert_ids))
-      return MOL_ERR_INVALID_ARG;
+    if (numel > 0 && (!topk_ids || !lora_ids || !vtopk_ids)) return MOL_ERR_INVALID_ARG;
+    if (capacity > 0 && (!sorted_token_ids || !expert_ids)) return MOL_ERR_INVALID_ARG;
     if (capacity < plan.capacity) return MOL_ERR_CAPACITY;
     if (plan.ws_bytes > 0 && (!workspace || workspace_bytes < plan.ws_bytes))
       return MOL_ERR_CAPACITY;

@@ -329,7 +329,6 @@ cudaError_t launch_align(const AlignPlan& plan, bool remap, const int32_t* src,
                          int32_t* vtopk_out, int num_vexperts, int32_t* sorted_ids,
                          int32_t* expert_ids, int32_t* ntpp, void* workspace,
                          cudaStream_t stream) {
-  if (plan.numel == 0) return cudaMemsetAsync(ntpp, 0, sizeof(int32_t), stream);
   int device = 0;
   cudaError_t e = cudaGetDevice(&device);
   if (e != cudaSuccess) return e;
