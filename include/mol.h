@@ -130,6 +130,33 @@ int32_t mol_align_block_size(const int32_t* vtopk_ids, int64_t numel, int32_t nu
                              void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * mol_align_block_size without a workspace argument, for callers that cannot
+ * allocate device memory where they route a batch: a runtime that has already
+ * reserved nearly all of HBM for its own pool and gives an operator only its
+ * inputs and outputs, or a latency-critical loop where an allocation's
+ * implicit device synchronisation is not acceptable. The pages have no
+ * counterpart of this call; it is a convenience of this library.
+ * The scratch is a fixed 1 MiB array compiled into the library (every GPU that
+ * loads the library holds it until the process exits). Sizes whose workspace
+ * (mol_workspace_bytes) exceeds 1 MiB are rejected with MOL_ERR_CAPACITY, for
+ * example more than about 100k pairs with 8192 buckets. Outputs, capacity and
+ * the other arguments are those of mol_align_block_size, and so are the results
+ * (bit-identical). No allocation of any kind is made.
+ * Every call shares the one array and it keeps the previous call's contents;
+ * nothing in it needs to start at zero (each word a call reads was written
+ * earlier by the same call). Calls that overlap on the GPU (several streams, or
+ * several host threads) race on it and must be serialised by the caller.
+ * The first call on each device looks the array's device address up
+ * (cudaGetSymbolAddress) with that device current; make that first call before
+ * any stream capture.
+ */
+int32_t mol_align_block_size_noalloc(const int32_t* vtopk_ids, int64_t numel,
+                                     int32_t num_vexperts, int32_t block_m,
+                                     int32_t* sorted_token_ids, int64_t capacity,
+                                     int32_t* expert_ids, int32_t* num_tokens_post_padded,
+                                     void* stream);
+
+/*
  * Step 3: LoRA shrink per block (fork PR #24 "Root cause" commit: the MoL
  * shrink stage is a fused-MoE GEMM over virtual experts with N = S*r, K = the
  * input width; code-review commit: weight layout [E, N, K]).

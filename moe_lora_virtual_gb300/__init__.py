@@ -28,7 +28,7 @@ MOL_MAX_NUMEL = 1 << 22
 EXPORTS = (
     "mol_version", "mol_status_string", "mol_last_cuda_error", "mol_align_capacity",
     "mol_workspace_bytes", "mol_virtual_topk", "mol_align_block_size", "mol_lora_shrink",
-    "mol_lora_expand", "mol_lora_forward",
+    "mol_lora_expand", "mol_lora_forward", "mol_align_block_size_noalloc",
 )
 
 _lib = None
@@ -46,6 +46,7 @@ _SIGS = {
     "mol_workspace_bytes": (_SZ, [_I64, _I32, _I32]),
     "mol_virtual_topk": (_I32, [_P, _P, _I64, _I32, _I32, _I32, _P, _P]),
     "mol_align_block_size": (_I32, [_P, _I64, _I32, _I32, _P, _I64, _P, _P, _P, _SZ, _P]),
+    "mol_align_block_size_noalloc": (_I32, [_P, _I64, _I32, _I32, _P, _I64, _P, _P, _P]),
     "mol_lora_shrink": (_I32, [_P, _I64, _I32, _I32, _P, _I32, _I32, _P, _P, _P, _I64, _I32, _I64,
                                _I32, _P, _P]),
     "mol_lora_expand": (_I32, [_P, _P, _I32, _I32, _I32, _F32, _P, _P, _P, _P, _I64, _I32, _I64,
@@ -175,6 +176,24 @@ def mol_align_block_size(vtopk_ids: torch.Tensor, num_vexperts: int, block_m: in
         _ptr(v), numel, num_vexperts, block_m, _ptr(routing.sorted_token_ids), routing.capacity,
         _ptr(routing.expert_ids), _ptr(routing.num_tokens_post_padded), _ptr(workspace), wsb,
         _stream(stream)))
+    return routing
+
+
+def mol_align_block_size_noalloc(vtopk_ids: torch.Tensor, num_vexperts: int, block_m: int,
+                                 routing: Optional[Routing] = None, stream=None) -> Routing:
+    """mol_align_block_size with the library's own 1 MiB scratch instead of a workspace.
+
+    For callers that cannot allocate device memory at routing time; calls that
+    overlap on the GPU share the scratch and must be serialised by the caller.
+    """
+    _need(vtopk_ids, torch.int32, "vtopk_ids")
+    v = vtopk_ids.reshape(-1)
+    numel = v.numel()
+    if routing is None:
+        routing = alloc_routing(numel, num_vexperts, block_m, v.device)._replace(vtopk_ids=v)
+    _check("mol_align_block_size_noalloc", library().mol_align_block_size_noalloc(
+        _ptr(v), numel, num_vexperts, block_m, _ptr(routing.sorted_token_ids), routing.capacity,
+        _ptr(routing.expert_ids), _ptr(routing.num_tokens_post_padded), _stream(stream)))
     return routing
 
 

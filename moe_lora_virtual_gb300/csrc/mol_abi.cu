@@ -268,3 +268,68 @@ int32_t mol_lora_forward(const void* x, int64_t x_row_stride, int32_t x_row_div,
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Align without any allocation: the scratch lives in this library.
+//
+// Some callers cannot call cudaMalloc (or any allocator) at the point where
+// they route a batch: an inference runtime that has already reserved nearly
+// all of device memory for its own pool and hands an operator only its input
+// and output buffers, or a latency-critical loop where an allocation's implicit
+// device synchronisation is not acceptable. For them, this variant of
+// mol_align_block_size takes no workspace argument and uses a fixed 1 MiB
+// array compiled into the library instead. Every GPU that loads the library
+// holds that 1 MiB until the process exits.
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(1) << 20;
+__device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+// Device address of g_noalloc_scratch, per device. In host code the array's
+// name is only a host-side stand-in, so the address is looked up once per
+// device with that device current.
+void* g_noalloc_scratch_addr[kMaxDevices] = {nullptr};
+
+int32_t noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return MOL_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_device_mutex);
+  if (g_noalloc_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e);
+    g_noalloc_scratch_addr[dev] = p;
+  }
+  *out = g_noalloc_scratch_addr[dev];
+  return MOL_OK;
+}
+
+}  // namespace
+
+extern "C" int32_t mol_align_block_size_noalloc(const int32_t* vtopk_ids, int64_t numel,
+                                                int32_t num_vexperts, int32_t block_m,
+                                                int32_t* sorted_token_ids, int64_t capacity,
+                                                int32_t* expert_ids,
+                                                int32_t* num_tokens_post_padded, void* stream) {
+  int32_t st = check_align_args(numel, num_vexperts, block_m);
+  if (st != MOL_OK) return st;
+  if (!num_tokens_post_padded || (numel > 0 && !vtopk_ids) ||
+      (capacity > 0 && (!sorted_token_ids || !expert_ids)))
+    return MOL_ERR_INVALID_ARG;
+  const mol::AlignPlan plan = mol::make_align_plan(numel, num_vexperts, block_m);
+  if (capacity < plan.capacity || capacity % block_m != 0) return MOL_ERR_CAPACITY;
+  if (plan.ws_bytes > kNoAllocScratchBytes) return MOL_ERR_CAPACITY;
+  st = ensure_device();
+  if (st != MOL_OK) return st;
+  void* scratch = nullptr;
+  st = noalloc_scratch(&scratch);
+  if (st != MOL_OK) return st;
+  mol::AlignPlan p = plan;
+  p.capacity = capacity;
+  cudaError_t e = mol::launch_align(p, false, vtopk_ids, nullptr, 1, 1, 1, nullptr, num_vexperts,
+                                    sorted_token_ids, expert_ids, num_tokens_post_padded, scratch,
+                                    static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOL_OK : cuda_fail(e);
+}
