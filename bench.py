@@ -7,10 +7,10 @@ reusing the routing. The workload is the bs=23 decode configuration (23
 tokens, 128 experts x 8 adapters = 1024 virtual experts, top-8, rank 32,
 gate_up 2048 -> 2x32 -> 2x768, down 768 -> 32 -> 2048), synthetic seeded data.
 
-Each step replays one CUDA graph of a whole layer. Steps rotate over
---layers distinct layers (own weights, routing and activations) so that a
-step never finds its weights in L2: 8 decode layers touch ~0.7 GB per cycle,
-over 5x the 129 MB L2.
+Steps rotate over --layers distinct layers (own weights, routing and
+activations) so that a step never finds its weights in L2: 8 decode layers
+touch ~0.7 GB per cycle, over 5x the 129 MB L2. As in a real decode step, one
+CUDA graph holds those layers back to back; exactly K steps are timed.
 
 Prints one JSON line (rank 0). Under torchrun every rank runs an independent
 replica (the path has no exchange step): weak scaling, value summed over ranks
@@ -250,7 +250,18 @@ def run_gpu(args):
     plan_tiles = 1 if mol.workspace_bytes(wl.numel, wl.V, wl.BM) == 0 else 3
     launches_per_step = plan_tiles + 2 * len(wl.stages)
 
+    # A real decode step replays all MoE layers inside one graph; here one graph
+    # holds the rotating layers back to back, and single-layer graphs cover the
+    # K mod layers remainder, so exactly K steps (layers) are timed.
     graphs = [capture(torch, lambda L_=L_: L_.forward(mol)) for L_ in layers]
+    multi = capture(torch, lambda: [L_.forward(mol) for L_ in layers])
+
+    def run_steps(n):
+        full, rest = divmod(n, len(layers))
+        for _ in range(full):
+            multi.replay()
+        for i in range(rest):
+            graphs[i].replay()
 
     props = torch.cuda.get_device_properties(dev)
     gpu_id = str(local)
@@ -262,8 +273,7 @@ def run_gpu(args):
     time.sleep(0.3)
 
     # ---- timed region: exactly K steps -----------------------------------------------
-    for i in range(args.warmup):
-        graphs[i % len(graphs)].replay()
+    run_steps(args.warmup)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -271,8 +281,7 @@ def run_gpu(args):
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0 = time.time()
     ev0.record()
-    for i in range(args.steps):
-        graphs[i % len(graphs)].replay()
+    run_steps(args.steps)
     ev1.record()
     torch.cuda.synchronize()
     t1 = time.time()
@@ -304,13 +313,17 @@ def run_gpu(args):
             return lambda: mol.mol_align_block_size(L_.routing.vtopk_ids, wl.V, wl.BM,
                                                     routing=L_.routing, workspace=L_.ws)
 
-        ksteps = max(200, min(args.steps, 5000))
-        kern["align"] = time_graphs(torch, [capture(torch, align_call(L_)) for L_ in layers],
-                                    ksteps, 20) * 1e3
+        reps = 4  # launches per graph = layers x reps, back to back on one stream
+
+        def per_launch_us(calls):
+            g = capture(torch, lambda: [f() for _ in range(reps) for f in calls])
+            n = max(20, min(args.steps, 2000) // (reps * len(calls)))
+            return time_graphs(torch, [g], n, 3) * 1e3 / (reps * len(calls))
+
+        kern["align"] = per_launch_us([align_call(L_) for L_ in layers])
         for si, st in enumerate(wl.stages):
             for which in ("shrink", "expand"):
-                gs = [capture(torch, stage_call(L_, si, which)) for L_ in layers]
-                kern[f"{which}_{st.name}"] = time_graphs(torch, gs, ksteps, 20) * 1e3
+                kern[f"{which}_{st.name}"] = per_launch_us([stage_call(L_, si, which) for L_ in layers])
         # dominant kernel: the stage kernel with the most algorithmic bytes
         best = None
         for si, st in enumerate(wl.stages):
@@ -344,6 +357,7 @@ def run_gpu(args):
                            stages=[f"{s.name} K={s.K} R={s.R} N={s.N}" for s in wl.stages],
                            pairs_per_layer=pairs_per_step, layers_rotated=args.layers,
                            l2="inputs larger than L2: steps rotate over distinct layers",
+                           graph=f"{args.layers} layers per graph replay (remainder: one layer per replay)",
                            parallelism=f"replicas{world}"),
                layer_hbm=dict(bytes=int(layer_bytes),
                               achieved_gbs=round(layer_bytes / (ms * 1e-3) / 1e9, 1),

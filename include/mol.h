@@ -168,8 +168,9 @@ int32_t mol_align_block_size_noalloc(const int32_t* vtopk_ids, int64_t numel,
  *   x_row_div  topk for token-row input (gate_up), 1 for per-pair input (down)
  *   lora_a     bf16 [num_vexperts, R, K], contiguous
  *   inter      fp32 [numel, R], contiguous
- * Contract: K % 8 == 0, R % 16 == 0, R <= 256, x_row_stride % 8 == 0,
- * x, lora_a, inter 16-byte aligned, capacity % block_m == 0.
+ * Contract: K % 8 == 0, K <= 65536, R % 16 == 0, R <= 1024, x_row_stride % 8 == 0,
+ * x, lora_a, inter 16-byte aligned, capacity % block_m == 0. x must hold
+ * ceil(numel / x_row_div) rows.
  */
 int32_t mol_lora_shrink(const void* x, int64_t x_row_stride, int32_t x_row_div, int32_t K,
                         const void* lora_a, int32_t num_slices, int32_t rank,

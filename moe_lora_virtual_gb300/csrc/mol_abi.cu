@@ -6,9 +6,6 @@
 #include "mol.h"
 #include "mol_internal.h"
 
-namespace mol {
-cudaError_t prepare_align_kernels();
-}
 
 namespace {
 
@@ -44,7 +41,7 @@ int32_t ensure_device() {
     if (major != 10 || minor != 3) {
       g_device_state[dev] = 2;
     } else {
-      e = mol::prepare_align_kernels();
+      e = mol::prepare_kernels();
       if (e != cudaSuccess) return cuda_fail(e);
       g_device_state[dev] = 1;
     }
@@ -75,7 +72,8 @@ int32_t check_shrink_args(const void* x, int64_t x_row_stride, int32_t x_row_div
   if (K <= 0 || x_row_div < 1 || num_slices < 1 || rank < 1 || x_row_stride < K)
     return MOL_ERR_INVALID_ARG;
   const int64_t R = (int64_t)num_slices * rank;
-  if (K % 8 != 0 || x_row_stride % 8 != 0 || R % 16 != 0 || R > 1024) return MOL_ERR_UNSUPPORTED;
+  if (K % 8 != 0 || K > mol::kShrinkMaxK || x_row_stride % 8 != 0 || R % 16 != 0 || R > 1024)
+    return MOL_ERR_UNSUPPORTED;
   if (numel > 0 && (!x || !lora_a || !inter)) return MOL_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(lora_a) || !aligned16(inter)) return MOL_ERR_UNSUPPORTED;
   return MOL_OK;
@@ -206,7 +204,7 @@ int32_t mol_lora_expand(const float* inter, const void* lora_b, int32_t num_slic
   cudaError_t e = mol::launch_expand(inter, lora_b, num_slices, rank, slice_n, scale, topk_weights,
                                      sorted_token_ids, expert_ids, num_tokens_post_padded,
                                      capacity, block_m, numel, num_vexperts, out, out_row_stride,
-                                     static_cast<cudaStream_t>(stream));
+                                     false, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MOL_OK : cuda_fail(e);
 }
 
@@ -263,7 +261,7 @@ int32_t mol_lora_forward(const void* x, int64_t x_row_stride, int32_t x_row_div,
   if (e != cudaSuccess) return cuda_fail(e);
   e = mol::launch_expand(inter, lora_b, num_slices, rank, slice_n, scale, topk_weights,
                          sorted_token_ids, expert_ids, num_tokens_post_padded, capacity, block_m,
-                         numel, V, out, out_row_stride, s);
+                         numel, V, out, out_row_stride, true, s);
   return e == cudaSuccess ? MOL_OK : cuda_fail(e);
 }
 

@@ -51,6 +51,8 @@ MOL_DEV int bucket_of(int vid, int num_vexperts) {
 __global__ void virtual_topk_kernel(const int* __restrict__ topk_ids, const int* __restrict__ lora_ids,
                                     int64_t numel, int topk, int num_experts, int max_loras,
                                     int* __restrict__ vtopk) {
+  pdl_wait();
+  pdl_launch_dependents();
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < numel;
        i += (int64_t)gridDim.x * blockDim.x) {
     vtopk[i] = remap_one(topk_ids[i], lora_ids[i / topk], num_experts, max_loras);
@@ -132,6 +134,14 @@ align_tile_kernel(const int* __restrict__ src, const int* __restrict__ lora_ids,
   int* offs = reinterpret_cast<int*>(keys + tile);     // [nb], single-tile only
   const bool fused = (tiles == 1);
 
+  if ((int)blockIdx.x < tiles) {  // shared memory only: may overlap the previous kernel
+    uint4* t4 = reinterpret_cast<uint4*>(tbl);
+    const int n4 = kAlignWarps * nb_pad / 8;
+    for (int q = tid; q < n4; q += kAlignThreads) t4[q] = make_uint4(0, 0, 0, 0);
+  }
+  pdl_wait();  // inputs and the routing buffers belong to earlier kernels until here
+  pdl_launch_dependents();
+
   // Every slot starts as padding (value numel); real pairs overwrite theirs.
   for (int64_t q = (int64_t)blockIdx.x * kAlignThreads + tid; q < capacity;
        q += (int64_t)gridDim.x * kAlignThreads)
@@ -150,11 +160,6 @@ align_tile_kernel(const int* __restrict__ src, const int* __restrict__ lora_ids,
       vid = src[i];
     }
     keys[q] = (uint16_t)bucket_of(vid, num_vexperts);
-  }
-  {
-    uint4* t4 = reinterpret_cast<uint4*>(tbl);
-    const int n4 = kAlignWarps * nb_pad / 8;
-    for (int q = tid; q < n4; q += kAlignThreads) t4[q] = make_uint4(0, 0, 0, 0);
   }
   __syncthreads();
 
@@ -222,6 +227,8 @@ align_scan_kernel(int* __restrict__ ws_hist, int* __restrict__ ws_offs, int tile
   extern __shared__ __align__(16) int counts[];
   __shared__ int sh_scan[kScanThreads / 32 + 1];
   const int nb = num_vexperts + 1;
+  pdl_wait();
+  pdl_launch_dependents();
   for (int b = threadIdx.x; b < nb; b += kScanThreads) {
     int run = 0;
     int p = 0;
@@ -253,6 +260,8 @@ __global__ void align_scatter_kernel(const int* __restrict__ vtopk, int64_t nume
                                      int tile, const int* __restrict__ ws_hist,
                                      const int* __restrict__ ws_offs,
                                      const int* __restrict__ ws_rank, int* __restrict__ sorted_ids) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= numel) return;
   const int key = bucket_of(vtopk[i], num_vexperts);
@@ -302,15 +311,19 @@ static int sm_count(int device) {
   return cache[device];
 }
 
-cudaError_t prepare_align_kernels() {
+cudaError_t prepare_lora_kernels();
+
+cudaError_t prepare_kernels() {
   cudaError_t e = cudaFuncSetAttribute(align_tile_kernel<true>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kAlignSmemMax);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(align_tile_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kAlignSmemMax);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(align_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              kAlignSmemMax);
+  e = cudaFuncSetAttribute(align_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kAlignSmemMax);
+  if (e != cudaSuccess) return e;
+  return prepare_lora_kernels();
 }
 
 cudaError_t launch_virtual_topk(const int32_t* topk_ids, const int32_t* lora_ids, int64_t numel,
@@ -319,9 +332,8 @@ cudaError_t launch_virtual_topk(const int32_t* topk_ids, const int32_t* lora_ids
   if (numel == 0) return cudaSuccess;
   const int threads = 256;
   const int64_t blocks = std::min<int64_t>((numel + threads - 1) / threads, 4096);
-  virtual_topk_kernel<<<(unsigned)blocks, threads, 0, stream>>>(topk_ids, lora_ids, numel, topk,
-                                                                num_experts, max_loras, vtopk);
-  return cudaGetLastError();
+  return launch_pdl(virtual_topk_kernel, dim3((unsigned)blocks), dim3(threads), 0, stream, topk_ids,
+                    lora_ids, numel, topk, num_experts, max_loras, vtopk);
 }
 
 cudaError_t launch_align(const AlignPlan& plan, bool remap, const int32_t* src,
@@ -344,27 +356,24 @@ cudaError_t launch_align(const AlignPlan& plan, bool remap, const int32_t* src,
     grid = (unsigned)std::max<int64_t>(plan.tiles, std::min<int64_t>(sm_count(device), fill_blocks));
   }
   if (remap) {
-    align_tile_kernel<true><<<grid, kAlignThreads, plan.smem_tile, stream>>>(
-        src, lora_ids, topk, num_experts, max_loras, vtopk_out, plan.numel, num_vexperts,
-        plan.block_m, plan.capacity, plan.tile, plan.tiles, plan.nb_pad, sorted_ids, expert_ids,
-        ntpp, ws_hist, ws_rank);
+    e = launch_pdl(align_tile_kernel<true>, dim3(grid), dim3(kAlignThreads), plan.smem_tile, stream,
+                   src, lora_ids, topk, num_experts, max_loras, vtopk_out, plan.numel, num_vexperts,
+                   plan.block_m, plan.capacity, plan.tile, plan.tiles, plan.nb_pad, sorted_ids,
+                   expert_ids, ntpp, ws_hist, ws_rank);
   } else {
-    align_tile_kernel<false><<<grid, kAlignThreads, plan.smem_tile, stream>>>(
-        src, nullptr, 1, 1, 1, nullptr, plan.numel, num_vexperts, plan.block_m, plan.capacity,
-        plan.tile, plan.tiles, plan.nb_pad, sorted_ids, expert_ids, ntpp, ws_hist, ws_rank);
+    e = launch_pdl(align_tile_kernel<false>, dim3(grid), dim3(kAlignThreads), plan.smem_tile, stream,
+                   src, static_cast<const int32_t*>(nullptr), 1, 1, 1, static_cast<int32_t*>(nullptr),
+                   plan.numel, num_vexperts, plan.block_m, plan.capacity, plan.tile, plan.tiles,
+                   plan.nb_pad, sorted_ids, expert_ids, ntpp, ws_hist, ws_rank);
   }
-  e = cudaGetLastError();
   if (e != cudaSuccess || plan.tiles == 1) return e;
-  align_scan_kernel<<<1, kScanThreads, (size_t)plan.nb * 4, stream>>>(
-      ws_hist, ws_offs, plan.tiles, num_vexperts, plan.block_m, plan.capacity, expert_ids, ntpp);
-  e = cudaGetLastError();
+  e = launch_pdl(align_scan_kernel, dim3(1), dim3(kScanThreads), (size_t)plan.nb * 4, stream, ws_hist,
+                 ws_offs, plan.tiles, num_vexperts, plan.block_m, plan.capacity, expert_ids, ntpp);
   if (e != cudaSuccess) return e;
   const int64_t sblocks = (plan.numel + 255) / 256;
   const int32_t* vt = remap ? vtopk_out : src;
-  align_scatter_kernel<<<(unsigned)sblocks, 256, 0, stream>>>(vt, plan.numel, num_vexperts,
-                                                              plan.tile, ws_hist, ws_offs, ws_rank,
-                                                              sorted_ids);
-  return cudaGetLastError();
+  return launch_pdl(align_scatter_kernel, dim3((unsigned)sblocks), dim3(256), 0, stream, vt,
+                    plan.numel, num_vexperts, plan.tile, ws_hist, ws_offs, ws_rank, sorted_ids);
 }
 
 }  // namespace mol

@@ -54,6 +54,80 @@ MOL_DEV uint2 ld_stream8(const void* p) {
 // 16-byte load of data other blocks reuse (activations, intermediates).
 MOL_DEV uint4 ld_keep16(const void* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
 MOL_DEV float4 ld_keep_f4(const float* p) { return __ldg(reinterpret_cast<const float4*>(p)); }
+// 16-byte load that bypasses L1 (data written by the preceding grid).
+MOL_DEV uint4 ld_l2_16(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+MOL_DEV float4 ld_l2_f4(const float* p) {
+  float4 r;
+  asm volatile("ld.global.cg.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
+               : "l"(p));
+  return r;
+}
+
+// Programmatic dependent launch. wait: block until the preceding grid in the
+// stream has completed and its writes are visible (a no-op when the launch
+// has no programmatic dependency). launch_dependents: let the next grid's
+// blocks be scheduled once every block of this grid has issued it.
+MOL_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+MOL_DEV void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// mbarrier + bulk async copy (TMA, 1-D) into shared memory.
+MOL_DEV uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+MOL_DEV void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+MOL_DEV void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+MOL_DEV void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+// Copy `bytes` (multiple of 16; both addresses 16-byte aligned) from global to
+// shared memory; completion is counted on `bar`.
+MOL_DEV void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+MOL_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait: gives up after `max_iter` polls (each poll may suspend the
+// thread for a short hardware-defined time) and returns false.
+MOL_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t max_iter) {
+  for (uint32_t i = 0; i < max_iter; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+
+MOL_DEV void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+// Barrier 1 among the first `threads` threads of the block (0 is __syncthreads).
+MOL_DEV void named_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+MOL_DEV uint4 lds16(const void* p) { return *reinterpret_cast<const uint4*>(p); }
+
+// Error bits a kernel records instead of hanging or trapping.
+constexpr unsigned kFaultBulkTimeout = 1u;
 
 MOL_DEV unsigned lanemask_lt() {
   unsigned m;
@@ -61,15 +135,13 @@ MOL_DEV unsigned lanemask_lt() {
   return m;
 }
 
-// Compact the valid pair ids of one block (ids in [0, numel)) into `rows`,
-// keeping slot order. Needs blockDim.x >= block_m and blockDim.x % 32 == 0;
-// every thread of the block must call it. Returns the number of rows.
-MOL_DEV int compact_block_rows(const int* __restrict__ slot_ids, int block_m, int64_t numel,
-                               int* rows, int* warp_counts) {
+// Compact the valid pair ids of one block into `rows`, keeping slot order.
+// `id` is this thread's slot of the block (-1 for threads past block_m); ids
+// outside [0, numel) are padding. Needs blockDim.x >= block_m and a multiple
+// of 32; every thread of the block must call it. Returns the row count.
+MOL_DEV int compact_block_rows(int id, int64_t numel, int* rows, int* warp_counts) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
-  int id = -1;
-  if (tid < block_m) id = slot_ids[tid];
-  const bool ok = tid < block_m && id >= 0 && (int64_t)id < numel;
+  const bool ok = id >= 0 && (int64_t)id < numel;
   const unsigned bal = __ballot_sync(0xffffffffu, ok);
   if (lane == 0) warp_counts[warp] = __popc(bal);
   __syncthreads();

@@ -22,7 +22,27 @@ struct AlignPlan {
 
 AlignPlan make_align_plan(int64_t numel, int num_vexperts, int block_m);
 
-cudaError_t prepare_kernels(int device);
+// Sets shared-memory limits of every kernel on the current device.
+cudaError_t prepare_kernels();
+
+// Launch with programmatic stream serialization: the kernel's blocks may be
+// scheduled while the previous kernel in the stream finishes; each kernel
+// guards its reads of that kernel's output with griddepcontrol.wait.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
 
 cudaError_t launch_virtual_topk(const int32_t* topk_ids, const int32_t* lora_ids, int64_t numel,
                                 int topk, int num_experts, int max_loras, int32_t* vtopk,
@@ -40,10 +60,16 @@ cudaError_t launch_shrink(const void* x, int64_t x_stride, int x_div, int K, con
                           const int32_t* ntpp, int64_t capacity, int block_m, int64_t numel,
                           int num_vexperts, float* inter, cudaStream_t stream);
 
+// early = true only when the preceding kernel is this library's shrink of the
+// same stage (mol_lora_forward): routing, weights and output rows are then read
+// before griddepcontrol.wait, the intermediate after it.
 cudaError_t launch_expand(const float* inter, const void* lora_b, int S, int r, int Ns, float scale,
                           const float* topk_weights, const int32_t* sorted_ids,
                           const int32_t* expert_ids, const int32_t* ntpp, int64_t capacity,
                           int block_m, int64_t numel, int num_vexperts, void* out,
-                          int64_t out_stride, cudaStream_t stream);
+                          int64_t out_stride, bool early, cudaStream_t stream);
+
+// Largest contraction width accepted by the shrink (it streams K in chunks).
+constexpr int kShrinkMaxK = 1 << 16;
 
 }  // namespace mol

@@ -36,101 +36,263 @@
 
 namespace mol {
 
-constexpr int kShrinkThreads = 128;  // 4 warps split the K range of one item
-constexpr int kShrinkNT = 2;         // 8-column mma tiles per item -> 16 weight rows
-constexpr int kShrinkUnroll = 4;     // 32-wide k blocks in flight per warp
-constexpr int kExpandThreads = 128;  // 4 warps x 32 output columns
-constexpr int kExpandCols = 128;
+constexpr uint32_t kWaitPolls = 1u << 22;  // bounded mbarrier waits
 
-template <int NT, int UNROLL>
-__global__ void __launch_bounds__(kShrinkThreads)
+// Faults recorded instead of hanging (see kFaultBulkTimeout).
+__device__ unsigned int g_fault_flags;
+
+// Shrink: a persistent, warp-specialised TMA pipeline.
+//
+// Work item = (routed block t, 16 weight rows jt). Block b of the grid (two
+// per SM) walks items b, b+G, b+2G, ... . Warp 4 is the producer: it prefetches
+// the next item's routing (expert id, slot ids) one item ahead, compacts the
+// block's real rows with warp ballots, splits them into jobs of at most 16 rows
+// and streams every job through a ring of shared-memory stages, one K-chunk
+// of 512 per stage: the 16 weight rows and the job's activation rows, each a
+// 16-byte aligned run copied by cp.async.bulk and counted on the stage's
+// "full" mbarrier. Warps 0-3 are consumers: they wait for a stage, run the
+// mma over their quarter of its k range from shared memory only, release the
+// stage on its "empty" mbarrier and, after a job's last chunk, add their four
+// partial sums in a fixed order and store the job's fp32 rows. Rows of a stage
+// are padded by 64 bytes so the 16-byte fragment reads of a quarter warp fall
+// in distinct banks. One thread issues bulk copies back to back at a limited
+// rate, so each SM runs two such blocks to keep 1 KB row-chunk copies at the
+// HBM rate. Every wait is bounded; a timeout records a fault bit and leaves
+// the kernel instead of hanging.
+namespace sp {
+constexpr int kConsumers = 4;                   // consumer warps
+constexpr int kThreads = (kConsumers + 1) * 32;  // + the producer warp
+constexpr int kJT = 16;                         // weight rows per item (two 8-column mma tiles)
+constexpr int kKC = 512;                        // k per stage
+constexpr int kPitch = kKC * 2 + 64;            // bytes per row in a stage
+constexpr int kStageBytes = (kJT + 16) * kPitch;  // weight rows + up to 16 activation rows
+constexpr int kStages = 3;
+constexpr int kBlocksPerSM = 2;                 // two issuing producers per SM (copy issue rate)
+constexpr int kMeta = kStages + 2;              // jobs whose rows a consumer may still read
+constexpr int kHeader = 1024;                   // barriers, stage headers, job meta
+constexpr size_t kSmem = kHeader + (size_t)kStages * kStageBytes;
+struct Job {
+  int v, jt, cm, pad;
+  int rows[16];
+};
+struct StageHdr {
+  int job;  // meta slot, -1 = end of work
+  int k0;
+  int pad0, pad1;
+};
+static_assert(2 * kStages * 8 + kStages * 16 + kMeta * (int)sizeof(Job) <= kHeader, "header");
+}  // namespace sp
+
+__global__ void __launch_bounds__(sp::kThreads, sp::kBlocksPerSM)
 lora_shrink_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, int K,
                    const uint16_t* __restrict__ lora_a, int R, const int* __restrict__ sorted_ids,
                    const int* __restrict__ expert_ids, const int* __restrict__ ntpp_ptr,
                    int block_m, int64_t numel, int num_vexperts, float* __restrict__ inter,
-                   int n_jt) {
-  constexpr int JT = 8 * NT;
-  constexpr int NW = kShrinkThreads / 32;
-  __shared__ int rows[128];
-  __shared__ int wcnt[NW];
-  __shared__ float red[NW - 1][NT * 4][32];
+                   int n_jt, int64_t n_items) {
+  using namespace sp;
+  extern __shared__ __align__(128) unsigned char smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* empty = full + kStages;
+  StageHdr* hdr = reinterpret_cast<StageHdr*>(smem + 2 * kStages * 8);
+  Job* meta = reinterpret_cast<Job*>(smem + 2 * kStages * 8 + kStages * sizeof(StageHdr));
+  unsigned char* stages = smem + kHeader;
+  __shared__ float red[kConsumers - 1][8][32];
+  __shared__ int prow[128];  // producer: compacted rows of the current block
 
-  const int t = blockIdx.x / n_jt;
-  const int jt = blockIdx.x - t * n_jt;
-  if ((int64_t)t * block_m >= (int64_t)__ldg(ntpp_ptr)) return;
-  const int v = __ldg(expert_ids + t);
-  if (v < 0 || v >= num_vexperts) return;
-  const int c = compact_block_rows(sorted_ids + (int64_t)t * block_m, block_m, numel, rows, wcnt);
-  if (c == 0) return;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    for (int st = 0; st < kStages; ++st) {
+      mbar_init(&full[st], 1);
+      mbar_init(&empty[st], kConsumers);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_wait();  // routing and activations come from earlier kernels
+  pdl_launch_dependents();
 
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, tq = lane & 3;
-  const int nkb = (K + 31) >> 5;
-  const int kb0 = warp * nkb / NW, kb1 = (warp + 1) * nkb / NW;
-  const int j0 = jt * JT;
-  const uint16_t* arow[NT];
+  if (warp == kConsumers) {
+    // ------------------------------------------------------------ producer
+    const int ntpp = __ldg(ntpp_ptr);
+    const int64_t G = gridDim.x;
+    uint32_t q = 0;  // stage uses issued
+    uint32_t jn = 0;  // jobs issued
+    auto fetch = [&](int64_t it, int& v, int (&sl)[4]) {
+      v = -1;
 #pragma unroll
-  for (int u = 0; u < NT; ++u) arow[u] = lora_a + ((int64_t)v * R + j0 + 8 * u + g) * K + 8 * tq;
-  const uint4 zero = make_uint4(0, 0, 0, 0);
-
-  for (int m0 = 0; m0 < c; m0 += 16) {
-    const int r0 = m0 + g, r1 = m0 + 8 + g;
-    const uint16_t* xr0 = r0 < c ? x + (int64_t)(rows[r0] / x_div) * x_stride + 8 * tq : nullptr;
-    const uint16_t* xr1 = r1 < c ? x + (int64_t)(rows[r1] / x_div) * x_stride + 8 * tq : nullptr;
-    float acc[NT][4];
+      for (int u = 0; u < 4; ++u) sl[u] = -1;
+      if (it >= n_items) return;
+      const int64_t t = it / n_jt;
+      v = (t * block_m < ntpp) ? __ldg(expert_ids + t) : -1;
 #pragma unroll
-    for (int u = 0; u < NT; ++u) acc[u][0] = acc[u][1] = acc[u][2] = acc[u][3] = 0.f;
-
-    for (int kb = kb0; kb < kb1; kb += UNROLL) {
-      uint4 a[UNROLL][NT], x0[UNROLL], x1[UNROLL];
-#pragma unroll
-      for (int uu = 0; uu < UNROLL; ++uu) {
-        const int k = (kb + uu) * 32;
-        const bool kin = (kb + uu < kb1) && (k + 8 * tq < K);
-#pragma unroll
-        for (int u = 0; u < NT; ++u) a[uu][u] = kin ? ld_stream16(arow[u] + k) : zero;
-        x0[uu] = (kin && xr0) ? ld_keep16(xr0 + k) : zero;
-        x1[uu] = (kin && xr1) ? ld_keep16(xr1 + k) : zero;
+      for (int u = 0; u < 4; ++u) {
+        const int idx = u * 32 + lane;
+        if (idx < block_m) sl[u] = __ldg(sorted_ids + t * block_m + idx);
       }
+    };
+    auto acquire = [&](int& st) -> bool {  // wait until stage q is free
+      st = (int)(q % kStages);
+      const uint32_t ph = (q / kStages) & 1;
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait(&empty[st], ph ^ 1, kWaitPolls);
+      return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    };
+    int v_n, sl_n[4];
+    int64_t item = blockIdx.x;
+    fetch(item, v_n, sl_n);
+    bool fault = false;
+    while (item < n_items && !fault) {
+      const int v = v_n;
+      int sl[4];
 #pragma unroll
-      for (int uu = 0; uu < UNROLL; ++uu) {
+      for (int u = 0; u < 4; ++u) sl[u] = sl_n[u];
+      const int64_t cur = item;
+      item += G;
+      fetch(item, v_n, sl_n);  // next item's routing is in flight while this one streams
+      if (v < 0 || v >= num_vexperts) continue;
+      int c = 0;
 #pragma unroll
-        for (int u = 0; u < NT; ++u) {
-          // k step 0 <- elements 8t..8t+3, k step 1 <- 8t+4..8t+7 (same map in both operands)
-          mma_16816(acc[u], x0[uu].x, x1[uu].x, x0[uu].y, x1[uu].y, a[uu][u].x, a[uu][u].y);
-          mma_16816(acc[u], x0[uu].z, x1[uu].z, x0[uu].w, x1[uu].w, a[uu][u].z, a[uu][u].w);
+      for (int u = 0; u < 4; ++u) {
+        const bool ok = sl[u] >= 0 && (int64_t)sl[u] < numel;
+        const unsigned bal = __ballot_sync(0xffffffffu, ok);
+        if (ok) prow[c + __popc(bal & lanemask_lt())] = sl[u];
+        c += __popc(bal);
+      }
+      __syncwarp();
+      const int jt = (int)(cur % n_jt);
+      const uint16_t* wsrc = lora_a + ((int64_t)v * R + jt * kJT + (lane & 15)) * K;
+      for (int m0 = 0; m0 < c && !fault; m0 += 16) {
+        const int cm = min(16, c - m0);
+        const int slot = (int)(jn % kMeta);
+        Job& jb = meta[slot];
+        if (lane == 0) {
+          jb.v = v;
+          jb.jt = jt;
+          jb.cm = cm;
+        }
+        if (lane < cm) jb.rows[lane] = prow[m0 + lane];
+        const uint16_t* xsrc =
+            (lane >= 16 && lane - 16 < cm) ? x + (int64_t)(prow[m0 + lane - 16] / x_div) * x_stride
+                                           : nullptr;
+        __syncwarp();
+        for (int k0 = 0; k0 < K; k0 += kKC) {
+          int st;
+          if (!acquire(st)) {
+            fault = true;
+            break;
+          }
+          const int len = min(kKC, K - k0);
+          unsigned char* base = stages + (size_t)st * kStageBytes;
+          if (lane == 0) {
+            hdr[st].job = slot;
+            hdr[st].k0 = k0;
+            mbar_arrive_expect_tx(&full[st], (uint32_t)((kJT + cm) * len * 2));
+          }
+          __syncwarp();
+          if (lane < 16)
+            bulk_g2s(base + lane * kPitch, wsrc + k0, len * 2, &full[st]);
+          else if (xsrc)
+            bulk_g2s(base + (kJT + lane - 16) * kPitch, xsrc + k0, len * 2, &full[st]);
+          ++q;
+        }
+        ++jn;
+      }
+    }
+    if (fault) {
+      if (lane == 0) atomicOr(&g_fault_flags, kFaultBulkTimeout);
+    } else {
+      int st;
+      if (acquire(st)) {
+        if (lane == 0) {
+          hdr[st].job = -1;
+          mbar_arrive(&full[st]);
+        }
+      } else if (lane == 0) {
+        atomicOr(&g_fault_flags, kFaultBulkTimeout);
+      }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int g = lane >> 2, tq = lane & 3;
+  const uint4 zero = make_uint4(0, 0, 0, 0);
+  float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  for (uint32_t q = 0;; ++q) {
+    const int st = (int)(q % kStages);
+    if (!mbar_wait(&full[st], (q / kStages) & 1, kWaitPolls)) {
+      if (lane == 0) atomicOr(&g_fault_flags, kFaultBulkTimeout);
+      return;
+    }
+    const int slot = hdr[st].job;
+    if (slot < 0) break;
+    const int k0 = hdr[st].k0;
+    const Job& jb = meta[slot];
+    const int cm = jb.cm;
+    const int len = min(kKC, K - k0);
+    if (k0 == 0) {
+#pragma unroll
+      for (int n = 0; n < 2; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+    }
+    const unsigned char* W = stages + (size_t)st * kStageBytes;
+    const unsigned char* X = W + kJT * kPitch;
+    const int nkb = (len + 31) >> 5;
+    const int kb0 = warp * nkb / kConsumers, kb1 = (warp + 1) * nkb / kConsumers;
+#pragma unroll 4
+    for (int kb = kb0; kb < kb1; ++kb) {
+      const int kk = kb * 32 + 8 * tq;
+      const bool kin = kk < len;
+      const uint4 xa = (kin && g < cm) ? lds16(X + g * kPitch + kk * 2) : zero;
+      const uint4 xb = (kin && g + 8 < cm) ? lds16(X + (g + 8) * kPitch + kk * 2) : zero;
+#pragma unroll
+      for (int n = 0; n < 2; ++n) {
+        const uint4 a = kin ? lds16(W + (8 * n + g) * kPitch + kk * 2) : zero;
+        // k step 0 <- elements 8t..8t+3, k step 1 <- 8t+4..8t+7 (same map in both operands)
+        mma_16816(acc[n], xa.x, xb.x, xa.y, xb.y, a.x, a.y);
+        mma_16816(acc[n], xa.z, xb.z, xa.w, xb.w, a.z, a.w);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[st]);
+    if (k0 + kKC >= K) {  // last chunk of the job: add the four partials, store
+      if (warp > 0) {
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) red[warp - 1][n * 4 + e][lane] = acc[n][e];
+      }
+      named_sync(1, kConsumers * 32);
+      if (warp == 0) {
+        const int j0 = jb.jt * kJT;
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+#pragma unroll
+            for (int w = 0; w < kConsumers - 1; ++w) acc[n][e] += red[w][n * 4 + e][lane];
+          const int col = j0 + 8 * n + 2 * tq;
+          if (g < cm)
+            *reinterpret_cast<float2*>(inter + (int64_t)jb.rows[g] * R + col) =
+                make_float2(acc[n][0], acc[n][1]);
+          if (g + 8 < cm)
+            *reinterpret_cast<float2*>(inter + (int64_t)jb.rows[g + 8] * R + col) =
+                make_float2(acc[n][2], acc[n][3]);
         }
       }
+      named_sync(1, kConsumers * 32);
     }
-
-    // Sum the four K-range partials in a fixed order (deterministic).
-    if (warp > 0) {
-#pragma unroll
-      for (int u = 0; u < NT; ++u)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) red[warp - 1][u * 4 + e][lane] = acc[u][e];
-    }
-    __syncthreads();
-    if (warp == 0) {
-#pragma unroll
-      for (int u = 0; u < NT; ++u) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-#pragma unroll
-          for (int w = 0; w < NW - 1; ++w) acc[u][e] += red[w][u * 4 + e][lane];
-        const int col = j0 + 8 * u + 2 * tq;
-        if (r0 < c)
-          *reinterpret_cast<float2*>(inter + (int64_t)rows[r0] * R + col) =
-              make_float2(acc[u][0], acc[u][1]);
-        if (r1 < c)
-          *reinterpret_cast<float2*>(inter + (int64_t)rows[r1] * R + col) =
-              make_float2(acc[u][2], acc[u][3]);
-      }
-    }
-    __syncthreads();
   }
 }
 
-template <int RK>
+// Expand. One item = (routed block t, slice s, 128 output columns), 4 warps x
+// 32 columns. Round 1 loads the routing words together, round 2 the weight
+// fragments and the output rows to update, round 3 the intermediate. With
+// EARLY (inside mol_lora_forward, right after this stage's shrink) rounds 1-2
+// run before griddepcontrol.wait, overlapping the shrink's tail.
+constexpr int kExpandThreads = 128;
+constexpr int kExpandCols = 128;
+
+template <int RK, bool EARLY>
 __global__ void __launch_bounds__(kExpandThreads)
 lora_expand_kernel(const float* __restrict__ inter, int R, const uint16_t* __restrict__ lora_b,
                    int S, int Ns, float scale, const float* __restrict__ topk_w,
@@ -143,18 +305,24 @@ lora_expand_kernel(const float* __restrict__ inter, int R, const uint16_t* __res
   __shared__ int rows[128];
   __shared__ int wcnt[kExpandThreads / 32];
 
+  const int tid = threadIdx.x;
   const int per_block = S * chunks_per_slice;
   const int t = blockIdx.x / per_block;
   const int rem = blockIdx.x - t * per_block;
   const int s = rem / chunks_per_slice;
   const int chunk = rem - s * chunks_per_slice;
-  if ((int64_t)t * block_m >= (int64_t)__ldg(ntpp_ptr)) return;
+  if (!EARLY) {
+    pdl_wait();
+    pdl_launch_dependents();
+  }
+  const int ntpp = __ldg(ntpp_ptr);
   const int v = __ldg(expert_ids + t);
-  if (v < 0 || v >= num_vexperts) return;
-  const int c = compact_block_rows(sorted_ids + (int64_t)t * block_m, block_m, numel, rows, wcnt);
+  const int slot = tid < block_m ? __ldg(sorted_ids + (int64_t)t * block_m + tid) : -1;
+  if ((int64_t)t * block_m >= ntpp || v < 0 || v >= num_vexperts) return;
+  const int c = compact_block_rows(slot, numel, rows, wcnt);
   if (c == 0) return;
 
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, tq = lane & 3;
+  const int lane = tid & 31, warp = tid >> 5, g = lane >> 2, tq = lane & 3;
   const int n_base = chunk * kExpandCols + warp * 32;  // column inside the slice
   if (n_base >= Ns) return;                            // warp-uniform; no block sync follows
 
@@ -163,8 +331,7 @@ lora_expand_kernel(const float* __restrict__ inter, int R, const uint16_t* __res
   // columns n_base + 8t .. n_base + 8t + 7 of each row.
   const int grp = n_base + 8 * (g >> 1);
   const bool bvalid = grp < Ns;
-  const uint16_t* bw =
-      lora_b + ((int64_t)v * S * Ns + (int64_t)s * Ns + grp + (g & 1)) * RK;
+  const uint16_t* bw = lora_b + ((int64_t)v * S * Ns + (int64_t)s * Ns + grp + (g & 1)) * RK;
   uint4 bf[KB][4];
 #pragma unroll
   for (int kb = 0; kb < KB; ++kb)
@@ -181,11 +348,24 @@ lora_expand_kernel(const float* __restrict__ inter, int R, const uint16_t* __res
   const bool ovalid = (n_base + 8 * tq) < Ns;
   const int64_t ocol = (int64_t)s * Ns + n_base + 8 * tq;
   const float4 zf = make_float4(0.f, 0.f, 0.f, 0.f);
+  const uint4 zu = make_uint4(0, 0, 0, 0);
+  // output rows of the first row tile, fetched with the weights
+  int i0 = g < c ? rows[g] : -1;
+  int i1 = 8 + g < c ? rows[8 + g] : -1;
+  uint4 o0 = (ovalid && i0 >= 0) ? *reinterpret_cast<const uint4*>(out + (int64_t)i0 * out_stride + ocol) : zu;
+  uint4 o1 = (ovalid && i1 >= 0) ? *reinterpret_cast<const uint4*>(out + (int64_t)i1 * out_stride + ocol) : zu;
+  if (EARLY) {
+    pdl_wait();  // the intermediate comes from the shrink that precedes this kernel
+    pdl_launch_dependents();
+  }
 
   for (int m0 = 0; m0 < c; m0 += 16) {
-    const int r0 = m0 + g, r1 = m0 + 8 + g;
-    const int i0 = r0 < c ? rows[r0] : -1;
-    const int i1 = r1 < c ? rows[r1] : -1;
+    if (m0 > 0) {
+      i0 = m0 + g < c ? rows[m0 + g] : -1;
+      i1 = m0 + 8 + g < c ? rows[m0 + 8 + g] : -1;
+      o0 = (ovalid && i0 >= 0) ? *reinterpret_cast<const uint4*>(out + (int64_t)i0 * out_stride + ocol) : zu;
+      o1 = (ovalid && i1 >= 0) ? *reinterpret_cast<const uint4*>(out + (int64_t)i1 * out_stride + ocol) : zu;
+    }
     float acc[4][4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) acc[u][0] = acc[u][1] = acc[u][2] = acc[u][3] = 0.f;
@@ -193,10 +373,15 @@ lora_expand_kernel(const float* __restrict__ inter, int R, const uint16_t* __res
 #pragma unroll
     for (int kb = 0; kb < KB; ++kb) {
       const int koff = s * RK + (K16 ? 4 * tq : kb * 32 + 8 * tq);
-      const float* p0 = inter + (int64_t)i0 * R + koff;
-      const float* p1 = inter + (int64_t)i1 * R + koff;
-      const float4 a0 = i0 >= 0 ? ld_keep_f4(p0) : zf;
-      const float4 a1 = i1 >= 0 ? ld_keep_f4(p1) : zf;
+      const float* p0 = inter + (int64_t)(i0 >= 0 ? i0 : 0) * R + koff;
+      const float* p1 = inter + (int64_t)(i1 >= 0 ? i1 : 0) * R + koff;
+      const float4 a0 = i0 >= 0 ? ld_l2_f4(p0) : zf;
+      const float4 a1 = i1 >= 0 ? ld_l2_f4(p1) : zf;
+      float4 b0 = zf, b1 = zf;
+      if constexpr (!K16) {
+        b0 = i0 >= 0 ? ld_l2_f4(p0 + 4) : zf;
+        b1 = i1 >= 0 ? ld_l2_f4(p1 + 4) : zf;
+      }
       uint32_t h0, l0, h1, l1, h2, l2, h3, l3;
       split_bf16x2(a0.x, a0.y, h0, l0);
       split_bf16x2(a1.x, a1.y, h1, l1);
@@ -208,8 +393,6 @@ lora_expand_kernel(const float* __restrict__ inter, int R, const uint16_t* __res
         mma_16816(acc[u], l0, l1, l2, l3, bf[kb][u].x, bf[kb][u].y);
       }
       if constexpr (!K16) {
-        const float4 b0 = i0 >= 0 ? ld_keep_f4(p0 + 4) : zf;
-        const float4 b1 = i1 >= 0 ? ld_keep_f4(p1 + 4) : zf;
         split_bf16x2(b0.x, b0.y, h0, l0);
         split_bf16x2(b1.x, b1.y, h1, l1);
         split_bf16x2(b0.z, b0.w, h2, l2);
@@ -228,8 +411,7 @@ lora_expand_kernel(const float* __restrict__ inter, int R, const uint16_t* __res
         const int i = h ? i1 : i0;
         if (i < 0) continue;
         const float sw = topk_w ? scale * __ldg(topk_w + i) : scale;
-        uint4* po = reinterpret_cast<uint4*>(out + (int64_t)i * out_stride + ocol);
-        uint4 o = *po;
+        uint4 o = h ? o1 : o0;
         uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -237,10 +419,27 @@ lora_expand_kernel(const float* __restrict__ inter, int R, const uint16_t* __res
           const float hi = fmaf(sw, acc[u][2 * h + 1], bf16_hi(ow[u]));
           ow[u] = pack_bf16x2(lo, hi);
         }
-        *po = o;
+        *reinterpret_cast<uint4*>(out + (int64_t)i * out_stride + ocol) = o;
       }
     }
   }
+}
+
+static int device_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+cudaError_t prepare_lora_kernels() {
+  return cudaFuncSetAttribute(lora_shrink_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)sp::kSmem);
 }
 
 cudaError_t launch_shrink(const void* x, int64_t x_stride, int x_div, int K, const void* lora_a,
@@ -249,32 +448,46 @@ cudaError_t launch_shrink(const void* x, int64_t x_stride, int x_div, int K, con
                           int num_vexperts, float* inter, cudaStream_t stream) {
   const int64_t nblk = capacity / block_m;
   if (numel == 0 || nblk == 0) return cudaSuccess;
-  const int n_jt = R / (8 * kShrinkNT);
-  const int64_t grid = nblk * n_jt;
-  lora_shrink_kernel<kShrinkNT, kShrinkUnroll><<<(unsigned)grid, kShrinkThreads, 0, stream>>>(
-      static_cast<const uint16_t*>(x), x_stride, x_div, K, static_cast<const uint16_t*>(lora_a),
-      R, sorted_ids, expert_ids, ntpp, block_m, numel, num_vexperts, inter, n_jt);
-  return cudaGetLastError();
+  const int n_jt = R / sp::kJT;
+  const int64_t n_items = nblk * n_jt;
+  const dim3 grid((unsigned)std::min<int64_t>(n_items, (int64_t)device_sms() * sp::kBlocksPerSM));
+  return launch_pdl(lora_shrink_kernel, grid, dim3(sp::kThreads), sp::kSmem, stream,
+                    static_cast<const uint16_t*>(x), x_stride, x_div, K,
+                    static_cast<const uint16_t*>(lora_a), R, sorted_ids, expert_ids, ntpp, block_m,
+                    numel, num_vexperts, inter, n_jt, n_items);
+}
+
+template <int RK, bool EARLY>
+static cudaError_t expand_rk(dim3 grid, cudaStream_t stream, const float* inter, int R,
+                             const uint16_t* b, int S, int Ns, float scale, const float* w,
+                             const int32_t* sorted_ids, const int32_t* expert_ids,
+                             const int32_t* ntpp, int block_m, int64_t numel, int num_vexperts,
+                             uint16_t* o, int64_t out_stride, int cps) {
+  return launch_pdl(lora_expand_kernel<RK, EARLY>, grid, dim3(kExpandThreads), 0, stream, inter, R,
+                    b, S, Ns, scale, w, sorted_ids, expert_ids, ntpp, block_m, numel, num_vexperts,
+                    o, out_stride, cps);
 }
 
 cudaError_t launch_expand(const float* inter, const void* lora_b, int S, int r, int Ns, float scale,
                           const float* topk_weights, const int32_t* sorted_ids,
                           const int32_t* expert_ids, const int32_t* ntpp, int64_t capacity,
                           int block_m, int64_t numel, int num_vexperts, void* out,
-                          int64_t out_stride, cudaStream_t stream) {
+                          int64_t out_stride, bool early, cudaStream_t stream) {
   const int64_t nblk = capacity / block_m;
   if (numel == 0 || nblk == 0) return cudaSuccess;
   const int cps = (Ns + kExpandCols - 1) / kExpandCols;
-  const int64_t grid = nblk * S * cps;
+  const dim3 grid((unsigned)(nblk * S * cps));
   const int R = S * r;
   const uint16_t* b = static_cast<const uint16_t*>(lora_b);
   uint16_t* o = static_cast<uint16_t*>(out);
-#define MOL_EXPAND_CASE(RK)                                                                  \
-  case RK:                                                                                   \
-    lora_expand_kernel<RK><<<(unsigned)grid, kExpandThreads, 0, stream>>>(                   \
-        inter, R, b, S, Ns, scale, topk_weights, sorted_ids, expert_ids, ntpp, block_m, numel, \
-        num_vexperts, o, out_stride, cps);                                                   \
-    break;
+#define MOL_EXPAND_CASE(RK)                                                                     \
+  case RK:                                                                                      \
+    return early ? expand_rk<RK, true>(grid, stream, inter, R, b, S, Ns, scale, topk_weights,   \
+                                       sorted_ids, expert_ids, ntpp, block_m, numel,            \
+                                       num_vexperts, o, out_stride, cps)                        \
+                 : expand_rk<RK, false>(grid, stream, inter, R, b, S, Ns, scale, topk_weights,  \
+                                        sorted_ids, expert_ids, ntpp, block_m, numel,           \
+                                        num_vexperts, o, out_stride, cps);
   switch (r) {
     MOL_EXPAND_CASE(16)
     MOL_EXPAND_CASE(32)
@@ -284,7 +497,6 @@ cudaError_t launch_expand(const float* inter, const void* lora_b, int S, int r, 
       return cudaErrorInvalidValue;
   }
 #undef MOL_EXPAND_CASE
-  return cudaGetLastError();
 }
 
 }  // namespace mol
