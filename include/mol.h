@@ -212,6 +212,9 @@ int32_t mol_lora_expand(const float* inter, const void* lora_b, int32_t num_slic
  * buffers as they are (the down stage reusing the gate_up routing) and
  * topk_ids / lora_ids / workspace may be NULL. Arguments are those of the
  * four calls above; numel = num_tokens * topk; V = num_experts * max_loras.
+ * Routing buffers passed with compute_routing = 0 must be complete when the
+ * call's first kernel starts (true unless the kernel just before the call
+ * lets its dependents start early, before writing them).
  */
 int32_t mol_lora_forward(const void* x, int64_t x_row_stride, int32_t x_row_div, int32_t K,
                          const int32_t* topk_ids, const int32_t* lora_ids, int64_t num_tokens,

@@ -1,6 +1,7 @@
 // Exported C ABI of the MoL LoRA library (declared in include/mol.h).
 // Host code only: validation, device checks, dispatch to the launchers.
 
+#include <algorithm>
 #include <mutex>
 
 #include "mol.h"
@@ -162,7 +163,7 @@ int32_t mol_align_block_size(const int32_t* vtopk_ids, int64_t numel, int32_t nu
   p.capacity = capacity;  // fill the caller's whole buffer
   cudaError_t e = mol::launch_align(p, false, vtopk_ids, nullptr, 1, 1, 1, nullptr, num_vexperts,
                                     sorted_token_ids, expert_ids, num_tokens_post_padded,
-                                    workspace, static_cast<cudaStream_t>(stream));
+                                    workspace, false, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MOL_OK : cuda_fail(e);
 }
 
@@ -182,7 +183,7 @@ int32_t mol_lora_shrink(const void* x, int64_t x_row_stride, int32_t x_row_div, 
   if (st != MOL_OK) return st;
   cudaError_t e = mol::launch_shrink(x, x_row_stride, x_row_div, K, lora_a, num_slices * rank,
                                      sorted_token_ids, expert_ids, num_tokens_post_padded,
-                                     capacity, block_m, numel, num_vexperts, inter,
+                                     capacity, block_m, numel, num_vexperts, inter, false,
                                      static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MOL_OK : cuda_fail(e);
 }
@@ -251,13 +252,13 @@ int32_t mol_lora_forward(const void* x, int64_t x_row_stride, int32_t x_row_div,
     mol::AlignPlan p = plan;
     p.capacity = capacity;
     e = mol::launch_align(p, true, topk_ids, lora_ids, topk, num_experts, max_loras, vtopk_ids, V,
-                          sorted_token_ids, expert_ids, num_tokens_post_padded, workspace, s);
+                          sorted_token_ids, expert_ids, num_tokens_post_padded, workspace, true, s);
     if (e != cudaSuccess) return cuda_fail(e);
   }
   if (numel == 0 || capacity == 0) return MOL_OK;
   e = mol::launch_shrink(x, x_row_stride, x_row_div, K, lora_a, num_slices * rank,
                          sorted_token_ids, expert_ids, num_tokens_post_padded, capacity, block_m,
-                         numel, V, inter, s);
+                         numel, V, inter, compute_routing == 0, s);
   if (e != cudaSuccess) return cuda_fail(e);
   e = mol::launch_expand(inter, lora_b, num_slices, rank, slice_n, scale, topk_weights,
                          sorted_token_ids, expert_ids, num_tokens_post_padded, capacity, block_m,
@@ -328,6 +329,6 @@ extern "C" int32_t mol_align_block_size_noalloc(const int32_t* vtopk_ids, int64_
   p.capacity = capacity;
   cudaError_t e = mol::launch_align(p, false, vtopk_ids, nullptr, 1, 1, 1, nullptr, num_vexperts,
                                     sorted_token_ids, expert_ids, num_tokens_post_padded, scratch,
-                                    static_cast<cudaStream_t>(stream));
+                                    false, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MOL_OK : cuda_fail(e);
 }

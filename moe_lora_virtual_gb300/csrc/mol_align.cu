@@ -124,7 +124,7 @@ align_tile_kernel(const int* __restrict__ src, const int* __restrict__ lora_ids,
                   int num_vexperts, int block_m, int64_t capacity, int tile, int tiles, int nb_pad,
                   int* __restrict__ sorted_ids, int* __restrict__ expert_ids,
                   int* __restrict__ ntpp_out, int* __restrict__ ws_hist,
-                  int* __restrict__ ws_rank) {
+                  int* __restrict__ ws_rank, int trigger) {
   extern __shared__ __align__(16) unsigned char smem[];
   __shared__ int sh_scan[kAlignWarps + 1];
   const int nb = num_vexperts + 1;
@@ -140,7 +140,13 @@ align_tile_kernel(const int* __restrict__ src, const int* __restrict__ lora_ids,
     for (int q = tid; q < n4; q += kAlignThreads) t4[q] = make_uint4(0, 0, 0, 0);
   }
   pdl_wait();  // inputs and the routing buffers belong to earlier kernels until here
-  pdl_launch_dependents();
+  // The single-block align writes the final routing. Called on its own it lets
+  // its dependents start only when it exits, so a kernel that follows it may
+  // read the routing before its own griddepcontrol.wait. Inside
+  // mol_lora_forward (trigger = 1) the next kernel waits before reading the
+  // routing, and may start early. With several tiles the scatter kernel is the
+  // last writer and plays that role.
+  if (tiles > 1 || trigger) pdl_launch_dependents();
 
   // Every slot starts as padding (value numel); real pairs overwrite theirs.
   for (int64_t q = (int64_t)blockIdx.x * kAlignThreads + tid; q < capacity;
@@ -259,9 +265,10 @@ align_scan_kernel(int* __restrict__ ws_hist, int* __restrict__ ws_offs, int tile
 __global__ void align_scatter_kernel(const int* __restrict__ vtopk, int64_t numel, int num_vexperts,
                                      int tile, const int* __restrict__ ws_hist,
                                      const int* __restrict__ ws_offs,
-                                     const int* __restrict__ ws_rank, int* __restrict__ sorted_ids) {
-  pdl_wait();
-  pdl_launch_dependents();
+                                     const int* __restrict__ ws_rank, int* __restrict__ sorted_ids,
+                                     int trigger) {
+  pdl_wait();  // last writer of the routing: dependents start when it exits unless trigger
+  if (trigger) pdl_launch_dependents();
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= numel) return;
   const int key = bucket_of(vtopk[i], num_vexperts);
@@ -339,8 +346,9 @@ cudaError_t launch_virtual_topk(const int32_t* topk_ids, const int32_t* lora_ids
 cudaError_t launch_align(const AlignPlan& plan, bool remap, const int32_t* src,
                          const int32_t* lora_ids, int topk, int num_experts, int max_loras,
                          int32_t* vtopk_out, int num_vexperts, int32_t* sorted_ids,
-                         int32_t* expert_ids, int32_t* ntpp, void* workspace,
+                         int32_t* expert_ids, int32_t* ntpp, void* workspace, bool trigger_early,
                          cudaStream_t stream) {
+  const int trig = trigger_early ? 1 : 0;
   int device = 0;
   cudaError_t e = cudaGetDevice(&device);
   if (e != cudaSuccess) return e;
@@ -359,12 +367,12 @@ cudaError_t launch_align(const AlignPlan& plan, bool remap, const int32_t* src,
     e = launch_pdl(align_tile_kernel<true>, dim3(grid), dim3(kAlignThreads), plan.smem_tile, stream,
                    src, lora_ids, topk, num_experts, max_loras, vtopk_out, plan.numel, num_vexperts,
                    plan.block_m, plan.capacity, plan.tile, plan.tiles, plan.nb_pad, sorted_ids,
-                   expert_ids, ntpp, ws_hist, ws_rank);
+                   expert_ids, ntpp, ws_hist, ws_rank, trig);
   } else {
     e = launch_pdl(align_tile_kernel<false>, dim3(grid), dim3(kAlignThreads), plan.smem_tile, stream,
                    src, static_cast<const int32_t*>(nullptr), 1, 1, 1, static_cast<int32_t*>(nullptr),
                    plan.numel, num_vexperts, plan.block_m, plan.capacity, plan.tile, plan.tiles,
-                   plan.nb_pad, sorted_ids, expert_ids, ntpp, ws_hist, ws_rank);
+                   plan.nb_pad, sorted_ids, expert_ids, ntpp, ws_hist, ws_rank, trig);
   }
   if (e != cudaSuccess || plan.tiles == 1) return e;
   e = launch_pdl(align_scan_kernel, dim3(1), dim3(kScanThreads), (size_t)plan.nb * 4, stream, ws_hist,
@@ -373,7 +381,7 @@ cudaError_t launch_align(const AlignPlan& plan, bool remap, const int32_t* src,
   const int64_t sblocks = (plan.numel + 255) / 256;
   const int32_t* vt = remap ? vtopk_out : src;
   return launch_pdl(align_scatter_kernel, dim3((unsigned)sblocks), dim3(256), 0, stream, vt,
-                    plan.numel, num_vexperts, plan.tile, ws_hist, ws_offs, ws_rank, sorted_ids);
+                    plan.numel, num_vexperts, plan.tile, ws_hist, ws_offs, ws_rank, sorted_ids, trig);
 }
 
 }  // namespace mol

@@ -17,7 +17,7 @@ struct AlignPlan {
   int tile;        // pairs per tile block
   int tiles;       // number of tile blocks (1 = single fused block)
   size_t smem_tile;
-  size_t ws_bytes;  // workspace needed (0 when tiles == 1)
+  size_t ws_bytes;  // workspace (0 when tiles == 1), 256-byte multiple
 };
 
 AlignPlan make_align_plan(int64_t numel, int num_vexperts, int block_m);
@@ -50,19 +50,31 @@ cudaError_t launch_virtual_topk(const int32_t* topk_ids, const int32_t* lora_ids
 
 // remap != 0: `src` is topk_ids and the remap is fused (vtopk written);
 // remap == 0: `src` is vtopk_ids.
+// trigger_early: let the next kernel start before the align exits (only when
+// that kernel reads the routing after griddepcontrol.wait, as in
+// mol_lora_forward); otherwise the next kernel starts once the routing is
+// complete and may read it early.
 cudaError_t launch_align(const AlignPlan& plan, bool remap, const int32_t* src,
                          const int32_t* lora_ids, int topk, int num_experts, int max_loras,
                          int32_t* vtopk_out, int num_vexperts, int32_t* sorted_ids,
-                         int32_t* expert_ids, int32_t* ntpp, void* workspace, cudaStream_t stream);
+                         int32_t* expert_ids, int32_t* ntpp, void* workspace, bool trigger_early,
+                         cudaStream_t stream);
 
+// early = true only inside mol_lora_forward reusing a routing (compute_routing
+// = 0): the routing and the weights are then read before griddepcontrol.wait,
+// the activations after it. The routing is then older than the kernel that
+// precedes the call (or was written by a standalone align, which lets its
+// dependents start only once it has exited).
 cudaError_t launch_shrink(const void* x, int64_t x_stride, int x_div, int K, const void* lora_a,
                           int R, const int32_t* sorted_ids, const int32_t* expert_ids,
                           const int32_t* ntpp, int64_t capacity, int block_m, int64_t numel,
-                          int num_vexperts, float* inter, cudaStream_t stream);
+                          int num_vexperts, float* inter, bool early, cudaStream_t stream);
 
 // early = true only when the preceding kernel is this library's shrink of the
 // same stage (mol_lora_forward): routing, weights and output rows are then read
-// before griddepcontrol.wait, the intermediate after it.
+// before griddepcontrol.wait, the intermediate after it. The shrink waits for
+// its own predecessor before it lets this kernel start, so everything older
+// than the shrink is complete.
 cudaError_t launch_expand(const float* inter, const void* lora_b, int S, int r, int Ns, float scale,
                           const float* topk_weights, const int32_t* sorted_ids,
                           const int32_t* expert_ids, const int32_t* ntpp, int64_t capacity,

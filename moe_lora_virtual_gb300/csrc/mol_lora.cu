@@ -41,46 +41,73 @@ constexpr uint32_t kWaitPolls = 1u << 22;  // bounded mbarrier waits
 // Faults recorded instead of hanging (see kFaultBulkTimeout).
 __device__ unsigned int g_fault_flags;
 
+// Routing words of one work item as loaded: a producer fetches them one item
+// ahead and evaluates them only when it reaches the item.
+struct Raw {
+  int64_t t;  // routed block, -1 past the last item
+  int ntpp, e;
+  int sl[4];  // slot ids of lanes u * 32 + lane
+};
+
 // Shrink: a persistent, warp-specialised TMA pipeline.
 //
-// Work item = (routed block t, 16 weight rows jt). Block b of the grid (two
-// per SM) walks items b, b+G, b+2G, ... . Warp 4 is the producer: it prefetches
-// the next item's routing (expert id, slot ids) one item ahead, compacts the
-// block's real rows with warp ballots, splits them into jobs of at most 16 rows
-// and streams every job through a ring of shared-memory stages, one K-chunk
-// of 512 per stage: the 16 weight rows and the job's activation rows, each a
-// 16-byte aligned run copied by cp.async.bulk and counted on the stage's
-// "full" mbarrier. Warps 0-3 are consumers: they wait for a stage, run the
-// mma over their quarter of its k range from shared memory only, release the
+// Work item = (routed block t, 8 weight rows jt). Block b of the grid (two per
+// SM) walks items b, b+G, b+2G, ... . Warp 4 is the producer: it fetches the
+// next item's routing (expert id, slot ids) one item ahead, compacts the
+// block's real rows with warp ballots, splits them into jobs of at most 16
+// rows and streams each job through a ring of two shared-memory stages. A job
+// whose 8 weight rows and activation rows fit one stage at the full width K
+// takes one stage: the weight rows, adjacent in memory, arrive in ONE bulk
+// copy and each activation row in one more. Otherwise the job is cut along k
+// into equal chunks, the widest that fit, and every row of a chunk is its own
+// copy into a row padded by 64 bytes (the 16-byte fragment reads of a quarter
+// warp then fall in distinct banks). Copies stay kilobytes long: one thread
+// issuing 1 KB copies cannot keep up with HBM, with 4 KB and more it can. Small
+// items (8 rows) keep the blocks' shares of the weight stream even.
+// Warps 0-3 consume: they wait for a stage, run the mma over their quarter of
+// its k range from shared memory only (two accumulator chains), release the
 // stage on its "empty" mbarrier and, after a job's last chunk, add their four
-// partial sums in a fixed order and store the job's fp32 rows. Rows of a stage
-// are padded by 64 bytes so the 16-byte fragment reads of a quarter warp fall
-// in distinct banks. One thread issues bulk copies back to back at a limited
-// rate, so each SM runs two such blocks to keep 1 KB row-chunk copies at the
-// HBM rate. Every wait is bounded; a timeout records a fault bit and leaves
-// the kernel instead of hanging.
+// partial sums in a fixed order and store the job's fp32 rows. Every wait is
+// bounded; a timeout records a fault bit and leaves the kernel instead of
+// hanging.
 namespace sp {
-constexpr int kConsumers = 4;                   // consumer warps
+constexpr int kConsumers = 4;                    // consumer warps
 constexpr int kThreads = (kConsumers + 1) * 32;  // + the producer warp
-constexpr int kJT = 16;                         // weight rows per item (two 8-column mma tiles)
-constexpr int kKC = 512;                        // k per stage
-constexpr int kPitch = kKC * 2 + 64;            // bytes per row in a stage
-constexpr int kStageBytes = (kJT + 16) * kPitch;  // weight rows + up to 16 activation rows
-constexpr int kStages = 3;
-constexpr int kBlocksPerSM = 2;                 // two issuing producers per SM (copy issue rate)
-constexpr int kMeta = kStages + 2;              // jobs whose rows a consumer may still read
-constexpr int kHeader = 1024;                   // barriers, stage headers, job meta
+constexpr int kJT = 8;                           // weight rows per item (one 8-column mma tile)
+constexpr int kXR = 16;                          // activation rows per job (one 16-row mma tile)
+constexpr int kStageBytes = 52 * 1024;
+constexpr int kStages = 2;
+constexpr int kBlocksPerSM = 2;                  // two issuing producers per SM
+constexpr int kMeta = kStages + 2;               // jobs whose rows a consumer may still read
+constexpr int kHeader = 1024;                    // barriers, stage headers, job meta
 constexpr size_t kSmem = kHeader + (size_t)kStages * kStageBytes;
 struct Job {
   int v, jt, cm, pad;
-  int rows[16];
+  int rows[kXR];
 };
 struct StageHdr {
-  int job;  // meta slot, -1 = end of work
-  int k0;
-  int pad0, pad1;
+  int job;    // meta slot, -1 = end of work
+  int k0;     // first k of the chunk
+  int len;    // k values in the chunk
+  int pitch;  // bytes between rows in the stage
 };
-static_assert(2 * kStages * 8 + kStages * 16 + kMeta * (int)sizeof(Job) <= kHeader, "header");
+static_assert(2 * kStages * 8 + kStages * (int)sizeof(StageHdr) + kMeta * (int)sizeof(Job) <= kHeader,
+              "header");
+
+// k chunk of a job with cm activation rows: all of K with unpadded rows when
+// that fits a stage, else equal chunks (multiples of 64) of padded rows.
+MOL_DEV void job_chunk(int K, int cm, int& len, int& pitch) {
+  const int rows = kJT + cm;
+  if (rows * K * 2 <= kStageBytes) {
+    len = K;
+    pitch = K * 2;
+    return;
+  }
+  const int lmax = (kStageBytes / rows - 64) / 2 / 64 * 64;
+  const int n = (K + lmax - 1) / lmax;
+  len = ((K + n - 1) / n + 63) / 64 * 64;
+  pitch = len * 2 + 64;
+}
 }  // namespace sp
 
 __global__ void __launch_bounds__(sp::kThreads, sp::kBlocksPerSM)
@@ -88,7 +115,7 @@ lora_shrink_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, 
                    const uint16_t* __restrict__ lora_a, int R, const int* __restrict__ sorted_ids,
                    const int* __restrict__ expert_ids, const int* __restrict__ ntpp_ptr,
                    int block_m, int64_t numel, int num_vexperts, float* __restrict__ inter,
-                   int n_jt, int64_t n_items) {
+                   int n_jt, int64_t n_items, int early) {
   using namespace sp;
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
@@ -96,7 +123,7 @@ lora_shrink_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, 
   StageHdr* hdr = reinterpret_cast<StageHdr*>(smem + 2 * kStages * 8);
   Job* meta = reinterpret_cast<Job*>(smem + 2 * kStages * 8 + kStages * sizeof(StageHdr));
   unsigned char* stages = smem + kHeader;
-  __shared__ float red[kConsumers - 1][8][32];
+  __shared__ float red[kConsumers - 1][4][32];
   __shared__ int prow[128];  // producer: compacted rows of the current block
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -108,28 +135,22 @@ lora_shrink_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, 
     fence_mbar_init();
   }
   __syncthreads();
-  pdl_wait();  // routing and activations come from earlier kernels
-  pdl_launch_dependents();
+  // The activations may come from the kernel right before this one: only the
+  // producer reads global memory, and it reads them after griddepcontrol.wait.
+  // With `early` (inside mol_lora_forward, routing reused) routing words and
+  // weight rows are older than that kernel and the producer reads them before
+  // the wait. Consumers wait before they store.
+  if (!early || warp != kConsumers) {
+    pdl_wait();
+    pdl_launch_dependents();
+  }
 
   if (warp == kConsumers) {
     // ------------------------------------------------------------ producer
-    const int ntpp = __ldg(ntpp_ptr);
     const int64_t G = gridDim.x;
-    uint32_t q = 0;  // stage uses issued
+    uint32_t q = 0;   // stage uses issued
     uint32_t jn = 0;  // jobs issued
-    auto fetch = [&](int64_t it, int& v, int (&sl)[4]) {
-      v = -1;
-#pragma unroll
-      for (int u = 0; u < 4; ++u) sl[u] = -1;
-      if (it >= n_items) return;
-      const int64_t t = it / n_jt;
-      v = (t * block_m < ntpp) ? __ldg(expert_ids + t) : -1;
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int idx = u * 32 + lane;
-        if (idx < block_m) sl[u] = __ldg(sorted_ids + t * block_m + idx);
-      }
-    };
+    bool waited = !early;
     auto acquire = [&](int& st) -> bool {  // wait until stage q is free
       st = (int)(q % kStages);
       const uint32_t ph = (q / kStages) & 1;
@@ -137,32 +158,49 @@ lora_shrink_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, 
       if (lane == 0) ok = mbar_wait(&empty[st], ph ^ 1, kWaitPolls);
       return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     };
-    int v_n, sl_n[4];
+    auto fetch = [&](int64_t it, Raw& r) {
+      r.t = it < n_items ? it / n_jt : -1;
+      r.ntpp = 0;
+      r.e = -1;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) r.sl[u] = -1;
+      if (r.t < 0) return;
+      r.ntpp = __ldg(ntpp_ptr);
+      r.e = __ldg(expert_ids + r.t);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int idx = u * 32 + lane;
+        if (idx < block_m) r.sl[u] = __ldg(sorted_ids + r.t * block_m + idx);
+      }
+    };
+    Raw nxt;
     int64_t item = blockIdx.x;
-    fetch(item, v_n, sl_n);
+    fetch(item, nxt);
     bool fault = false;
     while (item < n_items && !fault) {
-      const int v = v_n;
-      int sl[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) sl[u] = sl_n[u];
+      const Raw cur_r = nxt;
       const int64_t cur = item;
       item += G;
-      fetch(item, v_n, sl_n);  // next item's routing is in flight while this one streams
+      fetch(item, nxt);  // next item's routing is in flight while this one streams
+      const int v = (cur_r.t * block_m < cur_r.ntpp) ? cur_r.e : -1;
       if (v < 0 || v >= num_vexperts) continue;
       int c = 0;
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const bool ok = sl[u] >= 0 && (int64_t)sl[u] < numel;
+        const int slu = cur_r.sl[u];
+        const bool ok = slu >= 0 && (int64_t)slu < numel;
         const unsigned bal = __ballot_sync(0xffffffffu, ok);
-        if (ok) prow[c + __popc(bal & lanemask_lt())] = sl[u];
+        if (ok) prow[c + __popc(bal & lanemask_lt())] = slu;
         c += __popc(bal);
       }
       __syncwarp();
       const int jt = (int)(cur % n_jt);
-      const uint16_t* wsrc = lora_a + ((int64_t)v * R + jt * kJT + (lane & 15)) * K;
-      for (int m0 = 0; m0 < c && !fault; m0 += 16) {
-        const int cm = min(16, c - m0);
+      const uint16_t* wrows = lora_a + ((int64_t)v * R + jt * kJT) * K;
+      for (int m0 = 0; m0 < c && !fault; m0 += kXR) {
+        const int cm = min(kXR, c - m0);
+        int len, pitch;
+        job_chunk(K, cm, len, pitch);
+        const bool whole = (len == K && pitch == K * 2);
         const int slot = (int)(jn % kMeta);
         Job& jb = meta[slot];
         if (lane == 0) {
@@ -175,28 +213,42 @@ lora_shrink_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, 
             (lane >= 16 && lane - 16 < cm) ? x + (int64_t)(prow[m0 + lane - 16] / x_div) * x_stride
                                            : nullptr;
         __syncwarp();
-        for (int k0 = 0; k0 < K; k0 += kKC) {
+        for (int k0 = 0; k0 < K; k0 += len) {
           int st;
           if (!acquire(st)) {
             fault = true;
             break;
           }
-          const int len = min(kKC, K - k0);
+          const int cl = min(len, K - k0);
           unsigned char* base = stages + (size_t)st * kStageBytes;
           if (lane == 0) {
             hdr[st].job = slot;
             hdr[st].k0 = k0;
-            mbar_arrive_expect_tx(&full[st], (uint32_t)((kJT + cm) * len * 2));
+            hdr[st].len = cl;
+            hdr[st].pitch = pitch;
+            mbar_arrive_expect_tx(&full[st], (uint32_t)((kJT + cm) * cl * 2));
           }
           __syncwarp();
-          if (lane < 16)
-            bulk_g2s(base + lane * kPitch, wsrc + k0, len * 2, &full[st]);
-          else if (xsrc)
-            bulk_g2s(base + (kJT + lane - 16) * kPitch, xsrc + k0, len * 2, &full[st]);
+          if (whole) {
+            if (lane == 0) bulk_g2s(base, wrows, kJT * K * 2, &full[st]);
+          } else if (lane < kJT) {
+            bulk_g2s(base + lane * pitch, wrows + (int64_t)lane * K + k0, cl * 2, &full[st]);
+          }
+          if (!waited) {  // the weight copy is on its way; activations wait for the producer kernel
+            pdl_wait();
+            pdl_launch_dependents();
+            waited = true;
+          }
+          if (xsrc)
+            bulk_g2s(base + (kJT + lane - 16) * pitch, xsrc + k0, cl * 2, &full[st]);
           ++q;
         }
         ++jn;
       }
+    }
+    if (!waited) {
+      pdl_wait();
+      pdl_launch_dependents();
     }
     if (fault) {
       if (lane == 0) atomicOr(&g_fault_flags, kFaultBulkTimeout);
@@ -217,7 +269,8 @@ lora_shrink_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, 
   // -------------------------------------------------------------- consumers
   const int g = lane >> 2, tq = lane & 3;
   const uint4 zero = make_uint4(0, 0, 0, 0);
-  float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  float acc2[4] = {0.f, 0.f, 0.f, 0.f};  // odd k blocks: a second, independent mma chain
   for (uint32_t q = 0;; ++q) {
     const int st = (int)(q % kStages);
     if (!mbar_wait(&full[st], (q / kStages) & 1, kWaitPolls)) {
@@ -226,58 +279,58 @@ lora_shrink_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, 
     }
     const int slot = hdr[st].job;
     if (slot < 0) break;
-    const int k0 = hdr[st].k0;
+    const int k0 = hdr[st].k0, len = hdr[st].len, pitch = hdr[st].pitch;
     const Job& jb = meta[slot];
     const int cm = jb.cm;
-    const int len = min(kKC, K - k0);
     if (k0 == 0) {
 #pragma unroll
-      for (int n = 0; n < 2; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+      for (int e = 0; e < 4; ++e) acc[e] = acc2[e] = 0.f;
     }
     const unsigned char* W = stages + (size_t)st * kStageBytes;
-    const unsigned char* X = W + kJT * kPitch;
+    const unsigned char* X = W + kJT * pitch;
     const int nkb = (len + 31) >> 5;
     const int kb0 = warp * nkb / kConsumers, kb1 = (warp + 1) * nkb / kConsumers;
-#pragma unroll 4
-    for (int kb = kb0; kb < kb1; ++kb) {
-      const int kk = kb * 32 + 8 * tq;
-      const bool kin = kk < len;
-      const uint4 xa = (kin && g < cm) ? lds16(X + g * kPitch + kk * 2) : zero;
-      const uint4 xb = (kin && g + 8 < cm) ? lds16(X + (g + 8) * kPitch + kk * 2) : zero;
+#pragma unroll 2
+    for (int kb = kb0; kb < kb1; kb += 2) {
 #pragma unroll
-      for (int n = 0; n < 2; ++n) {
-        const uint4 a = kin ? lds16(W + (8 * n + g) * kPitch + kk * 2) : zero;
+      for (int h = 0; h < 2; ++h) {
+        const int kk = (kb + h) * 32 + 8 * tq;
+        const bool kin = kb + h < kb1 && kk < len;
+        const uint4 xa = (kin && g < cm) ? lds16(X + g * pitch + kk * 2) : zero;
+        const uint4 xb = (kin && g + 8 < cm) ? lds16(X + (g + 8) * pitch + kk * 2) : zero;
+        const uint4 a = kin ? lds16(W + g * pitch + kk * 2) : zero;
         // k step 0 <- elements 8t..8t+3, k step 1 <- 8t+4..8t+7 (same map in both operands)
-        mma_16816(acc[n], xa.x, xb.x, xa.y, xb.y, a.x, a.y);
-        mma_16816(acc[n], xa.z, xb.z, xa.w, xb.w, a.z, a.w);
+        if (h == 0) {
+          mma_16816(acc, xa.x, xb.x, xa.y, xb.y, a.x, a.y);
+          mma_16816(acc, xa.z, xb.z, xa.w, xb.w, a.z, a.w);
+        } else {
+          mma_16816(acc2, xa.x, xb.x, xa.y, xb.y, a.x, a.y);
+          mma_16816(acc2, xa.z, xb.z, xa.w, xb.w, a.z, a.w);
+        }
       }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[st]);
-    if (k0 + kKC >= K) {  // last chunk of the job: add the four partials, store
+    if (k0 + len >= K) {  // last chunk of the job: add the four partials, store
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[e] += acc2[e];
       if (warp > 0) {
 #pragma unroll
-        for (int n = 0; n < 2; ++n)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) red[warp - 1][n * 4 + e][lane] = acc[n][e];
+        for (int e = 0; e < 4; ++e) red[warp - 1][e][lane] = acc[e];
       }
       named_sync(1, kConsumers * 32);
       if (warp == 0) {
-        const int j0 = jb.jt * kJT;
 #pragma unroll
-        for (int n = 0; n < 2; ++n) {
+        for (int e = 0; e < 4; ++e)
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-#pragma unroll
-            for (int w = 0; w < kConsumers - 1; ++w) acc[n][e] += red[w][n * 4 + e][lane];
-          const int col = j0 + 8 * n + 2 * tq;
-          if (g < cm)
-            *reinterpret_cast<float2*>(inter + (int64_t)jb.rows[g] * R + col) =
-                make_float2(acc[n][0], acc[n][1]);
-          if (g + 8 < cm)
-            *reinterpret_cast<float2*>(inter + (int64_t)jb.rows[g + 8] * R + col) =
-                make_float2(acc[n][2], acc[n][3]);
-        }
+          for (int w = 0; w < kConsumers - 1; ++w) acc[e] += red[w][e][lane];
+        const int col = jb.jt * kJT + 2 * tq;
+        if (g < cm)
+          *reinterpret_cast<float2*>(inter + (int64_t)jb.rows[g] * R + col) =
+              make_float2(acc[0], acc[1]);
+        if (g + 8 < cm)
+          *reinterpret_cast<float2*>(inter + (int64_t)jb.rows[g + 8] * R + col) =
+              make_float2(acc[2], acc[3]);
       }
       named_sync(1, kConsumers * 32);
     }
@@ -445,7 +498,7 @@ cudaError_t prepare_lora_kernels() {
 cudaError_t launch_shrink(const void* x, int64_t x_stride, int x_div, int K, const void* lora_a,
                           int R, const int32_t* sorted_ids, const int32_t* expert_ids,
                           const int32_t* ntpp, int64_t capacity, int block_m, int64_t numel,
-                          int num_vexperts, float* inter, cudaStream_t stream) {
+                          int num_vexperts, float* inter, bool early, cudaStream_t stream) {
   const int64_t nblk = capacity / block_m;
   if (numel == 0 || nblk == 0) return cudaSuccess;
   const int n_jt = R / sp::kJT;
@@ -454,7 +507,7 @@ cudaError_t launch_shrink(const void* x, int64_t x_stride, int x_div, int K, con
   return launch_pdl(lora_shrink_kernel, grid, dim3(sp::kThreads), sp::kSmem, stream,
                     static_cast<const uint16_t*>(x), x_stride, x_div, K,
                     static_cast<const uint16_t*>(lora_a), R, sorted_ids, expert_ids, ntpp, block_m,
-                    numel, num_vexperts, inter, n_jt, n_items);
+                    numel, num_vexperts, inter, n_jt, n_items, early ? 1 : 0);
 }
 
 template <int RK, bool EARLY>
