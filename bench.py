@@ -420,8 +420,9 @@ def run_e2e(args, torch, mol, wl, layers, pairs_per_step, world, dev):
 
 
 # traffic (dram bytes read + written) per launch from ncu captures, keyed by
-# (workload, kernel); None until the current kernel has been captured.
-TRAFFIC = {}
+# (workload, kernel); None until the current kernel has been captured. Source:
+# profiles/decode_stage_kernels_ncu_full.md (one decode layer, 8-row shrink).
+TRAFFIC = {("decode", "shrink_gate_up"): 35506688 + 5888}
 
 
 # --------------------------------------------------------------------------- CPU (oracle)
