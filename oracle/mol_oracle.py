@@ -38,7 +38,13 @@ function that takes it):
   contracted dim; slice s of lora_b contracts with inter columns
   [s*r, (s+1)*r);
 * the shrink writes fp32 intermediates; the expand accumulates, scales, adds
-  into the bf16 output and rounds once to nearest-even.
+  into the bf16 output and rounds once to nearest-even;
+* per-adapter ranks: the weights of an adapter of rank r_l < r are zero-padded,
+  so intermediate columns [r_l, r) of each slice are 0 and the expand uses
+  only the first r_l; rank 0 returns early (no row written); an optional
+  per-adapter scaling multiplies the scalar scale;
+* per-token adapter ids come from per-request slot indices; a negative slot,
+  one past max_loras, or an adapter of rank 0 gives -1 (no delta).
 """
 
 from __future__ import annotations
@@ -197,8 +203,23 @@ def _blocks(sorted_ids, expert_ids, ntpp: int, block_m: int, numel: int):
             yield v, ids
 
 
+def _rank_of(v: int, num_experts, lora_ranks, full_rank: int) -> int:
+    """Rank of the adapter of virtual expert v, clamped to [0, full_rank].
+
+    [PR24] "fix(lora): complete the '-1 = no adapter' sentinel guards":
+    kernels index lora_ranks by adapter slot and return early on rank 0.
+    The adapter of virtual expert v is v // num_experts ([PR24171] remap:
+    v = base + lora * E).
+    """
+    if lora_ranks is None:
+        return full_rank
+    rl = int(lora_ranks[v // int(num_experts)])
+    return min(max(rl, 0), full_rank)
+
+
 def lora_shrink(x, x_row_div: int, lora_a, sorted_ids, expert_ids, ntpp: int,
-                block_m: int, numel: int, inter):
+                block_m: int, numel: int, inter, num_slices: int = 1, num_experts=None,
+                lora_ranks=None):
     """inter[i, j] = sum_k x[i // x_row_div, k] * lora_a[v, j, k] for pairs i of virtual expert v.
 
     [PR24] "Root cause" commit: the shrink stage is a fused-MoE GEMM over the
@@ -207,18 +228,30 @@ def lora_shrink(x, x_row_div: int, lora_a, sorted_ids, expert_ids, ntpp: int,
     (taken as the correction of the PR body's [E, K, N]).
     Accumulated in float64, rounded once to fp32. Rows of pairs that are in no
     processed block are left as they were.
+    With ``lora_ranks`` (per adapter, with ``num_experts``): an adapter of rank
+    0 writes nothing; of rank r_l < r writes 0 to columns [r_l, r) of every
+    slice (its weight rows there are zero padding and are not read).
     """
     inter = np.array(inter, dtype=np.float32, copy=True)
+    R = np.asarray(inter).shape[1]
+    r = R // int(num_slices)
     for v, ids in _blocks(sorted_ids, expert_ids, ntpp, block_m, numel):
+        rl = _rank_of(v, num_experts, lora_ranks, r)
+        if rl == 0:
+            continue
         X = bf16_to_f64(_rows(x, ids // x_row_div))        # [c, K]
         Av = bf16_to_f64(lora_a[v])                         # [R, K]
-        inter[ids] = (X @ Av.T).astype(np.float32)
+        res = np.zeros((ids.size, R), np.float64)
+        for s in range(int(num_slices)):
+            res[:, s * r:s * r + rl] = X @ Av[s * r:s * r + rl].T
+        inter[ids] = res.astype(np.float32)
     return inter
 
 
 def lora_expand(inter, lora_b, num_slices: int, rank: int, slice_n: int, scale: float,
                 topk_weights, sorted_ids, expert_ids, ntpp: int, block_m: int, numel: int,
-                out, return_f64: bool = False):
+                out, return_f64: bool = False, num_experts=None, lora_ranks=None,
+                lora_scalings=None):
     """out[i, s*Ns+n] = bf16(out + scale * w_i * sum_j inter[i, s*r+j] * lora_b[v, s*Ns+n, j]).
 
     [PR24] PR body "Background (measured attribution)": the expand is an
@@ -229,19 +262,29 @@ def lora_expand(inter, lora_b, num_slices: int, rank: int, slice_n: int, scale: 
     bf16. ``topk_weights`` (optional, per pair) multiplies the delta. Rows of
     pairs in no processed block are bit-unchanged ([PR24] "-1 = no adapter":
     no delta is written).
+    With ``lora_ranks``: the sum runs over j < r_l only, and rank 0 returns
+    early (rows bit-unchanged, [PR24] "complete the '-1 = no adapter'
+    sentinel guards": same meaning as the rank == 0 branch). With
+    ``lora_scalings``: the delta is further multiplied by the adapter's scaling.
     """
     out = np.array(out, dtype=np.uint16, copy=True)
     S, r, Ns = int(num_slices), int(rank), int(slice_n)
     pre = np.full(out.shape, np.nan) if return_f64 else None
     I_all = np.asarray(inter)
     for v, ids in _blocks(sorted_ids, expert_ids, ntpp, block_m, numel):
+        rl = _rank_of(v, num_experts, lora_ranks, r)
+        if rl == 0:
+            continue
+        sc = float(scale)
+        if lora_scalings is not None:
+            sc *= float(np.float32(lora_scalings[v // int(num_experts)]))
         Bv = bf16_to_f64(lora_b[v])                          # [S*Ns, r]
         w = 1.0 if topk_weights is None else np.asarray(topk_weights, np.float64)[ids][:, None]
         for s in range(S):
-            I = I_all[ids, s * r:(s + 1) * r].astype(np.float64)   # [c, r]
-            acc = I @ Bv[s * Ns:(s + 1) * Ns, :].T                 # [c, Ns]
+            I = I_all[ids, s * r:s * r + rl].astype(np.float64)    # [c, r_l]
+            acc = I @ Bv[s * Ns:(s + 1) * Ns, :rl].T               # [c, Ns]
             cols = slice(s * Ns, (s + 1) * Ns)
-            new = bf16_to_f64(out[ids, cols]) + scale * w * acc
+            new = bf16_to_f64(out[ids, cols]) + sc * w * acc
             if pre is not None:
                 pre[ids, cols] = new
             out[ids, cols] = f64_to_bf16(new)
@@ -250,7 +293,8 @@ def lora_expand(inter, lora_b, num_slices: int, rank: int, slice_n: int, scale: 
 
 def lora_forward_stage(x, x_row_div, topk_ids, lora_ids, num_experts, max_loras,
                        lora_a, lora_b, num_slices, rank, slice_n, scale, topk_weights,
-                       out, block_m, inter_fill=np.nan, routing=None):
+                       out, block_m, inter_fill=np.nan, routing=None, lora_ranks=None,
+                       lora_scalings=None):
     """One stage end to end: remap -> align -> shrink -> expand (a1..a4).
 
     ``routing`` = (vtopk, sorted_ids, expert_ids, ntpp) reuses a routing (the
@@ -267,9 +311,12 @@ def lora_forward_stage(x, x_row_div, topk_ids, lora_ids, num_experts, max_loras,
         vtopk, sorted_ids, expert_ids, ntpp = routing
     R = num_slices * rank
     inter0 = np.full((numel, R), inter_fill, dtype=np.float32)
-    inter = lora_shrink(x, x_row_div, lora_a, sorted_ids, expert_ids, ntpp, block_m, numel, inter0)
+    inter = lora_shrink(x, x_row_div, lora_a, sorted_ids, expert_ids, ntpp, block_m, numel, inter0,
+                        num_slices, num_experts, lora_ranks)
     new_out = lora_expand(inter, lora_b, num_slices, rank, slice_n, scale, topk_weights,
-                          sorted_ids, expert_ids, ntpp, block_m, numel, out)
+                          sorted_ids, expert_ids, ntpp, block_m, numel, out,
+                          num_experts=num_experts, lora_ranks=lora_ranks,
+                          lora_scalings=lora_scalings)
     return dict(vtopk=vtopk, sorted_ids=sorted_ids, expert_ids=expert_ids, ntpp=ntpp,
                 inter=inter, out=new_out)
 
@@ -279,7 +326,8 @@ def lora_forward_stage(x, x_row_div, topk_ids, lora_ids, num_experts, max_loras,
 # ---------------------------------------------------------------------------
 
 def brute_force_stage(topk_ids, lora_ids, num_experts, max_loras, x, x_row_div,
-                      lora_a, lora_b, num_slices, rank, slice_n, scale, topk_weights, out):
+                      lora_a, lora_b, num_slices, rank, slice_n, scale, topk_weights, out,
+                      lora_ranks=None, lora_scalings=None):
     """Delta of every (token, slot) pair computed straight from (expert e, adapter l).
 
     Weights of (e, l) are read from the lora-major stacks viewed as
@@ -299,12 +347,19 @@ def brute_force_stage(topk_ids, lora_ids, num_experts, max_loras, x, x_row_div,
             pair = t * k + kk
             if e < 0 or e >= num_experts or l < 0 or l >= max_loras:
                 continue
+            rl = r if lora_ranks is None else min(max(int(lora_ranks[l]), 0), r)
+            if rl == 0:  # rank 0: early return, nothing written
+                continue
+            sc = scale if lora_scalings is None else scale * float(np.float32(lora_scalings[l]))
             slot = l * num_experts + e
             xa = [float(v) for v in bf16_to_f64(x[pair // x_row_div])]
             Aw = bf16_to_f64(lora_a[slot])
             Bw = bf16_to_f64(lora_b[slot])
             h = []
             for j in range(S * r):
+                if j % r >= rl:  # beyond the adapter's rank: zero padding
+                    h.append(0.0)
+                    continue
                 row = Aw[j]
                 h.append(float(np.float32(sum(xa[q] * float(row[q]) for q in range(len(xa))))))
             inters[pair] = h
@@ -312,7 +367,41 @@ def brute_force_stage(topk_ids, lora_ids, num_experts, max_loras, x, x_row_div,
             for s in range(S):
                 for n in range(Ns):
                     col = s * Ns + n
-                    acc = sum(h[s * r + j] * float(Bw[col, j]) for j in range(r))
+                    acc = sum(h[s * r + j] * float(Bw[col, j]) for j in range(rl))
                     old = float(bf16_to_f64(out[pair, col]))
-                    out[pair, col] = f64_to_bf16(old + scale * w * acc)
+                    out[pair, col] = f64_to_bf16(old + sc * w * acc)
     return inters, out
+
+
+# ---------------------------------------------------------------------------
+# per-request adapter slots -> per-token adapter ids (the step before a1)
+# ---------------------------------------------------------------------------
+
+def token_lora_ids(weight_indices, seg_indptr, num_tokens: int, max_loras: int,
+                   lora_ranks=None) -> np.ndarray:
+    """lora_ids[t] = the adapter slot of the request that token t belongs to, or -1.
+
+    [PR24] "feat(lora): base takes no pool slot": a request without an
+    adapter has weight index -1 ("no adapter"); "fix(lora): complete the
+    '-1 = no adapter' sentinel guards": every consumer checks for a negative
+    index BEFORE it indexes lora_ranks, with the meaning of the existing
+    rank == 0 branch (no delta), and the CPU path of _compute_moe_lora_info
+    filters negative indices before its scatter. Request q owns tokens
+    [seg_indptr[q], seg_indptr[q+1]). Reading: a slot outside [0, max_loras),
+    or of rank 0 when lora_ranks is given, gives -1; tokens outside every
+    request's segment get -1.
+    """
+    wi = np.asarray(weight_indices, dtype=np.int64)
+    seg = np.asarray(seg_indptr, dtype=np.int64)
+    out = np.full(int(num_tokens), -1, dtype=np.int32)
+    for q in range(wi.size):
+        w = int(wi[q])
+        if w < 0 or w >= max_loras:
+            continue
+        if lora_ranks is not None and int(lora_ranks[w]) <= 0:
+            continue
+        lo, hi = max(int(seg[q]), 0), min(int(seg[q + 1]), int(num_tokens))
+        if hi > lo:
+            out[lo:hi] = w
+    return out
+
