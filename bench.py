@@ -49,6 +49,8 @@ def parse_args(argv=None):
     p.add_argument("--config", default="decode")
     p.add_argument("--layers", type=int, default=8, help="distinct layers rotated across steps")
     p.add_argument("--seed", type=int, default=0)
+    p.add_argument("--ranks", default=None,
+                   help="per-adapter ranks, comma separated (one per adapter; scaling 16/rank)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--no-kernels", action="store_true", help="skip the per-kernel timing phase")
@@ -147,8 +149,14 @@ def shard_tokens(num_tokens: int, world: int, rank: int):
 class LayerState:
     """Device tensors of one layer: routing, workspace, per-stage inputs and outputs."""
 
-    def __init__(self, wl, li, dev, mol, torch):
+    def __init__(self, wl, li, dev, mol, torch, ranks=None):
         self.wl, self.li = wl, li
+        self.ranks = None if ranks is None else np.asarray(ranks, np.int32)
+        self.ranks_d = self.scal_d = None
+        if ranks is not None:
+            self.ranks_d = torch.from_numpy(self.ranks).to(dev)
+            scal = np.array([16.0 / r if r > 0 else 0.0 for r in self.ranks], np.float32)
+            self.scal_d = torch.from_numpy(scal).to(dev)
         self.topk = torch.from_numpy(li.topk_ids).to(dev)
         self.lora = torch.from_numpy(li.lora_ids).to(dev)
         self.routing = mol.alloc_routing(wl.numel, wl.V, wl.BM, dev)
@@ -165,22 +173,29 @@ class LayerState:
         for si, d in enumerate(self.stages):
             mol.mol_lora_forward(d["x"], d["st"].x_row_div, self.topk, self.lora, wl.E, wl.L,
                                  d["A"], d["B"], d["st"].stage.S, wl.scale, d["out"], self.routing,
-                                 d["inter"], compute_routing=(si == 0), workspace=self.ws)
+                                 d["inter"], compute_routing=(si == 0), workspace=self.ws,
+                                 lora_ranks=self.ranks_d, lora_scalings=self.scal_d)
 
     def counts(self):
-        """Valid pairs, touched virtual experts and distinct token rows, from the routing output."""
+        """Pairs that get a delta, their touched virtual experts' adapters and distinct token
+        rows, from the routing output (pairs of rank-0 adapters get none)."""
         vt = self.routing.vtopk_ids.cpu().numpy().reshape(-1)
         valid = vt >= 0
+        if self.ranks is not None:
+            valid &= self.ranks[np.maximum(vt, 0) // self.wl.E] > 0
         touched = np.unique(vt[valid])
         rows = np.unique(np.nonzero(valid)[0] // self.wl.topk)
-        return int(valid.sum()), int(touched.size), int(rows.size)
+        return int(valid.sum()), int(touched.size), int(rows.size), touched // self.wl.E
 
-    def stage_bytes(self, si, pairs, touched, token_rows):
-        """Algorithmic HBM bytes of one stage's shrink and expand."""
+    def stage_bytes(self, si, pairs, touched, token_rows, adapters):
+        """Algorithmic HBM bytes of one stage's shrink and expand (an adapter of rank r_l needs
+        r_l of the r rows of each slice of lora_a and r_l of the r columns of lora_b)."""
         st = self.stages[si]["st"].stage
         x_rows = token_rows if self.stages[si]["st"].x_row_div > 1 else pairs
-        shrink = touched * st.R * st.K * 2 + x_rows * st.K * 2 + pairs * st.R * 4
-        expand = touched * st.N * st.r * 2 + pairs * st.R * 4 + pairs * st.N * 2 * 2
+        rank_sum = touched * st.r if self.ranks is None else \
+            int(np.minimum(self.ranks[adapters], st.r).sum())
+        shrink = st.S * rank_sum * st.K * 2 + x_rows * st.K * 2 + pairs * st.R * 4
+        expand = st.N * rank_sum * 2 + pairs * st.R * 4 + pairs * st.N * 2 * 2
         return shrink, expand
 
     def align_bytes(self):
@@ -240,8 +255,13 @@ def run_gpu(args):
     mol.library()
 
     wl = WORKLOADS[args.config]
-    layers = [LayerState(wl, make_layer(wl, args.seed + 1000 * rank, layer=i), dev, mol, torch)
-              for i in range(args.layers)]
+    ranks = None
+    if args.ranks:
+        ranks = [int(v) for v in args.ranks.split(",")]
+        if len(ranks) != wl.L:
+            raise SystemExit(f"--ranks: expected {wl.L} values (one per adapter)")
+    layers = [LayerState(wl, make_layer(wl, args.seed + 1000 * rank, layer=i), dev, mol, torch,
+                         ranks) for i in range(args.layers)]
     for L_ in layers:
         L_.forward(mol)
     torch.cuda.synchronize()
@@ -305,9 +325,11 @@ def run_gpu(args):
             st = d["st"]
             if which == "shrink":
                 return lambda: mol.mol_lora_shrink(d["x"], st.x_row_div, d["A"], st.stage.S,
-                                                   L_.routing, d["inter"])
+                                                   L_.routing, d["inter"], lora_ranks=L_.ranks_d,
+                                                   num_experts=wl.E)
             return lambda: mol.mol_lora_expand(d["inter"], d["B"], st.stage.S, wl.scale,
-                                               L_.routing, d["out"])
+                                               L_.routing, d["out"], lora_ranks=L_.ranks_d,
+                                               lora_scalings=L_.scal_d, num_experts=wl.E)
 
         def align_call(L_):
             return lambda: mol.mol_align_block_size(L_.routing.vtopk_ids, wl.V, wl.BM,
@@ -321,6 +343,15 @@ def run_gpu(args):
             return time_graphs(torch, [g], n, 3) * 1e3 / (reps * len(calls))
 
         kern["align"] = per_launch_us([align_call(L_) for L_ in layers])
+        # per-token adapter ids of the batch: one request per token (decode) or
+        # requests of 64 tokens, adapter slots of the layer's tokens
+        req_len = 1 if wl.T <= 256 else 64
+        nreq = (wl.T + req_len - 1) // req_len
+        wi = torch.from_numpy(layers[0].li.lora_ids[::req_len].astype(np.int32)).to(dev)
+        seg = torch.from_numpy(np.minimum(np.arange(nreq + 1) * req_len, wl.T).astype(np.int32)).to(dev)
+        tok_ids = torch.empty(wl.T, dtype=torch.int32, device=dev)
+        kern["token_lora_ids"] = per_launch_us(
+            [lambda: mol.mol_token_lora_ids(wi, seg, wl.T, wl.L, layers[0].ranks_d, tok_ids)])
         for si, st in enumerate(wl.stages):
             for which in ("shrink", "expand"):
                 kern[f"{which}_{st.name}"] = per_launch_us([stage_call(L_, si, which) for L_ in layers])
@@ -356,6 +387,7 @@ def run_gpu(args):
                            max_loras=wl.L, num_vexperts=wl.V, block_m=wl.BM,
                            stages=[f"{s.name} K={s.K} R={s.R} N={s.N}" for s in wl.stages],
                            pairs_per_layer=pairs_per_step, layers_rotated=args.layers,
+                           adapter_ranks=ranks,
                            l2="inputs larger than L2: steps rotate over distinct layers",
                            graph=f"{args.layers} layers per graph replay (remainder: one layer per replay)",
                            parallelism=f"replicas{world}"),

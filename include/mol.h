@@ -171,13 +171,25 @@ int32_t mol_align_block_size_noalloc(const int32_t* vtopk_ids, int64_t numel,
  * Contract: K % 8 == 0, K <= 65536, R % 16 == 0, R <= 1024, x_row_stride % 8 == 0,
  * x, lora_a, inter 16-byte aligned, capacity % block_m == 0. x must hold
  * ceil(numel / x_row_div) rows.
+ * Per-adapter ranks (fork PR #24 "fix(lora): complete the '-1 = no adapter'
+ * sentinel guards": kernels index lora_ranks per adapter slot and return
+ * early on rank 0):
+ *   lora_ranks   int32 [num_vexperts / num_experts] or NULL (all adapters of
+ *                rank `rank`). The adapter of virtual expert v is
+ *                v / num_experts. With rank r_l (clamped to [0, rank]) the
+ *                adapter's weights are zero padding past r_l: inter columns
+ *                [s*rank + r_l, (s+1)*rank) of each slice are written as 0 and
+ *                those lora_a rows are not read; r_l = 0 writes nothing.
+ *                Needs rank % 8 == 0 and num_vexperts / num_experts <= 2048;
+ *                read like lora_a (not produced by the kernel right before).
+ *   num_experts  routed experts (used only with lora_ranks).
  */
 int32_t mol_lora_shrink(const void* x, int64_t x_row_stride, int32_t x_row_div, int32_t K,
                         const void* lora_a, int32_t num_slices, int32_t rank,
                         const int32_t* sorted_token_ids, const int32_t* expert_ids,
                         const int32_t* num_tokens_post_padded, int64_t capacity,
                         int32_t block_m, int64_t numel, int32_t num_vexperts, float* inter,
-                        void* stream);
+                        int32_t num_experts, const int32_t* lora_ranks, void* stream);
 
 /*
  * Step 4: LoRA expand per block, added into the MoE output (fork PR #24 PR
@@ -196,13 +208,23 @@ int32_t mol_lora_shrink(const void* x, int64_t x_row_stride, int32_t x_row_div, 
  *   out          bf16, row i at out + i * out_row_stride (elements), updated in place
  * Contract: rank in {16, 32, 64, 128}, slice_n % 8 == 0, out_row_stride % 8 == 0,
  * out_row_stride >= num_slices * slice_n, inter/lora_b/out 16-byte aligned.
+ * Per-adapter rank and scaling (adapter of v = v / num_experts):
+ *   lora_ranks     int32 [num_vexperts / num_experts] or NULL: the sum runs over
+ *                  j < r_l (clamped to [0, rank]); r_l = 0 leaves the pair's
+ *                  output rows bit-unchanged. Needs rank % 8 == 0 and at most
+ *                  2048 adapters.
+ *   lora_scalings  fp32 [num_vexperts / num_experts] or NULL: the delta is
+ *                  multiplied by scale * lora_scalings[adapter].
+ *   num_experts    routed experts (used only with either array).
+ * Both arrays are read like lora_b.
  */
 int32_t mol_lora_expand(const float* inter, const void* lora_b, int32_t num_slices, int32_t rank,
                         int32_t slice_n, float scale, const float* topk_weights,
                         const int32_t* sorted_token_ids, const int32_t* expert_ids,
                         const int32_t* num_tokens_post_padded, int64_t capacity, int32_t block_m,
                         int64_t numel, int32_t num_vexperts, void* out, int64_t out_row_stride,
-                        void* stream);
+                        int32_t num_experts, const int32_t* lora_ranks,
+                        const float* lora_scalings, void* stream);
 
 /*
  * One MoL LoRA stage end to end (fork PR #24 PR body "Background": per layer
@@ -214,7 +236,9 @@ int32_t mol_lora_expand(const float* inter, const void* lora_b, int32_t num_slic
  * four calls above; numel = num_tokens * topk; V = num_experts * max_loras.
  * Routing buffers passed with compute_routing = 0 must be complete when the
  * call's first kernel starts (true unless the kernel just before the call
- * lets its dependents start early, before writing them).
+ * lets its dependents start early, before writing them). lora_ranks and
+ * lora_scalings (each NULL or one entry per adapter) are those of the shrink
+ * and the expand.
  */
 int32_t mol_lora_forward(const void* x, int64_t x_row_stride, int32_t x_row_div, int32_t K,
                          const int32_t* topk_ids, const int32_t* lora_ids, int64_t num_tokens,
@@ -225,7 +249,31 @@ int32_t mol_lora_forward(const void* x, int64_t x_row_stride, int32_t x_row_div,
                          int32_t block_m, int32_t compute_routing, int32_t* vtopk_ids,
                          int32_t* sorted_token_ids, int64_t capacity, int32_t* expert_ids,
                          int32_t* num_tokens_post_padded, float* inter,
+                         const int32_t* lora_ranks, const float* lora_scalings,
                          void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * The step before step 1: per-token adapter ids from per-request adapter
+ * slots (fork PR #24, "feat(lora): base takes no pool slot": a request
+ * without an adapter has weight index -1; "fix(lora): complete the '-1 = no
+ * adapter' sentinel guards": consumers check for a negative index before
+ * indexing lora_ranks, with the meaning of the rank == 0 branch, and the
+ * per-token mapping of _compute_moe_lora_info filters negatives first).
+ *   lora_ids[t] = w = weight_indices[q]  for t in [seg_indptr[q], seg_indptr[q+1]),
+ *                                        if 0 <= w < max_loras and (lora_ranks
+ *                                        is NULL or lora_ranks[w] > 0)
+ *               = -1                     otherwise, and for tokens in no segment.
+ *   weight_indices int32 [num_reqs]; seg_indptr int32 [num_reqs + 1],
+ *   non-decreasing (token offsets of the requests); lora_ranks int32
+ *   [max_loras] or NULL; lora_ids int32 [num_tokens] (written in full).
+ * lora_ranks is indexed only after the range check, so -1 never reads it.
+ * Contract: num_tokens <= MOL_MAX_NUMEL. With a decreasing seg_indptr every
+ * token still gets some value in {-1} U [0, max_loras) and nothing is read out
+ * of bounds.
+ */
+int32_t mol_token_lora_ids(const int32_t* weight_indices, const int32_t* seg_indptr,
+                           int32_t num_reqs, int64_t num_tokens, int32_t max_loras,
+                           const int32_t* lora_ranks, int32_t* lora_ids, void* stream);
 
 #ifdef __cplusplus
 }

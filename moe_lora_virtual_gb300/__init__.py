@@ -28,7 +28,7 @@ MOL_MAX_NUMEL = 1 << 22
 EXPORTS = (
     "mol_version", "mol_status_string", "mol_last_cuda_error", "mol_align_capacity",
     "mol_workspace_bytes", "mol_virtual_topk", "mol_align_block_size", "mol_lora_shrink",
-    "mol_lora_expand", "mol_lora_forward", "mol_align_block_size_noalloc",
+    "mol_lora_expand", "mol_lora_forward", "mol_align_block_size_noalloc", "mol_token_lora_ids",
 )
 
 _lib = None
@@ -48,12 +48,13 @@ _SIGS = {
     "mol_align_block_size": (_I32, [_P, _I64, _I32, _I32, _P, _I64, _P, _P, _P, _SZ, _P]),
     "mol_align_block_size_noalloc": (_I32, [_P, _I64, _I32, _I32, _P, _I64, _P, _P, _P]),
     "mol_lora_shrink": (_I32, [_P, _I64, _I32, _I32, _P, _I32, _I32, _P, _P, _P, _I64, _I32, _I64,
-                               _I32, _P, _P]),
+                               _I32, _P, _I32, _P, _P]),
     "mol_lora_expand": (_I32, [_P, _P, _I32, _I32, _I32, _F32, _P, _P, _P, _P, _I64, _I32, _I64,
-                               _I32, _P, _I64, _P]),
+                               _I32, _P, _I64, _I32, _P, _P, _P]),
     "mol_lora_forward": (_I32, [_P, _I64, _I32, _I32, _P, _P, _I64, _I32, _I32, _I32, _P, _P, _I32,
                                 _I32, _I32, _F32, _P, _P, _I64, _I32, _I32, _P, _P, _I64, _P, _P,
-                                _P, _P, _SZ, _P]),
+                                _P, _P, _P, _P, _SZ, _P]),
+    "mol_token_lora_ids": (_I32, [_P, _P, _I32, _I64, _I32, _P, _P, _P]),
 }
 
 
@@ -197,9 +198,18 @@ def mol_align_block_size_noalloc(vtopk_ids: torch.Tensor, num_vexperts: int, blo
     return routing
 
 
+def _adapter_arrays(lora_ranks, lora_scalings):
+    if lora_ranks is not None:
+        _need(lora_ranks, torch.int32, "lora_ranks")
+    if lora_scalings is not None:
+        _need(lora_scalings, torch.float32, "lora_scalings")
+
+
 def mol_lora_shrink(x: torch.Tensor, x_row_div: int, lora_a: torch.Tensor, num_slices: int,
-                    routing: Routing, inter: Optional[torch.Tensor] = None, stream=None):
+                    routing: Routing, inter: Optional[torch.Tensor] = None, stream=None,
+                    lora_ranks: Optional[torch.Tensor] = None, num_experts: int = 0):
     _need(x, torch.bfloat16, "x")
+    _adapter_arrays(lora_ranks, None)
     _need(lora_a, torch.bfloat16, "lora_a")
     V, R, K = lora_a.shape
     if inter is None:
@@ -209,14 +219,17 @@ def mol_lora_shrink(x: torch.Tensor, x_row_div: int, lora_a: torch.Tensor, num_s
         _ptr(x), _row_stride(x, "x"), x_row_div, K, _ptr(lora_a), num_slices, R // num_slices,
         _ptr(routing.sorted_token_ids), _ptr(routing.expert_ids),
         _ptr(routing.num_tokens_post_padded), routing.capacity, routing.block_m, routing.numel,
-        routing.num_vexperts, _ptr(inter), _stream(stream)))
+        routing.num_vexperts, _ptr(inter), num_experts, _ptr(lora_ranks), _stream(stream)))
     return inter
 
 
 def mol_lora_expand(inter: torch.Tensor, lora_b: torch.Tensor, num_slices: int, scale: float,
                     routing: Routing, out: torch.Tensor,
-                    topk_weights: Optional[torch.Tensor] = None, stream=None):
+                    topk_weights: Optional[torch.Tensor] = None, stream=None,
+                    lora_ranks: Optional[torch.Tensor] = None,
+                    lora_scalings: Optional[torch.Tensor] = None, num_experts: int = 0):
     _need(inter, torch.float32, "inter")
+    _adapter_arrays(lora_ranks, lora_scalings)
     _need(lora_b, torch.bfloat16, "lora_b")
     _need(out, torch.bfloat16, "out")
     if topk_weights is not None:
@@ -226,7 +239,8 @@ def mol_lora_expand(inter: torch.Tensor, lora_b: torch.Tensor, num_slices: int, 
         _ptr(inter), _ptr(lora_b), num_slices, r, N // num_slices, float(scale), _ptr(topk_weights),
         _ptr(routing.sorted_token_ids), _ptr(routing.expert_ids),
         _ptr(routing.num_tokens_post_padded), routing.capacity, routing.block_m, routing.numel,
-        routing.num_vexperts, _ptr(out), _row_stride(out, "out"), _stream(stream)))
+        routing.num_vexperts, _ptr(out), _row_stride(out, "out"), num_experts, _ptr(lora_ranks),
+        _ptr(lora_scalings), _stream(stream)))
     return out
 
 
@@ -236,9 +250,12 @@ def mol_lora_forward(x: torch.Tensor, x_row_div: int, topk_ids: Optional[torch.T
                      out: torch.Tensor, routing: Routing, inter: torch.Tensor,
                      compute_routing: bool = True, topk_weights: Optional[torch.Tensor] = None,
                      workspace: Optional[torch.Tensor] = None, num_tokens: Optional[int] = None,
-                     topk: Optional[int] = None, stream=None) -> None:
+                     topk: Optional[int] = None, stream=None,
+                     lora_ranks: Optional[torch.Tensor] = None,
+                     lora_scalings: Optional[torch.Tensor] = None) -> None:
     """One MoL LoRA stage; with compute_routing the routing buffers are (re)computed."""
     _need(x, torch.bfloat16, "x")
+    _adapter_arrays(lora_ranks, lora_scalings)
     if topk_ids is not None:
         _need(topk_ids, torch.int32, "topk_ids")
         num_tokens, topk = topk_ids.shape
@@ -253,4 +270,25 @@ def mol_lora_forward(x: torch.Tensor, x_row_div: int, topk_ids: Optional[torch.T
         N // num_slices, float(scale), _ptr(topk_weights), _ptr(out), _row_stride(out, "out"),
         routing.block_m, int(bool(compute_routing)), _ptr(routing.vtopk_ids),
         _ptr(routing.sorted_token_ids), routing.capacity, _ptr(routing.expert_ids),
-        _ptr(routing.num_tokens_post_padded), _ptr(inter), _ptr(workspace), wsb, _stream(stream)))
+        _ptr(routing.num_tokens_post_padded), _ptr(inter), _ptr(lora_ranks), _ptr(lora_scalings),
+        _ptr(workspace), wsb, _stream(stream)))
+
+
+def mol_token_lora_ids(weight_indices: torch.Tensor, seg_indptr: torch.Tensor, num_tokens: int,
+                       max_loras: int, lora_ranks: Optional[torch.Tensor] = None,
+                       lora_ids: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Per-token adapter ids from per-request slots (-1 = no adapter)."""
+    _need(weight_indices, torch.int32, "weight_indices")
+    _need(seg_indptr, torch.int32, "seg_indptr")
+    _adapter_arrays(lora_ranks, None)
+    num_reqs = weight_indices.numel()
+    if seg_indptr.numel() != num_reqs + 1:
+        raise ValueError("seg_indptr: expected num_reqs + 1 entries")
+    if lora_ids is None:
+        lora_ids = torch.empty(num_tokens, dtype=torch.int32, device=weight_indices.device)
+    _need(lora_ids, torch.int32, "lora_ids")
+    _check("mol_token_lora_ids", library().mol_token_lora_ids(
+        _ptr(weight_indices), _ptr(seg_indptr), num_reqs, num_tokens, max_loras, _ptr(lora_ranks),
+        _ptr(lora_ids), _stream(stream)))
+    return lora_ids
+

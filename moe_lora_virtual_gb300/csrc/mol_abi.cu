@@ -92,6 +92,17 @@ int32_t check_expand_args(const float* inter, const void* lora_b, int32_t num_sl
   return MOL_OK;
 }
 
+// Per-adapter ranks / scalings (either may be NULL): the adapter of virtual
+// expert v is v / num_experts; the shrink keeps the ranks in shared memory.
+int32_t check_adapter_args(const int32_t* lora_ranks, const float* lora_scalings,
+                           int32_t num_experts, int32_t num_vexperts, int32_t rank) {
+  if (!lora_ranks && !lora_scalings) return MOL_OK;
+  if (num_experts < 1 || num_vexperts % num_experts != 0) return MOL_ERR_INVALID_ARG;
+  if (lora_ranks && (num_vexperts / num_experts > mol::kMaxLoraTable || rank % 8 != 0))
+    return MOL_ERR_UNSUPPORTED;
+  return MOL_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -144,6 +155,21 @@ int32_t mol_virtual_topk(const int32_t* topk_ids, const int32_t* lora_ids, int64
   return e == cudaSuccess ? MOL_OK : cuda_fail(e);
 }
 
+int32_t mol_token_lora_ids(const int32_t* weight_indices, const int32_t* seg_indptr,
+                           int32_t num_reqs, int64_t num_tokens, int32_t max_loras,
+                           const int32_t* lora_ranks, int32_t* lora_ids, void* stream) {
+  if (num_reqs < 0 || num_tokens < 0 || max_loras < 1) return MOL_ERR_INVALID_ARG;
+  if (num_tokens > MOL_MAX_NUMEL) return MOL_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return MOL_OK;
+  if (!lora_ids || (num_reqs > 0 && (!weight_indices || !seg_indptr))) return MOL_ERR_INVALID_ARG;
+  int32_t st = ensure_device();
+  if (st != MOL_OK) return st;
+  cudaError_t e = mol::launch_token_lora_ids(weight_indices, seg_indptr, num_reqs, num_tokens,
+                                             max_loras, lora_ranks, lora_ids,
+                                             static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOL_OK : cuda_fail(e);
+}
+
 int32_t mol_align_block_size(const int32_t* vtopk_ids, int64_t numel, int32_t num_vexperts,
                              int32_t block_m, int32_t* sorted_token_ids, int64_t capacity,
                              int32_t* expert_ids, int32_t* num_tokens_post_padded,
@@ -172,11 +198,13 @@ int32_t mol_lora_shrink(const void* x, int64_t x_row_stride, int32_t x_row_div, 
                         const int32_t* sorted_token_ids, const int32_t* expert_ids,
                         const int32_t* num_tokens_post_padded, int64_t capacity,
                         int32_t block_m, int64_t numel, int32_t num_vexperts, float* inter,
-                        void* stream) {
+                        int32_t num_experts, const int32_t* lora_ranks, void* stream) {
   int32_t st = check_routing_in(sorted_token_ids, expert_ids, num_tokens_post_padded, capacity,
                                 block_m, numel, num_vexperts);
   if (st != MOL_OK) return st;
   st = check_shrink_args(x, x_row_stride, x_row_div, K, lora_a, num_slices, rank, inter, numel);
+  if (st != MOL_OK) return st;
+  st = check_adapter_args(lora_ranks, nullptr, num_experts, num_vexperts, rank);
   if (st != MOL_OK) return st;
   if (numel == 0 || capacity == 0) return MOL_OK;
   st = ensure_device();
@@ -184,7 +212,8 @@ int32_t mol_lora_shrink(const void* x, int64_t x_row_stride, int32_t x_row_div, 
   cudaError_t e = mol::launch_shrink(x, x_row_stride, x_row_div, K, lora_a, num_slices * rank,
                                      sorted_token_ids, expert_ids, num_tokens_post_padded,
                                      capacity, block_m, numel, num_vexperts, inter, false,
-                                     static_cast<cudaStream_t>(stream));
+                                     static_cast<cudaStream_t>(stream), rank, lora_ranks,
+                                     num_experts);
   return e == cudaSuccess ? MOL_OK : cuda_fail(e);
 }
 
@@ -193,11 +222,14 @@ int32_t mol_lora_expand(const float* inter, const void* lora_b, int32_t num_slic
                         const int32_t* sorted_token_ids, const int32_t* expert_ids,
                         const int32_t* num_tokens_post_padded, int64_t capacity, int32_t block_m,
                         int64_t numel, int32_t num_vexperts, void* out, int64_t out_row_stride,
-                        void* stream) {
+                        int32_t num_experts, const int32_t* lora_ranks,
+                        const float* lora_scalings, void* stream) {
   int32_t st = check_routing_in(sorted_token_ids, expert_ids, num_tokens_post_padded, capacity,
                                 block_m, numel, num_vexperts);
   if (st != MOL_OK) return st;
   st = check_expand_args(inter, lora_b, num_slices, rank, slice_n, out, out_row_stride, numel);
+  if (st != MOL_OK) return st;
+  st = check_adapter_args(lora_ranks, lora_scalings, num_experts, num_vexperts, rank);
   if (st != MOL_OK) return st;
   if (numel == 0 || capacity == 0) return MOL_OK;
   st = ensure_device();
@@ -205,7 +237,8 @@ int32_t mol_lora_expand(const float* inter, const void* lora_b, int32_t num_slic
   cudaError_t e = mol::launch_expand(inter, lora_b, num_slices, rank, slice_n, scale, topk_weights,
                                      sorted_token_ids, expert_ids, num_tokens_post_padded,
                                      capacity, block_m, numel, num_vexperts, out, out_row_stride,
-                                     false, static_cast<cudaStream_t>(stream));
+                                     false, static_cast<cudaStream_t>(stream), lora_ranks,
+                                     lora_scalings, num_experts);
   return e == cudaSuccess ? MOL_OK : cuda_fail(e);
 }
 
@@ -218,6 +251,7 @@ int32_t mol_lora_forward(const void* x, int64_t x_row_stride, int32_t x_row_div,
                          int32_t block_m, int32_t compute_routing, int32_t* vtopk_ids,
                          int32_t* sorted_token_ids, int64_t capacity, int32_t* expert_ids,
                          int32_t* num_tokens_post_padded, float* inter,
+                         const int32_t* lora_ranks, const float* lora_scalings,
                          void* workspace, size_t workspace_bytes, void* stream) {
   if (num_tokens < 0 || topk < 1 || num_experts < 1 || max_loras < 1) return MOL_ERR_INVALID_ARG;
   if (compute_routing != 0 && compute_routing != 1) return MOL_ERR_INVALID_ARG;
@@ -233,6 +267,8 @@ int32_t mol_lora_forward(const void* x, int64_t x_row_stride, int32_t x_row_div,
   st = check_shrink_args(x, x_row_stride, x_row_div, K, lora_a, num_slices, rank, inter, numel);
   if (st != MOL_OK) return st;
   st = check_expand_args(inter, lora_b, num_slices, rank, slice_n, out, out_row_stride, numel);
+  if (st != MOL_OK) return st;
+  st = check_adapter_args(lora_ranks, lora_scalings, num_experts, V, rank);
   if (st != MOL_OK) return st;
   const mol::AlignPlan plan = mol::make_align_plan(numel, V, block_m);
   if (compute_routing) {
@@ -258,11 +294,12 @@ int32_t mol_lora_forward(const void* x, int64_t x_row_stride, int32_t x_row_div,
   if (numel == 0 || capacity == 0) return MOL_OK;
   e = mol::launch_shrink(x, x_row_stride, x_row_div, K, lora_a, num_slices * rank,
                          sorted_token_ids, expert_ids, num_tokens_post_padded, capacity, block_m,
-                         numel, V, inter, compute_routing == 0, s);
+                         numel, V, inter, compute_routing == 0, s, rank, lora_ranks, num_experts);
   if (e != cudaSuccess) return cuda_fail(e);
   e = mol::launch_expand(inter, lora_b, num_slices, rank, slice_n, scale, topk_weights,
                          sorted_token_ids, expert_ids, num_tokens_post_padded, capacity, block_m,
-                         numel, V, out, out_row_stride, true, s);
+                         numel, V, out, out_row_stride, true, s, lora_ranks, lora_scalings,
+                         num_experts);
   return e == cudaSuccess ? MOL_OK : cuda_fail(e);
 }
 

@@ -59,6 +59,38 @@ __global__ void virtual_topk_kernel(const int* __restrict__ topk_ids, const int*
   }
 }
 
+// Per-token adapter ids (fork PR #24, "feat(lora): base takes no pool slot"
+// and "fix(lora): complete the '-1 = no adapter' sentinel guards"): token t
+// takes the slot of the request whose segment [seg[q], seg[q+1]) holds it,
+// found by binary search; a negative slot, one >= max_loras, or (checked only
+// after those two) an adapter of rank 0 gives -1, as does a token outside
+// every segment.
+__global__ void token_lora_ids_kernel(const int* __restrict__ weight_indices,
+                                      const int* __restrict__ seg_indptr, int num_reqs,
+                                      int64_t num_tokens, int max_loras,
+                                      const int* __restrict__ lora_ranks, int* __restrict__ out) {
+  pdl_wait();
+  pdl_launch_dependents();
+  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < num_tokens;
+       t += (int64_t)gridDim.x * blockDim.x) {
+    int lo = 0, hi = num_reqs;  // first q with seg[q] > t
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if ((int64_t)__ldg(seg_indptr + mid) <= t)
+        lo = mid + 1;
+      else
+        hi = mid;
+    }
+    const int q = lo - 1;
+    int id = -1;
+    if (q >= 0 && t < (int64_t)__ldg(seg_indptr + q + 1)) {
+      const int w = __ldg(weight_indices + q);
+      if (w >= 0 && w < max_loras && (!lora_ranks || __ldg(lora_ranks + w) > 0)) id = w;
+    }
+    out[t] = id;
+  }
+}
+
 // Exclusive scan of one int per thread over the block; `total` = sum of all.
 template <int THREADS>
 MOL_DEV int block_exclusive_scan(int v, int* sh, int& total) {
@@ -331,6 +363,18 @@ cudaError_t prepare_kernels() {
                            kAlignSmemMax);
   if (e != cudaSuccess) return e;
   return prepare_lora_kernels();
+}
+
+cudaError_t launch_token_lora_ids(const int32_t* weight_indices, const int32_t* seg_indptr,
+                                  int num_reqs, int64_t num_tokens, int max_loras,
+                                  const int32_t* lora_ranks, int32_t* lora_ids,
+                                  cudaStream_t stream) {
+  if (num_tokens == 0) return cudaSuccess;
+  const int threads = 256;
+  const int64_t blocks = std::min<int64_t>((num_tokens + threads - 1) / threads, 4096);
+  return launch_pdl(token_lora_ids_kernel, dim3((unsigned)blocks), dim3(threads), 0, stream,
+                    weight_indices, seg_indptr, num_reqs, num_tokens, max_loras, lora_ranks,
+                    lora_ids);
 }
 
 cudaError_t launch_virtual_topk(const int32_t* topk_ids, const int32_t* lora_ids, int64_t numel,

@@ -44,6 +44,12 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// Per-token adapter ids from per-request slots (seg_indptr non-decreasing).
+cudaError_t launch_token_lora_ids(const int32_t* weight_indices, const int32_t* seg_indptr,
+                                  int num_reqs, int64_t num_tokens, int max_loras,
+                                  const int32_t* lora_ranks, int32_t* lora_ids,
+                                  cudaStream_t stream);
+
 cudaError_t launch_virtual_topk(const int32_t* topk_ids, const int32_t* lora_ids, int64_t numel,
                                 int topk, int num_experts, int max_loras, int32_t* vtopk,
                                 cudaStream_t stream);
@@ -60,6 +66,10 @@ cudaError_t launch_align(const AlignPlan& plan, bool remap, const int32_t* src,
                          int32_t* expert_ids, int32_t* ntpp, void* workspace, bool trigger_early,
                          cudaStream_t stream);
 
+// r1: rank per slice; lora_ranks (per adapter, adapter = v / num_experts, may
+// be NULL) limit the columns computed: rank 0 writes nothing, columns past
+// the rank are written as 0. Ranks are read like the weights (before
+// griddepcontrol.wait with `early`).
 // early = true only inside mol_lora_forward reusing a routing (compute_routing
 // = 0): the routing and the weights are then read before griddepcontrol.wait,
 // the activations after it. The routing is then older than the kernel that
@@ -68,7 +78,8 @@ cudaError_t launch_align(const AlignPlan& plan, bool remap, const int32_t* src,
 cudaError_t launch_shrink(const void* x, int64_t x_stride, int x_div, int K, const void* lora_a,
                           int R, const int32_t* sorted_ids, const int32_t* expert_ids,
                           const int32_t* ntpp, int64_t capacity, int block_m, int64_t numel,
-                          int num_vexperts, float* inter, bool early, cudaStream_t stream);
+                          int num_vexperts, float* inter, bool early, cudaStream_t stream,
+                          int r1, const int32_t* lora_ranks, int num_experts);
 
 // early = true only when the preceding kernel is this library's shrink of the
 // same stage (mol_lora_forward): routing, weights and output rows are then read
@@ -79,7 +90,11 @@ cudaError_t launch_expand(const float* inter, const void* lora_b, int S, int r, 
                           const float* topk_weights, const int32_t* sorted_ids,
                           const int32_t* expert_ids, const int32_t* ntpp, int64_t capacity,
                           int block_m, int64_t numel, int num_vexperts, void* out,
-                          int64_t out_stride, bool early, cudaStream_t stream);
+                          int64_t out_stride, bool early, cudaStream_t stream,
+                          const int32_t* lora_ranks, const float* lora_scalings, int num_experts);
+
+// Per-adapter ranks: the shrink keeps one rank per adapter in shared memory.
+constexpr int kMaxLoraTable = 2048;
 
 // Largest contraction width accepted by the shrink (it streams K in chunks).
 constexpr int kShrinkMaxK = 1 << 16;

@@ -82,7 +82,7 @@ constexpr int kMeta = kStages + 2;               // jobs whose rows a consumer m
 constexpr int kHeader = 1024;                    // barriers, stage headers, job meta
 constexpr size_t kSmem = kHeader + (size_t)kStages * kStageBytes;
 struct Job {
-  int v, jt, cm, pad;
+  int v, jt, cm, ncols;  // ncols: leading columns of the item inside the adapter's rank
   int rows[kXR];
 };
 struct StageHdr {
@@ -110,12 +110,14 @@ MOL_DEV void job_chunk(int K, int cm, int& len, int& pitch) {
 }
 }  // namespace sp
 
+template <bool RANKS>
 __global__ void __launch_bounds__(sp::kThreads, sp::kBlocksPerSM)
 lora_shrink_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, int K,
                    const uint16_t* __restrict__ lora_a, int R, const int* __restrict__ sorted_ids,
                    const int* __restrict__ expert_ids, const int* __restrict__ ntpp_ptr,
                    int block_m, int64_t numel, int num_vexperts, float* __restrict__ inter,
-                   int n_jt, int64_t n_items, int early) {
+                   int n_jt, int64_t n_items, int early, int r1,
+                   const int* __restrict__ lora_ranks, int num_experts, int num_loras) {
   using namespace sp;
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
@@ -125,6 +127,7 @@ lora_shrink_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, 
   unsigned char* stages = smem + kHeader;
   __shared__ float red[kConsumers - 1][4][32];
   __shared__ int prow[128];  // producer: compacted rows of the current block
+  __shared__ uint16_t s_rank[RANKS ? kMaxLoraTable : 1];  // producer: adapter ranks in [0, r1]
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
@@ -176,6 +179,13 @@ lora_shrink_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, 
     Raw nxt;
     int64_t item = blockIdx.x;
     fetch(item, nxt);
+    if constexpr (RANKS) {  // per-adapter ranks, read like the weights
+      for (int l = lane; l < num_loras; l += 32) {
+        const int rk = __ldg(lora_ranks + l);
+        s_rank[l] = (uint16_t)(rk < 0 ? 0 : (rk > r1 ? r1 : rk));
+      }
+      __syncwarp();
+    }
     bool fault = false;
     while (item < n_items && !fault) {
       const Raw cur_r = nxt;
@@ -184,6 +194,15 @@ lora_shrink_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, 
       fetch(item, nxt);  // next item's routing is in flight while this one streams
       const int v = (cur_r.t * block_m < cur_r.ntpp) ? cur_r.e : -1;
       if (v < 0 || v >= num_vexperts) continue;
+      // Columns of this item inside the adapter's rank: rank 0 writes nothing,
+      // an item wholly past the rank writes zeros (its weights are padding).
+      const int jt_c = (int)(cur % n_jt);
+      int in_rank = kJT;  // columns of the item below the rank (r1 % 8 == 0 with ranks)
+      if constexpr (RANKS) {
+        const int rl = (int)s_rank[v / num_experts];
+        if (rl == 0) continue;
+        in_rank = rl - (jt_c * kJT) % r1;
+      }
       int c = 0;
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
@@ -194,7 +213,19 @@ lora_shrink_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, 
         c += __popc(bal);
       }
       __syncwarp();
-      const int jt = (int)(cur % n_jt);
+      const int jt = jt_c;
+      if (RANKS && in_rank <= 0) {
+        if (!waited) {  // the zeros overwrite rows the previous kernel may still read
+          pdl_wait();
+          pdl_launch_dependents();
+          waited = true;
+        }
+        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int q2 = lane; q2 < 2 * c; q2 += 32)
+          *reinterpret_cast<float4*>(inter + (int64_t)prow[q2 >> 1] * R + jt * kJT + 4 * (q2 & 1)) = z;
+        __syncwarp();
+        continue;
+      }
       const uint16_t* wrows = lora_a + ((int64_t)v * R + jt * kJT) * K;
       for (int m0 = 0; m0 < c && !fault; m0 += kXR) {
         const int cm = min(kXR, c - m0);
@@ -207,6 +238,7 @@ lora_shrink_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, 
           jb.v = v;
           jb.jt = jt;
           jb.cm = cm;
+          jb.ncols = in_rank < kJT ? in_rank : kJT;
         }
         if (lane < cm) jb.rows[lane] = prow[m0 + lane];
         const uint16_t* xsrc =
@@ -325,12 +357,14 @@ lora_shrink_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, 
 #pragma unroll
           for (int w = 0; w < kConsumers - 1; ++w) acc[e] += red[w][e][lane];
         const int col = jb.jt * kJT + 2 * tq;
+        // columns past the adapter's rank are zero padding: written as 0
+        const bool k0v = !RANKS || 2 * tq < jb.ncols, k1v = !RANKS || 2 * tq + 1 < jb.ncols;
         if (g < cm)
           *reinterpret_cast<float2*>(inter + (int64_t)jb.rows[g] * R + col) =
-              make_float2(acc[0], acc[1]);
+              make_float2(k0v ? acc[0] : 0.f, k1v ? acc[1] : 0.f);
         if (g + 8 < cm)
           *reinterpret_cast<float2*>(inter + (int64_t)jb.rows[g + 8] * R + col) =
-              make_float2(acc[2], acc[3]);
+              make_float2(k0v ? acc[2] : 0.f, k1v ? acc[3] : 0.f);
       }
       named_sync(1, kConsumers * 32);
     }
@@ -345,14 +379,23 @@ lora_shrink_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, 
 constexpr int kExpandThreads = 128;
 constexpr int kExpandCols = 128;
 
-template <int RK, bool EARLY>
+// Zeroes the elements of a (columns j .. j+3) at or past column rl.
+MOL_DEV void mask_cols(float4& a, int j, int rl) {
+  if (j >= rl) a.x = 0.f;
+  if (j + 1 >= rl) a.y = 0.f;
+  if (j + 2 >= rl) a.z = 0.f;
+  if (j + 3 >= rl) a.w = 0.f;
+}
+
+template <int RK, bool EARLY, bool ADAPT>
 __global__ void __launch_bounds__(kExpandThreads)
 lora_expand_kernel(const float* __restrict__ inter, int R, const uint16_t* __restrict__ lora_b,
                    int S, int Ns, float scale, const float* __restrict__ topk_w,
                    const int* __restrict__ sorted_ids, const int* __restrict__ expert_ids,
                    const int* __restrict__ ntpp_ptr, int block_m, int64_t numel,
                    int num_vexperts, uint16_t* __restrict__ out, int64_t out_stride,
-                   int chunks_per_slice) {
+                   int chunks_per_slice, const int* __restrict__ lora_ranks,
+                   const float* __restrict__ lora_scalings, int num_experts) {
   constexpr bool K16 = (RK == 16);
   constexpr int KB = K16 ? 1 : RK / 32;  // k blocks (32 wide, or one 16-wide block)
   __shared__ int rows[128];
@@ -372,6 +415,13 @@ lora_expand_kernel(const float* __restrict__ inter, int R, const uint16_t* __res
   const int v = __ldg(expert_ids + t);
   const int slot = tid < block_m ? __ldg(sorted_ids + (int64_t)t * block_m + tid) : -1;
   if ((int64_t)t * block_m >= ntpp || v < 0 || v >= num_vexperts) return;
+  // the adapter's rank and scaling, loaded with the weights below
+  int rk_raw = RK;
+  float scl = 1.f;
+  if constexpr (ADAPT) {
+    if (lora_ranks) rk_raw = __ldg(lora_ranks + v / num_experts);
+    if (lora_scalings) scl = __ldg(lora_scalings + v / num_experts);
+  }
   const int c = compact_block_rows(slot, numel, rows, wcnt);
   if (c == 0) return;
 
@@ -411,6 +461,10 @@ lora_expand_kernel(const float* __restrict__ inter, int R, const uint16_t* __res
     pdl_wait();  // the intermediate comes from the shrink that precedes this kernel
     pdl_launch_dependents();
   }
+  // rank 0: the adapter writes no delta; past rank rl the intermediate is padding
+  const int rl = rk_raw < 0 ? 0 : (rk_raw > RK ? RK : rk_raw);
+  if (ADAPT && rl == 0) return;
+  const float scale_v = ADAPT ? scale * scl : scale;
 
   for (int m0 = 0; m0 < c; m0 += 16) {
     if (m0 > 0) {
@@ -428,12 +482,19 @@ lora_expand_kernel(const float* __restrict__ inter, int R, const uint16_t* __res
       const int koff = s * RK + (K16 ? 4 * tq : kb * 32 + 8 * tq);
       const float* p0 = inter + (int64_t)(i0 >= 0 ? i0 : 0) * R + koff;
       const float* p1 = inter + (int64_t)(i1 >= 0 ? i1 : 0) * R + koff;
-      const float4 a0 = i0 >= 0 ? ld_l2_f4(p0) : zf;
-      const float4 a1 = i1 >= 0 ? ld_l2_f4(p1) : zf;
+      float4 a0 = i0 >= 0 ? ld_l2_f4(p0) : zf;
+      float4 a1 = i1 >= 0 ? ld_l2_f4(p1) : zf;
       float4 b0 = zf, b1 = zf;
       if constexpr (!K16) {
         b0 = i0 >= 0 ? ld_l2_f4(p0 + 4) : zf;
         b1 = i1 >= 0 ? ld_l2_f4(p1 + 4) : zf;
+      }
+      if (ADAPT && rl < RK) {  // intermediate columns j >= rl count as zero
+        const int j = K16 ? 4 * tq : kb * 32 + 8 * tq;
+        mask_cols(a0, j, rl);
+        mask_cols(a1, j, rl);
+        mask_cols(b0, j + 4, rl);
+        mask_cols(b1, j + 4, rl);
       }
       uint32_t h0, l0, h1, l1, h2, l2, h3, l3;
       split_bf16x2(a0.x, a0.y, h0, l0);
@@ -463,7 +524,7 @@ lora_expand_kernel(const float* __restrict__ inter, int R, const uint16_t* __res
       for (int h = 0; h < 2; ++h) {
         const int i = h ? i1 : i0;
         if (i < 0) continue;
-        const float sw = topk_w ? scale * __ldg(topk_w + i) : scale;
+        const float sw = topk_w ? scale_v * __ldg(topk_w + i) : scale_v;
         uint4 o = h ? o1 : o0;
         uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
 #pragma unroll
@@ -491,23 +552,30 @@ static int device_sms() {
 }
 
 cudaError_t prepare_lora_kernels() {
-  return cudaFuncSetAttribute(lora_shrink_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(lora_shrink_kernel<false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sp::kSmem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(lora_shrink_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)sp::kSmem);
 }
 
 cudaError_t launch_shrink(const void* x, int64_t x_stride, int x_div, int K, const void* lora_a,
                           int R, const int32_t* sorted_ids, const int32_t* expert_ids,
                           const int32_t* ntpp, int64_t capacity, int block_m, int64_t numel,
-                          int num_vexperts, float* inter, bool early, cudaStream_t stream) {
+                          int num_vexperts, float* inter, bool early, cudaStream_t stream,
+                          int r1, const int32_t* lora_ranks, int num_experts) {
   const int64_t nblk = capacity / block_m;
   if (numel == 0 || nblk == 0) return cudaSuccess;
   const int n_jt = R / sp::kJT;
+  const int num_loras = lora_ranks ? num_vexperts / num_experts : 0;
   const int64_t n_items = nblk * n_jt;
   const dim3 grid((unsigned)std::min<int64_t>(n_items, (int64_t)device_sms() * sp::kBlocksPerSM));
-  return launch_pdl(lora_shrink_kernel, grid, dim3(sp::kThreads), sp::kSmem, stream,
+  return launch_pdl(lora_ranks ? lora_shrink_kernel<true> : lora_shrink_kernel<false>, grid,
+                    dim3(sp::kThreads), sp::kSmem, stream,
                     static_cast<const uint16_t*>(x), x_stride, x_div, K,
                     static_cast<const uint16_t*>(lora_a), R, sorted_ids, expert_ids, ntpp, block_m,
-                    numel, num_vexperts, inter, n_jt, n_items, early ? 1 : 0);
+                    numel, num_vexperts, inter, n_jt, n_items, early ? 1 : 0, r1, lora_ranks,
+                    num_experts < 1 ? 1 : num_experts, num_loras);
 }
 
 template <int RK, bool EARLY>
@@ -515,17 +583,21 @@ static cudaError_t expand_rk(dim3 grid, cudaStream_t stream, const float* inter,
                              const uint16_t* b, int S, int Ns, float scale, const float* w,
                              const int32_t* sorted_ids, const int32_t* expert_ids,
                              const int32_t* ntpp, int block_m, int64_t numel, int num_vexperts,
-                             uint16_t* o, int64_t out_stride, int cps) {
-  return launch_pdl(lora_expand_kernel<RK, EARLY>, grid, dim3(kExpandThreads), 0, stream, inter, R,
+                             uint16_t* o, int64_t out_stride, int cps, const int32_t* ranks,
+                             const float* scalings, int num_experts) {
+  const bool adapt = ranks != nullptr || scalings != nullptr;
+  return launch_pdl(adapt ? lora_expand_kernel<RK, EARLY, true> : lora_expand_kernel<RK, EARLY, false>,
+                    grid, dim3(kExpandThreads), 0, stream, inter, R,
                     b, S, Ns, scale, w, sorted_ids, expert_ids, ntpp, block_m, numel, num_vexperts,
-                    o, out_stride, cps);
+                    o, out_stride, cps, ranks, scalings, num_experts < 1 ? 1 : num_experts);
 }
 
 cudaError_t launch_expand(const float* inter, const void* lora_b, int S, int r, int Ns, float scale,
                           const float* topk_weights, const int32_t* sorted_ids,
                           const int32_t* expert_ids, const int32_t* ntpp, int64_t capacity,
                           int block_m, int64_t numel, int num_vexperts, void* out,
-                          int64_t out_stride, bool early, cudaStream_t stream) {
+                          int64_t out_stride, bool early, cudaStream_t stream,
+                          const int32_t* lora_ranks, const float* lora_scalings, int num_experts) {
   const int64_t nblk = capacity / block_m;
   if (numel == 0 || nblk == 0) return cudaSuccess;
   const int cps = (Ns + kExpandCols - 1) / kExpandCols;
@@ -537,10 +609,12 @@ cudaError_t launch_expand(const float* inter, const void* lora_b, int S, int r, 
   case RK:                                                                                      \
     return early ? expand_rk<RK, true>(grid, stream, inter, R, b, S, Ns, scale, topk_weights,   \
                                        sorted_ids, expert_ids, ntpp, block_m, numel,            \
-                                       num_vexperts, o, out_stride, cps)                        \
+                                       num_vexperts, o, out_stride, cps, lora_ranks,            \
+                                       lora_scalings, num_experts)                              \
                  : expand_rk<RK, false>(grid, stream, inter, R, b, S, Ns, scale, topk_weights,  \
                                         sorted_ids, expert_ids, ntpp, block_m, numel,           \
-                                        num_vexperts, o, out_stride, cps);
+                                        num_vexperts, o, out_stride, cps, lora_ranks,           \
+                                        lora_scalings, num_experts);
   switch (r) {
     MOL_EXPAND_CASE(16)
     MOL_EXPAND_CASE(32)

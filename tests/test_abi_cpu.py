@@ -43,7 +43,7 @@ def declared_functions():
 def test_exports_every_declared_symbol(mol):
     lib = mol.library()
     names = declared_functions()
-    assert len(names) == 11
+    assert len(names) == 12
     for n in names:
         assert hasattr(lib, n), n
     assert set(names) == set(mol.EXPORTS)
@@ -88,22 +88,34 @@ def test_validation_rejects_before_any_launch(mol):
     assert lib.mol_align_block_size(P(16), 70000, 16, 16, P(16), 1 << 20, P(16), P(16), None, 0, None) == -2
     assert lib.mol_align_block_size(P(16), (1 << 22) + 1, 16, 16, P(16), 1 << 30, P(16), P(16), None, 0, None) == -3
     # shrink / expand contracts
-    assert lib.mol_lora_shrink(P(16), 64, 1, 60, P(16), 1, 16, P(16), P(16), P(16), 64, 16, 8, 4, P(16), None) == -3
-    assert lib.mol_lora_shrink(P(16), 64, 1, 64, P(16), 1, 8, P(16), P(16), P(16), 64, 16, 8, 4, P(16), None) == -3
-    assert lib.mol_lora_shrink(P(18), 64, 1, 64, P(16), 1, 16, P(16), P(16), P(16), 64, 16, 8, 4, P(16), None) == -3
-    assert lib.mol_lora_shrink(P(16), 64, 0, 64, P(16), 1, 16, P(16), P(16), P(16), 64, 16, 8, 4, P(16), None) == -1
-    assert lib.mol_lora_shrink(P(16), 64, 1, 64, P(16), 1, 16, P(16), P(16), P(16), 65, 16, 8, 4, P(16), None) == -1
-    assert lib.mol_lora_expand(P(16), P(16), 1, 24, 16, 1.0, None, P(16), P(16), P(16), 64, 16, 8, 4, P(16), 16, None) == -3
-    assert lib.mol_lora_expand(P(16), P(16), 1, 16, 12, 1.0, None, P(16), P(16), P(16), 64, 16, 8, 4, P(16), 16, None) == -3
-    assert lib.mol_lora_expand(P(16), P(16), 2, 16, 64, 1.0, None, P(16), P(16), P(16), 64, 16, 8, 4, P(16), 64, None) == -1
-    assert lib.mol_lora_expand(P(16), P(16), 1, 16, 64, 1.0, None, P(16), P(16), P(16), 64, 16, 8, 4, P(24), 64, None) == -3
+    assert lib.mol_lora_shrink(P(16), 64, 1, 60, P(16), 1, 16, P(16), P(16), P(16), 64, 16, 8, 4, P(16), 0, None, None) == -3
+    assert lib.mol_lora_shrink(P(16), 64, 1, 64, P(16), 1, 8, P(16), P(16), P(16), 64, 16, 8, 4, P(16), 0, None, None) == -3
+    assert lib.mol_lora_shrink(P(18), 64, 1, 64, P(16), 1, 16, P(16), P(16), P(16), 64, 16, 8, 4, P(16), 0, None, None) == -3
+    assert lib.mol_lora_shrink(P(16), 64, 0, 64, P(16), 1, 16, P(16), P(16), P(16), 64, 16, 8, 4, P(16), 0, None, None) == -1
+    assert lib.mol_lora_shrink(P(16), 64, 1, 64, P(16), 1, 16, P(16), P(16), P(16), 65, 16, 8, 4, P(16), 0, None, None) == -1
+    assert lib.mol_lora_expand(P(16), P(16), 1, 24, 16, 1.0, None, P(16), P(16), P(16), 64, 16, 8, 4, P(16), 16, 0, None, None, None) == -3
+    assert lib.mol_lora_expand(P(16), P(16), 1, 16, 12, 1.0, None, P(16), P(16), P(16), 64, 16, 8, 4, P(16), 16, 0, None, None, None) == -3
+    assert lib.mol_lora_expand(P(16), P(16), 2, 16, 64, 1.0, None, P(16), P(16), P(16), 64, 16, 8, 4, P(16), 64, 0, None, None, None) == -1
+    assert lib.mol_lora_expand(P(16), P(16), 1, 16, 64, 1.0, None, P(16), P(16), P(16), 64, 16, 8, 4, P(24), 64, 0, None, None, None) == -3
+    # per-adapter ranks / scalings: num_experts missing or not dividing V, too many adapters
+    assert lib.mol_lora_shrink(P(16), 64, 1, 64, P(16), 1, 16, P(16), P(16), P(16), 64, 16, 8, 4, P(16), 0, P(16), None) == -1
+    assert lib.mol_lora_shrink(P(16), 64, 1, 64, P(16), 1, 16, P(16), P(16), P(16), 64, 16, 8, 6, P(16), 4, P(16), None) == -1
+    assert lib.mol_lora_shrink(P(16), 64, 1, 64, P(16), 1, 16, P(16), P(16), P(16), 64, 16, 8, 4100, P(16), 2, P(16), None) == -3
+    assert lib.mol_lora_expand(P(16), P(16), 1, 16, 16, 1.0, None, P(16), P(16), P(16), 64, 16, 8, 4, P(16), 16, 3, None, P(16), None) == -1
+    # per-token adapter ids
+    assert lib.mol_token_lora_ids(P(16), P(16), -1, 8, 4, None, P(16), None) == -1
+    assert lib.mol_token_lora_ids(P(16), P(16), 2, 8, 0, None, P(16), None) == -1
+    assert lib.mol_token_lora_ids(P(16), P(16), 2, (1 << 22) + 1, 4, None, P(16), None) == -3
+    assert lib.mol_token_lora_ids(None, P(16), 2, 8, 4, None, P(16), None) == -1
+    assert lib.mol_token_lora_ids(P(16), P(16), 2, 8, 4, None, None, None) == -1
+    assert lib.mol_token_lora_ids(None, None, 0, 0, 4, None, None, None) == 0
     # remap
     assert lib.mol_virtual_topk(P(16), P(16), -1, 8, 4, 4, P(16), None) == -1
     assert lib.mol_virtual_topk(P(16), P(16), 1 << 20, 8, 4, 4, P(16), None) == -3
     # forward: V + 1 over the bucket cap
     assert lib.mol_lora_forward(P(16), 64, 1, 64, P(16), P(16), 4, 2, 4096, 2, P(16), P(16), 1, 16, 16,
                                 1.0, None, P(16), 16, 16, 1, P(16), P(16), 4096, P(16), P(16), P(16),
-                                None, 0, None) == -3
+                                None, None, None, 0, None) == -3
 
 
 def test_binding_fails_loudly_without_library(tmp_path):

@@ -285,12 +285,12 @@ def test_invalid_arguments_launch_nothing():
     A = torch.zeros((16, 16, 64), dtype=torch.bfloat16, device=dev)
     inter = torch.zeros((64, 16), dtype=torch.float32, device=dev)
     # K not a multiple of 8, rank/slices not giving R % 16 == 0, misaligned pointer
-    assert lib.mol_lora_shrink(P(x), 64, 8, 60, P(A), 1, 16, P(s), P(e), P(n), 4096, 16, 64, 16, P(inter), st()) == mol.MOL_ERR_UNSUPPORTED
-    assert lib.mol_lora_shrink(P(x), 64, 8, 64, P(A), 1, 8, P(s), P(e), P(n), 4096, 16, 64, 16, P(inter), st()) == mol.MOL_ERR_UNSUPPORTED
-    assert lib.mol_lora_shrink(P(x) + 2, 64, 8, 64, P(A), 1, 16, P(s), P(e), P(n), 4096, 16, 64, 16, P(inter), st()) == mol.MOL_ERR_UNSUPPORTED
-    assert lib.mol_lora_expand(P(inter), P(A), 1, 24, 16, 1.0, None, P(s), P(e), P(n), 4096, 16, 64, 16, P(x), 64, st()) == mol.MOL_ERR_UNSUPPORTED
-    assert lib.mol_lora_expand(P(inter), P(A), 1, 16, 12, 1.0, None, P(s), P(e), P(n), 4096, 16, 64, 16, P(x), 64, st()) == mol.MOL_ERR_UNSUPPORTED
-    assert lib.mol_lora_expand(P(inter), P(A), 2, 16, 64, 1.0, None, P(s), P(e), P(n), 4096, 16, 64, 16, P(x), 64, st()) == mol.MOL_ERR_INVALID_ARG
+    assert lib.mol_lora_shrink(P(x), 64, 8, 60, P(A), 1, 16, P(s), P(e), P(n), 4096, 16, 64, 16, P(inter), 0, None, st()) == mol.MOL_ERR_UNSUPPORTED
+    assert lib.mol_lora_shrink(P(x), 64, 8, 64, P(A), 1, 8, P(s), P(e), P(n), 4096, 16, 64, 16, P(inter), 0, None, st()) == mol.MOL_ERR_UNSUPPORTED
+    assert lib.mol_lora_shrink(P(x) + 2, 64, 8, 64, P(A), 1, 16, P(s), P(e), P(n), 4096, 16, 64, 16, P(inter), 0, None, st()) == mol.MOL_ERR_UNSUPPORTED
+    assert lib.mol_lora_expand(P(inter), P(A), 1, 24, 16, 1.0, None, P(s), P(e), P(n), 4096, 16, 64, 16, P(x), 64, 0, None, None, st()) == mol.MOL_ERR_UNSUPPORTED
+    assert lib.mol_lora_expand(P(inter), P(A), 1, 16, 12, 1.0, None, P(s), P(e), P(n), 4096, 16, 64, 16, P(x), 64, 0, None, None, st()) == mol.MOL_ERR_UNSUPPORTED
+    assert lib.mol_lora_expand(P(inter), P(A), 2, 16, 64, 1.0, None, P(s), P(e), P(n), 4096, 16, 64, 16, P(x), 64, 0, None, None, st()) == mol.MOL_ERR_INVALID_ARG
     torch.cuda.synchronize()
     assert torch.all(s == -5) and torch.all(e == -5) and torch.all(n == -5)
     assert torch.all(inter == 0)
