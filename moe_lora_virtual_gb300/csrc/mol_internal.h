@@ -96,6 +96,17 @@ cudaError_t launch_expand(const float* inter, const void* lora_b, int S, int r, 
 // Per-adapter ranks: the shrink keeps one rank per adapter in shared memory.
 constexpr int kMaxLoraTable = 2048;
 
+// Shrink on tcgen05 tensor cores for batches with many rows per virtual
+// expert: R % 128 == 0, K % 64 == 0, block_m in {64, 128}, at least 32 pairs per
+// virtual expert on average, no per-adapter ranks. Reads everything after
+// griddepcontrol.wait.
+bool shrink_tc_fits(int64_t numel, int num_vexperts, int R, int K, int block_m);
+cudaError_t prepare_tc_kernels();
+cudaError_t launch_shrink_tc(const void* x, int64_t x_stride, int x_div, int K, const void* lora_a,
+                             int R, const int32_t* sorted_ids, const int32_t* expert_ids,
+                             const int32_t* ntpp, int64_t capacity, int block_m, int64_t numel,
+                             int num_vexperts, float* inter, cudaStream_t stream);
+
 // Largest contraction width accepted by the shrink (it streams K in chunks).
 constexpr int kShrinkMaxK = 1 << 16;
 

@@ -552,7 +552,9 @@ static int device_sms() {
 }
 
 cudaError_t prepare_lora_kernels() {
-  cudaError_t e = cudaFuncSetAttribute(lora_shrink_kernel<false>,
+  cudaError_t e = prepare_tc_kernels();
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(lora_shrink_kernel<false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sp::kSmem);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(lora_shrink_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -566,6 +568,9 @@ cudaError_t launch_shrink(const void* x, int64_t x_stride, int x_div, int K, con
                           int r1, const int32_t* lora_ranks, int num_experts) {
   const int64_t nblk = capacity / block_m;
   if (numel == 0 || nblk == 0) return cudaSuccess;
+  if (!lora_ranks && shrink_tc_fits(numel, num_vexperts, R, K, block_m))
+    return launch_shrink_tc(x, x_stride, x_div, K, lora_a, R, sorted_ids, expert_ids, ntpp,
+                            capacity, block_m, numel, num_vexperts, inter, stream);
   const int n_jt = R / sp::kJT;
   const int num_loras = lora_ranks ? num_vexperts / num_experts : 0;
   const int64_t n_items = nblk * n_jt;
