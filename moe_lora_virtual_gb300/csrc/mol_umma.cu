@@ -19,10 +19,11 @@
 //              and one lane issues the MMAs of a stage (four K=16 steps) and
 //              commits them to the stage's "empty" barrier and, after the
 //              item's last stage, to the accumulator's "full" barrier;
-//   warps 2-5  gather: the block's x rows, 128 bytes of each per stage, with
-//              cp.async into the same 128-byte-swizzled layout (zeros for
-//              padding slots), kept two groups ahead, then a proxy fence and
-//              an arrival on the stage's "full" barrier;
+//   warps 2-5  gather: the block's x rows, 128 bytes of each per stage (eight
+//              lanes per row, whole lines per instruction), with cp.async into
+//              the same 128-byte-swizzled layout (zeros for padding slots),
+//              kept two groups ahead, then a proxy fence and an arrival on
+//              the stage's "full" barrier;
 //   warps 6-9  epilogue: wait for an accumulator, read it with tcgen05.ld
 //              (each warp its 32-lane quarter of tensor memory = 32 lora_a
 //              rows), release it to the MMA warp, store fp32 rows.
@@ -248,28 +249,38 @@ lora_shrink_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
     }
   } else if (warp < 2 + kGatherWarps) {
     // ------------------------------------------------------------ x gather
+    // Eight lanes cover one row's 128 bytes, so each instruction of a warp
+    // moves four whole rows (full lines); thread g takes chunk g % 8 of rows
+    // g / 8, g / 8 + 16, ... .
     const int g = tid - 64;
-    constexpr int kThrPerRow = (kGatherWarps * 32) / BN;  // 2 (BN = 64) or 1 (BN = 128)
-    constexpr int kChunks = 8 / kThrPerRow;                // 16-byte chunks per thread and stage
-    const int r = g / kThrPerRow, c0 = (g % kThrPerRow) * kChunks;
+    constexpr int kRowsPerThr = BN / 16;
+    const int c = g & 7, r0 = g >> 3;
     uint32_t q = 0, arrived = 0;
     for (int64_t it = blockIdx.x; it < n_items && !fault; it += Gs) {
       int64_t t;
       int mt, v;
       if (!item(it, t, mt, v)) continue;
-      const int pid = __ldg(sorted_ids + t * BN + r);
-      const bool ok = pid >= 0 && (int64_t)pid < numel;
-      const uint16_t* src = ok ? x + (int64_t)(pid / x_div) * x_stride : x;
+      const uint16_t* src[kRowsPerThr];
+      uint32_t nbytes[kRowsPerThr];
+#pragma unroll
+      for (int i = 0; i < kRowsPerThr; ++i) {
+        const int pid = __ldg(sorted_ids + t * BN + r0 + 16 * i);
+        const bool ok = pid >= 0 && (int64_t)pid < numel;
+        src[i] = (ok ? x + (int64_t)(pid / x_div) * x_stride : x) + c * 8;
+        nbytes[i] = ok ? 16u : 0u;
+      }
       for (int ks = 0; ks < nk; ++ks, ++q) {
         const int s = (int)(q % kStages);
         if (!mbar_wait(&empty[s], ((q / kStages) & 1) ^ 1, kPolls)) {
           fault = true;
           break;
         }
-        unsigned char* row = stageA(q) + kATile + r * 128;
+        unsigned char* tile = stageA(q) + kATile;
 #pragma unroll
-        for (int c = c0; c < c0 + kChunks; ++c)
-          cp_async16_zfill(row + ((c ^ (r & 7)) << 4), src + ks * kKStep + c * 8, ok ? 16u : 0u);
+        for (int i = 0; i < kRowsPerThr; ++i) {
+          const int r = r0 + 16 * i;
+          cp_async16_zfill(tile + r * 128 + ((c ^ (r & 7)) << 4), src[i] + ks * kKStep, nbytes[i]);
+        }
         cp_async_commit();
         if (q + 1 - arrived > (uint32_t)kAhead) {  // the oldest group has landed
           cp_async_wait_ahead();
