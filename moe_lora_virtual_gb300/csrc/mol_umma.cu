@@ -21,9 +21,11 @@
 //              item's last stage, to the accumulator's "full" barrier;
 //   warps 2-5  gather: the block's x rows, 128 bytes of each per stage (eight
 //              lanes per row, whole lines per instruction), with cp.async into
-//              the same 128-byte-swizzled layout (zeros for padding slots),
-//              kept two groups ahead, then a proxy fence and an arrival on
-//              the stage's "full" barrier;
+//              the same 128-byte-swizzled layout (zeros for padding slots);
+//              each thread's arrival on the stage's "full" barrier fires when
+//              its copies land (cp.async.mbarrier.arrive.noinc), so the gather
+//              never waits for data, and the MMA lane fences the generic and
+//              async proxies before the MMAs read the stage;
 //   warps 6-9  epilogue: wait for an accumulator, read it with tcgen05.ld
 //              (each warp its 32-lane quarter of tensor memory = 32 lora_a
 //              rows), release it to the MMA warp, store fp32 rows.
@@ -50,9 +52,7 @@ constexpr int kATile = kM * 128;          // 16 KB
 constexpr int kGatherWarps = 4;
 constexpr int kEpiWarps = 4;
 constexpr int kThreads = (2 + kGatherWarps + kEpiWarps) * 32;
-constexpr int kAhead = 2;                 // cp.async groups a gather thread keeps in flight
 constexpr uint32_t kPolls = 1u << 22;
-static_assert(kAhead + 2 <= kStages, "gather arrivals must precede the reuse of their stage");
 template <int BN>
 struct Geo {
   static constexpr int kXTile = BN * 128;
@@ -89,9 +89,13 @@ MOL_DEV void cp_async16_zfill(void* dst, const void* src, uint32_t src_bytes) {
                "r"(src_bytes)
                : "memory");
 }
-MOL_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-MOL_DEV void cp_async_wait_ahead() { asm volatile("cp.async.wait_group 2;" ::: "memory"); }
-MOL_DEV void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+// Arrives on `bar` once every cp.async this thread issued so far has landed
+// (the barrier's expected count includes this arrival).
+MOL_DEV void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+MOL_DEV void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 MOL_DEV void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 MOL_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 MOL_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -233,6 +237,9 @@ lora_shrink_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
             fault = true;
             break;
           }
+          // the x rows arrived through cp.async (generic proxy); the MMAs read
+          // them through the async proxy
+          fence_proxy_async_smem();
           tc_fence_after();
           const uint32_t sa = smem_u32(stageA(q));
           const uint32_t sx = sa + kATile;
@@ -255,7 +262,7 @@ lora_shrink_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
     const int g = tid - 64;
     constexpr int kRowsPerThr = BN / 16;
     const int c = g & 7, r0 = g >> 3;
-    uint32_t q = 0, arrived = 0;
+    uint32_t q = 0;
     for (int64_t it = blockIdx.x; it < n_items && !fault; it += Gs) {
       int64_t t;
       int mt, v;
@@ -281,19 +288,10 @@ lora_shrink_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
           const int r = r0 + 16 * i;
           cp_async16_zfill(tile + r * 128 + ((c ^ (r & 7)) << 4), src[i] + ks * kKStep, nbytes[i]);
         }
-        cp_async_commit();
-        if (q + 1 - arrived > (uint32_t)kAhead) {  // the oldest group has landed
-          cp_async_wait_ahead();
-          fence_proxy_async_smem();
-          mbar_arrive(&full[arrived % kStages]);
-          ++arrived;
-        }
+        cp_async_arrive_noinc(&full[s]);
       }
     }
-    cp_async_wait_all();
-    fence_proxy_async_smem();
-    if (!fault)
-      for (; arrived < q; ++arrived) mbar_arrive(&full[arrived % kStages]);
+    cp_async_wait_all();  // no copy of this thread is left in flight at exit
   } else {
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;  // tensor-memory lanes 32*quarter .. +31
