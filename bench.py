@@ -319,6 +319,7 @@ def run_gpu(args):
     peaks = measured_peaks()
     kern = {}
     roof = None
+    shrink_tensor = None
     if not args.no_kernels:
         def stage_call(L_, si, which):
             d = L_.stages[si]
@@ -370,6 +371,19 @@ def run_gpu(args):
                     unit="GB/s", frac=round(achieved / peaks["hbm_gbs"], 4),
                     traffic=TRAFFIC.get((args.config, name)), bytes_per_launch=int(nbytes),
                     us_per_launch=round(us, 3), peak_source=peaks["source"])
+        # the first stage's shrink against the bf16 tensor peak (a real dense
+        # contraction only when the routed blocks are full, as in `dense`)
+        st0 = wl.stages[0]
+        sname = f"shrink_{st0.name}"
+        flops = 2.0 * pairs_per_step * st0.K * st0.R
+        tflops = flops / (kern[sname] * 1e-6) / 1e12
+        tc_path = (st0.R % 128 == 0 and st0.K % 64 == 0 and wl.BM in (64, 128) and ranks is None
+                   and wl.numel >= 32 * min(wl.numel, wl.V))
+        shrink_tensor = dict(kernel=sname, bound="tensor", achieved=round(tflops, 1),
+                             peak=peaks["bf16_tflops"], unit="TFLOP/s",
+                             frac=round(tflops / peaks["bf16_tflops"], 4),
+                             path="tcgen05" if tc_path else "mma.sync",
+                             flops_per_launch=flops, peak_source=peaks["source"])
 
     layer_bytes = float(np.mean([sum(sum(L_.stage_bytes(si, *c)) for si in range(len(wl.stages)))
                                  + L_.align_bytes() for L_, c in zip(layers, cnt)]))
@@ -395,7 +409,8 @@ def run_gpu(args):
                               achieved_gbs=round(layer_bytes / (ms * 1e-3) / 1e9, 1),
                               frac=round(layer_bytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)),
                kernels_us={k: round(v, 3) for k, v in kern.items()},
-               roofline=roof, e2e=e2e, gpu_launches=launches_per_step * args.steps,
+               roofline=roof, shrink_tensor=shrink_tensor, e2e=e2e,
+               gpu_launches=launches_per_step * args.steps,
                clocks=dict(sm_mhz=clk["sm_mhz"], sm_max_mhz=clk["sm_max_mhz"],
                            reasons=clk["reasons"], samples=clk["samples"]))
     if rank == 0 and not args.no_cpu:
