@@ -423,53 +423,74 @@ def run_gpu(args):
 
 
 def run_e2e(args, torch, mol, wl, layers, pairs_per_step, world, dev):
-    """Per step: pinned host -> device copies of the step's inputs, the layer, device -> host copy
-    of the outputs; captured (copies included) in one graph per layer."""
-    host = []
+    """Per step: one pinned host -> device copy of the step's inputs, the layer, one device ->
+    host copy of its outputs; captured (copies included) in one graph per layer.
+
+    Each layer's inputs (top-k ids, adapter ids, every stage's activations and the output rows
+    the expand updates) live in one device buffer, 256-byte aligned segments with the outputs
+    last, mirrored by a pinned host buffer: a step moves the same bytes as per-tensor copies
+    in one copy each way. The library receives ordinary tensor views of that buffer."""
+    def rup(n):
+        return (n + 255) // 256 * 256
+
+    packs = []
     for L_ in layers:
-        h = dict(topk=torch.from_numpy(L_.li.topk_ids).pin_memory(),
-                 lora=torch.from_numpy(L_.li.lora_ids).pin_memory(), x=[], out_in=[], out_back=[])
-        for d in L_.stages:
-            h["x"].append(d["x"].cpu().pin_memory())
-            h["out_in"].append(d["out"].cpu().pin_memory())
-            h["out_back"].append(torch.empty_like(h["out_in"][-1]).pin_memory())
-        host.append(h)
+        segs = [("topk", L_.topk), ("lora", L_.lora)]
+        segs += [(f"x{i}", d["x"]) for i, d in enumerate(L_.stages)]
+        segs += [(f"out{i}", d["out"]) for i, d in enumerate(L_.stages)]
+        offs, total = {}, 0
+        for name, t in segs:
+            offs[name] = total
+            total += rup(t.numel() * t.element_size())
+        dev_buf = torch.empty(total, dtype=torch.uint8, device=dev)
+        host_in = torch.empty(total, dtype=torch.uint8).pin_memory()
 
-    def step(L_, h):
-        L_.topk.copy_(h["topk"], non_blocking=True)
-        L_.lora.copy_(h["lora"], non_blocking=True)
-        for d, x, o in zip(L_.stages, h["x"], h["out_in"]):
-            d["x"].copy_(x, non_blocking=True)
-            d["out"].copy_(o, non_blocking=True)
+        def view(buf, name, t, offs=offs):
+            nb = t.numel() * t.element_size()
+            return buf[offs[name]:offs[name] + nb].view(t.dtype).view(t.shape)
+
+        for name, t in segs:
+            view(host_in, name, t).copy_(t.cpu())
+        L_.topk, L_.lora = view(dev_buf, "topk", L_.topk), view(dev_buf, "lora", L_.lora)
+        for i, d in enumerate(L_.stages):
+            d["x"] = view(dev_buf, f"x{i}", d["x"])
+            d["out"] = view(dev_buf, f"out{i}", d["out"])
+        out_lo = offs["out0"]
+        host_out = torch.empty(total - out_lo, dtype=torch.uint8).pin_memory()
+        packs.append((dev_buf, host_in, host_out, out_lo))
+
+    def step(L_, pk):
+        dev_buf, host_in, host_out, out_lo = pk
+        dev_buf.copy_(host_in, non_blocking=True)
         L_.forward(mol)
-        for d, ob in zip(L_.stages, h["out_back"]):
-            ob.copy_(d["out"], non_blocking=True)
+        host_out.copy_(dev_buf[out_lo:], non_blocking=True)
 
-    graphs = [capture(torch, lambda L_=L_, h=h: step(L_, h)) for L_, h in zip(layers, host)]
+    graphs = [capture(torch, lambda L_=L_, pk=pk: step(L_, pk)) for L_, pk in zip(layers, packs)]
     steps = min(args.steps, 5000)
     ms = time_graphs(torch, graphs, steps, min(args.warmup, 50))
-    h0 = host[0]
-    bi = h0["topk"].nbytes + h0["lora"].nbytes + sum(t.nbytes for t in h0["x"] + h0["out_in"])
-    bo = sum(t.nbytes for t in h0["out_back"])
+    bi = packs[0][1].numel()
+    bo = packs[0][2].numel()
     # eager calls (no graph) for reference
     n_e = min(steps, 500)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for i in range(n_e):
-        step(layers[i % len(layers)], host[i % len(host)])
+        step(layers[i % len(layers)], packs[i % len(packs)])
     torch.cuda.synchronize()
     ms_eager = (time.perf_counter() - t0) * 1e3 / n_e
     return dict(value=round(pairs_per_step * world / (ms * 1e-3), 1), unit=UNIT,
                 h2d_bytes_per_step=int(bi), d2h_bytes_per_step=int(bo), ms_per_step=round(ms, 6),
-                mode="graph replay of pinned-host copies + mol_lora_forward calls",
+                mode="graph replay: one pinned-host copy of the packed step inputs, the "
+                     "mol_lora_forward calls, one copy of the outputs back",
                 eager_value=round(pairs_per_step * world / (ms_eager * 1e-3), 1),
                 eager_ms_per_step=round(ms_eager, 6), steps=steps)
 
 
 # traffic (dram bytes read + written) per launch from ncu captures, keyed by
 # (workload, kernel); None until the current kernel has been captured. Source:
-# profiles/decode_stage_kernels_ncu_full.md (one decode layer, 8-row shrink).
-TRAFFIC = {("decode", "shrink_gate_up"): 35506688 + 5888}
+# profiles/decode_stage_kernels_ncu_full.md (one decode layer, 8-row shrink,
+# the instance without per-adapter ranks).
+TRAFFIC = {("decode", "shrink_gate_up"): 35508736 + 0}
 
 
 # --------------------------------------------------------------------------- CPU (oracle)
