@@ -123,28 +123,31 @@ MOL_DEV int block_exclusive_scan(int v, int* sh, int& total) {
 }
 
 // counts[b] -> exclusive offsets of the BM-padded buckets (in place), then
-// expert_ids of every block and num_tokens_post_padded.
+// expert_ids of every block and num_tokens_post_padded. block_m is a power of
+// two (validated on the host): padding and block indices are masks and shifts.
 template <int THREADS>
 MOL_DEV void bucket_offsets(int* counts, int nb, int num_vexperts, int block_m, int64_t capacity,
                             int* __restrict__ expert_ids, int* __restrict__ ntpp_out, int* sh) {
+  const int lg = __ffs(block_m) - 1;
+  const int pad = block_m - 1;
   const int per = (nb + THREADS - 1) / THREADS;
   const int b0 = min((int)threadIdx.x * per, nb), b1 = min(b0 + per, nb);
   int local = 0;
-  for (int b = b0; b < b1; ++b) local += (counts[b] + block_m - 1) / block_m * block_m;
+  for (int b = b0; b < b1; ++b) local += (counts[b] + pad) & ~pad;
   int total;
   int run = block_exclusive_scan<THREADS>(local, sh, total);
   for (int b = b0; b < b1; ++b) {
-    const int pb = (counts[b] + block_m - 1) / block_m * block_m;
+    const int pb = (counts[b] + pad) & ~pad;
     counts[b] = run;
     if (b < num_vexperts) {
-      const int t0 = run / block_m;
-      for (int k = 0; k < pb / block_m; ++k) expert_ids[t0 + k] = b;
+      const int t0 = run >> lg;
+      for (int k = 0; k < (pb >> lg); ++k) expert_ids[t0 + k] = b;
     }
     run += pb;
   }
   __syncthreads();
-  const int64_t nblk = capacity / block_m;
-  for (int64_t t = counts[num_vexperts] / block_m + threadIdx.x; t < nblk; t += THREADS)
+  const int64_t nblk = capacity >> lg;
+  for (int64_t t = (counts[num_vexperts] >> lg) + threadIdx.x; t < nblk; t += THREADS)
     expert_ids[t] = -1;
   if (threadIdx.x == 0) *ntpp_out = total;
 }
