@@ -28,6 +28,7 @@ CASES = [
     (512, 2, 4, 128, 192, 2, 128, 72, True, 0.05),
     (200, 8, 16, 64, 1024, 2, 64, 40, True, 0.0),
     (130, 2, 2, 128, 128, 1, 128, 32, False, 0.2),
+    (256, 2, 4, 64, 64, 2, 64, 32, True, 0.0),      # one k stage
 ]
 
 
