@@ -271,6 +271,18 @@ int32_t mol_lora_forward(const void* x, int64_t x_row_stride, int32_t x_row_div,
  * token still gets some value in {-1} U [0, max_loras) and nothing is read out
  * of bounds.
  */
+/*
+ * Every wait inside this library's kernels (on a barrier, a bulk copy or a
+ * tensor-core accumulator) is bounded; when one runs out the kernel records a
+ * fault bit, stops its work early and exits instead of hanging, so its outputs
+ * are then incomplete. This call waits for the current device to be idle
+ * (cudaDeviceSynchronize), writes the bits recorded since the last call to
+ * *flags (0 = none; bit 0 = a wait ran out) and clears them. It synchronizes,
+ * so it belongs in checks and tests, not in a captured or timed sequence.
+ * (No counterpart on the pages: the pages' kernels have no bounded waits.)
+ */
+int32_t mol_take_fault_flags(uint32_t* flags);
+
 int32_t mol_token_lora_ids(const int32_t* weight_indices, const int32_t* seg_indptr,
                            int32_t num_reqs, int64_t num_tokens, int32_t max_loras,
                            const int32_t* lora_ranks, int32_t* lora_ids, void* stream);

@@ -29,6 +29,7 @@ EXPORTS = (
     "mol_version", "mol_status_string", "mol_last_cuda_error", "mol_align_capacity",
     "mol_workspace_bytes", "mol_virtual_topk", "mol_align_block_size", "mol_lora_shrink",
     "mol_lora_expand", "mol_lora_forward", "mol_align_block_size_noalloc", "mol_token_lora_ids",
+    "mol_take_fault_flags",
 )
 
 _lib = None
@@ -55,6 +56,7 @@ _SIGS = {
                                 _I32, _I32, _F32, _P, _P, _I64, _I32, _I32, _P, _P, _I64, _P, _P,
                                 _P, _P, _P, _P, _SZ, _P]),
     "mol_token_lora_ids": (_I32, [_P, _P, _I32, _I64, _I32, _P, _P, _P]),
+    "mol_take_fault_flags": (_I32, [ctypes.POINTER(ctypes.c_uint32)]),
 }
 
 
@@ -291,4 +293,12 @@ def mol_token_lora_ids(weight_indices: torch.Tensor, seg_indptr: torch.Tensor, n
         _ptr(weight_indices), _ptr(seg_indptr), num_reqs, num_tokens, max_loras, _ptr(lora_ranks),
         _ptr(lora_ids), _stream(stream)))
     return lora_ids
+
+
+def mol_take_fault_flags() -> int:
+    """Bits recorded by kernels whose bounded waits ran out since the last call (0 = none);
+    synchronizes the device and clears them."""
+    v = ctypes.c_uint32(0)
+    _check("mol_take_fault_flags", library().mol_take_fault_flags(ctypes.byref(v)))
+    return int(v.value)
 

@@ -155,6 +155,20 @@ int32_t mol_virtual_topk(const int32_t* topk_ids, const int32_t* lora_ids, int64
   return e == cudaSuccess ? MOL_OK : cuda_fail(e);
 }
 
+int32_t mol_take_fault_flags(uint32_t* flags) {
+  if (!flags) return MOL_ERR_INVALID_ARG;
+  int32_t st = ensure_device();
+  if (st != MOL_OK) return st;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e);
+  unsigned a = 0, b = 0;
+  e = mol::take_lora_faults(&a);
+  if (e == cudaSuccess) e = mol::take_tc_faults(&b);
+  if (e != cudaSuccess) return cuda_fail(e);
+  *flags = a | b;
+  return MOL_OK;
+}
+
 int32_t mol_token_lora_ids(const int32_t* weight_indices, const int32_t* seg_indptr,
                            int32_t num_reqs, int64_t num_tokens, int32_t max_loras,
                            const int32_t* lora_ranks, int32_t* lora_ids, void* stream) {

@@ -107,6 +107,11 @@ cudaError_t launch_shrink_tc(const void* x, int64_t x_stride, int x_div, int K, 
                              const int32_t* ntpp, int64_t capacity, int block_m, int64_t numel,
                              int num_vexperts, float* inter, cudaStream_t stream);
 
+// Fault words of the pipelined kernels (bit 0: a bounded barrier or copy wait
+// ran out); read and cleared by mol_take_fault_flags.
+cudaError_t take_lora_faults(unsigned* out);
+cudaError_t take_tc_faults(unsigned* out);
+
 // Largest contraction width accepted by the shrink (it streams K in chunks).
 constexpr int kShrinkMaxK = 1 << 16;
 

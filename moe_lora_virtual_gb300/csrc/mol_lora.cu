@@ -41,6 +41,13 @@ constexpr uint32_t kWaitPolls = 1u << 22;  // bounded mbarrier waits
 // Faults recorded instead of hanging (see kFaultBulkTimeout).
 __device__ unsigned int g_fault_flags;
 
+cudaError_t take_lora_faults(unsigned* out) {
+  cudaError_t e = cudaMemcpyFromSymbol(out, g_fault_flags, sizeof(unsigned));
+  if (e != cudaSuccess) return e;
+  const unsigned zero = 0;
+  return cudaMemcpyToSymbol(g_fault_flags, &zero, sizeof(unsigned));
+}
+
 // Routing words of one work item as loaded: a producer fetches them one item
 // ahead and evaluates them only when it reaches the item.
 struct Raw {
@@ -388,7 +395,7 @@ MOL_DEV void mask_cols(float4& a, int j, int rl) {
 }
 
 template <int RK, bool EARLY, bool ADAPT>
-__global__ void __launch_bounds__(kExpandThreads)
+__global__ void __launch_bounds__(kExpandThreads, RK == 16 ? 9 : RK == 32 ? 8 : RK == 64 ? 5 : 4)
 lora_expand_kernel(const float* __restrict__ inter, int R, const uint16_t* __restrict__ lora_b,
                    int S, int Ns, float scale, const float* __restrict__ topk_w,
                    const int* __restrict__ sorted_ids, const int* __restrict__ expert_ids,

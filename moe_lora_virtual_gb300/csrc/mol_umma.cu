@@ -65,6 +65,13 @@ struct Geo {
 
 __device__ unsigned int g_tc_fault_flags;
 
+cudaError_t take_tc_faults(unsigned* out) {
+  cudaError_t e = cudaMemcpyFromSymbol(out, g_tc_fault_flags, sizeof(unsigned));
+  if (e != cudaSuccess) return e;
+  const unsigned zero = 0;
+  return cudaMemcpyToSymbol(g_tc_fault_flags, &zero, sizeof(unsigned));
+}
+
 // --- tcgen05 / TMA helpers (inline PTX) ------------------------------------
 
 // Shared-memory matrix descriptor: K-major operand in 8-row groups of 128-byte

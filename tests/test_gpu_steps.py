@@ -296,3 +296,25 @@ def test_invalid_arguments_launch_nothing():
     assert torch.all(inter == 0)
     with pytest.raises(mol.MolError):
         mol.mol_align_block_size(vid, 8191, 48)
+
+
+def test_no_wait_ran_out():
+    """After a forward on every path, no kernel recorded a bounded wait running out."""
+    torch = torch_cuda()
+    mol = mol_lib()
+    mol.mol_take_fault_flags()  # clear whatever earlier tests left
+    dev = torch.device("cuda:0")
+    rng = np.random.default_rng(11)
+    for (T, k, E, BM, K, R, N) in [(23, 8, 16, 16, 2048, 64, 256), (256, 2, 4, 64, 256, 128, 64)]:
+        numel, V = T * k, E
+        topk = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+        lora = np.zeros(T, np.int32)
+        x = to_dev_bf16(oracle.f64_to_bf16(rng.standard_normal((T, K))), dev)
+        A = to_dev_bf16(oracle.f64_to_bf16(rng.standard_normal((V, R, K)) * 0.05), dev)
+        B = to_dev_bf16(oracle.f64_to_bf16(rng.standard_normal((V, 2 * N, R // 2)) * 0.05), dev)
+        out = torch.zeros((numel, 2 * N), dtype=torch.bfloat16, device=dev)
+        routing = mol.alloc_routing(numel, V, BM, dev)
+        inter = torch.empty((numel, R), dtype=torch.float32, device=dev)
+        mol.mol_lora_forward(x, k, to_dev_i32(topk, dev), to_dev_i32(lora, dev), E, 1, A, B, 2, 1.0,
+                             out, routing, inter)
+    assert mol.mol_take_fault_flags() == 0
