@@ -377,7 +377,7 @@ def run_gpu(args):
         sname = f"shrink_{st0.name}"
         flops = 2.0 * pairs_per_step * st0.K * st0.R
         tflops = flops / (kern[sname] * 1e-6) / 1e12
-        tc_path = (st0.R % 128 == 0 and st0.K % 64 == 0 and wl.BM in (64, 128) and ranks is None
+        tc_path = (st0.R % 64 == 0 and st0.K % 64 == 0 and wl.BM in (64, 128) and ranks is None
                    and wl.numel >= 32 * min(wl.numel, wl.V))
         shrink_tensor = dict(kernel=sname, bound="tensor", achieved=round(tflops, 1),
                              peak=peaks["bf16_tflops"], unit="TFLOP/s",

@@ -97,7 +97,7 @@ cudaError_t launch_expand(const float* inter, const void* lora_b, int S, int r, 
 constexpr int kMaxLoraTable = 2048;
 
 // Shrink on tcgen05 tensor cores for batches with many rows per virtual
-// expert: R % 128 == 0, K % 64 == 0, block_m in {64, 128}, at least 32 pairs per
+// expert: R % 64 == 0, K % 64 == 0, block_m in {64, 128}, at least 32 pairs per
 // virtual expert on average, no per-adapter ranks. Reads everything after
 // griddepcontrol.wait.
 bool shrink_tc_fits(int64_t numel, int num_vexperts, int R, int K, int block_m);

@@ -6,7 +6,9 @@
 // fork PR #24 "Root cause" commit, the MoL shrink is a fused-MoE GEMM over the
 // virtual experts with N = S*r and K = the input width; code-review commit,
 // weights laid out [E, N, K]. This kernel computes, per routed block t of
-// virtual expert v and per 128 lora_a rows (mt),
+// virtual expert v and per 128 lora_a rows (mt; when R is not a multiple of
+// 128 the last tile reaches past R into the next expert's rows, or zeros past
+// the last expert: those rows are computed and not stored),
 //   D[j, n] = sum_k lora_a[v, mt*128 + j, k] * x[row(n), k]     (j < 128, n < BM)
 // as tcgen05.mma M=128 x N=BM x K=16 steps (bf16 in, fp32 in tensor memory),
 // and writes inter[pair(n), mt*128 + j] = D[j, n] for the block's real rows.
@@ -329,7 +331,7 @@ lora_shrink_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const int pid = __shfl_sync(0xffffffffu, src, (n0 + e) & 31);
-          if (pid >= 0 && (int64_t)pid < numel) inter[(int64_t)pid * R + j] = val[e];
+          if (j < R && pid >= 0 && (int64_t)pid < numel) inter[(int64_t)pid * R + j] = val[e];
         }
       }
       tc_fence_before();
@@ -366,7 +368,7 @@ int tc_device_sms() {
 }  // namespace
 
 bool shrink_tc_fits(int64_t numel, int num_vexperts, int R, int K, int block_m) {
-  if (numel <= 0 || R % tc::kM != 0 || K % tc::kKStep != 0) return false;
+  if (numel <= 0 || R % 64 != 0 || K % tc::kKStep != 0) return false;
   if (block_m != 64 && block_m != 128) return false;
   // many rows per virtual expert: on average at least 32 pairs each
   return numel >= 32 * std::min<int64_t>(numel, num_vexperts);
@@ -407,7 +409,7 @@ cudaError_t launch_shrink_tc(const void* x, int64_t x_stride, int x_div, int K, 
                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
-  const int mtiles = R / tc::kM;
+  const int mtiles = (R + tc::kM - 1) / tc::kM;
   const int64_t n_items = nblk * mtiles;
   const uint16_t* xp = static_cast<const uint16_t*>(x);
   if (block_m == 64) {

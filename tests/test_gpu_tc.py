@@ -1,7 +1,7 @@
 """The tensor-core (tcgen05) shrink against the oracle.
 
 It runs when every routed block is full enough for a real contraction: at
-least 32 pairs per virtual expert on average, R a multiple of 128, K a
+least 32 pairs per virtual expert on average, R a multiple of 64, K a
 multiple of 64 and BLOCK_M 64 or 128 (one adapter for every token, as in the
 `dense` workload). Shapes here take that path with several k stages, several
 128-row tiles of R, partial blocks, sentinels and both BLOCK_M values.
@@ -29,6 +29,8 @@ CASES = [
     (200, 8, 16, 64, 1024, 2, 64, 40, True, 0.0),
     (130, 2, 2, 128, 128, 1, 128, 32, False, 0.2),
     (256, 2, 4, 64, 64, 2, 64, 32, True, 0.0),      # one k stage
+    (300, 4, 8, 64, 512, 1, 64, 64, False, 0.1),    # R = 64: half a tile
+    (256, 3, 4, 64, 256, 3, 64, 48, True, 0.0),     # R = 192: one and a half tiles
 ]
 
 
@@ -40,7 +42,7 @@ def test_tc_shrink_matches_oracle(case):
     T, k, E, BM, K, S, r, Ns, token_rows, sent = case
     rng = np.random.default_rng(sum(case[:8]))
     L, V, R, N, numel = 1, E, S * r, S * Ns, T * k
-    assert numel >= 32 * min(numel, V) and R % 128 == 0 and K % 64 == 0
+    assert numel >= 32 * min(numel, V) and R % 64 == 0 and K % 64 == 0
     topk = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
     topk[rng.random((T, k)) < sent] = -1
     lora = np.zeros(T, np.int32)
