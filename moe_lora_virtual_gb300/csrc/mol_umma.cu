@@ -267,9 +267,10 @@ lora_shrink_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
     // ------------------------------------------------------------ x gather
     // Eight lanes cover one row's 128 bytes, so each instruction of a warp
     // moves four whole rows (full lines); thread g takes chunk g % 8 of rows
-    // g / 8, g / 8 + 16, ... .
+    // g / 8, g / 8 + kRowStep, ... .
     const int g = tid - 64;
-    constexpr int kRowsPerThr = BN / 16;
+    constexpr int kRowStep = kGatherWarps * 32 / 8;
+    constexpr int kRowsPerThr = BN / kRowStep;
     const int c = g & 7, r0 = g >> 3;
     uint32_t q = 0;
     for (int64_t it = blockIdx.x; it < n_items && !fault; it += Gs) {
@@ -280,7 +281,7 @@ lora_shrink_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
       uint32_t nbytes[kRowsPerThr];
 #pragma unroll
       for (int i = 0; i < kRowsPerThr; ++i) {
-        const int pid = __ldg(sorted_ids + t * BN + r0 + 16 * i);
+        const int pid = __ldg(sorted_ids + t * BN + r0 + kRowStep * i);
         const bool ok = pid >= 0 && (int64_t)pid < numel;
         src[i] = (ok ? x + (int64_t)(pid / x_div) * x_stride : x) + c * 8;
         nbytes[i] = ok ? 16u : 0u;
@@ -294,7 +295,7 @@ lora_shrink_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
         unsigned char* tile = stageA(q) + kATile;
 #pragma unroll
         for (int i = 0; i < kRowsPerThr; ++i) {
-          const int r = r0 + 16 * i;
+          const int r = r0 + kRowStep * i;
           cp_async16_zfill(tile + r * 128 + ((c ^ (r & 7)) << 4), src[i] + ks * kKStep, nbytes[i]);
         }
         cp_async_arrive_noinc(&full[s]);
