@@ -51,17 +51,7 @@ MOL_DEV uint2 ld_stream8(const void* p) {
   asm("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
   return r;
 }
-// 16-byte load of data other blocks reuse (activations, intermediates).
-MOL_DEV uint4 ld_keep16(const void* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
-MOL_DEV float4 ld_keep_f4(const float* p) { return __ldg(reinterpret_cast<const float4*>(p)); }
 // 16-byte load that bypasses L1 (data written by the preceding grid).
-MOL_DEV uint4 ld_l2_16(const void* p) {
-  uint4 r;
-  asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
-  return r;
-}
 MOL_DEV float4 ld_l2_f4(const float* p) {
   float4 r;
   asm volatile("ld.global.cg.v4.f32 {%0,%1,%2,%3}, [%4];"
