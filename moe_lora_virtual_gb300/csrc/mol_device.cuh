@@ -99,11 +99,24 @@ MOL_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait: gives up after `max_iter` polls (each poll may suspend the
-// thread for a short hardware-defined time) and returns false.
+MOL_DEV uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Longest time a barrier wait may take before it gives up (the waits inside
+// these kernels last microseconds; no kernel runs for more than milliseconds).
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+// Bounded wait: gives up, returning false, after `max_iter` polls or one
+// second of wall-clock time, whichever comes first (a poll may suspend the
+// thread for a hardware-defined time, so the clock bounds the total).
 MOL_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t max_iter) {
-  for (uint32_t i = 0; i < max_iter; ++i)
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 0; i < max_iter; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  }
   return false;
 }
 
