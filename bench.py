@@ -369,7 +369,8 @@ def run_gpu(args):
         achieved = nbytes / (us * 1e-6) / 1e9
         roof = dict(kernel=name, bound="hbm", achieved=round(achieved, 1), peak=peaks["hbm_gbs"],
                     unit="GB/s", frac=round(achieved / peaks["hbm_gbs"], 4),
-                    traffic=TRAFFIC.get((args.config, name)), bytes_per_launch=int(nbytes),
+                    traffic=None if ranks is not None else TRAFFIC.get((args.config, name)),
+                    bytes_per_launch=int(nbytes),
                     us_per_launch=round(us, 3), peak_source=peaks["source"])
         # the first stage's shrink against the bf16 tensor peak (a real dense
         # contraction only when the routed blocks are full, as in `dense`)

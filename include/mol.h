@@ -177,9 +177,10 @@ int32_t mol_align_block_size_noalloc(const int32_t* vtopk_ids, int64_t numel,
  *   lora_ranks   int32 [num_vexperts / num_experts] or NULL (all adapters of
  *                rank `rank`). The adapter of virtual expert v is
  *                v / num_experts. With rank r_l (clamped to [0, rank]) the
- *                adapter's weights are zero padding past r_l: inter columns
- *                [s*rank + r_l, (s+1)*rank) of each slice are written as 0 and
- *                those lora_a rows are not read; r_l = 0 writes nothing.
+ *                adapter's lora_a rows past r_l are padding: inter columns
+ *                [s*rank + r_l, (s+1)*rank) of each slice are written as 0,
+ *                whatever those rows hold (8-row groups wholly past r_l are
+ *                not read); r_l = 0 writes nothing.
  *                Needs rank % 8 == 0 and num_vexperts / num_experts <= 2048;
  *                read like lora_a (not produced by the kernel right before).
  *   num_experts  routed experts (used only with lora_ranks).
@@ -210,9 +211,11 @@ int32_t mol_lora_shrink(const void* x, int64_t x_row_stride, int32_t x_row_div, 
  * out_row_stride >= num_slices * slice_n, inter/lora_b/out 16-byte aligned.
  * Per-adapter rank and scaling (adapter of v = v / num_experts):
  *   lora_ranks     int32 [num_vexperts / num_experts] or NULL: the sum runs over
- *                  j < r_l (clamped to [0, rank]); r_l = 0 leaves the pair's
- *                  output rows bit-unchanged. Needs rank % 8 == 0 and at most
- *                  2048 adapters.
+ *                  j < r_l (clamped to [0, rank]), so inter columns and lora_b
+ *                  columns at or past r_l take no part, whatever they hold
+ *                  (8-column groups of lora_b wholly past r_l are not read);
+ *                  r_l = 0 leaves the pair's output rows bit-unchanged. Needs
+ *                  rank % 8 == 0 and at most 2048 adapters.
  *   lora_scalings  fp32 [num_vexperts / num_experts] or NULL: the delta is
  *                  multiplied by scale * lora_scalings[adapter].
  *   num_experts    routed experts (used only with either array).

@@ -393,6 +393,17 @@ MOL_DEV void mask_cols(float4& a, int j, int rl) {
   if (j + 2 >= rl) a.z = 0.f;
   if (j + 3 >= rl) a.w = 0.f;
 }
+// Zeroes the bf16 elements of b (columns j .. j+7, two per word, lower column
+// in the low half) at or past column rl.
+MOL_DEV void mask_bf16x8(uint4& b, int j, int rl) {
+  uint32_t* w = reinterpret_cast<uint32_t*>(&b);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int c = j + 2 * q;
+    if (c >= rl) w[q] = 0u;
+    else if (c + 1 >= rl) w[q] &= 0xFFFFu;
+  }
+}
 
 template <int RK, bool EARLY, bool ADAPT>
 __global__ void __launch_bounds__(kExpandThreads, RK == 16 ? 9 : RK == 32 ? 8 : RK == 64 ? 5 : 4)
@@ -429,6 +440,9 @@ lora_expand_kernel(const float* __restrict__ inter, int R, const uint16_t* __res
     if (lora_ranks) rk_raw = __ldg(lora_ranks + v / num_experts);
     if (lora_scalings) scl = __ldg(lora_scalings + v / num_experts);
   }
+  // rank 0: the adapter writes no delta; past rank rl the intermediate and
+  // the weight columns are padding and take no part in the sum
+  const int rl = rk_raw < 0 ? 0 : (rk_raw > RK ? RK : rk_raw);
   const int c = compact_block_rows(slot, numel, rows, wcnt);
   if (c == 0) return;
 
@@ -447,11 +461,14 @@ lora_expand_kernel(const float* __restrict__ inter, int R, const uint16_t* __res
   for (int kb = 0; kb < KB; ++kb)
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
+      // with ranks, weight columns wholly past rl are not read
+      const int j0 = K16 ? 4 * tq : kb * 32 + 8 * tq;
+      const bool kin = bvalid && (!ADAPT || j0 < rl);
       if constexpr (K16) {
-        const uint2 q = bvalid ? ld_stream8(bw + 2 * u * RK + 4 * tq) : make_uint2(0, 0);
+        const uint2 q = kin ? ld_stream8(bw + 2 * u * RK + 4 * tq) : make_uint2(0, 0);
         bf[kb][u] = make_uint4(q.x, q.y, 0, 0);
       } else {
-        bf[kb][u] = bvalid ? ld_stream16(bw + 2 * u * RK + kb * 32 + 8 * tq) : make_uint4(0, 0, 0, 0);
+        bf[kb][u] = kin ? ld_stream16(bw + 2 * u * RK + kb * 32 + 8 * tq) : make_uint4(0, 0, 0, 0);
       }
     }
 
@@ -468,9 +485,13 @@ lora_expand_kernel(const float* __restrict__ inter, int R, const uint16_t* __res
     pdl_wait();  // the intermediate comes from the shrink that precedes this kernel
     pdl_launch_dependents();
   }
-  // rank 0: the adapter writes no delta; past rank rl the intermediate is padding
-  const int rl = rk_raw < 0 ? 0 : (rk_raw > RK ? RK : rk_raw);
   if (ADAPT && rl == 0) return;
+  if (ADAPT && rl < RK) {  // the chunk that straddles rl keeps only its columns below rl
+#pragma unroll
+    for (int kb = 0; kb < KB; ++kb)
+#pragma unroll
+      for (int u = 0; u < 4; ++u) mask_bf16x8(bf[kb][u], K16 ? 4 * tq : kb * 32 + 8 * tq, rl);
+  }
   const float scale_v = ADAPT ? scale * scl : scale;
 
   for (int m0 = 0; m0 < c; m0 += 16) {

@@ -68,6 +68,10 @@ CASES = [
     (30, 6, 5, 3, 64, 520, 2, 64, 72, True, [40, 64, 16]),
     (9, 8, 4, 2, 16, 4104, 1, 128, 136, True, [128, 56]),
     (200, 8, 8, 2, 128, 256, 2, 32, 48, False, [16, 32]),
+    # ranks that are not multiples of 8: weight chunks straddle the rank
+    (40, 8, 8, 4, 16, 1032, 2, 32, 104, True, [5, 32, 19, 1]),
+    (24, 4, 6, 3, 32, 776, 1, 16, 64, False, [3, 13, 16]),
+    (16, 8, 8, 2, 64, 1544, 2, 64, 40, True, [33, 61]),
 ]
 
 
@@ -137,6 +141,64 @@ def test_ranks_and_scalings(case, path):
             rl = c["ranks"][vt[i] // E]
             for sl in range(S):
                 assert np.all(g_inter[i, sl * r + rl:(sl + 1) * r] == 0)
+
+
+@pytest.mark.parametrize("case", CASES)
+def test_padding_past_rank_is_ignored(case):
+    """NaN in lora_a rows and lora_b columns past each adapter's rank, and (for the expand alone)
+    in the intermediate columns past it, leaves every result as the oracle's, which reads none
+    of them."""
+    torch = torch_cuda()
+    mol = mol_lib()
+    dev = torch.device("cuda:0")
+    c = _setup(case, 11 + sum(case[:9]))
+    E, L, V, BM, numel, S, r, Ns = c["E"], c["L"], c["V"], c["BM"], c["numel"], c["S"], c["r"], c["Ns"]
+    A, B = c["A"].copy(), c["B"].copy()
+    for v in range(V):
+        rl = int(c["ranks"][v // E])
+        for sl in range(S):
+            A[v, sl * r + rl:(sl + 1) * r, :] = 0x7FC0
+        B[v, :, rl:] = 0x7FC0
+    vt = oracle.virtual_topk(c["topk"], c["lora"], E, L).reshape(-1)
+    s, e, n = oracle.align_block_size(vt, V, BM)
+    ref_inter = oracle.lora_shrink(c["x"], c["xdiv"], A, s, e, n, BM, numel,
+                                   np.full((numel, c["R"]), np.nan, np.float32), S, E, c["ranks"])
+    ref_out = oracle.lora_expand(ref_inter, B, S, r, Ns, 0.5, None, s, e, n, BM, numel, c["out0"],
+                                 num_experts=E, lora_ranks=c["ranks"], lora_scalings=c["scalings"])
+    pairs = valid_pairs(s, e, n, BM, numel)
+    live = np.array([i for i in pairs if c["ranks"][vt[i] // E] > 0], np.int64)
+    assert live.size > 0
+
+    routing = mol.alloc_routing(numel, V, BM, dev)
+    xd, Ad, Bd = to_dev_bf16(c["x"], dev), to_dev_bf16(A, dev), to_dev_bf16(B, dev)
+    ranks_d, scal_d = to_dev_i32(c["ranks"], dev), torch.from_numpy(c["scalings"]).to(dev)
+    out = to_dev_bf16(c["out0"], dev)
+    inter = torch.full((numel, c["R"]), float("nan"), dtype=torch.float32, device=dev)
+    mol.mol_lora_forward(xd, c["xdiv"], to_dev_i32(c["topk"], dev), to_dev_i32(c["lora"], dev),
+                         E, L, Ad, Bd, S, 0.5, out, routing, inter, compute_routing=True,
+                         workspace=mol.alloc_workspace(numel, V, BM, dev),
+                         lora_ranks=ranks_d, lora_scalings=scal_d)
+    torch.cuda.synchronize()
+    check_inter(inter.cpu().numpy(), ref_inter, live)
+    check_out(bf16_host(out), ref_out, live)
+
+    # the expand alone, on an intermediate whose columns past each rank hold NaN
+    poisoned = ref_inter.copy()
+    for i in live:
+        rl = int(c["ranks"][vt[i] // E])
+        for sl in range(S):
+            poisoned[i, sl * r + rl:(sl + 1) * r] = np.nan
+    ref_out2 = oracle.lora_expand(poisoned, B, S, r, Ns, 0.5, None, s, e, n, BM, numel, c["out0"],
+                                  num_experts=E, lora_ranks=c["ranks"], lora_scalings=c["scalings"])
+    assert np.array_equal(ref_out2, ref_out)
+    out2 = to_dev_bf16(c["out0"], dev)
+    mol.mol_lora_expand(torch.from_numpy(poisoned).to(dev), Bd, S, 0.5, routing, out2,
+                        lora_ranks=ranks_d, lora_scalings=scal_d, num_experts=E)
+    torch.cuda.synchronize()
+    g_out2 = bf16_host(out2)
+    check_out(g_out2, ref_out, live)
+    untouched = np.setdiff1d(np.arange(numel), live)
+    assert np.array_equal(g_out2[untouched], c["out0"][untouched])
 
 
 def test_full_ranks_unit_scalings_bit_identical():

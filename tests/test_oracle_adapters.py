@@ -135,6 +135,30 @@ def test_rank_equals_zero_padded_weights(seed):
     assert np.array_equal(ranked["out"], padded["out"])
 
 
+@pytest.mark.parametrize("seed", [0, 1])
+def test_weights_past_rank_take_no_part(seed):
+    """Weight rows of lora_a and columns of lora_b past an adapter's rank are padding: NaN
+    there changes nothing (the sums run over j < r_l only)."""
+    wl, li, st, routing = _stage("tiny", seed)
+    rng = np.random.default_rng(200 + seed)
+    r, S = st.stage.r, st.stage.S
+    ranks = [0, int(rng.integers(1, r))]
+    A, B = st.A.host_all().copy(), st.B.host_all().copy()
+    nan_bits = np.uint16(0x7FC0)
+    for v in range(wl.V):
+        rl = ranks[v // wl.E]
+        for s in range(S):
+            A[v, s * r + rl:(s + 1) * r, :] = nan_bits
+        B[v, :, rl:] = nan_bits
+    clean = _run(wl, li, st, routing, ranks=ranks)
+    poisoned = _run(wl, li, st, routing, ranks=ranks, A=A, B=B)
+    assert np.array_equal(clean["inter"], poisoned["inter"], equal_nan=True)
+    assert np.array_equal(clean["out"], poisoned["out"])
+    vt = routing[0]
+    live = vt >= wl.E  # adapter 1, rank >= 1
+    assert live.any() and not np.any(np.isnan(poisoned["inter"][live]))
+
+
 def test_rank_zero_writes_nothing():
     wl, li, st, routing = _stage("tiny", 0)
     res = _run(wl, li, st, routing, ranks=[0, st.stage.r])
