@@ -128,6 +128,16 @@ MOL_DEV void named_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 MOL_DEV uint4 lds16(const void* p) { return *reinterpret_cast<const uint4*>(p); }
+MOL_DEV uint2 lds8(const void* p) { return *reinterpret_cast<const uint2*>(p); }
+// 16-byte copy global -> shared through L2 (cp.async): src_bytes of 16 are
+// read, the rest of the 16 bytes zero-filled (0: nothing is read).
+MOL_DEV void cp_async16_zfill(void* dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+// Waits until every cp.async this thread issued has landed.
+MOL_DEV void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // Error bits a kernel records instead of hanging or trapping.
 constexpr unsigned kFaultBulkTimeout = 1u;

@@ -567,6 +567,178 @@ lora_expand_kernel(const float* __restrict__ inter, int R, const uint16_t* __res
   }
 }
 
+// Staged expand, rank 16 or 32, no adapter arrays. One item = (routed block
+// t, slice s, 256 output columns). One thread copies the item's lora_b rows
+// (256 x RK bf16, contiguous in [V, N, r]) into shared memory with a bulk
+// copy, and every thread copies its pieces of the output rows to update with
+// cp.async, so neither takes registers while in flight; each warp covers 64
+// columns (two 32-column groups) with the intermediate it loads once. At 64
+// registers eight blocks fit an SM, enough to run the decode expands in about
+// one wave. Fragment layout, MMA order per accumulator and rounding are those
+// of lora_expand_kernel, so both kernels give bit-identical outputs.
+constexpr int kStCols = 256;
+constexpr int kStGroups = kStCols / (kExpandThreads / 32) / 32;  // column groups per warp
+constexpr int kStOutPitch = kStCols + 32;  // staged output row, elements (64-byte skew per row)
+
+template <int RK, bool EARLY>
+__global__ void __launch_bounds__(kExpandThreads, 8)
+lora_expand_st_kernel(const float* __restrict__ inter, int R, const uint16_t* __restrict__ lora_b,
+                      int S, int Ns, float scale, const float* __restrict__ topk_w,
+                      const int* __restrict__ sorted_ids, const int* __restrict__ expert_ids,
+                      const int* __restrict__ ntpp_ptr, int block_m, int64_t numel,
+                      int num_vexperts, uint16_t* __restrict__ out, int64_t out_stride,
+                      int chunks_per_slice) {
+  static_assert(RK == 16 || RK == 32, "staged expand: rank 16 or 32");
+  constexpr bool K16 = (RK == 16);
+  __shared__ __align__(128) uint16_t wsm[kStCols * RK];
+  __shared__ __align__(16) uint16_t osm[16 * kStOutPitch];  // output rows of one row tile
+  __shared__ uint64_t wbar;
+  __shared__ int rows[128];
+  __shared__ int wcnt[kExpandThreads / 32];
+
+  const int tid = threadIdx.x;
+  const int per_block = S * chunks_per_slice;
+  const int t = blockIdx.x / per_block;
+  const int rem = blockIdx.x - t * per_block;
+  const int s = rem / chunks_per_slice;
+  const int chunk = rem - s * chunks_per_slice;
+  if (!EARLY) {
+    pdl_wait();
+    pdl_launch_dependents();
+  }
+  const int ntpp = __ldg(ntpp_ptr);
+  const int v = __ldg(expert_ids + t);
+  const int slot = tid < block_m ? __ldg(sorted_ids + (int64_t)t * block_m + tid) : -1;
+  if ((int64_t)t * block_m >= ntpp || v < 0 || v >= num_vexperts) return;
+  if (tid == 0) {
+    mbar_init(&wbar, 1);
+    fence_mbar_init();
+  }
+  const int c = compact_block_rows(slot, numel, rows, wcnt);  // its barriers publish the init
+  if (c == 0) return;
+  // columns [col0, col0 + ncols) of the slice; ncols > 0 (chunk < ceil(Ns / kStCols)) and a
+  // multiple of 8, so the copy is a multiple of 16 bytes from a 16-byte aligned row
+  const int col0 = chunk * kStCols;
+  const int ncols = min(kStCols, Ns - col0);
+  if (tid == 0) {
+    const uint32_t bytes = (uint32_t)ncols * RK * 2;
+    mbar_arrive_expect_tx(&wbar, bytes);
+    bulk_g2s(wsm, lora_b + ((int64_t)v * S * Ns + (int64_t)s * Ns + col0) * RK, bytes, &wbar);
+  }
+
+  const int lane = tid & 31, warp = tid >> 5, g = lane >> 2, tq = lane & 3;
+  const int wcol = warp * 32 * kStGroups;  // the warp's first column inside the item
+  const float4 zf = make_float4(0.f, 0.f, 0.f, 0.f);
+  const uint4 zu = make_uint4(0, 0, 0, 0);
+  int i0 = g < c ? rows[g] : -1;
+  int i1 = 8 + g < c ? rows[8 + g] : -1;
+  // output rows to update, every column group of the warp (thread tq: 8 columns
+  // each), staged at osm[(8 * hh + g) * kStOutPitch + column inside the item];
+  // each thread later reads back only what it copied itself
+  auto osm_at = [&](int hh, int col) { return osm + (8 * hh + g) * kStOutPitch + col; };
+  auto load_out = [&]() {
+#pragma unroll
+    for (int cg = 0; cg < kStGroups; ++cg) {
+      const int col = wcol + cg * 32 + 8 * tq;
+      const bool ok = col0 + col < Ns;
+      const int64_t oc = (int64_t)s * Ns + col0 + col;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int i = hh ? i1 : i0;
+        if (ok && i >= 0) cp_async16_zfill(osm_at(hh, col), out + (int64_t)i * out_stride + oc, 16u);
+      }
+    }
+  };
+  load_out();
+  if (EARLY) {
+    pdl_wait();  // the intermediate comes from the shrink that precedes this kernel
+    pdl_launch_dependents();
+  }
+
+  bool landed = false;
+  for (int m0 = 0; m0 < c; m0 += 16) {
+    if (m0 > 0) {
+      i0 = m0 + g < c ? rows[m0 + g] : -1;
+      i1 = m0 + 8 + g < c ? rows[m0 + 8 + g] : -1;
+      load_out();
+    }
+    // the intermediate fragments, split into bf16 head and tail, serve every column group
+    const int koff = s * RK + (K16 ? 4 * tq : 8 * tq);
+    const float* p0 = inter + (int64_t)(i0 >= 0 ? i0 : 0) * R + koff;
+    const float* p1 = inter + (int64_t)(i1 >= 0 ? i1 : 0) * R + koff;
+    uint32_t h[8], l[8];
+    {
+      const float4 a0 = i0 >= 0 ? ld_l2_f4(p0) : zf;
+      const float4 a1 = i1 >= 0 ? ld_l2_f4(p1) : zf;
+      split_bf16x2(a0.x, a0.y, h[0], l[0]);
+      split_bf16x2(a1.x, a1.y, h[1], l[1]);
+      split_bf16x2(a0.z, a0.w, h[2], l[2]);
+      split_bf16x2(a1.z, a1.w, h[3], l[3]);
+    }
+    if constexpr (!K16) {
+      const float4 b0 = i0 >= 0 ? ld_l2_f4(p0 + 4) : zf;
+      const float4 b1 = i1 >= 0 ? ld_l2_f4(p1 + 4) : zf;
+      split_bf16x2(b0.x, b0.y, h[4], l[4]);
+      split_bf16x2(b1.x, b1.y, h[5], l[5]);
+      split_bf16x2(b0.z, b0.w, h[6], l[6]);
+      split_bf16x2(b1.z, b1.w, h[7], l[7]);
+    }
+    if (!landed) {  // every thread sees the weight copy land before it reads the tile
+      if (!mbar_wait(&wbar, 0, kWaitPolls)) {
+        atomicOr(&g_fault_flags, kFaultBulkTimeout);
+        cp_async_wait_all();
+        return;
+      }
+      landed = true;
+    }
+    cp_async_wait_all();  // this thread's output pieces
+#pragma unroll
+    for (int cg = 0; cg < kStGroups; ++cg) {
+      const int nb = wcol + cg * 32;  // the group's first column inside the item
+      if (nb >= ncols) break;         // warp-uniform
+      float acc[4][4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) acc[u][0] = acc[u][1] = acc[u][2] = acc[u][3] = 0.f;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        // weight row of output column nb + 8*(g/2) + 2u + (g%2): thread tq ends with
+        // columns nb + 8tq .. nb + 8tq + 7
+        const int wr = nb + 8 * (g >> 1) + 2 * u + (g & 1);
+        const bool bv = wr < ncols;
+        if constexpr (K16) {
+          const uint2 q = bv ? lds8(wsm + wr * RK + 4 * tq) : make_uint2(0, 0);
+          mma_16816(acc[u], h[0], h[1], h[2], h[3], q.x, q.y);
+          mma_16816(acc[u], l[0], l[1], l[2], l[3], q.x, q.y);
+        } else {
+          const uint4 q = bv ? lds16(wsm + wr * RK + 8 * tq) : zu;
+          mma_16816(acc[u], h[0], h[1], h[2], h[3], q.x, q.y);
+          mma_16816(acc[u], l[0], l[1], l[2], l[3], q.x, q.y);
+          mma_16816(acc[u], h[4], h[5], h[6], h[7], q.z, q.w);
+          mma_16816(acc[u], l[4], l[5], l[6], l[7], q.z, q.w);
+        }
+      }
+      if (nb + 8 * tq < ncols) {
+        const int64_t oc = (int64_t)s * Ns + col0 + nb + 8 * tq;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int i = hh ? i1 : i0;
+          if (i < 0) continue;
+          const float sw = topk_w ? scale * __ldg(topk_w + i) : scale;
+          uint4 ov = lds16(osm_at(hh, nb + 8 * tq));
+          uint32_t* ow = reinterpret_cast<uint32_t*>(&ov);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float lo = fmaf(sw, acc[u][2 * hh], bf16_lo(ow[u]));
+            const float hi = fmaf(sw, acc[u][2 * hh + 1], bf16_hi(ow[u]));
+            ow[u] = pack_bf16x2(lo, hi);
+          }
+          *reinterpret_cast<uint4*>(out + (int64_t)i * out_stride + oc) = ov;
+        }
+      }
+    }
+  }
+}
+
 static int device_sms() {
   static int cache[64] = {0};
   int dev = 0;
@@ -633,11 +805,22 @@ cudaError_t launch_expand(const float* inter, const void* lora_b, int S, int r, 
                           const int32_t* lora_ranks, const float* lora_scalings, int num_experts) {
   const int64_t nblk = capacity / block_m;
   if (numel == 0 || nblk == 0) return cudaSuccess;
-  const int cps = (Ns + kExpandCols - 1) / kExpandCols;
-  const dim3 grid((unsigned)(nblk * S * cps));
   const int R = S * r;
   const uint16_t* b = static_cast<const uint16_t*>(lora_b);
   uint16_t* o = static_cast<uint16_t*>(out);
+  if (!lora_ranks && !lora_scalings && (r == 16 || r == 32)) {
+    const int cps_st = (Ns + kStCols - 1) / kStCols;
+    const dim3 grid_st((unsigned)(nblk * S * cps_st));
+#define MOL_EXPAND_ST(RK, E)                                                                    \
+  launch_pdl(lora_expand_st_kernel<RK, E>, grid_st, dim3(kExpandThreads), 0, stream, inter, R, \
+             b, S, Ns, scale, topk_weights, sorted_ids, expert_ids, ntpp, block_m, numel,       \
+             num_vexperts, o, out_stride, cps_st)
+    if (r == 16) return early ? MOL_EXPAND_ST(16, true) : MOL_EXPAND_ST(16, false);
+    return early ? MOL_EXPAND_ST(32, true) : MOL_EXPAND_ST(32, false);
+#undef MOL_EXPAND_ST
+  }
+  const int cps = (Ns + kExpandCols - 1) / kExpandCols;
+  const dim3 grid((unsigned)(nblk * S * cps));
 #define MOL_EXPAND_CASE(RK)                                                                     \
   case RK:                                                                                      \
     return early ? expand_rk<RK, true>(grid, stream, inter, R, b, S, Ns, scale, topk_weights,   \

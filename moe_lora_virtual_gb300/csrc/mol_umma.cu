@@ -93,18 +93,12 @@ MOL_DEV void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
 }
-MOL_DEV void cp_async16_zfill(void* dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
-               "r"(src_bytes)
-               : "memory");
-}
 // Arrives on `bar` once every cp.async this thread issued so far has landed
 // (the barrier's expected count includes this arrival).
 MOL_DEV void cp_async_arrive_noinc(uint64_t* bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
 }
-MOL_DEV void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 MOL_DEV void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 MOL_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 MOL_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }

@@ -119,7 +119,9 @@ SHAPES = [
     (64, 8, 2, 2, 32, 512, 1, 128, 72, False, 8, 8, True, 0.0),
     (97, 3, 5, 3, 16, 8, 2, 16, 8, False, 0, 0, False, 0.5),
     (12, 4, 3, 2, 16, 7168, 1, 16, 64, True, 0, 0, False, 0.0),    # one weight-tile buffer
-    (40, 8, 6, 2, 32, 4096, 2, 32, 96, True, 0, 0, False, 0.1),    # two buffers, largest K
+    (40, 8, 6, 2, 32, 4096, 2, 32, 96, True, 0, 0, False, 0.1),    # two buffers
+    (6, 2, 2, 1, 16, 65536, 1, 16, 16, True, 8, 0, False, 0.0),    # largest K of the contract
+    (20, 2, 2, 1, 32, 64, 8, 128, 16, False, 0, 8, False, 0.0),    # largest R = 8 x 128
 ]
 
 

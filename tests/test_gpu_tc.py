@@ -31,6 +31,7 @@ CASES = [
     (256, 2, 4, 64, 64, 2, 64, 32, True, 0.0),      # one k stage
     (300, 4, 8, 64, 512, 1, 64, 64, False, 0.1),    # R = 64: half a tile
     (256, 3, 4, 64, 256, 3, 64, 48, True, 0.0),     # R = 192: one and a half tiles
+    (256, 2, 4, 64, 8192, 1, 64, 32, True, 0.0),    # long K: 128 stages per item
 ]
 
 
