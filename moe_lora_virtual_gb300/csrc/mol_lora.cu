@@ -581,15 +581,16 @@ constexpr int kStGroups = kStCols / (kExpandThreads / 32) / 32;  // column group
 constexpr int kStOutPitch = kStCols + 32;  // staged output row, elements (64-byte skew per row)
 
 template <int RK, bool EARLY>
-__global__ void __launch_bounds__(kExpandThreads, 8)
+__global__ void __launch_bounds__(kExpandThreads, RK == 64 ? 5 : 8)
 lora_expand_st_kernel(const float* __restrict__ inter, int R, const uint16_t* __restrict__ lora_b,
                       int S, int Ns, float scale, const float* __restrict__ topk_w,
                       const int* __restrict__ sorted_ids, const int* __restrict__ expert_ids,
                       const int* __restrict__ ntpp_ptr, int block_m, int64_t numel,
                       int num_vexperts, uint16_t* __restrict__ out, int64_t out_stride,
                       int chunks_per_slice) {
-  static_assert(RK == 16 || RK == 32, "staged expand: rank 16 or 32");
+  static_assert(RK == 16 || RK == 32 || RK == 64, "staged expand: rank 16, 32 or 64");
   constexpr bool K16 = (RK == 16);
+  constexpr int KB = K16 ? 1 : RK / 32;  // k blocks (32 wide, or one 16-wide block)
   __shared__ __align__(128) uint16_t wsm[kStCols * RK];
   __shared__ __align__(16) uint16_t osm[16 * kStOutPitch];  // output rows of one row tile
   __shared__ uint64_t wbar;
@@ -666,22 +667,23 @@ lora_expand_st_kernel(const float* __restrict__ inter, int R, const uint16_t* __
     const int koff = s * RK + (K16 ? 4 * tq : 8 * tq);
     const float* p0 = inter + (int64_t)(i0 >= 0 ? i0 : 0) * R + koff;
     const float* p1 = inter + (int64_t)(i1 >= 0 ? i1 : 0) * R + koff;
-    uint32_t h[8], l[8];
-    {
-      const float4 a0 = i0 >= 0 ? ld_l2_f4(p0) : zf;
-      const float4 a1 = i1 >= 0 ? ld_l2_f4(p1) : zf;
-      split_bf16x2(a0.x, a0.y, h[0], l[0]);
-      split_bf16x2(a1.x, a1.y, h[1], l[1]);
-      split_bf16x2(a0.z, a0.w, h[2], l[2]);
-      split_bf16x2(a1.z, a1.w, h[3], l[3]);
-    }
-    if constexpr (!K16) {
-      const float4 b0 = i0 >= 0 ? ld_l2_f4(p0 + 4) : zf;
-      const float4 b1 = i1 >= 0 ? ld_l2_f4(p1 + 4) : zf;
-      split_bf16x2(b0.x, b0.y, h[4], l[4]);
-      split_bf16x2(b1.x, b1.y, h[5], l[5]);
-      split_bf16x2(b0.z, b0.w, h[6], l[6]);
-      split_bf16x2(b1.z, b1.w, h[7], l[7]);
+    uint32_t h[KB][8], l[KB][8];
+#pragma unroll
+    for (int kb = 0; kb < KB; ++kb) {
+      const float4 a0 = i0 >= 0 ? ld_l2_f4(p0 + kb * 32) : zf;
+      const float4 a1 = i1 >= 0 ? ld_l2_f4(p1 + kb * 32) : zf;
+      split_bf16x2(a0.x, a0.y, h[kb][0], l[kb][0]);
+      split_bf16x2(a1.x, a1.y, h[kb][1], l[kb][1]);
+      split_bf16x2(a0.z, a0.w, h[kb][2], l[kb][2]);
+      split_bf16x2(a1.z, a1.w, h[kb][3], l[kb][3]);
+      if constexpr (!K16) {
+        const float4 b0 = i0 >= 0 ? ld_l2_f4(p0 + kb * 32 + 4) : zf;
+        const float4 b1 = i1 >= 0 ? ld_l2_f4(p1 + kb * 32 + 4) : zf;
+        split_bf16x2(b0.x, b0.y, h[kb][4], l[kb][4]);
+        split_bf16x2(b1.x, b1.y, h[kb][5], l[kb][5]);
+        split_bf16x2(b0.z, b0.w, h[kb][6], l[kb][6]);
+        split_bf16x2(b1.z, b1.w, h[kb][7], l[kb][7]);
+      }
     }
     if (!landed) {  // every thread sees the weight copy land before it reads the tile
       if (!mbar_wait(&wbar, 0, kWaitPolls)) {
@@ -707,14 +709,17 @@ lora_expand_st_kernel(const float* __restrict__ inter, int R, const uint16_t* __
         const bool bv = wr < ncols;
         if constexpr (K16) {
           const uint2 q = bv ? lds8(wsm + wr * RK + 4 * tq) : make_uint2(0, 0);
-          mma_16816(acc[u], h[0], h[1], h[2], h[3], q.x, q.y);
-          mma_16816(acc[u], l[0], l[1], l[2], l[3], q.x, q.y);
+          mma_16816(acc[u], h[0][0], h[0][1], h[0][2], h[0][3], q.x, q.y);
+          mma_16816(acc[u], l[0][0], l[0][1], l[0][2], l[0][3], q.x, q.y);
         } else {
-          const uint4 q = bv ? lds16(wsm + wr * RK + 8 * tq) : zu;
-          mma_16816(acc[u], h[0], h[1], h[2], h[3], q.x, q.y);
-          mma_16816(acc[u], l[0], l[1], l[2], l[3], q.x, q.y);
-          mma_16816(acc[u], h[4], h[5], h[6], h[7], q.z, q.w);
-          mma_16816(acc[u], l[4], l[5], l[6], l[7], q.z, q.w);
+#pragma unroll
+          for (int kb = 0; kb < KB; ++kb) {
+            const uint4 q = bv ? lds16(wsm + wr * RK + kb * 32 + 8 * tq) : zu;
+            mma_16816(acc[u], h[kb][0], h[kb][1], h[kb][2], h[kb][3], q.x, q.y);
+            mma_16816(acc[u], l[kb][0], l[kb][1], l[kb][2], l[kb][3], q.x, q.y);
+            mma_16816(acc[u], h[kb][4], h[kb][5], h[kb][6], h[kb][7], q.z, q.w);
+            mma_16816(acc[u], l[kb][4], l[kb][5], l[kb][6], l[kb][7], q.z, q.w);
+          }
         }
       }
       if (nb + 8 * tq < ncols) {
@@ -808,7 +813,7 @@ cudaError_t launch_expand(const float* inter, const void* lora_b, int S, int r, 
   const int R = S * r;
   const uint16_t* b = static_cast<const uint16_t*>(lora_b);
   uint16_t* o = static_cast<uint16_t*>(out);
-  if (!lora_ranks && !lora_scalings && (r == 16 || r == 32)) {
+  if (!lora_ranks && !lora_scalings && (r == 16 || r == 32 || r == 64)) {
     const int cps_st = (Ns + kStCols - 1) / kStCols;
     const dim3 grid_st((unsigned)(nblk * S * cps_st));
 #define MOL_EXPAND_ST(RK, E)                                                                    \
@@ -816,7 +821,8 @@ cudaError_t launch_expand(const float* inter, const void* lora_b, int S, int r, 
              b, S, Ns, scale, topk_weights, sorted_ids, expert_ids, ntpp, block_m, numel,       \
              num_vexperts, o, out_stride, cps_st)
     if (r == 16) return early ? MOL_EXPAND_ST(16, true) : MOL_EXPAND_ST(16, false);
-    return early ? MOL_EXPAND_ST(32, true) : MOL_EXPAND_ST(32, false);
+    if (r == 32) return early ? MOL_EXPAND_ST(32, true) : MOL_EXPAND_ST(32, false);
+    return early ? MOL_EXPAND_ST(64, true) : MOL_EXPAND_ST(64, false);
 #undef MOL_EXPAND_ST
   }
   const int cps = (Ns + kExpandCols - 1) / kExpandCols;
