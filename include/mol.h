@@ -213,9 +213,9 @@ int32_t mol_lora_shrink(const void* x, int64_t x_row_stride, int32_t x_row_div, 
  *   lora_ranks     int32 [num_vexperts / num_experts] or NULL: the sum runs over
  *                  j < r_l (clamped to [0, rank]), so inter columns and lora_b
  *                  columns at or past r_l take no part, whatever they hold
- *                  (8-column groups of lora_b wholly past r_l are not read);
- *                  r_l = 0 leaves the pair's output rows bit-unchanged. Needs
- *                  rank % 8 == 0 and at most 2048 adapters.
+ *                  (they may still be read); r_l = 0 leaves the pair's output
+ *                  rows bit-unchanged. Needs rank % 8 == 0 and at most 2048
+ *                  adapters.
  *   lora_scalings  fp32 [num_vexperts / num_experts] or NULL: the delta is
  *                  multiplied by scale * lora_scalings[adapter].
  *   num_experts    routed experts (used only with either array).

@@ -567,27 +567,30 @@ lora_expand_kernel(const float* __restrict__ inter, int R, const uint16_t* __res
   }
 }
 
-// Staged expand, rank 16 or 32, no adapter arrays. One item = (routed block
+// Staged expand, rank 16, 32 or 64. One item = (routed block
 // t, slice s, 256 output columns). One thread copies the item's lora_b rows
 // (256 x RK bf16, contiguous in [V, N, r]) into shared memory with a bulk
 // copy, and every thread copies its pieces of the output rows to update with
 // cp.async, so neither takes registers while in flight; each warp covers 64
 // columns (two 32-column groups) with the intermediate it loads once. At 64
 // registers eight blocks fit an SM, enough to run the decode expands in about
-// one wave. Fragment layout, MMA order per accumulator and rounding are those
+// one wave. Fragment layout, MMA order per accumulator, rounding and the
+// handling of adapter arrays (ADAPT: rank 0 writes nothing; both operands are
+// zeroed past the adapter's rank; the delta is scaled by its scaling) are those
 // of lora_expand_kernel, so both kernels give bit-identical outputs.
 constexpr int kStCols = 256;
 constexpr int kStGroups = kStCols / (kExpandThreads / 32) / 32;  // column groups per warp
 constexpr int kStOutPitch = kStCols + 32;  // staged output row, elements (64-byte skew per row)
 
-template <int RK, bool EARLY>
+template <int RK, bool EARLY, bool ADAPT>
 __global__ void __launch_bounds__(kExpandThreads, RK == 64 ? 5 : 8)
 lora_expand_st_kernel(const float* __restrict__ inter, int R, const uint16_t* __restrict__ lora_b,
                       int S, int Ns, float scale, const float* __restrict__ topk_w,
                       const int* __restrict__ sorted_ids, const int* __restrict__ expert_ids,
                       const int* __restrict__ ntpp_ptr, int block_m, int64_t numel,
                       int num_vexperts, uint16_t* __restrict__ out, int64_t out_stride,
-                      int chunks_per_slice) {
+                      int chunks_per_slice, const int* __restrict__ lora_ranks,
+                      const float* __restrict__ lora_scalings, int num_experts) {
   static_assert(RK == 16 || RK == 32 || RK == 64, "staged expand: rank 16, 32 or 64");
   constexpr bool K16 = (RK == 16);
   constexpr int KB = K16 ? 1 : RK / 32;  // k blocks (32 wide, or one 16-wide block)
@@ -611,12 +614,24 @@ lora_expand_st_kernel(const float* __restrict__ inter, int R, const uint16_t* __
   const int v = __ldg(expert_ids + t);
   const int slot = tid < block_m ? __ldg(sorted_ids + (int64_t)t * block_m + tid) : -1;
   if ((int64_t)t * block_m >= ntpp || v < 0 || v >= num_vexperts) return;
+  // the adapter's rank and scaling, in flight over the row compaction
+  int rk_raw = RK;
+  float scl = 1.f;
+  if constexpr (ADAPT) {
+    if (lora_ranks) rk_raw = __ldg(lora_ranks + v / num_experts);
+    if (lora_scalings) scl = __ldg(lora_scalings + v / num_experts);
+  }
   if (tid == 0) {
     mbar_init(&wbar, 1);
     fence_mbar_init();
   }
   const int c = compact_block_rows(slot, numel, rows, wcnt);  // its barriers publish the init
   if (c == 0) return;
+  // rank 0: the adapter writes no delta (nothing is copied); past rank rl the
+  // intermediate and the weight columns are padding and take no part
+  const int rl = rk_raw < 0 ? 0 : (rk_raw > RK ? RK : rk_raw);
+  if (ADAPT && rl == 0) return;
+  const float scale_v = ADAPT ? scale * scl : scale;
   // columns [col0, col0 + ncols) of the slice; ncols > 0 (chunk < ceil(Ns / kStCols)) and a
   // multiple of 8, so the copy is a multiple of 16 bytes from a 16-byte aligned row
   const int col0 = chunk * kStCols;
@@ -670,15 +685,23 @@ lora_expand_st_kernel(const float* __restrict__ inter, int R, const uint16_t* __
     uint32_t h[KB][8], l[KB][8];
 #pragma unroll
     for (int kb = 0; kb < KB; ++kb) {
-      const float4 a0 = i0 >= 0 ? ld_l2_f4(p0 + kb * 32) : zf;
-      const float4 a1 = i1 >= 0 ? ld_l2_f4(p1 + kb * 32) : zf;
+      float4 a0 = i0 >= 0 ? ld_l2_f4(p0 + kb * 32) : zf;
+      float4 a1 = i1 >= 0 ? ld_l2_f4(p1 + kb * 32) : zf;
+      if (ADAPT && rl < RK) {
+        mask_cols(a0, (K16 ? 4 * tq : kb * 32 + 8 * tq), rl);
+        mask_cols(a1, (K16 ? 4 * tq : kb * 32 + 8 * tq), rl);
+      }
       split_bf16x2(a0.x, a0.y, h[kb][0], l[kb][0]);
       split_bf16x2(a1.x, a1.y, h[kb][1], l[kb][1]);
       split_bf16x2(a0.z, a0.w, h[kb][2], l[kb][2]);
       split_bf16x2(a1.z, a1.w, h[kb][3], l[kb][3]);
       if constexpr (!K16) {
-        const float4 b0 = i0 >= 0 ? ld_l2_f4(p0 + kb * 32 + 4) : zf;
-        const float4 b1 = i1 >= 0 ? ld_l2_f4(p1 + kb * 32 + 4) : zf;
+        float4 b0 = i0 >= 0 ? ld_l2_f4(p0 + kb * 32 + 4) : zf;
+        float4 b1 = i1 >= 0 ? ld_l2_f4(p1 + kb * 32 + 4) : zf;
+        if (ADAPT && rl < RK) {
+          mask_cols(b0, kb * 32 + 8 * tq + 4, rl);
+          mask_cols(b1, kb * 32 + 8 * tq + 4, rl);
+        }
         split_bf16x2(b0.x, b0.y, h[kb][4], l[kb][4]);
         split_bf16x2(b1.x, b1.y, h[kb][5], l[kb][5]);
         split_bf16x2(b0.z, b0.w, h[kb][6], l[kb][6]);
@@ -708,13 +731,16 @@ lora_expand_st_kernel(const float* __restrict__ inter, int R, const uint16_t* __
         const int wr = nb + 8 * (g >> 1) + 2 * u + (g & 1);
         const bool bv = wr < ncols;
         if constexpr (K16) {
-          const uint2 q = bv ? lds8(wsm + wr * RK + 4 * tq) : make_uint2(0, 0);
+          const uint2 q2 = bv ? lds8(wsm + wr * RK + 4 * tq) : make_uint2(0, 0);
+          uint4 q = make_uint4(q2.x, q2.y, 0, 0);
+          if (ADAPT && rl < RK) mask_bf16x8(q, 4 * tq, rl);
           mma_16816(acc[u], h[0][0], h[0][1], h[0][2], h[0][3], q.x, q.y);
           mma_16816(acc[u], l[0][0], l[0][1], l[0][2], l[0][3], q.x, q.y);
         } else {
 #pragma unroll
           for (int kb = 0; kb < KB; ++kb) {
-            const uint4 q = bv ? lds16(wsm + wr * RK + kb * 32 + 8 * tq) : zu;
+            uint4 q = bv ? lds16(wsm + wr * RK + kb * 32 + 8 * tq) : zu;
+            if (ADAPT && rl < RK) mask_bf16x8(q, kb * 32 + 8 * tq, rl);
             mma_16816(acc[u], h[kb][0], h[kb][1], h[kb][2], h[kb][3], q.x, q.y);
             mma_16816(acc[u], l[kb][0], l[kb][1], l[kb][2], l[kb][3], q.x, q.y);
             mma_16816(acc[u], h[kb][4], h[kb][5], h[kb][6], h[kb][7], q.z, q.w);
@@ -728,7 +754,7 @@ lora_expand_st_kernel(const float* __restrict__ inter, int R, const uint16_t* __
         for (int hh = 0; hh < 2; ++hh) {
           const int i = hh ? i1 : i0;
           if (i < 0) continue;
-          const float sw = topk_w ? scale * __ldg(topk_w + i) : scale;
+          const float sw = topk_w ? scale_v * __ldg(topk_w + i) : scale_v;
           uint4 ov = lds16(osm_at(hh, nb + 8 * tq));
           uint32_t* ow = reinterpret_cast<uint32_t*>(&ov);
 #pragma unroll
@@ -813,16 +839,22 @@ cudaError_t launch_expand(const float* inter, const void* lora_b, int S, int r, 
   const int R = S * r;
   const uint16_t* b = static_cast<const uint16_t*>(lora_b);
   uint16_t* o = static_cast<uint16_t*>(out);
-  if (!lora_ranks && !lora_scalings && (r == 16 || r == 32 || r == 64)) {
+  if (r == 16 || r == 32 || r == 64) {
     const int cps_st = (Ns + kStCols - 1) / kStCols;
     const dim3 grid_st((unsigned)(nblk * S * cps_st));
-#define MOL_EXPAND_ST(RK, E)                                                                    \
-  launch_pdl(lora_expand_st_kernel<RK, E>, grid_st, dim3(kExpandThreads), 0, stream, inter, R, \
-             b, S, Ns, scale, topk_weights, sorted_ids, expert_ids, ntpp, block_m, numel,       \
-             num_vexperts, o, out_stride, cps_st)
-    if (r == 16) return early ? MOL_EXPAND_ST(16, true) : MOL_EXPAND_ST(16, false);
-    if (r == 32) return early ? MOL_EXPAND_ST(32, true) : MOL_EXPAND_ST(32, false);
-    return early ? MOL_EXPAND_ST(64, true) : MOL_EXPAND_ST(64, false);
+    const bool adapt = lora_ranks != nullptr || lora_scalings != nullptr;
+    const int ne = num_experts < 1 ? 1 : num_experts;
+#define MOL_EXPAND_ST(RK, E, A)                                                                   \
+  launch_pdl(lora_expand_st_kernel<RK, E, A>, grid_st, dim3(kExpandThreads), 0, stream, inter, R, \
+             b, S, Ns, scale, topk_weights, sorted_ids, expert_ids, ntpp, block_m, numel,         \
+             num_vexperts, o, out_stride, cps_st, lora_ranks, lora_scalings, ne)
+#define MOL_EXPAND_ST_RK(RK)                                                  \
+  return early ? (adapt ? MOL_EXPAND_ST(RK, true, true) : MOL_EXPAND_ST(RK, true, false)) \
+               : (adapt ? MOL_EXPAND_ST(RK, false, true) : MOL_EXPAND_ST(RK, false, false))
+    if (r == 16) MOL_EXPAND_ST_RK(16);
+    if (r == 32) MOL_EXPAND_ST_RK(32);
+    MOL_EXPAND_ST_RK(64);
+#undef MOL_EXPAND_ST_RK
 #undef MOL_EXPAND_ST
   }
   const int cps = (Ns + kExpandCols - 1) / kExpandCols;
