@@ -138,6 +138,13 @@ MOL_DEV void cp_async16_zfill(void* dst, const void* src, uint32_t src_bytes) {
 }
 // Waits until every cp.async this thread issued has landed.
 MOL_DEV void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// Closes this thread's current group of cp.async copies.
+MOL_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Waits until at most N of this thread's committed groups are still in flight.
+template <int N>
+MOL_DEV void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 // Error bits a kernel records instead of hanging or trapping.
 constexpr unsigned kFaultBulkTimeout = 1u;

@@ -578,12 +578,18 @@ lora_expand_kernel(const float* __restrict__ inter, int R, const uint16_t* __res
 // handling of adapter arrays (ADAPT: rank 0 writes nothing; both operands are
 // zeroed past the adapter's rank; the delta is scaled by its scaling) are those
 // of lora_expand_kernel, so both kernels give bit-identical outputs.
+// DB (blocks of many rows): two staged row tiles, the next tile's output rows
+// are copied while the current one computes.
 constexpr int kStCols = 256;
 constexpr int kStGroups = kStCols / (kExpandThreads / 32) / 32;  // column groups per warp
 constexpr int kStOutPitch = kStCols + 32;  // staged output row, elements (64-byte skew per row)
+// dynamic shared memory of one block: the lora_b tile, then the output row tile(s)
+constexpr size_t expand_st_smem(int rk, bool db) {
+  return (size_t)kStCols * rk * 2 + (size_t)(db ? 2 : 1) * 16 * kStOutPitch * 2;
+}
 
-template <int RK, bool EARLY, bool ADAPT>
-__global__ void __launch_bounds__(kExpandThreads, RK == 64 ? 5 : 8)
+template <int RK, bool EARLY, bool ADAPT, bool DB>
+__global__ void __launch_bounds__(kExpandThreads, RK == 64 ? (DB ? 4 : 5) : (DB ? 6 : 8))
 lora_expand_st_kernel(const float* __restrict__ inter, int R, const uint16_t* __restrict__ lora_b,
                       int S, int Ns, float scale, const float* __restrict__ topk_w,
                       const int* __restrict__ sorted_ids, const int* __restrict__ expert_ids,
@@ -594,8 +600,9 @@ lora_expand_st_kernel(const float* __restrict__ inter, int R, const uint16_t* __
   static_assert(RK == 16 || RK == 32 || RK == 64, "staged expand: rank 16, 32 or 64");
   constexpr bool K16 = (RK == 16);
   constexpr int KB = K16 ? 1 : RK / 32;  // k blocks (32 wide, or one 16-wide block)
-  __shared__ __align__(128) uint16_t wsm[kStCols * RK];
-  __shared__ __align__(16) uint16_t osm[16 * kStOutPitch];  // output rows of one row tile
+  extern __shared__ __align__(128) unsigned char st_smem[];
+  uint16_t* wsm = reinterpret_cast<uint16_t*>(st_smem);  // kStCols x RK lora_b rows
+  uint16_t* osm = wsm + kStCols * RK;                     // (DB ? 2 : 1) x 16 output rows
   __shared__ uint64_t wbar;
   __shared__ int rows[128];
   __shared__ int wcnt[kExpandThreads / 32];
@@ -648,11 +655,14 @@ lora_expand_st_kernel(const float* __restrict__ inter, int R, const uint16_t* __
   const uint4 zu = make_uint4(0, 0, 0, 0);
   int i0 = g < c ? rows[g] : -1;
   int i1 = 8 + g < c ? rows[8 + g] : -1;
-  // output rows to update, every column group of the warp (thread tq: 8 columns
-  // each), staged at osm[(8 * hh + g) * kStOutPitch + column inside the item];
-  // each thread later reads back only what it copied itself
-  auto osm_at = [&](int hh, int col) { return osm + (8 * hh + g) * kStOutPitch + col; };
-  auto load_out = [&]() {
+  // output rows to update (rows r0 and r1 of a row tile), every column group of
+  // the warp (thread tq: 8 columns each), staged at
+  // osm[(16 * buf + 8 * hh + g) * kStOutPitch + column inside the item]; each
+  // thread later reads back only what it copied itself
+  auto osm_at = [&](int buf, int hh, int col) {
+    return osm + ((DB ? 16 * buf : 0) + 8 * hh + g) * kStOutPitch + col;
+  };
+  auto load_out = [&](int buf, int r0, int r1) {
 #pragma unroll
     for (int cg = 0; cg < kStGroups; ++cg) {
       const int col = wcol + cg * 32 + 8 * tq;
@@ -660,12 +670,13 @@ lora_expand_st_kernel(const float* __restrict__ inter, int R, const uint16_t* __
       const int64_t oc = (int64_t)s * Ns + col0 + col;
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
-        const int i = hh ? i1 : i0;
-        if (ok && i >= 0) cp_async16_zfill(osm_at(hh, col), out + (int64_t)i * out_stride + oc, 16u);
+        const int i = hh ? r1 : r0;
+        if (ok && i >= 0) cp_async16_zfill(osm_at(buf, hh, col), out + (int64_t)i * out_stride + oc, 16u);
       }
     }
+    cp_async_commit();
   };
-  load_out();
+  load_out(0, i0, i1);
   if (EARLY) {
     pdl_wait();  // the intermediate comes from the shrink that precedes this kernel
     pdl_launch_dependents();
@@ -673,11 +684,16 @@ lora_expand_st_kernel(const float* __restrict__ inter, int R, const uint16_t* __
 
   bool landed = false;
   for (int m0 = 0; m0 < c; m0 += 16) {
+    const int buf = DB ? (m0 >> 4) & 1 : 0;
     if (m0 > 0) {
       i0 = m0 + g < c ? rows[m0 + g] : -1;
       i1 = m0 + 8 + g < c ? rows[m0 + 8 + g] : -1;
-      load_out();
+      if (!DB) load_out(0, i0, i1);
     }
+    const bool ahead = DB && m0 + 16 < c;
+    if (ahead)  // the next tile's output rows, into the other buffer (read last in the previous tile)
+      load_out(buf ^ 1, m0 + 16 + g < c ? rows[m0 + 16 + g] : -1,
+               m0 + 24 + g < c ? rows[m0 + 24 + g] : -1);
     // the intermediate fragments, split into bf16 head and tail, serve every column group
     const int koff = s * RK + (K16 ? 4 * tq : 8 * tq);
     const float* p0 = inter + (int64_t)(i0 >= 0 ? i0 : 0) * R + koff;
@@ -716,7 +732,10 @@ lora_expand_st_kernel(const float* __restrict__ inter, int R, const uint16_t* __
       }
       landed = true;
     }
-    cp_async_wait_all();  // this thread's output pieces
+    if (ahead)
+      cp_async_wait_group<1>();  // this tile's output pieces; the next tile's stay in flight
+    else
+      cp_async_wait_all();  // this thread's output pieces
 #pragma unroll
     for (int cg = 0; cg < kStGroups; ++cg) {
       const int nb = wcol + cg * 32;  // the group's first column inside the item
@@ -755,7 +774,7 @@ lora_expand_st_kernel(const float* __restrict__ inter, int R, const uint16_t* __
           const int i = hh ? i1 : i0;
           if (i < 0) continue;
           const float sw = topk_w ? scale_v * __ldg(topk_w + i) : scale_v;
-          uint4 ov = lds16(osm_at(hh, nb + 8 * tq));
+          uint4 ov = lds16(osm_at(buf, hh, nb + 8 * tq));
           uint32_t* ow = reinterpret_cast<uint32_t*>(&ov);
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
@@ -782,8 +801,31 @@ static int device_sms() {
   return cache[dev];
 }
 
+// Opts the staged expand instances above 48 KB of dynamic shared memory in.
+template <int RK, bool DB>
+static cudaError_t prepare_expand_st() {
+  const int bytes = (int)expand_st_smem(RK, DB);
+  cudaError_t e = cudaSuccess;
+  for (auto k : {lora_expand_st_kernel<RK, false, false, DB>, lora_expand_st_kernel<RK, false, true, DB>,
+                 lora_expand_st_kernel<RK, true, false, DB>, lora_expand_st_kernel<RK, true, true, DB>})
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  return e;
+}
+
 cudaError_t prepare_lora_kernels() {
   cudaError_t e = prepare_tc_kernels();
+  if (e != cudaSuccess) return e;
+  e = prepare_expand_st<64, true>();
+  if (e != cudaSuccess) return e;
+  e = prepare_expand_st<64, false>();
+  if (e != cudaSuccess) return e;
+  e = prepare_expand_st<32, true>();
+  if (e != cudaSuccess) return e;
+  e = prepare_expand_st<32, false>();
+  if (e != cudaSuccess) return e;
+  e = prepare_expand_st<16, true>();
+  if (e != cudaSuccess) return e;
+  e = prepare_expand_st<16, false>();
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(lora_shrink_kernel<false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sp::kSmem);
@@ -844,17 +886,23 @@ cudaError_t launch_expand(const float* inter, const void* lora_b, int S, int r, 
     const dim3 grid_st((unsigned)(nblk * S * cps_st));
     const bool adapt = lora_ranks != nullptr || lora_scalings != nullptr;
     const int ne = num_experts < 1 ? 1 : num_experts;
-#define MOL_EXPAND_ST(RK, E, A)                                                                   \
-  launch_pdl(lora_expand_st_kernel<RK, E, A>, grid_st, dim3(kExpandThreads), 0, stream, inter, R, \
-             b, S, Ns, scale, topk_weights, sorted_ids, expert_ids, ntpp, block_m, numel,         \
-             num_vexperts, o, out_stride, cps_st, lora_ranks, lora_scalings, ne)
-#define MOL_EXPAND_ST_RK(RK)                                                  \
-  return early ? (adapt ? MOL_EXPAND_ST(RK, true, true) : MOL_EXPAND_ST(RK, true, false)) \
-               : (adapt ? MOL_EXPAND_ST(RK, false, true) : MOL_EXPAND_ST(RK, false, false))
+    // many rows per virtual expert (on average at least 32 pairs each): blocks hold
+    // several row tiles, so the output rows of the next one are prefetched
+    const bool db = numel >= 32 * std::min<int64_t>(numel, num_vexperts);
+#define MOL_EXPAND_ST(RK, E, A, D)                                                            \
+  launch_pdl(lora_expand_st_kernel<RK, E, A, D>, grid_st, dim3(kExpandThreads),               \
+             expand_st_smem(RK, D), stream, inter, R, b, S, Ns, scale, topk_weights, sorted_ids, \
+             expert_ids, ntpp, block_m, numel, num_vexperts, o, out_stride, cps_st, lora_ranks, \
+             lora_scalings, ne)
+#define MOL_EXPAND_ST_A(RK, E, A) (db ? MOL_EXPAND_ST(RK, E, A, true) : MOL_EXPAND_ST(RK, E, A, false))
+#define MOL_EXPAND_ST_RK(RK)                                                              \
+  return early ? (adapt ? MOL_EXPAND_ST_A(RK, true, true) : MOL_EXPAND_ST_A(RK, true, false)) \
+               : (adapt ? MOL_EXPAND_ST_A(RK, false, true) : MOL_EXPAND_ST_A(RK, false, false))
     if (r == 16) MOL_EXPAND_ST_RK(16);
     if (r == 32) MOL_EXPAND_ST_RK(32);
     MOL_EXPAND_ST_RK(64);
 #undef MOL_EXPAND_ST_RK
+#undef MOL_EXPAND_ST_A
 #undef MOL_EXPAND_ST
   }
   const int cps = (Ns + kExpandCols - 1) / kExpandCols;
