@@ -526,7 +526,7 @@ def run_e2e(args, torch, mol, wl, layers, pairs_per_step, world, dev):
 # (workload, kernel); None until the current kernel has been captured. Source:
 # profiles/decode_stage_kernels_ncu_full.md (one decode layer, 8-row shrink,
 # the instance without per-adapter ranks).
-TRAFFIC = {("decode", "shrink_gate_up"): 35506176 + 512}
+TRAFFIC = {("decode", "shrink_gate_up"): 35505920 + 0}
 
 
 # --------------------------------------------------------------------------- CPU (oracle)

@@ -200,6 +200,43 @@ def test_small_integers_bit_exact(r, BM):
     assert np.array_equal(bf16_host(out), ref_out)
 
 
+@pytest.mark.parametrize("E,BM,r,few_rows", [
+    (64, 64, 32, True),    # 64 virtual experts, 128 pairs: one staged row tile at a time
+    (64, 128, 64, True),
+    (4, 64, 32, False),    # 4 virtual experts: the next row tile is prefetched
+    (4, 128, 16, False),
+])
+def test_expand_hot_expert_many_row_tiles(E, BM, r, few_rows):
+    """One expert takes most pairs, so its routed blocks hold up to block_m rows (several
+    16-row tiles), whether or not the call counts as many rows per virtual expert."""
+    torch, dev = _dev()
+    mol = mol_lib()
+    rng = np.random.default_rng(E + BM + r)
+    T, k, L, K, S, Ns = 64, 2, 1, 64, 2, 264
+    numel, V, R, N = T * k, E * L, S * r, S * Ns
+    assert (numel < 32 * min(numel, V)) == few_rows
+    topk = np.where(rng.random((T, k)) < 0.85, 0, rng.integers(1, E, (T, k))).astype(np.int32)
+    topk[:, 1] = np.where(topk[:, 0] == topk[:, 1], (topk[:, 1] + 1) % E, topk[:, 1])
+    lora = np.zeros(T, np.int32)
+    vid = oracle.virtual_topk(topk, lora, E, L).reshape(-1)
+    routing, s, e, n = _routing_from_oracle(mol, vid, V, BM, dev)
+    assert np.bincount(vid, minlength=V).max() > 32
+    inter = rng.standard_normal((numel, R)).astype(np.float32)
+    B = bits(rng.standard_normal((V, N, r)) * 0.05)
+    out0 = bits(rng.standard_normal((numel, N)))
+    w = rng.random(numel).astype(np.float32)
+    out_d = to_dev_bf16(out0, dev)
+    mol.mol_lora_expand(torch.from_numpy(inter).to(dev), to_dev_bf16(B, dev), S, 0.5, routing, out_d,
+                        topk_weights=torch.from_numpy(w).to(dev))
+    torch.cuda.synchronize()
+    ref = oracle.lora_expand(inter, B, S, r, Ns, 0.5, w, s, e, n, BM, numel, out0)
+    pairs = valid_pairs(s, e, n, BM, numel)
+    g_out = bf16_host(out_d)
+    check_out(g_out, ref, pairs)
+    others = np.setdiff1d(np.arange(numel), pairs)
+    assert np.array_equal(g_out[others], out0[others])
+
+
 def test_expand_ignores_poisoned_rows():
     """NaN intermediates on rows outside every block never reach the output."""
     torch, dev = _dev()
