@@ -425,8 +425,9 @@ def run_gpu(args):
 
 def run_e2e(args, torch, mol, wl, layers, pairs_per_step, world, dev):
     """Per step: one pinned host -> device copy of the step's inputs, the layer, one device ->
-    host copy of its outputs; the rotating steps captured (copies included) in one graph whose
-    copies run on their own streams, ordered by events, beside the compute of other steps.
+    host copy of its outputs; the rotating steps, E2E_ROUNDS times over, captured (copies
+    included) in one graph whose copies run on their own streams, ordered by events, beside
+    the compute of other steps.
 
     Each layer's inputs (top-k ids, adapter ids, every stage's activations and the output rows
     the expand updates) live in one device buffer, 256-byte aligned segments with the outputs
@@ -467,11 +468,17 @@ def run_e2e(args, torch, mol, wl, layers, pairs_per_step, world, dev):
         L_.forward(mol)
         host_out.copy_(dev_buf[out_lo:], non_blocking=True)
 
-    # All rotating layers in one graph over three streams: step i's inputs are
-    # copied in on s_in, its layer runs on the capturing stream once they have
-    # landed, and its outputs go back on s_out once it is done, so the copies
-    # of neighbouring steps overlap a step's compute (whole-job throughput).
+    # The rotating layers, E2E_ROUNDS times over, in one graph on three streams:
+    # step k's inputs are copied in on s_in, its layer runs on the capturing
+    # stream once they have landed, and its outputs go back on s_out once it is
+    # done, so the copies of neighbouring steps overlap a step's compute
+    # (whole-job throughput). A layer's buffers are reused by the step one
+    # rotation later, whose copy-in waits for this step's copy-out. More steps
+    # per graph spread the first copy-in and the last copy-out over more steps,
+    # as a graph of a whole model's layers would.
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    nl = len(layers)
+    n_steps = E2E_ROUNDS * nl
 
     def all_steps():
         main = torch.cuda.current_stream()
@@ -479,10 +486,13 @@ def run_e2e(args, torch, mol, wl, layers, pairs_per_step, world, dev):
         start.record(main)
         s_in.wait_event(start)
         s_out.wait_event(start)
-        for L_, pk in zip(layers, packs):
-            dev_buf, host_in, host_out, out_lo = pk
-            landed, done = torch.cuda.Event(), torch.cuda.Event()
+        copied_out = []
+        for k in range(n_steps):
+            L_, (dev_buf, host_in, host_out, out_lo) = layers[k % nl], packs[k % nl]
+            landed, done, back = torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event()
             with torch.cuda.stream(s_in):
+                if k >= nl:
+                    s_in.wait_event(copied_out[k - nl])
                 dev_buf.copy_(host_in, non_blocking=True)
                 landed.record(s_in)
             main.wait_event(landed)
@@ -491,13 +501,15 @@ def run_e2e(args, torch, mol, wl, layers, pairs_per_step, world, dev):
             s_out.wait_event(done)
             with torch.cuda.stream(s_out):
                 host_out.copy_(dev_buf[out_lo:], non_blocking=True)
+                back.record(s_out)
+            copied_out.append(back)
         main.wait_stream(s_in)
         main.wait_stream(s_out)
 
     graph = capture(torch, all_steps)
-    replays = max(1, min(args.steps, 5000) // len(layers))
-    ms = time_graphs(torch, [graph], replays, max(1, min(args.warmup, 50) // len(layers))) / len(layers)
-    steps = replays * len(layers)
+    replays = max(1, min(args.steps, 5000) // n_steps)
+    ms = time_graphs(torch, [graph], replays, max(1, min(args.warmup, 50) // n_steps)) / n_steps
+    steps = replays * n_steps
     # one step at a time (copy in, layer, copy out in order), graph per layer, for reference
     graphs = [capture(torch, lambda L_=L_, pk=pk: step(L_, pk)) for L_, pk in zip(layers, packs)]
     ms_serial = time_graphs(torch, graphs, min(args.steps, 5000), min(args.warmup, 50))
@@ -513,13 +525,18 @@ def run_e2e(args, torch, mol, wl, layers, pairs_per_step, world, dev):
     ms_eager = (time.perf_counter() - t0) * 1e3 / n_e
     return dict(value=round(pairs_per_step * world / (ms * 1e-3), 1), unit=UNIT,
                 h2d_bytes_per_step=int(bi), d2h_bytes_per_step=int(bo), ms_per_step=round(ms, 6),
-                mode="graph replay of the rotating steps: per step one pinned-host copy of the "
-                     "packed inputs, the mol_lora_forward calls, one copy of the outputs back; "
-                     "copies on their own streams overlap neighbouring steps' compute",
+                mode=f"graph replay of {n_steps} steps ({E2E_ROUNDS} rotations of the layers): per "
+                     "step one pinned-host copy of the packed inputs, the mol_lora_forward calls, "
+                     "one copy of the outputs back; copies on their own streams overlap "
+                     "neighbouring steps' compute",
                 serial_value=round(pairs_per_step * world / (ms_serial * 1e-3), 1),
                 serial_ms_per_step=round(ms_serial, 6),
                 eager_value=round(pairs_per_step * world / (ms_eager * 1e-3), 1),
                 eager_ms_per_step=round(ms_eager, 6), steps=steps)
+
+
+# rotations of the layers inside the end-to-end graph
+E2E_ROUNDS = 4
 
 
 # traffic (dram bytes read + written) per launch from ncu captures, keyed by
