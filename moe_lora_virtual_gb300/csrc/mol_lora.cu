@@ -378,11 +378,13 @@ lora_shrink_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, 
   }
 }
 
-// Expand. One item = (routed block t, slice s, 128 output columns), 4 warps x
-// 32 columns. Round 1 loads the routing words together, round 2 the weight
-// fragments and the output rows to update, round 3 the intermediate. With
-// EARLY (inside mol_lora_forward, right after this stage's shrink) rounds 1-2
-// run before griddepcontrol.wait, overlapping the shrink's tail.
+// Expand with the weight fragments in registers (rank 128; ranks 16-64 take
+// the staged expand below). One item = (routed block t, slice s, 128 output
+// columns), 4 warps x 32 columns. Round 1 loads the routing words together,
+// round 2 the weight fragments and the output rows to update, round 3 the
+// intermediate. With EARLY (inside mol_lora_forward, right after this stage's
+// shrink) rounds 1-2 run before griddepcontrol.wait, overlapping the shrink's
+// tail.
 constexpr int kExpandThreads = 128;
 constexpr int kExpandCols = 128;
 
@@ -883,6 +885,7 @@ cudaError_t launch_expand(const float* inter, const void* lora_b, int S, int r, 
   uint16_t* o = static_cast<uint16_t*>(out);
   if (r == 16 || r == 32 || r == 64) {
     const int cps_st = (Ns + kStCols - 1) / kStCols;
+    if (nblk * S * cps_st > INT32_MAX) return cudaErrorInvalidConfiguration;
     const dim3 grid_st((unsigned)(nblk * S * cps_st));
     const bool adapt = lora_ranks != nullptr || lora_scalings != nullptr;
     const int ne = num_experts < 1 ? 1 : num_experts;
@@ -906,6 +909,7 @@ cudaError_t launch_expand(const float* inter, const void* lora_b, int S, int r, 
 #undef MOL_EXPAND_ST
   }
   const int cps = (Ns + kExpandCols - 1) / kExpandCols;
+  if (nblk * S * cps > INT32_MAX) return cudaErrorInvalidConfiguration;
   const dim3 grid((unsigned)(nblk * S * cps));
 #define MOL_EXPAND_CASE(RK)                                                                     \
   case RK:                                                                                      \
