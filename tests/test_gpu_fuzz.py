@@ -1,0 +1,125 @@
+"""Seeded random configurations across the library's contract, one stage end to end on the GPU
+(routing computed, shrink, expand; with and without per-adapter arrays; padded row strides;
+routed weights; skewed routing) against the oracle."""
+
+import numpy as np
+import pytest
+
+import oracle
+from tests.gpu_util import (bf16_host, check_inter, check_out, mol_lib, to_dev_bf16, to_dev_i32,
+                            torch_cuda)
+
+pytestmark = pytest.mark.gpu
+
+N_CASES = 40
+MAX_ELEMS = 12_000_000  # per weight tensor, so that each case stays small on the host
+
+
+def bits(a):
+    return oracle.f64_to_bf16(np.asarray(a, np.float64))
+
+
+def _draw(seed):
+    rng = np.random.default_rng(7000 + seed)
+    BM = int(rng.choice([16, 32, 64, 128]))
+    r = int(rng.choice([16, 32, 64, 128]))
+    S = int(rng.integers(1, 4))
+    E = int(rng.integers(1, 48))
+    L = int(rng.integers(1, 6))
+    k = int(rng.integers(1, min(E, 8) + 1))
+    T = int(rng.integers(0, 240))
+    K = int(rng.choice([8, 64, 200, 520, 1024, 2056, 4096]))
+    Ns = 8 * int(rng.integers(1, 90))
+    dense = rng.random() < 0.25  # one adapter, few experts: full routed blocks, tensor cores
+    if dense:
+        E, L = int(rng.integers(2, 7)), 1
+        BM, r, S = int(rng.choice([64, 128])), int(rng.choice([32, 64])), int(rng.integers(1, 3))
+        K = int(rng.choice([64, 256, 1024]))
+        k = int(rng.integers(1, min(E, 8) + 1))
+        T = int(rng.integers(32 * E, 300))
+    V, R = E * L, S * r
+    while V * R * K > MAX_ELEMS and K > 8:
+        K = max(8, (K // 2) // 8 * 8)
+    while V * S * Ns * r > MAX_ELEMS and Ns > 8:
+        Ns = max(8, (Ns // 2) // 8 * 8)
+    c = dict(seed=seed, BM=BM, r=r, S=S, E=E, L=L, k=k, T=T, K=K, Ns=Ns, V=V, R=R,
+             token_rows=bool(rng.integers(0, 2)), x_pad=8 * int(rng.integers(0, 3)),
+             out_pad=8 * int(rng.integers(0, 3)), use_w=bool(rng.integers(0, 2)),
+             sparse=float(rng.choice([0.0, 0.1, 0.5, 1.0])), hot=bool(rng.integers(0, 2)),
+             adapters=bool(rng.integers(0, 2)) and not dense)
+    numel = T * k
+    # top-k ids: distinct per token; "hot" puts expert 0 first in most tokens
+    topk = np.zeros((T, k), np.int32)
+    for t in range(T):
+        topk[t] = rng.permutation(E)[:k]
+    if c["hot"] and T > 0:
+        for t in range(T):
+            if rng.random() < 0.8 and 0 not in topk[t]:
+                topk[t, 0] = 0
+    topk[rng.random((T, k)) < c["sparse"]] = -1
+    lora = rng.integers(-1, L + 1, size=T).astype(np.int32)  # L is out of range: no delta
+    xrows = T if c["token_rows"] else numel
+    c["topk"], c["lora"] = topk, lora
+    c["x"] = bits(rng.standard_normal((xrows, K + c["x_pad"])))
+    c["A"] = bits(rng.standard_normal((V, R, K)) * 0.05)
+    c["B"] = bits(rng.standard_normal((V, S * Ns, r)) * 0.05)
+    c["out0"] = bits(rng.standard_normal((numel, S * Ns + c["out_pad"])))
+    c["w"] = rng.random(numel).astype(np.float32) if c["use_w"] else None
+    if c["adapters"]:
+        c["ranks"] = rng.integers(0, r + 1, L).astype(np.int32)
+        c["ranks"][rng.random(L) < 0.3] = r
+        c["scalings"] = rng.uniform(0.25, 2.0, L).astype(np.float32)
+    else:
+        c["ranks"] = c["scalings"] = None
+    return c
+
+
+@pytest.mark.parametrize("seed", range(N_CASES))
+def test_random_stage(seed):
+    torch = torch_cuda()
+    mol = mol_lib()
+    dev = torch.device("cuda:0")
+    c = _draw(seed)
+    E, L, V, BM, S, r, Ns, K, R = c["E"], c["L"], c["V"], c["BM"], c["S"], c["r"], c["Ns"], c["K"], c["R"]
+    T, k = c["T"], c["k"]
+    numel, N = T * k, S * Ns
+    xdiv = k if c["token_rows"] else 1
+    ref = oracle.lora_forward_stage(c["x"][:, :K], xdiv, c["topk"], c["lora"], E, L, c["A"], c["B"],
+                                    S, r, Ns, 0.5, c["w"], c["out0"][:, :N], BM,
+                                    lora_ranks=c["ranks"], lora_scalings=c["scalings"])
+
+    routing = mol.alloc_routing(numel, V, BM, dev)
+    ws = mol.alloc_workspace(numel, V, BM, dev)
+    x_d = to_dev_bf16(c["x"], dev)[:, :K]
+    out_d = to_dev_bf16(c["out0"], dev)
+    inter = torch.full((numel, R), float("nan"), dtype=torch.float32, device=dev)
+    kw = {}
+    if c["adapters"]:
+        kw = dict(lora_ranks=to_dev_i32(c["ranks"], dev),
+                  lora_scalings=torch.from_numpy(c["scalings"]).to(dev))
+    mol.mol_lora_forward(x_d, xdiv, to_dev_i32(c["topk"], dev), to_dev_i32(c["lora"], dev), E, L,
+                         to_dev_bf16(c["A"], dev), to_dev_bf16(c["B"], dev), S, 0.5, out_d[:, :N],
+                         routing, inter, compute_routing=True, workspace=ws,
+                         topk_weights=None if c["w"] is None else torch.from_numpy(c["w"]).to(dev),
+                         **kw)
+    torch.cuda.synchronize()
+    assert mol.mol_take_fault_flags() == 0
+
+    # routing: bit-exact
+    ntpp = int(routing.num_tokens_post_padded.cpu().item())
+    assert ntpp == ref["ntpp"]
+    assert np.array_equal(routing.sorted_token_ids.cpu().numpy()[:ntpp], ref["sorted_ids"][:ntpp])
+    assert np.array_equal(routing.expert_ids.cpu().numpy()[:ntpp // BM], ref["expert_ids"][:ntpp // BM])
+
+    # pairs that get a delta: in a real block, and of an adapter of rank > 0
+    vt = ref["vtopk"].reshape(-1)
+    live = np.nonzero(vt >= 0)[0]
+    if c["ranks"] is not None:
+        live = live[c["ranks"][vt[live] // E] > 0]
+    g_inter, g_out = inter.cpu().numpy(), bf16_host(out_d)
+    check_inter(g_inter, ref["inter"], live)
+    check_out(g_out[:, :N], ref["out"], live)
+    rest = np.setdiff1d(np.arange(numel), live)
+    assert np.all(np.isnan(g_inter[rest]))
+    assert np.array_equal(g_out[rest], c["out0"][rest])
+    assert np.array_equal(g_out[:, N:], c["out0"][:, N:])  # padding columns never written
