@@ -569,19 +569,19 @@ lora_expand_kernel(const float* __restrict__ inter, int R, const uint16_t* __res
   }
 }
 
-// Staged expand, rank 16, 32 or 64. One item = (routed block
-// t, slice s, 256 output columns). One thread copies the item's lora_b rows
-// (256 x RK bf16, contiguous in [V, N, r]) into shared memory with a bulk
-// copy, and every thread copies its pieces of the output rows to update with
-// cp.async, so neither takes registers while in flight; each warp covers 64
-// columns (two 32-column groups) with the intermediate it loads once. At 64
-// registers eight blocks fit an SM, enough to run the decode expands in about
-// one wave. Fragment layout, MMA order per accumulator, rounding and the
-// handling of adapter arrays (ADAPT: rank 0 writes nothing; both operands are
-// zeroed past the adapter's rank; the delta is scaled by its scaling) are those
-// of lora_expand_kernel, so both kernels give bit-identical outputs.
-// DB (blocks of many rows): two staged row tiles, the next tile's output rows
-// are copied while the current one computes.
+// Staged expand, rank 16, 32 or 64. One item = (routed block t, slice s, 256
+// output columns). One thread copies the item's lora_b rows (256 x RK bf16,
+// contiguous in [V, N, r]) into shared memory with a bulk copy, and every
+// thread copies its pieces of the output rows to update with cp.async, so
+// neither takes registers while in flight; each warp covers 64 columns (two
+// 32-column groups) with the intermediate it loads once. At rank 32, 64
+// registers and 26 KB let eight blocks share an SM, enough to run the decode
+// expands in about one wave. Fragment layout, MMA order per accumulator,
+// rounding and the handling of adapter arrays (ADAPT: rank 0 writes nothing;
+// both operands are zeroed past the adapter's rank; the delta is scaled by its
+// scaling) are those of lora_expand_kernel, so both kernels give bit-identical
+// outputs. DB (blocks of many rows): two staged row tiles, the next tile's
+// output rows are copied while the current one computes.
 constexpr int kStCols = 256;
 constexpr int kStGroups = kStCols / (kExpandThreads / 32) / 32;  // column groups per warp
 constexpr int kStOutPitch = kStCols + 32;  // staged output row, elements (64-byte skew per row)
