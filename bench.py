@@ -367,9 +367,11 @@ def run_gpu(args):
         name, nbytes = best
         us = kern[name]
         achieved = nbytes / (us * 1e-6) / 1e9
+        cap = None if ranks is not None else TRAFFIC.get((args.config, name))
         roof = dict(kernel=name, bound="hbm", achieved=round(achieved, 1), peak=peaks["hbm_gbs"],
                     unit="GB/s", frac=round(achieved / peaks["hbm_gbs"], 4),
-                    traffic=None if ranks is not None else TRAFFIC.get((args.config, name)),
+                    traffic=None if cap is None else cap[0],
+                    traffic_launch_alg_bytes=None if cap is None else cap[1],
                     bytes_per_launch=int(nbytes),
                     us_per_launch=round(us, 3), peak_source=peaks["source"])
         # the first stage's shrink against the bf16 tensor peak (a real dense
@@ -539,11 +541,16 @@ def run_e2e(args, torch, mol, wl, layers, pairs_per_step, world, dev):
 E2E_ROUNDS = 4
 
 
-# traffic (dram bytes read + written) per launch from ncu captures, keyed by
-# (workload, kernel); None until the current kernel has been captured. Source:
-# profiles/decode_stage_kernels_ncu_full.md (one decode layer, 8-row shrink,
-# the instance without per-adapter ranks).
-TRAFFIC = {("decode", "shrink_gate_up"): 35505920 + 0}
+# traffic (dram bytes read + written) of one captured launch, with the algorithmic bytes of
+# that same launch (the first layer of the workload, seed 0), keyed by (workload, kernel);
+# absent until the current kernel has been captured. Sources:
+# profiles/decode_stage_kernels_ncu_full.md and profiles/dominant_kernels_traffic.md.
+TRAFFIC = {
+    ("decode", "shrink_gate_up"): (35505920 + 0, 35506176),
+    ("wide", "expand_down"): (41633280 + 39680, 43469824),
+    ("ep", "shrink_gate_up"): (569522432 + 6452736, 572089984),
+    ("dense", "expand_down"): (344121088 + 215358976, 612368384),
+}
 
 
 # --------------------------------------------------------------------------- CPU (oracle)

@@ -34,7 +34,7 @@ def _stale() -> bool:
 
 
 def build_library(force: bool = False, verbose: bool = False) -> str:
-    """Compile the three translation units in parallel into one shared library."""
+    """Compile the translation units (nvcc --threads 4) into one shared library."""
     if not force and not _stale():
         return LIB_PATH
     tmp = LIB_PATH + f".tmp{os.getpid()}"
