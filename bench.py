@@ -54,6 +54,9 @@ def parse_args(argv=None):
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--no-kernels", action="store_true", help="skip the per-kernel timing phase")
+    p.add_argument("--extra", default="wide,wide1k,ep,prefill,dense",
+                   help="other workloads timed briefly after the main line (comma separated; "
+                        "'none' to skip)")
     p.add_argument("--cpu-worker", action="store_true", help=argparse.SUPPRESS)
     p.add_argument("--cpu-budget", type=float, default=15.0, help=argparse.SUPPRESS)
     return p.parse_args(argv)
@@ -218,6 +221,19 @@ def time_graphs(torch, graphs, steps, warmup):
     return s.elapsed_time(e) / steps
 
 
+def event_ms(torch, fn, reps):
+    """ms per call of fn() (which enqueues work on the current stream), CUDA events around
+    `reps` calls, synchronized on both sides."""
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    ev0.record()
+    for _ in range(reps):
+        fn()
+    ev1.record()
+    torch.cuda.synchronize()
+    return ev0.elapsed_time(ev1) / reps
+
+
 def capture(torch, fn):
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
@@ -230,6 +246,174 @@ def capture(torch, fn):
         fn()
     torch.cuda.synchronize()
     return g
+
+
+def layer_steps_timer(torch, mol, layers, steps):
+    """Graphs that run exactly `steps` layer steps: the rotating layers back to back in one
+    graph (replayed steps // len(layers) times) and, for the remainder, one graph of the first
+    steps % len(layers) layers. Returns (run, warm): run() enqueues the K steps; warm(w) replays
+    every graph the timed region uses at least twice and covers at least w warm-up steps."""
+    nl = len(layers)
+    full, rest = divmod(steps, nl)
+    multi = capture(torch, lambda: [L_.forward(mol) for L_ in layers]) if full else None
+    tail = capture(torch, lambda: [L_.forward(mol) for L_ in layers[:rest]]) if rest else None
+
+    def run():
+        for _ in range(full):
+            multi.replay()
+        if tail is not None:
+            tail.replay()
+
+    def warm(w):
+        done = 0
+        for g, n in ((multi, nl), (tail, rest)):
+            if g is None:
+                continue
+            for _ in range(2):
+                g.replay()
+                done += n
+        while done < w:
+            (multi or tail).replay()
+            done += nl if multi else rest
+        torch.cuda.synchronize()
+
+    return run, warm
+
+
+def kernel_times(torch, mol, wl, layers, cnt, ranks, steps, config):
+    """Each stage kernel (and the align, the per-token adapter ids) alone in its own graphs,
+    over the same rotation of layers; the dominant kernel against the HBM roofline and the
+    first stage's shrink against the bf16 tensor peak."""
+    peaks = measured_peaks()
+    dev = layers[0].topk.device
+    kern = {}
+
+    def stage_call(L_, si, which):
+        d = L_.stages[si]
+        st = d["st"]
+        if which == "shrink":
+            return lambda: mol.mol_lora_shrink(d["x"], st.x_row_div, d["A"], st.stage.S,
+                                               L_.routing, d["inter"], lora_ranks=L_.ranks_d,
+                                               num_experts=wl.E)
+        return lambda: mol.mol_lora_expand(d["inter"], d["B"], st.stage.S, wl.scale,
+                                           L_.routing, d["out"], lora_ranks=L_.ranks_d,
+                                           lora_scalings=L_.scal_d, num_experts=wl.E)
+
+    def align_call(L_):
+        return lambda: mol.mol_align_block_size(L_.routing.vtopk_ids, wl.V, wl.BM,
+                                                routing=L_.routing, workspace=L_.ws)
+
+    reps = 4  # launches per graph = layers x reps, back to back on one stream
+
+    def per_launch_us(calls):
+        g = capture(torch, lambda: [f() for _ in range(reps) for f in calls])
+        n = max(20, min(steps, 2000) // (reps * len(calls)))
+        return time_graphs(torch, [g], n, 3) * 1e3 / (reps * len(calls))
+
+    kern["align"] = per_launch_us([align_call(L_) for L_ in layers])
+    # per-token adapter ids of the batch: one request per token (decode) or
+    # requests of 64 tokens, adapter slots of the layer's tokens
+    req_len = 1 if wl.T <= 256 else 64
+    nreq = (wl.T + req_len - 1) // req_len
+    wi = torch.from_numpy(layers[0].li.lora_ids[::req_len].astype(np.int32)).to(dev)
+    seg = torch.from_numpy(np.minimum(np.arange(nreq + 1) * req_len, wl.T).astype(np.int32)).to(dev)
+    tok_ids = torch.empty(wl.T, dtype=torch.int32, device=dev)
+    kern["token_lora_ids"] = per_launch_us(
+        [lambda: mol.mol_token_lora_ids(wi, seg, wl.T, wl.L, layers[0].ranks_d, tok_ids)])
+    for si, st in enumerate(wl.stages):
+        for which in ("shrink", "expand"):
+            kern[f"{which}_{st.name}"] = per_launch_us([stage_call(L_, si, which) for L_ in layers])
+    # dominant kernel: the stage kernel with the most algorithmic bytes
+    best = None
+    for si, st in enumerate(wl.stages):
+        sb = [L_.stage_bytes(si, *c) for L_, c in zip(layers, cnt)]
+        for j, which in enumerate(("shrink", "expand")):
+            b = float(np.mean([x[j] for x in sb]))
+            if best is None or b > best[1]:
+                best = (f"{which}_{st.name}", b)
+    name, nbytes = best
+    us = kern[name]
+    achieved = nbytes / (us * 1e-6) / 1e9
+    cap = None if ranks is not None else TRAFFIC.get((config, name))
+    fresh = cap is not None and cap[2] == kernel_source_digest()
+    roof = dict(kernel=name, bound="hbm", achieved=round(achieved, 1), peak=peaks["hbm_gbs"],
+                unit="GB/s", frac=round(achieved / peaks["hbm_gbs"], 4),
+                traffic=cap[0] if fresh else None,
+                traffic_launch_alg_bytes=cap[1] if fresh else None,
+                traffic_note=None if fresh else (
+                    "no ncu capture of this kernel and workload" if cap is None else
+                    "kernel sources changed since the ncu capture"),
+                bytes_per_launch=int(nbytes), us_per_launch=round(us, 3),
+                peak_source=peaks["source"])
+    # the first stage's shrink against the bf16 tensor peak (a real dense
+    # contraction only when the routed blocks are full, as in `dense`)
+    pairs_per_step = float(np.mean([c[0] for c in cnt]))
+    st0 = wl.stages[0]
+    sname = f"shrink_{st0.name}"
+    flops = 2.0 * pairs_per_step * st0.K * st0.R
+    tflops = flops / (kern[sname] * 1e-6) / 1e12
+    tc_path = (st0.R % 64 == 0 and st0.K % 64 == 0 and wl.BM in (64, 128) and ranks is None
+               and wl.numel >= 32 * min(wl.numel, wl.V))
+    shrink_tensor = dict(kernel=sname, bound="tensor", achieved=round(tflops, 1),
+                         peak=peaks["bf16_tflops"], unit="TFLOP/s",
+                         frac=round(tflops / peaks["bf16_tflops"], 4),
+                         path="tcgen05" if tc_path else "mma.sync",
+                         flops_per_launch=flops, peak_source=peaks["source"])
+    return kern, roof, shrink_tensor
+
+
+def make_layers(torch, mol, wl, n, seed, dev, ranks=None, first=0):
+    from synth import make_layer
+
+    layers = [LayerState(wl, make_layer(wl, seed, layer=i), dev, mol, torch, ranks)
+              for i in range(first, first + n)]
+    for L_ in layers:
+        L_.forward(mol)
+    torch.cuda.synchronize()
+    return layers
+
+
+def layer_alg_bytes(L_, c):
+    """Algorithmic HBM bytes of one layer (both stages and the align) for its counts c."""
+    return sum(sum(L_.stage_bytes(si, *c)) for si in range(len(L_.stages))) + L_.align_bytes()
+
+
+L2_BYTES = 129e6
+
+
+def measure_workload(torch, mol, name, seed, dev, budget_s=0.15):
+    """Short figures for one more workload, same method as the main line: layers rotated
+    past L2, graphs warmed, then a CUDA-event-timed run of whole rotations."""
+    from synth import WORKLOADS
+
+    wl = WORKLOADS[name]
+    layers = make_layers(torch, mol, wl, 1, seed, dev)
+    # distinct layers so that one rotation moves over 3x the L2 (at most 8)
+    nl = int(min(8, max(1, -(-3 * L2_BYTES // layer_alg_bytes(layers[0], layers[0].counts())))))
+    layers += make_layers(torch, mol, wl, nl - 1, seed, dev, first=1)
+    cnt = [L_.counts() for L_ in layers]
+    pairs = float(np.mean([c[0] for c in cnt]))
+    probe_run, probe_warm = layer_steps_timer(torch, mol, layers, nl)
+    probe_warm(nl)
+    ms_rotation = event_ms(torch, probe_run, 3)
+    steps = nl * max(2, int(budget_s / max(ms_rotation * 1e-3, 1e-6)))
+    run, warm = layer_steps_timer(torch, mol, layers, steps)
+    warm(3)
+    ms = event_ms(torch, run, 1) / steps
+    kern, roof, shrink_tensor = kernel_times(torch, mol, wl, layers, cnt, None, steps, name)
+    layer_bytes = float(np.mean([layer_alg_bytes(L_, c) for L_, c in zip(layers, cnt)]))
+    peaks = measured_peaks()
+    out = dict(workload=f"{name}: {wl.note}", steps=steps, layers_rotated=nl,
+               us_per_layer=round(ms * 1e3, 3), value=round(pairs / (ms * 1e-3), 1), unit=UNIT,
+               pairs_per_layer=pairs,
+               layer_hbm=dict(bytes=int(layer_bytes),
+                              achieved_gbs=round(layer_bytes / (ms * 1e-3) / 1e9, 1),
+                              frac=round(layer_bytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)),
+               kernels_us={k: round(v, 3) for k, v in kern.items()}, roofline=roof,
+               shrink_tensor=shrink_tensor)
+    del layers
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_gpu(args):
@@ -271,17 +455,11 @@ def run_gpu(args):
     launches_per_step = plan_tiles + 2 * len(wl.stages)
 
     # A real decode step replays all MoE layers inside one graph; here one graph
-    # holds the rotating layers back to back, and single-layer graphs cover the
-    # K mod layers remainder, so exactly K steps (layers) are timed.
-    graphs = [capture(torch, lambda L_=L_: L_.forward(mol)) for L_ in layers]
-    multi = capture(torch, lambda: [L_.forward(mol) for L_ in layers])
-
-    def run_steps(n):
-        full, rest = divmod(n, len(layers))
-        for _ in range(full):
-            multi.replay()
-        for i in range(rest):
-            graphs[i].replay()
+    # holds the rotating layers back to back, and one more graph holds the first
+    # K mod layers of them, so exactly K steps (layers) are timed and no step runs
+    # as an isolated single-layer graph. Every graph the timed region replays is
+    # replayed before it (at least twice), whatever --warmup is.
+    run_steps, warm_steps = layer_steps_timer(torch, mol, layers, args.steps)
 
     props = torch.cuda.get_device_properties(dev)
     gpu_id = str(local)
@@ -293,15 +471,14 @@ def run_gpu(args):
     time.sleep(0.3)
 
     # ---- timed region: exactly K steps -----------------------------------------------
-    run_steps(args.warmup)
-    torch.cuda.synchronize()
+    warm_steps(args.warmup)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0 = time.time()
     ev0.record()
-    run_steps(args.steps)
+    run_steps()
     ev1.record()
     torch.cuda.synchronize()
     t1 = time.time()
@@ -317,76 +494,10 @@ def run_gpu(args):
 
     # ---- per-kernel timing (each kernel alone in its own graphs, same rotation) -------
     peaks = measured_peaks()
-    kern = {}
-    roof = None
-    shrink_tensor = None
+    kern, roof, shrink_tensor = {}, None, None
     if not args.no_kernels:
-        def stage_call(L_, si, which):
-            d = L_.stages[si]
-            st = d["st"]
-            if which == "shrink":
-                return lambda: mol.mol_lora_shrink(d["x"], st.x_row_div, d["A"], st.stage.S,
-                                                   L_.routing, d["inter"], lora_ranks=L_.ranks_d,
-                                                   num_experts=wl.E)
-            return lambda: mol.mol_lora_expand(d["inter"], d["B"], st.stage.S, wl.scale,
-                                               L_.routing, d["out"], lora_ranks=L_.ranks_d,
-                                               lora_scalings=L_.scal_d, num_experts=wl.E)
-
-        def align_call(L_):
-            return lambda: mol.mol_align_block_size(L_.routing.vtopk_ids, wl.V, wl.BM,
-                                                    routing=L_.routing, workspace=L_.ws)
-
-        reps = 4  # launches per graph = layers x reps, back to back on one stream
-
-        def per_launch_us(calls):
-            g = capture(torch, lambda: [f() for _ in range(reps) for f in calls])
-            n = max(20, min(args.steps, 2000) // (reps * len(calls)))
-            return time_graphs(torch, [g], n, 3) * 1e3 / (reps * len(calls))
-
-        kern["align"] = per_launch_us([align_call(L_) for L_ in layers])
-        # per-token adapter ids of the batch: one request per token (decode) or
-        # requests of 64 tokens, adapter slots of the layer's tokens
-        req_len = 1 if wl.T <= 256 else 64
-        nreq = (wl.T + req_len - 1) // req_len
-        wi = torch.from_numpy(layers[0].li.lora_ids[::req_len].astype(np.int32)).to(dev)
-        seg = torch.from_numpy(np.minimum(np.arange(nreq + 1) * req_len, wl.T).astype(np.int32)).to(dev)
-        tok_ids = torch.empty(wl.T, dtype=torch.int32, device=dev)
-        kern["token_lora_ids"] = per_launch_us(
-            [lambda: mol.mol_token_lora_ids(wi, seg, wl.T, wl.L, layers[0].ranks_d, tok_ids)])
-        for si, st in enumerate(wl.stages):
-            for which in ("shrink", "expand"):
-                kern[f"{which}_{st.name}"] = per_launch_us([stage_call(L_, si, which) for L_ in layers])
-        # dominant kernel: the stage kernel with the most algorithmic bytes
-        best = None
-        for si, st in enumerate(wl.stages):
-            sb = [L_.stage_bytes(si, *c) for L_, c in zip(layers, cnt)]
-            for j, which in enumerate(("shrink", "expand")):
-                b = float(np.mean([x[j] for x in sb]))
-                if best is None or b > best[1]:
-                    best = (f"{which}_{st.name}", b)
-        name, nbytes = best
-        us = kern[name]
-        achieved = nbytes / (us * 1e-6) / 1e9
-        cap = None if ranks is not None else TRAFFIC.get((args.config, name))
-        roof = dict(kernel=name, bound="hbm", achieved=round(achieved, 1), peak=peaks["hbm_gbs"],
-                    unit="GB/s", frac=round(achieved / peaks["hbm_gbs"], 4),
-                    traffic=None if cap is None else cap[0],
-                    traffic_launch_alg_bytes=None if cap is None else cap[1],
-                    bytes_per_launch=int(nbytes),
-                    us_per_launch=round(us, 3), peak_source=peaks["source"])
-        # the first stage's shrink against the bf16 tensor peak (a real dense
-        # contraction only when the routed blocks are full, as in `dense`)
-        st0 = wl.stages[0]
-        sname = f"shrink_{st0.name}"
-        flops = 2.0 * pairs_per_step * st0.K * st0.R
-        tflops = flops / (kern[sname] * 1e-6) / 1e12
-        tc_path = (st0.R % 64 == 0 and st0.K % 64 == 0 and wl.BM in (64, 128) and ranks is None
-                   and wl.numel >= 32 * min(wl.numel, wl.V))
-        shrink_tensor = dict(kernel=sname, bound="tensor", achieved=round(tflops, 1),
-                             peak=peaks["bf16_tflops"], unit="TFLOP/s",
-                             frac=round(tflops / peaks["bf16_tflops"], 4),
-                             path="tcgen05" if tc_path else "mma.sync",
-                             flops_per_launch=flops, peak_source=peaks["source"])
+        kern, roof, shrink_tensor = kernel_times(torch, mol, wl, layers, cnt, ranks, args.steps,
+                                                 args.config)
 
     layer_bytes = float(np.mean([sum(sum(L_.stage_bytes(si, *c)) for si in range(len(wl.stages)))
                                  + L_.align_bytes() for L_, c in zip(layers, cnt)]))
@@ -395,6 +506,17 @@ def run_gpu(args):
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, torch, mol, wl, layers, pairs_per_step, world, dev)
+
+    # ---- the other workloads, short (rank 0 of a single-process run) ------------------
+    extra = {}
+    names = [] if args.extra in ("", "none") else [n for n in args.extra.split(",") if n]
+    if world == 1 and names:
+        del layers
+        torch.cuda.empty_cache()
+        for name in names:
+            if name == args.config:
+                continue
+            extra[name] = measure_workload(torch, mol, name, args.seed, dev)
 
     out = dict(metric=METRIC, value=round(value, 1), unit=UNIT, n_gpus=world, steps=args.steps,
                warmup=args.warmup, ms_per_step=round(ms, 6), us_per_layer=round(ms * 1e3, 3),
@@ -406,7 +528,9 @@ def run_gpu(args):
                            pairs_per_layer=pairs_per_step, layers_rotated=args.layers,
                            adapter_ranks=ranks,
                            l2="inputs larger than L2: steps rotate over distinct layers",
-                           graph=f"{args.layers} layers per graph replay (remainder: one layer per replay)",
+                           graph=f"{args.layers} layers per graph replay; the K mod {args.layers} "
+                                 "remainder in one more graph of that many layers; every graph "
+                                 "replayed at least twice before the timed region",
                            parallelism=f"replicas{world}"),
                layer_hbm=dict(bytes=int(layer_bytes),
                               achieved_gbs=round(layer_bytes / (ms * 1e-3) / 1e9, 1),
@@ -415,7 +539,8 @@ def run_gpu(args):
                roofline=roof, shrink_tensor=shrink_tensor, e2e=e2e,
                gpu_launches=launches_per_step * args.steps,
                clocks=dict(sm_mhz=clk["sm_mhz"], sm_max_mhz=clk["sm_max_mhz"],
-                           reasons=clk["reasons"], samples=clk["samples"]))
+                           reasons=clk["reasons"], samples=clk["samples"]),
+               workloads=extra or None)
     if rank == 0 and not args.no_cpu:
         out["cpu_baseline"] = cpu_baseline(args)
     if world > 1:
@@ -542,15 +667,25 @@ E2E_ROUNDS = 4
 
 
 # traffic (dram bytes read + written) of one captured launch, with the algorithmic bytes of
-# that same launch (the first layer of the workload, seed 0), keyed by (workload, kernel);
-# absent until the current kernel has been captured. Sources:
-# profiles/decode_stage_kernels_ncu_full.md and profiles/dominant_kernels_traffic.md.
+# that same launch (the first layer of the workload, seed 0) and the digest of the kernel
+# sources it was captured with, keyed by (workload, kernel). An entry whose digest differs
+# from the current sources is stale and reported as null. Sources: the ncu summaries under
+# profiles/.
 TRAFFIC = {
-    ("decode", "shrink_gate_up"): (35505920 + 0, 35506176),
-    ("wide", "expand_down"): (41633280 + 39680, 43469824),
-    ("ep", "shrink_gate_up"): (569522432 + 6452736, 572089984),
-    ("dense", "expand_down"): (344121088 + 215358976, 612368384),
 }
+
+
+def kernel_source_digest() -> str:
+    """sha256 (first 16 hex digits) over the library's CUDA sources and headers."""
+    import hashlib
+
+    csrc = os.path.join(ROOT, "moe_lora_virtual_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(f.encode())
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
 
 
 # --------------------------------------------------------------------------- CPU (oracle)

@@ -59,7 +59,11 @@ extern "C" {
 /* Bucket cap of align: V + 1 (sentinel) <= 8192 (sglang PR 24262 prhub summary,
  * "Implementation breakdown" item 2 and "Risks" item 2: at most 8191 virtual experts). */
 #define MOL_MAX_BUCKETS 8192
-/* Largest number of (token, slot) pairs one call accepts. */
+/* Largest number of (token, slot) pairs one call accepts: 4 Mi pairs (half a
+ * million tokens at top-8). The align sets it: a tile of pairs keeps its
+ * bucket keys in shared memory (2 bytes each, at most 32768 per tile), at
+ * most 128 tiles take part, and each warp counts its pairs per bucket in
+ * 16-bit counters. */
 #define MOL_MAX_NUMEL (1 << 22)
 
 /* Library ABI version (major * 100 + minor). */
@@ -138,8 +142,11 @@ int32_t mol_align_block_size(const int32_t* vtopk_ids, int64_t numel, int32_t nu
  * counterpart of this call; it is a convenience of this library.
  * The scratch is a fixed 1 MiB array compiled into the library (every GPU that
  * loads the library holds it until the process exits). Sizes whose workspace
- * (mol_workspace_bytes) exceeds 1 MiB are rejected with MOL_ERR_CAPACITY, for
- * example more than about 100k pairs with 8192 buckets. Outputs, capacity and
+ * (mol_workspace_bytes) exceeds 1 MiB are rejected with MOL_ERR_CAPACITY. Up to
+ * 524288 pairs that workspace is 4 * (tiles * (V + 1) + (V + 1) + numel) bytes
+ * rounded up to 256, with tiles = ceil(numel / 4096) (0 bytes up to 4096
+ * pairs), so the largest accepted size is 81920 pairs at V = 8191 and 126976
+ * pairs at V = 4095. Outputs, capacity and
  * the other arguments are those of mol_align_block_size, and so are the results
  * (bit-identical). No allocation of any kind is made.
  * Every call shares the one array and it keeps the previous call's contents;
@@ -168,7 +175,7 @@ int32_t mol_align_block_size_noalloc(const int32_t* vtopk_ids, int64_t numel,
  *   x_row_div  topk for token-row input (gate_up), 1 for per-pair input (down)
  *   lora_a     bf16 [num_vexperts, R, K], contiguous
  *   inter      fp32 [numel, R], contiguous
- * Contract: K % 8 == 0, K <= 65536, R % 16 == 0, R <= 1024, x_row_stride % 8 == 0,
+ * Contract: K % 8 == 0, K <= 65536, R % 8 == 0, R <= 1024, x_row_stride % 8 == 0,
  * x, lora_a, inter 16-byte aligned, capacity % block_m == 0. x must hold
  * ceil(numel / x_row_div) rows.
  * Per-adapter ranks (fork PR #24 "fix(lora): complete the '-1 = no adapter'
@@ -207,7 +214,7 @@ int32_t mol_lora_shrink(const void* x, int64_t x_row_stride, int32_t x_row_div, 
  *   lora_b       bf16 [num_vexperts, num_slices*slice_n, rank], contiguous
  *   topk_weights fp32 [numel] or NULL
  *   out          bf16, row i at out + i * out_row_stride (elements), updated in place
- * Contract: rank in {16, 32, 64, 128}, slice_n % 8 == 0, out_row_stride % 8 == 0,
+ * Contract: rank in {8, 16, 32, 64, 128}, slice_n % 8 == 0, out_row_stride % 8 == 0,
  * out_row_stride >= num_slices * slice_n, inter/lora_b/out 16-byte aligned.
  * Per-adapter rank and scaling (adapter of v = v / num_experts):
  *   lora_ranks     int32 [num_vexperts / num_experts] or NULL: the sum runs over
@@ -274,21 +281,39 @@ int32_t mol_lora_forward(const void* x, int64_t x_row_stride, int32_t x_row_div,
  * token still gets some value in {-1} U [0, max_loras) and nothing is read out
  * of bounds.
  */
+int32_t mol_token_lora_ids(const int32_t* weight_indices, const int32_t* seg_indptr,
+                           int32_t num_reqs, int64_t num_tokens, int32_t max_loras,
+                           const int32_t* lora_ranks, int32_t* lora_ids, void* stream);
+
+
 /*
  * Every wait inside this library's kernels (on a barrier, a bulk copy or a
  * tensor-core accumulator) is bounded; when one runs out the kernel records a
- * fault bit, stops its work early and exits instead of hanging, so its outputs
- * are then incomplete. This call waits for the current device to be idle
- * (cudaDeviceSynchronize), writes the bits recorded since the last call to
- * *flags (0 = none; bit 0 = a wait ran out) and clears them. It synchronizes,
- * so it belongs in checks and tests, not in a captured or timed sequence.
+ * fault bit, stops its work early and exits instead of hanging. This call
+ * waits for the current device to be idle (cudaDeviceSynchronize), writes the
+ * bits recorded since the last call to *flags (0 = none; bit 0 = a wait ran
+ * out) and clears them. It synchronizes, so it belongs in checks and tests,
+ * not in a captured or timed sequence.
+ * After a wait ran out, the outputs of the call that recorded it are undefined
+ * (rows may be missing or partial). The shrink's producer waits, bounded, for
+ * the copies it issued before its block exits; the tensor-core shrink cannot
+ * observe its weight copies apart from the row copies that share their
+ * barrier, so a block of it that gives up may exit with a copy in flight.
  * (No counterpart on the pages: the pages' kernels have no bounded waits.)
  */
 int32_t mol_take_fault_flags(uint32_t* flags);
 
-int32_t mol_token_lora_ids(const int32_t* weight_indices, const int32_t* seg_indptr,
-                           int32_t num_reqs, int64_t num_tokens, int32_t max_loras,
-                           const int32_t* lora_ranks, int32_t* lora_ids, void* stream);
+/*
+ * Test hook of the bounded waits (no counterpart on the pages). With
+ * stall_producer = 1 the producer warp of every block of mol_lora_shrink (and
+ * of the shrink inside mol_lora_forward, on the mma path) leaves before it
+ * issues any copy, so the consumers' waits run out with nothing in flight and
+ * record bit 0 of mol_take_fault_flags; 0 restores normal operation.
+ * wait_limit_ns bounds every wait of that shrink (0 = the default, one
+ * second). Synchronizes the device; for tests only, never while another
+ * thread uses the library. Returns MOL_ERR_INVALID_ARG for stall_producer > 1.
+ */
+int32_t mol_debug_wait_test(uint32_t stall_producer, uint64_t wait_limit_ns);
 
 #ifdef __cplusplus
 }

@@ -29,7 +29,7 @@ EXPORTS = (
     "mol_version", "mol_status_string", "mol_last_cuda_error", "mol_align_capacity",
     "mol_workspace_bytes", "mol_virtual_topk", "mol_align_block_size", "mol_lora_shrink",
     "mol_lora_expand", "mol_lora_forward", "mol_align_block_size_noalloc", "mol_token_lora_ids",
-    "mol_take_fault_flags",
+    "mol_take_fault_flags", "mol_debug_wait_test",
 )
 
 _lib = None
@@ -57,6 +57,7 @@ _SIGS = {
                                 _P, _P, _P, _P, _SZ, _P]),
     "mol_token_lora_ids": (_I32, [_P, _P, _I32, _I64, _I32, _P, _P, _P]),
     "mol_take_fault_flags": (_I32, [ctypes.POINTER(ctypes.c_uint32)]),
+    "mol_debug_wait_test": (_I32, [ctypes.c_uint32, ctypes.c_uint64]),
 }
 
 
@@ -302,3 +303,11 @@ def mol_take_fault_flags() -> int:
     _check("mol_take_fault_flags", library().mol_take_fault_flags(ctypes.byref(v)))
     return int(v.value)
 
+
+
+def mol_debug_wait_test(stall_producer: bool, wait_limit_ns: int = 0) -> None:
+    """Test hook of the bounded waits: with stall_producer the shrink's producer warps issue
+    nothing, so its consumers' waits run out (after wait_limit_ns; 0 = one second) and record
+    a fault bit. Synchronizes the device."""
+    _check("mol_debug_wait_test", library().mol_debug_wait_test(int(bool(stall_producer)),
+                                                                int(wait_limit_ns)))

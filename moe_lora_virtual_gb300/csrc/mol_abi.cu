@@ -2,6 +2,7 @@
 // Host code only: validation, device checks, dispatch to the launchers.
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "mol.h"
@@ -21,8 +22,9 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 bool valid_block_m(int32_t bm) { return bm == 16 || bm == 32 || bm == 64 || bm == 128; }
 
 // Per device: 0 = unchecked, 1 = ready (sm_103, kernels prepared), 2 = unsupported.
+// Read without the lock on every call; written under it once per device.
 constexpr int kMaxDevices = 64;
-int g_device_state[kMaxDevices] = {0};
+std::atomic<int> g_device_state[kMaxDevices] = {};
 std::mutex g_device_mutex;
 
 // Checks the current device is an sm_103 part and prepares kernel attributes
@@ -32,22 +34,22 @@ int32_t ensure_device() {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e);
   if (dev < 0 || dev >= kMaxDevices) return MOL_ERR_UNSUPPORTED;
-  if (g_device_state[dev] == 1) return MOL_OK;
+  if (g_device_state[dev].load(std::memory_order_acquire) == 1) return MOL_OK;
   std::lock_guard<std::mutex> lock(g_device_mutex);
-  if (g_device_state[dev] == 0) {
+  if (g_device_state[dev].load(std::memory_order_relaxed) == 0) {
     int major = 0, minor = 0;
     e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
     if (e != cudaSuccess) return cuda_fail(e);
     if (major != 10 || minor != 3) {
-      g_device_state[dev] = 2;
+      g_device_state[dev].store(2, std::memory_order_release);
     } else {
       e = mol::prepare_kernels();
       if (e != cudaSuccess) return cuda_fail(e);
-      g_device_state[dev] = 1;
+      g_device_state[dev].store(1, std::memory_order_release);
     }
   }
-  return g_device_state[dev] == 1 ? MOL_OK : MOL_ERR_UNSUPPORTED;
+  return g_device_state[dev].load(std::memory_order_relaxed) == 1 ? MOL_OK : MOL_ERR_UNSUPPORTED;
 }
 
 int32_t check_align_args(int64_t numel, int32_t num_vexperts, int32_t block_m) {
@@ -73,7 +75,7 @@ int32_t check_shrink_args(const void* x, int64_t x_row_stride, int32_t x_row_div
   if (K <= 0 || x_row_div < 1 || num_slices < 1 || rank < 1 || x_row_stride < K)
     return MOL_ERR_INVALID_ARG;
   const int64_t R = (int64_t)num_slices * rank;
-  if (K % 8 != 0 || K > mol::kShrinkMaxK || x_row_stride % 8 != 0 || R % 16 != 0 || R > 1024)
+  if (K % 8 != 0 || K > mol::kShrinkMaxK || x_row_stride % 8 != 0 || R % 8 != 0 || R > 1024)
     return MOL_ERR_UNSUPPORTED;
   if (numel > 0 && (!x || !lora_a || !inter)) return MOL_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(lora_a) || !aligned16(inter)) return MOL_ERR_UNSUPPORTED;
@@ -85,7 +87,8 @@ int32_t check_expand_args(const float* inter, const void* lora_b, int32_t num_sl
                           int64_t numel) {
   if (num_slices < 1 || rank < 1 || slice_n < 1) return MOL_ERR_INVALID_ARG;
   if (out_row_stride < (int64_t)num_slices * slice_n) return MOL_ERR_INVALID_ARG;
-  if (!(rank == 16 || rank == 32 || rank == 64 || rank == 128)) return MOL_ERR_UNSUPPORTED;
+  if (!(rank == 8 || rank == 16 || rank == 32 || rank == 64 || rank == 128))
+    return MOL_ERR_UNSUPPORTED;
   if (slice_n % 8 != 0 || out_row_stride % 8 != 0) return MOL_ERR_UNSUPPORTED;
   if (numel > 0 && (!inter || !lora_b || !out)) return MOL_ERR_INVALID_ARG;
   if (!aligned16(inter) || !aligned16(lora_b) || !aligned16(out)) return MOL_ERR_UNSUPPORTED;
@@ -167,6 +170,15 @@ int32_t mol_take_fault_flags(uint32_t* flags) {
   if (e != cudaSuccess) return cuda_fail(e);
   *flags = a | b;
   return MOL_OK;
+}
+
+int32_t mol_debug_wait_test(uint32_t stall_producer, uint64_t wait_limit_ns) {
+  if (stall_producer > 1) return MOL_ERR_INVALID_ARG;
+  int32_t st = ensure_device();
+  if (st != MOL_OK) return st;
+  const unsigned long long lim = wait_limit_ns == 0 ? 1000000000ull : wait_limit_ns;
+  cudaError_t e = mol::set_wait_test(stall_producer, lim);
+  return e == cudaSuccess ? MOL_OK : cuda_fail(e);
 }
 
 int32_t mol_token_lora_ids(const int32_t* weight_indices, const int32_t* seg_indptr,
@@ -337,22 +349,26 @@ constexpr size_t kNoAllocScratchBytes = size_t(1) << 20;
 __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 // Device address of g_noalloc_scratch, per device. In host code the array's
 // name is only a host-side stand-in, so the address is looked up once per
-// device with that device current.
-void* g_noalloc_scratch_addr[kMaxDevices] = {nullptr};
+// device with that device current; later calls read the cached address
+// without taking a lock.
+std::atomic<void*> g_noalloc_scratch_addr[kMaxDevices] = {};
 
 int32_t noalloc_scratch(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e);
   if (dev < 0 || dev >= kMaxDevices) return MOL_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_device_mutex);
-  if (g_noalloc_scratch_addr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess) return cuda_fail(e);
-    g_noalloc_scratch_addr[dev] = p;
+  void* p = g_noalloc_scratch_addr[dev].load(std::memory_order_acquire);
+  if (p == nullptr) {
+    std::lock_guard<std::mutex> lock(g_device_mutex);
+    p = g_noalloc_scratch_addr[dev].load(std::memory_order_relaxed);
+    if (p == nullptr) {
+      e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+      if (e != cudaSuccess) return cuda_fail(e);
+      g_noalloc_scratch_addr[dev].store(p, std::memory_order_release);
+    }
   }
-  *out = g_noalloc_scratch_addr[dev];
+  *out = p;
   return MOL_OK;
 }
 

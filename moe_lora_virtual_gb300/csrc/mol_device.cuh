@@ -107,15 +107,17 @@ MOL_DEV uint64_t global_ns() {
 // Longest time a barrier wait may take before it gives up (the waits inside
 // these kernels last microseconds; no kernel runs for more than milliseconds).
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
-// Bounded wait: gives up, returning false, after `max_iter` polls or one
-// second of wall-clock time, whichever comes first (a poll may suspend the
-// thread for a hardware-defined time, so the clock bounds the total).
-MOL_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t max_iter) {
+// Bounded wait: gives up, returning false, after `max_iter` polls or
+// `limit_ns` of wall-clock time (one second by default), whichever comes first
+// (a poll may suspend the thread for a hardware-defined time, so the clock
+// bounds the total).
+MOL_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t max_iter,
+                       uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t i = 0; i < max_iter; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (global_ns() - t0 > kWaitLimitNs) return false;
+    if (global_ns() - t0 > limit_ns) return false;
   }
   return false;
 }

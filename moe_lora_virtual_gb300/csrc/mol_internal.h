@@ -111,6 +111,8 @@ cudaError_t launch_shrink_tc(const void* x, int64_t x_stride, int x_div, int K, 
 // ran out); read and cleared by mol_take_fault_flags.
 cudaError_t take_lora_faults(unsigned* out);
 cudaError_t take_tc_faults(unsigned* out);
+// Test controls of the shrink's bounded waits (mol_debug_wait_test).
+cudaError_t set_wait_test(unsigned stall, unsigned long long limit_ns);
 
 // Largest contraction width accepted by the shrink (it streams K in chunks).
 constexpr int kShrinkMaxK = 1 << 16;

@@ -41,11 +41,27 @@ constexpr uint32_t kWaitPolls = 1u << 22;  // bounded mbarrier waits
 // Faults recorded instead of hanging (see kFaultBulkTimeout).
 __device__ unsigned int g_fault_flags;
 
+// Test controls of the shrink's bounded waits, set only through
+// mol_debug_wait_test: bit 0 of g_test_stall makes the producer warp leave
+// before it issues any copy (so the consumers' waits run out with nothing in
+// flight), and g_wait_limit_ns is the wall-clock limit of every wait of the
+// shrink. Both are read once per block.
+__device__ unsigned int g_test_stall;
+__device__ unsigned long long g_wait_limit_ns = kWaitLimitNs;
+
 cudaError_t take_lora_faults(unsigned* out) {
   cudaError_t e = cudaMemcpyFromSymbol(out, g_fault_flags, sizeof(unsigned));
   if (e != cudaSuccess) return e;
   const unsigned zero = 0;
   return cudaMemcpyToSymbol(g_fault_flags, &zero, sizeof(unsigned));
+}
+
+cudaError_t set_wait_test(unsigned stall, unsigned long long limit_ns) {
+  cudaError_t e = cudaDeviceSynchronize();  // no shrink may be running while they change
+  if (e != cudaSuccess) return e;
+  e = cudaMemcpyToSymbol(g_test_stall, &stall, sizeof(unsigned));
+  if (e != cudaSuccess) return e;
+  return cudaMemcpyToSymbol(g_wait_limit_ns, &limit_ns, sizeof(unsigned long long));
 }
 
 // Routing words of one work item as loaded: a producer fetches them one item
@@ -145,6 +161,7 @@ lora_shrink_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, 
     fence_mbar_init();
   }
   __syncthreads();
+  const uint64_t wlim = g_wait_limit_ns;
   // The activations may come from the kernel right before this one: only the
   // producer reads global memory, and it reads them after griddepcontrol.wait.
   // With `early` (inside mol_lora_forward, routing reused) routing words and
@@ -157,6 +174,7 @@ lora_shrink_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, 
 
   if (warp == kConsumers) {
     // ------------------------------------------------------------ producer
+    if (g_test_stall & 1u) return;  // test control: nothing is issued, the consumers' waits run out
     const int64_t G = gridDim.x;
     uint32_t q = 0;   // stage uses issued
     uint32_t jn = 0;  // jobs issued
@@ -165,7 +183,7 @@ lora_shrink_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, 
       st = (int)(q % kStages);
       const uint32_t ph = (q / kStages) & 1;
       bool ok = true;
-      if (lane == 0) ok = mbar_wait(&empty[st], ph ^ 1, kWaitPolls);
+      if (lane == 0) ok = mbar_wait(&empty[st], ph ^ 1, kWaitPolls, wlim);
       return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     };
     auto fetch = [&](int64_t it, Raw& r) {
@@ -289,19 +307,26 @@ lora_shrink_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, 
       pdl_wait();
       pdl_launch_dependents();
     }
-    if (fault) {
-      if (lane == 0) atomicOr(&g_fault_flags, kFaultBulkTimeout);
-    } else {
+    if (!fault) {
       int st;
       if (acquire(st)) {
         if (lane == 0) {
           hdr[st].job = -1;
           mbar_arrive(&full[st]);
         }
-      } else if (lane == 0) {
-        atomicOr(&g_fault_flags, kFaultBulkTimeout);
+      } else {
+        fault = true;
       }
     }
+    if (fault && lane == 0) {
+      atomicOr(&g_fault_flags, kFaultBulkTimeout);
+      // Let the copies of the last uses of each stage land (bounded) before the
+      // block exits and its shared memory is released: a stage's full barrier
+      // completes when its copies have arrived, whether or not anyone reads them.
+      for (uint32_t u = q > (uint32_t)kStages ? q - kStages : 0; u < q; ++u)
+        mbar_wait(&full[u % kStages], (u / kStages) & 1, kWaitPolls, wlim);
+    }
+    __syncwarp();
     return;
   }
 
@@ -312,7 +337,7 @@ lora_shrink_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, 
   float acc2[4] = {0.f, 0.f, 0.f, 0.f};  // odd k blocks: a second, independent mma chain
   for (uint32_t q = 0;; ++q) {
     const int st = (int)(q % kStages);
-    if (!mbar_wait(&full[st], (q / kStages) & 1, kWaitPolls)) {
+    if (!mbar_wait(&full[st], (q / kStages) & 1, kWaitPolls, wlim)) {
       if (lane == 0) atomicOr(&g_fault_flags, kFaultBulkTimeout);
       return;
     }
@@ -569,7 +594,7 @@ lora_expand_kernel(const float* __restrict__ inter, int R, const uint16_t* __res
   }
 }
 
-// Staged expand, rank 16, 32 or 64. One item = (routed block t, slice s, 256
+// Staged expand, rank 8, 16, 32 or 64. One item = (routed block t, slice s, 256
 // output columns). One thread copies the item's lora_b rows (256 x RK bf16,
 // contiguous in [V, N, r]) into shared memory with a bulk copy, and every
 // thread copies its pieces of the output rows to update with cp.async, so
@@ -581,7 +606,9 @@ lora_expand_kernel(const float* __restrict__ inter, int R, const uint16_t* __res
 // both operands are zeroed past the adapter's rank; the delta is scaled by its
 // scaling) are those of lora_expand_kernel, so both kernels give bit-identical
 // outputs. DB (blocks of many rows): two staged row tiles, the next tile's
-// output rows are copied while the current one computes.
+// output rows are copied while the current one computes. Rank 8 runs the
+// rank-16 step (k = 16) with the upper eight k columns zero in both operands:
+// quads tq = 2, 3 of a warp, which would hold them, load nothing.
 constexpr int kStCols = 256;
 constexpr int kStGroups = kStCols / (kExpandThreads / 32) / 32;  // column groups per warp
 constexpr int kStOutPitch = kStCols + 32;  // staged output row, elements (64-byte skew per row)
@@ -599,8 +626,8 @@ lora_expand_st_kernel(const float* __restrict__ inter, int R, const uint16_t* __
                       int num_vexperts, uint16_t* __restrict__ out, int64_t out_stride,
                       int chunks_per_slice, const int* __restrict__ lora_ranks,
                       const float* __restrict__ lora_scalings, int num_experts) {
-  static_assert(RK == 16 || RK == 32 || RK == 64, "staged expand: rank 16, 32 or 64");
-  constexpr bool K16 = (RK == 16);
+  static_assert(RK == 8 || RK == 16 || RK == 32 || RK == 64, "staged expand: rank 8, 16, 32 or 64");
+  constexpr bool K16 = (RK <= 16);
   constexpr int KB = K16 ? 1 : RK / 32;  // k blocks (32 wide, or one 16-wide block)
   extern __shared__ __align__(128) unsigned char st_smem[];
   uint16_t* wsm = reinterpret_cast<uint16_t*>(st_smem);  // kStCols x RK lora_b rows
@@ -652,6 +679,7 @@ lora_expand_st_kernel(const float* __restrict__ inter, int R, const uint16_t* __
   }
 
   const int lane = tid & 31, warp = tid >> 5, g = lane >> 2, tq = lane & 3;
+  const bool kq = RK != 8 || tq < 2;       // this quad's k columns exist (rank 8: the first two)
   const int wcol = warp * 32 * kStGroups;  // the warp's first column inside the item
   const float4 zf = make_float4(0.f, 0.f, 0.f, 0.f);
   const uint4 zu = make_uint4(0, 0, 0, 0);
@@ -703,8 +731,8 @@ lora_expand_st_kernel(const float* __restrict__ inter, int R, const uint16_t* __
     uint32_t h[KB][8], l[KB][8];
 #pragma unroll
     for (int kb = 0; kb < KB; ++kb) {
-      float4 a0 = i0 >= 0 ? ld_l2_f4(p0 + kb * 32) : zf;
-      float4 a1 = i1 >= 0 ? ld_l2_f4(p1 + kb * 32) : zf;
+      float4 a0 = (kq && i0 >= 0) ? ld_l2_f4(p0 + kb * 32) : zf;
+      float4 a1 = (kq && i1 >= 0) ? ld_l2_f4(p1 + kb * 32) : zf;
       if (ADAPT && rl < RK) {
         mask_cols(a0, (K16 ? 4 * tq : kb * 32 + 8 * tq), rl);
         mask_cols(a1, (K16 ? 4 * tq : kb * 32 + 8 * tq), rl);
@@ -752,7 +780,7 @@ lora_expand_st_kernel(const float* __restrict__ inter, int R, const uint16_t* __
         const int wr = nb + 8 * (g >> 1) + 2 * u + (g & 1);
         const bool bv = wr < ncols;
         if constexpr (K16) {
-          const uint2 q2 = bv ? lds8(wsm + wr * RK + 4 * tq) : make_uint2(0, 0);
+          const uint2 q2 = (bv && kq) ? lds8(wsm + wr * RK + 4 * tq) : make_uint2(0, 0);
           uint4 q = make_uint4(q2.x, q2.y, 0, 0);
           if (ADAPT && rl < RK) mask_bf16x8(q, 4 * tq, rl);
           mma_16816(acc[u], h[0][0], h[0][1], h[0][2], h[0][3], q.x, q.y);
@@ -829,6 +857,10 @@ cudaError_t prepare_lora_kernels() {
   if (e != cudaSuccess) return e;
   e = prepare_expand_st<16, false>();
   if (e != cudaSuccess) return e;
+  e = prepare_expand_st<8, true>();
+  if (e != cudaSuccess) return e;
+  e = prepare_expand_st<8, false>();
+  if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(lora_shrink_kernel<false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sp::kSmem);
   if (e != cudaSuccess) return e;
@@ -883,7 +915,7 @@ cudaError_t launch_expand(const float* inter, const void* lora_b, int S, int r, 
   const int R = S * r;
   const uint16_t* b = static_cast<const uint16_t*>(lora_b);
   uint16_t* o = static_cast<uint16_t*>(out);
-  if (r == 16 || r == 32 || r == 64) {
+  if (r == 8 || r == 16 || r == 32 || r == 64) {
     const int cps_st = (Ns + kStCols - 1) / kStCols;
     if (nblk * S * cps_st > INT32_MAX) return cudaErrorInvalidConfiguration;
     const dim3 grid_st((unsigned)(nblk * S * cps_st));
@@ -901,6 +933,7 @@ cudaError_t launch_expand(const float* inter, const void* lora_b, int S, int r, 
 #define MOL_EXPAND_ST_RK(RK)                                                              \
   return early ? (adapt ? MOL_EXPAND_ST_A(RK, true, true) : MOL_EXPAND_ST_A(RK, true, false)) \
                : (adapt ? MOL_EXPAND_ST_A(RK, false, true) : MOL_EXPAND_ST_A(RK, false, false))
+    if (r == 8) MOL_EXPAND_ST_RK(8);
     if (r == 16) MOL_EXPAND_ST_RK(16);
     if (r == 32) MOL_EXPAND_ST_RK(32);
     MOL_EXPAND_ST_RK(64);

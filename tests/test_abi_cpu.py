@@ -43,7 +43,7 @@ def declared_functions():
 def test_exports_every_declared_symbol(mol):
     lib = mol.library()
     names = declared_functions()
-    assert len(names) == 13
+    assert len(names) == 14
     for n in names:
         assert hasattr(lib, n), n
     assert set(names) == set(mol.EXPORTS)
@@ -89,7 +89,12 @@ def test_validation_rejects_before_any_launch(mol):
     assert lib.mol_align_block_size(P(16), (1 << 22) + 1, 16, 16, P(16), 1 << 30, P(16), P(16), None, 0, None) == -3
     # shrink / expand contracts
     assert lib.mol_lora_shrink(P(16), 64, 1, 60, P(16), 1, 16, P(16), P(16), P(16), 64, 16, 8, 4, P(16), 0, None, None) == -3
-    assert lib.mol_lora_shrink(P(16), 64, 1, 64, P(16), 1, 8, P(16), P(16), P(16), 64, 16, 8, 4, P(16), 0, None, None) == -3
+    assert lib.mol_lora_shrink(P(16), 64, 1, 64, P(16), 1, 12, P(16), P(16), P(16), 64, 16, 8, 4, P(16), 0, None, None) == -3
+    # rank 8 is inside the contract: the shape checks pass and the missing pointer is reported
+    assert lib.mol_lora_shrink(None, 64, 1, 64, P(16), 1, 8, P(16), P(16), P(16), 64, 16, 8, 4, P(16), 0, None, None) == -1
+    assert lib.mol_lora_expand(None, P(16), 1, 8, 16, 1.0, None, P(16), P(16), P(16), 64, 16, 8, 4, P(16), 16, 0, None, None, None) == -1
+    assert lib.mol_lora_expand(None, P(16), 1, 12, 16, 1.0, None, P(16), P(16), P(16), 64, 16, 8, 4, P(16), 16, 0, None, None, None) == -3
+    assert lib.mol_debug_wait_test(2, 0) == -1
     assert lib.mol_lora_shrink(P(18), 64, 1, 64, P(16), 1, 16, P(16), P(16), P(16), 64, 16, 8, 4, P(16), 0, None, None) == -3
     assert lib.mol_lora_shrink(P(16), 64, 0, 64, P(16), 1, 16, P(16), P(16), P(16), 64, 16, 8, 4, P(16), 0, None, None) == -1
     assert lib.mol_lora_shrink(P(16), 64, 1, 64, P(16), 1, 16, P(16), P(16), P(16), 65, 16, 8, 4, P(16), 0, None, None) == -1

@@ -65,7 +65,8 @@ def test_byte_model_matches_walked_blocks(name):
 @pytest.mark.parametrize("key", sorted(bench.TRAFFIC))
 def test_traffic_entries_belong_to_their_launch(key):
     name, kernel = key
-    traffic, launch_bytes = bench.TRAFFIC[key]
+    traffic, launch_bytes, digest = bench.TRAFFIC[key]
+    assert len(digest) == 16 and int(digest, 16) >= 0
     wl, li, vt, s, e, n = _routing(name)
     kind, stage_name = kernel.split("_", 1)
     si = [st.stage.name for st in li.stages].index(stage_name)
@@ -74,3 +75,50 @@ def test_traffic_entries_belong_to_their_launch(key):
     # no re-reads: at most the algorithmic bytes plus a little (partial sectors); output rows
     # written into L2 may reach DRAM only after the launch, so the capture can be lower
     assert 0.85 * launch_bytes <= traffic <= 1.02 * launch_bytes
+
+
+class _FakeGraph:
+    def __init__(self, fn, log):
+        self.fn, self.log = fn, log
+
+    def replay(self):
+        self.fn()
+
+
+def test_timed_steps_are_exact_and_every_graph_is_warmed(monkeypatch):
+    """The timed region runs exactly K layer steps, no layer as a graph of its own when K is
+    not a multiple of the rotation, and every graph it replays was replayed before."""
+    log = []
+    graphs = []
+
+    def fake_capture(torch, fn):
+        g = _FakeGraph(fn, log)
+        graphs.append(g)
+        return g
+
+    class L:
+        def __init__(self, i):
+            self.i = i
+
+        def forward(self, mol):
+            log.append(self.i)
+
+    monkeypatch.setattr(bench, "capture", fake_capture)
+    torch = SimpleNamespace(cuda=SimpleNamespace(synchronize=lambda: None))
+    layers = [L(i) for i in range(8)]
+    for steps in (20, 16, 5, 1):
+        graphs.clear()
+        run, warm = bench.layer_steps_timer(torch, None, layers, steps)
+        replayed = set()
+        for g in graphs:
+            orig = g.replay
+            g.replay = (lambda o=orig, g=g: (replayed.add(id(g)), o()))
+        log.clear()
+        warm(5)
+        assert len(log) >= 5
+        assert replayed == {id(g) for g in graphs}     # every graph warmed
+        log.clear()
+        run()
+        assert len(log) == steps
+        assert log == [i % 8 for i in range(8 * (steps // 8))] + list(range(steps % 8))
+        assert len(graphs) == (steps >= 8) + (steps % 8 != 0)

@@ -11,7 +11,7 @@ from tests.gpu_util import (bf16_host, check_inter, check_out, mol_lib, to_dev_b
 
 pytestmark = pytest.mark.gpu
 
-N_CASES = 40
+N_CASES = 48  # seeds 40..47: rank 8
 MAX_ELEMS = 12_000_000  # per weight tensor, so that each case stays small on the host
 
 
@@ -31,6 +31,8 @@ def _draw(seed):
     K = int(rng.choice([8, 64, 200, 520, 1024, 2056, 4096]))
     Ns = 8 * int(rng.integers(1, 90))
     dense = rng.random() < 0.25  # one adapter, few experts: full routed blocks, tensor cores
+    if seed >= 40:  # rank 8 (the expand's k = 16 step with half of k zero)
+        dense, r = False, 8
     if dense:
         E, L = int(rng.integers(2, 7)), 1
         BM, r, S = int(rng.choice([64, 128])), int(rng.choice([32, 64])), int(rng.integers(1, 3))

@@ -122,6 +122,8 @@ SHAPES = [
     (40, 8, 6, 2, 32, 4096, 2, 32, 96, True, 0, 0, False, 0.1),    # two buffers
     (6, 2, 2, 1, 16, 65536, 1, 16, 16, True, 8, 0, False, 0.0),    # largest K of the contract
     (20, 2, 2, 1, 32, 64, 8, 128, 16, False, 0, 8, False, 0.0),    # largest R = 8 x 128
+    (30, 4, 5, 2, 16, 320, 1, 8, 200, True, 8, 8, True, 0.1),      # rank 8, one slice (R = 8)
+    (25, 2, 3, 2, 32, 128, 2, 8, 48, False, 0, 0, False, 0.2),     # rank 8, two slices
 ]
 
 
@@ -169,7 +171,7 @@ def test_shrink_and_expand_entries(shape):
     assert np.array_equal(g_out[:, N:], out_full[:, N:])            # padding columns untouched
 
 
-@pytest.mark.parametrize("r", [16, 32, 64, 128])
+@pytest.mark.parametrize("r", [8, 16, 32, 64, 128])
 @pytest.mark.parametrize("BM", [16, 128])
 def test_small_integers_bit_exact(r, BM):
     """Integer-valued inputs make every fp32 sum exact: the GPU must match bit for bit."""
@@ -205,6 +207,7 @@ def test_small_integers_bit_exact(r, BM):
     (64, 128, 64, True),
     (4, 64, 32, False),    # 4 virtual experts: the next row tile is prefetched
     (4, 128, 16, False),
+    (4, 64, 8, False),
 ])
 def test_expand_hot_expert_many_row_tiles(E, BM, r, few_rows):
     """One expert takes most pairs, so its routed blocks hold up to block_m rows (several
@@ -323,9 +326,9 @@ def test_invalid_arguments_launch_nothing():
     x = torch.zeros((8, 64), dtype=torch.bfloat16, device=dev)
     A = torch.zeros((16, 16, 64), dtype=torch.bfloat16, device=dev)
     inter = torch.zeros((64, 16), dtype=torch.float32, device=dev)
-    # K not a multiple of 8, rank/slices not giving R % 16 == 0, misaligned pointer
+    # K not a multiple of 8, rank/slices not giving R % 8 == 0, misaligned pointer
     assert lib.mol_lora_shrink(P(x), 64, 8, 60, P(A), 1, 16, P(s), P(e), P(n), 4096, 16, 64, 16, P(inter), 0, None, st()) == mol.MOL_ERR_UNSUPPORTED
-    assert lib.mol_lora_shrink(P(x), 64, 8, 64, P(A), 1, 8, P(s), P(e), P(n), 4096, 16, 64, 16, P(inter), 0, None, st()) == mol.MOL_ERR_UNSUPPORTED
+    assert lib.mol_lora_shrink(P(x), 64, 8, 64, P(A), 1, 12, P(s), P(e), P(n), 4096, 16, 64, 16, P(inter), 0, None, st()) == mol.MOL_ERR_UNSUPPORTED
     assert lib.mol_lora_shrink(P(x) + 2, 64, 8, 64, P(A), 1, 16, P(s), P(e), P(n), 4096, 16, 64, 16, P(inter), 0, None, st()) == mol.MOL_ERR_UNSUPPORTED
     assert lib.mol_lora_expand(P(inter), P(A), 1, 24, 16, 1.0, None, P(s), P(e), P(n), 4096, 16, 64, 16, P(x), 64, 0, None, None, st()) == mol.MOL_ERR_UNSUPPORTED
     assert lib.mol_lora_expand(P(inter), P(A), 1, 16, 12, 1.0, None, P(s), P(e), P(n), 4096, 16, 64, 16, P(x), 64, 0, None, None, st()) == mol.MOL_ERR_UNSUPPORTED

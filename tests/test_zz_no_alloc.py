@@ -16,6 +16,7 @@ import ctypes
 import numpy as np
 import pytest
 
+import oracle
 from tests.gpu_util import mol_lib, to_dev_i32, torch_cuda
 
 pytestmark = pytest.mark.gpu
@@ -63,6 +64,50 @@ def test_noalloc_matches_regular_two_calls_in_a_row(numel, V, BM):
         torch.cuda.synchronize()
         for g, w in zip(got[:3], want[:3]):
             assert torch.equal(g, w), f"call {call}: outputs differ"
+        # and against the oracle directly (the sorted ids, block experts and padded count)
+        s, e, n = oracle.align_block_size(vid.cpu().numpy(), V, BM, capacity=got[3])
+        assert int(got[2].item()) == n
+        assert np.array_equal(got[0].cpu().numpy(), s)
+        assert np.array_equal(got[1].cpu().numpy(), e)
+
+
+def _largest_accepted(mol, V, BM):
+    """Largest numel whose align workspace fits the 1 MiB scratch (workspace grows with numel)."""
+    lo, hi = 0, mol.MOL_MAX_NUMEL
+    while lo < hi:
+        mid = (lo + hi + 1) // 2
+        if mol.workspace_bytes(mid, V, BM) <= (1 << 20):
+            lo = mid
+        else:
+            hi = mid - 1
+    return lo
+
+
+def test_noalloc_accepts_the_largest_size_that_fits_and_rejects_the_next():
+    torch = torch_cuda()
+    mol = mol_lib()
+    lib = mol.library()
+    dev = torch.device("cuda:0")
+    V, BM = 8191, 16
+    top = _largest_accepted(mol, V, BM)
+    assert top == 81920  # the size the header states for 8192 buckets
+    rng = np.random.default_rng(77)
+    for _ in range(2):  # two calls in a row on the shared scratch
+        vid = to_dev_i32(rng.integers(-1, V + 1, size=top).astype(np.int32), dev)
+        out = _routing(torch, mol, top, V, BM, dev, -11)
+        assert _noalloc(lib, torch, vid, top, V, BM, out) == mol.MOL_OK
+        torch.cuda.synchronize()
+        s, e, n = oracle.align_block_size(vid.cpu().numpy(), V, BM, capacity=out[3])
+        assert int(out[2].item()) == n
+        assert np.array_equal(out[0].cpu().numpy(), s)
+        assert np.array_equal(out[1].cpu().numpy(), e)
+    over = top + 1
+    assert mol.workspace_bytes(over, V, BM) > (1 << 20)
+    vid = torch.zeros(over, dtype=torch.int32, device=dev)
+    out = _routing(torch, mol, over, V, BM, dev, -12)
+    assert _noalloc(lib, torch, vid, over, V, BM, out) == mol.MOL_ERR_CAPACITY
+    torch.cuda.synchronize()
+    assert torch.all(out[0] == -12) and torch.all(out[2] == -12)
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
