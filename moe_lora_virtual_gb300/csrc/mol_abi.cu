@@ -164,11 +164,12 @@ int32_t mol_take_fault_flags(uint32_t* flags) {
   if (st != MOL_OK) return st;
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cuda_fail(e);
-  unsigned a = 0, b = 0;
+  unsigned a = 0, b = 0, c = 0;
   e = mol::take_lora_faults(&a);
   if (e == cudaSuccess) e = mol::take_tc_faults(&b);
+  if (e == cudaSuccess) e = mol::take_stage_faults(&c);
   if (e != cudaSuccess) return cuda_fail(e);
-  *flags = a | b;
+  *flags = a | b | c;
   return MOL_OK;
 }
 
@@ -318,6 +319,14 @@ int32_t mol_lora_forward(const void* x, int64_t x_row_stride, int32_t x_row_div,
     if (e != cudaSuccess) return cuda_fail(e);
   }
   if (numel == 0 || capacity == 0) return MOL_OK;
+  if (mol::stage_fused_fits(numel, V, num_slices * rank, rank, K, block_m,
+                            lora_ranks != nullptr || lora_scalings != nullptr)) {
+    e = mol::launch_stage(x, x_row_stride, x_row_div, K, lora_a, lora_b, num_slices, rank, slice_n,
+                          scale, topk_weights, sorted_token_ids, expert_ids,
+                          num_tokens_post_padded, capacity, block_m, numel, V, inter, out,
+                          out_row_stride, compute_routing == 0, s);
+    return e == cudaSuccess ? MOL_OK : cuda_fail(e);
+  }
   e = mol::launch_shrink(x, x_row_stride, x_row_div, K, lora_a, num_slices * rank,
                          sorted_token_ids, expert_ids, num_tokens_post_padded, capacity, block_m,
                          numel, V, inter, compute_routing == 0, s, rank, lora_ranks, num_experts);

@@ -365,6 +365,8 @@ cudaError_t prepare_kernels() {
   e = cudaFuncSetAttribute(align_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kAlignSmemMax);
   if (e != cudaSuccess) return e;
+  e = prepare_stage_kernels();
+  if (e != cudaSuccess) return e;
   return prepare_lora_kernels();
 }
 
