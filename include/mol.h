@@ -86,8 +86,9 @@ int64_t mol_align_capacity(int64_t numel, int32_t num_vexperts, int32_t block_m)
 
 /*
  * Bytes of device workspace mol_align_block_size / mol_lora_forward need for
- * these sizes (0 when one thread block does the whole align). Pure host
- * arithmetic. Returns 0 on invalid arguments (the call itself then fails).
+ * these sizes: 0 up to 131072 pairs (one thread block, or one thread-block
+ * cluster, does the whole align), else per-tile histograms and ranks. Pure
+ * host arithmetic. Returns 0 on invalid arguments (the call itself then fails).
  */
 size_t mol_workspace_bytes(int64_t numel, int32_t num_vexperts, int32_t block_m);
 
@@ -142,11 +143,12 @@ int32_t mol_align_block_size(const int32_t* vtopk_ids, int64_t numel, int32_t nu
  * counterpart of this call; it is a convenience of this library.
  * The scratch is a fixed 1 MiB array compiled into the library (every GPU that
  * loads the library holds it until the process exits). Sizes whose workspace
- * (mol_workspace_bytes) exceeds 1 MiB are rejected with MOL_ERR_CAPACITY. Up to
- * 524288 pairs that workspace is 4 * (tiles * (V + 1) + (V + 1) + numel) bytes
- * rounded up to 256, with tiles = ceil(numel / 4096) (0 bytes up to 4096
- * pairs), so the largest accepted size is 81920 pairs at V = 8191 and 126976
- * pairs at V = 4095. Outputs, capacity and
+ * (mol_workspace_bytes) exceeds 1 MiB are rejected with MOL_ERR_CAPACITY. That
+ * workspace is 0 up to 131072 pairs (one block, or one cluster of blocks,
+ * does the whole align) and, from there to 524288 pairs,
+ * 4 * (tiles * (V + 1) + (V + 1) + numel) bytes rounded up to 256 with
+ * tiles = ceil(numel / 4096): the largest accepted size is 131072 pairs at
+ * V = 8191 or 4095, more with fewer buckets. Outputs, capacity and
  * the other arguments are those of mol_align_block_size, and so are the results
  * (bit-identical). No allocation of any kind is made.
  * Every call shares the one array and it keeps the previous call's contents;

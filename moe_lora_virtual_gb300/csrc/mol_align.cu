@@ -20,9 +20,14 @@
 // per-warp bases, pass 2 recomputes each pair's stable rank inside the tile.
 // Everything is ordered by construction (tile < warp < round < lane), so the
 // result is bit-reproducible with no atomics. With one tile the same block
-// finishes the job (bucket scan, expert_ids, scatter): one launch. With more
-// tiles, per-tile histograms go to the workspace, one block scans them, and a
-// third launch scatters.
+// finishes the job (bucket scan, expert_ids, scatter): one launch. Up to
+// 131072 pairs the tiles are the thread blocks of one cluster (up to 16) and
+// the cross-tile steps go through distributed shared memory: each block sums
+// the tiles' counts of its share of the buckets, the shares' padded totals
+// are exchanged, and each block writes back, into every tile's shared memory,
+// that tile's base in each of its buckets -- one launch, no workspace, three
+// cluster barriers. Beyond that, per-tile histograms go to the workspace, one
+// block scans them, and a third launch scatters.
 
 #include <algorithm>
 
@@ -37,6 +42,9 @@ constexpr int kScanThreads = 1024;
 constexpr int kTileMin = 4096;
 constexpr int kMaxTiles = 128;
 constexpr int kAlignSmemMax = 200 * 1024;
+constexpr int kClusterTileMax = 16384;  // pairs per block of the cluster align
+constexpr int kClusterMax = 16;         // blocks in one cluster (above 8 where the device allows)
+constexpr int64_t kClusterPairs = 8LL * kClusterTileMax;  // largest numel of the cluster align
 
 MOL_DEV int remap_one(int base, int lora, int num_experts, int max_loras) {
   if (base < 0) return base;
@@ -152,6 +160,53 @@ MOL_DEV void bucket_offsets(int* counts, int nb, int num_vexperts, int block_m, 
   if (threadIdx.x == 0) *ntpp_out = total;
 }
 
+// Pass 1: the warp's bucket counts over its contiguous segment [s0, s1) of the
+// tile's keys, in rounds of 32 in order, into its 16-bit table `mine`.
+MOL_DEV void warp_count(const uint16_t* keys, int s0, int s1, uint16_t* mine, int lane) {
+  for (int r = s0; r < s1; r += 32) {
+    const int q = r + lane;
+    const bool valid = q < s1;
+    const unsigned key = valid ? keys[q] : 0xFFFFu;
+    const unsigned peers = __match_any_sync(0xffffffffu, key);
+    if (valid && lane == __ffs(peers) - 1) mine[key] = (uint16_t)(mine[key] + __popc(peers));
+    __syncwarp();
+  }
+}
+
+// Pass 2: the same rounds again; `mine` holds the warp's base in each bucket
+// inside the tile. emit(q, key, rank) gets each pair's stable rank in the tile.
+template <typename F>
+MOL_DEV void warp_rank(const uint16_t* keys, int s0, int s1, uint16_t* mine, int lane, F&& emit) {
+  for (int r = s0; r < s1; r += 32) {
+    const int q = r + lane;
+    const bool valid = q < s1;
+    const unsigned key = valid ? keys[q] : 0xFFFFu;
+    const unsigned peers = __match_any_sync(0xffffffffu, key);
+    const int base = valid ? (int)mine[key] : 0;
+    __syncwarp();
+    if (valid && lane == __ffs(peers) - 1) mine[key] = (uint16_t)(base + __popc(peers));
+    __syncwarp();
+    if (valid) emit(q, (int)key, base + __popc(peers & lanemask_lt()));
+  }
+}
+
+// Column scan: the warp tables become exclusive per-warp bases inside the tile;
+// total(b, n) receives the tile's count of bucket b.
+template <typename F>
+MOL_DEV void column_scan(uint16_t* tbl, int nb, int nb_pad, F&& total) {
+  for (int b = threadIdx.x; b < nb; b += kAlignThreads) {
+    int run = 0;
+#pragma unroll
+    for (int w = 0; w < kAlignWarps; ++w) {
+      uint16_t* p = tbl + w * nb_pad + b;
+      const int c = *p;
+      *p = (uint16_t)run;
+      run += c;
+    }
+    total(b, run);
+  }
+}
+
 template <bool REMAP>
 __global__ void __launch_bounds__(kAlignThreads, 1)
 align_tile_kernel(const int* __restrict__ src, const int* __restrict__ lora_ids, int topk,
@@ -208,56 +263,182 @@ align_tile_kernel(const int* __restrict__ src, const int* __restrict__ lora_ids,
   const int seg = tile / kAlignWarps;
   const int s0 = warp * seg, s1 = min(s0 + seg, tlen);
   uint16_t* mine = tbl + warp * nb_pad;
-  for (int r = s0; r < s1; r += 32) {
-    const int q = r + lane;
-    const bool valid = q < s1;
-    const unsigned key = valid ? keys[q] : 0xFFFFu;
-    const unsigned peers = __match_any_sync(0xffffffffu, key);
-    if (valid && lane == __ffs(peers) - 1) mine[key] = (uint16_t)(mine[key] + __popc(peers));
-    __syncwarp();
-  }
+  warp_count(keys, s0, s1, mine, lane);
   __syncthreads();
 
   // Column scan: warp tables become exclusive bases; the tile total per bucket
   // goes to shared memory (one tile) or to the workspace histogram.
-  for (int b = tid; b < nb; b += kAlignThreads) {
-    int run = 0;
-#pragma unroll
-    for (int w = 0; w < kAlignWarps; ++w) {
-      uint16_t* p = tbl + w * nb_pad + b;
-      const int c = *p;
-      *p = (uint16_t)run;
-      run += c;
-    }
+  column_scan(tbl, nb, nb_pad, [&](int b, int n) {
     if (fused)
-      offs[b] = run;
+      offs[b] = n;
     else
-      ws_hist[(int64_t)blockIdx.x * nb + b] = run;
-  }
+      ws_hist[(int64_t)blockIdx.x * nb + b] = n;
+  });
   __syncthreads();
   if (fused)
     bucket_offsets<kAlignThreads>(offs, nb, num_vexperts, block_m, capacity, expert_ids, ntpp_out,
                                   sh_scan);
 
   // Pass 2: stable rank of every pair inside the tile.
-  for (int r = s0; r < s1; r += 32) {
-    const int q = r + lane;
-    const bool valid = q < s1;
-    const unsigned key = valid ? keys[q] : 0xFFFFu;
-    const unsigned peers = __match_any_sync(0xffffffffu, key);
-    const int base = valid ? (int)mine[key] : 0;
-    __syncwarp();
-    if (valid && lane == __ffs(peers) - 1) mine[key] = (uint16_t)(base + __popc(peers));
-    __syncwarp();
-    if (valid) {
-      const int lr = base + __popc(peers & lanemask_lt());
-      const int64_t i = t0 + q;
-      if (fused)
-        sorted_ids[offs[key] + lr] = (int)i;
-      else
-        ws_rank[i] = lr;
+  warp_rank(keys, s0, s1, mine, lane, [&](int q, int key, int lr) {
+    const int64_t i = t0 + q;
+    if (fused)
+      sorted_ids[offs[key] + lr] = (int)i;
+    else
+      ws_rank[i] = lr;
+  });
+}
+
+// ---------------------------------------------------------------------------
+// Cluster align: the tiles are the blocks of one thread-block cluster.
+
+MOL_DEV uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+MOL_DEV uint32_t cluster_blocks() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+// Every thread of every block of the cluster: memory operations before it are
+// visible to every thread of the cluster after it (shared and global memory).
+MOL_DEV void cluster_barrier() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+// Address of the same shared-memory word in block `rank` of the cluster.
+MOL_DEV uint32_t peer_smem(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+MOL_DEV int ld_peer(uint32_t a) {
+  int v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  return v;
+}
+MOL_DEV void st_peer(uint32_t a, int v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
+
+// Block p of the cluster holds tile p (`tile` pairs from p * tile). After the
+// tile's counts (cnt[b]), block c takes buckets [c * per, (c + 1) * per):
+// it sums the tiles' counts of each (remote reads), pads, scans its share and
+// sends the share's padded total to every block. Then, with the offset o_b of
+// each of its buckets, it writes o_b + (counts of the tiles before p) into
+// block p's cnt[b] (remote writes), and the bucket's expert_ids. After the third
+// barrier every block scatters its pairs: cnt[key] + the pair's stable rank in
+// the tile. Every block reaches every barrier (no early exit, no data-dependent
+// wait), and no block reads or writes another's shared memory after the last.
+template <bool REMAP>
+__global__ void __launch_bounds__(kAlignThreads, 1)
+align_cluster_kernel(const int* __restrict__ src, const int* __restrict__ lora_ids, int topk,
+                     int num_experts, int max_loras, int* __restrict__ vtopk_out, int64_t numel,
+                     int num_vexperts, int block_m, int64_t capacity, int tile, int nb_pad,
+                     int* __restrict__ sorted_ids, int* __restrict__ expert_ids,
+                     int* __restrict__ ntpp_out, int trigger) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  __shared__ int sh_scan[kAlignWarps + 1];
+  __shared__ int rsum[kClusterMax];  // padded total of each block's share of the buckets
+  __shared__ int s_sentinel;         // offset of the sentinel bucket (in the block that holds it)
+  const int nb = num_vexperts + 1;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int CL = (int)cluster_blocks(), me = (int)cluster_rank();
+  uint16_t* tbl = reinterpret_cast<uint16_t*>(smem);  // [kAlignWarps][nb_pad]
+  uint16_t* keys = tbl + kAlignWarps * nb_pad;        // [tile]
+  int* cnt = reinterpret_cast<int*>(keys + tile);     // [nb]: counts, then this tile's bases
+  int* opad = cnt + nb;                               // [per]: offsets inside this block's share
+
+  {
+    uint4* t4 = reinterpret_cast<uint4*>(tbl);
+    const int n4 = kAlignWarps * nb_pad / 8;
+    for (int q = tid; q < n4; q += kAlignThreads) t4[q] = make_uint4(0, 0, 0, 0);
+  }
+  pdl_wait();  // inputs and routing buffers belong to earlier kernels until here
+  if (trigger) pdl_launch_dependents();  // see align_tile_kernel
+
+  for (int64_t q = (int64_t)me * kAlignThreads + tid; q < capacity;
+       q += (int64_t)CL * kAlignThreads)
+    sorted_ids[q] = (int)numel;
+  const int64_t t0 = (int64_t)me * tile;
+  const int tlen = (int)max((int64_t)0, min((int64_t)tile, numel - t0));
+  for (int q = tid; q < tlen; q += kAlignThreads) {
+    const int64_t i = t0 + q;
+    int vid;
+    if (REMAP) {
+      vid = remap_one(src[i], lora_ids[i / topk], num_experts, max_loras);
+      vtopk_out[i] = vid;
+    } else {
+      vid = src[i];
+    }
+    keys[q] = (uint16_t)bucket_of(vid, num_vexperts);
+  }
+  __syncthreads();
+  const int seg = tile / kAlignWarps;
+  const int s0 = warp * seg, s1 = min(s0 + seg, tlen);
+  uint16_t* mine = tbl + warp * nb_pad;
+  warp_count(keys, s0, s1, mine, lane);
+  __syncthreads();
+  column_scan(tbl, nb, nb_pad, [&](int b, int n) { cnt[b] = n; });
+  cluster_barrier();  // 1: every tile's counts are in its block's shared memory
+
+  const int per = (nb + CL - 1) / CL;
+  const int b0 = min(me * per, nb), b1 = min(b0 + per, nb);
+  const int ppt = (per + kAlignThreads - 1) / kAlignThreads;
+  const int c0 = min(b0 + tid * ppt, b1), c1 = min(c0 + ppt, b1);
+  const int pad = block_m - 1, lg = __ffs(block_m) - 1;
+  int local = 0;
+  for (int b = c0; b < c1; ++b) {
+    int tot = 0;
+    for (int p = 0; p < CL; ++p) tot += ld_peer(peer_smem(cnt + b, p));
+    const int pb = (tot + pad) & ~pad;
+    opad[b - b0] = pb;
+    local += pb;
+  }
+  int share_total;
+  int run = block_exclusive_scan<kAlignThreads>(local, sh_scan, share_total);
+  for (int b = c0; b < c1; ++b) {
+    const int pb = opad[b - b0];
+    opad[b - b0] = run;
+    run += pb;
+  }
+  if (tid < CL) st_peer(peer_smem(rsum + me, tid), share_total);
+  cluster_barrier();  // 2: every share's padded total is in every block
+
+  int base = 0, ntpp = 0;
+  for (int c = 0; c < CL; ++c) {
+    const int v = rsum[c];
+    base += c < me ? v : 0;
+    ntpp += v;
+  }
+  for (int b = c0; b < c1; ++b) {
+    const int o = base + opad[b - b0];
+    int r = o;
+    for (int p = 0; p < CL; ++p) {
+      const uint32_t a = peer_smem(cnt + b, p);
+      const int c = ld_peer(a);
+      st_peer(a, r);
+      r += c;
+    }
+    if (b < num_vexperts) {
+      const int nblk = ((r - o) + pad) >> lg;
+      for (int k = 0; k < nblk; ++k) expert_ids[(o >> lg) + k] = b;
+    } else {
+      s_sentinel = o;  // b == V: the last bucket
     }
   }
+  if (me == 0 && tid == 0) *ntpp_out = ntpp;
+  __syncthreads();
+  if (b0 < nb && b1 == nb) {  // the sentinel's blocks and every block past them carry -1
+    for (int64_t t = (s_sentinel >> lg) + tid; t < (capacity >> lg); t += kAlignThreads)
+      expert_ids[t] = -1;
+  }
+  cluster_barrier();  // 3: cnt[b] is this tile's base in bucket b; the pad fill is done
+
+  warp_rank(keys, s0, s1, mine, lane,
+            [&](int q, int key, int lr) { sorted_ids[cnt[key] + lr] = (int)(t0 + q); });
 }
 
 // Multi-tile: per-bucket prefix over tiles, bucket offsets, expert_ids, ntpp.
@@ -321,9 +502,17 @@ AlignPlan make_align_plan(int64_t numel, int num_vexperts, int block_m) {
   p.block_m = block_m;
   const int64_t nonempty = std::min<int64_t>(numel, p.nb);
   p.capacity = (numel + nonempty * (block_m - 1) + block_m - 1) / block_m * block_m;
+  p.cluster = false;
   if (numel <= kTileMin) {
     p.tile = (int)std::max<int64_t>(256, (numel + 255) / 256 * 256);
     p.tiles = 1;
+  } else if (numel <= kClusterPairs) {
+    p.cluster = true;  // tile and block count are chosen at launch for the device
+    p.tile = 0;
+    p.tiles = 0;
+    p.smem_tile = 0;
+    p.ws_bytes = 0;
+    return p;
   } else {
     const int64_t want = (numel + kMaxTiles - 1) / kMaxTiles;
     p.tile = (int)std::max<int64_t>(kTileMin, (want + 255) / 256 * 256);
@@ -339,6 +528,40 @@ AlignPlan make_align_plan(int64_t numel, int num_vexperts, int block_m) {
     p.ws_bytes = (ints * 4 + 255) / 256 * 256;
   }
   return p;
+}
+
+// Largest cluster of the cluster align on each device (8, or 16 where a
+// 16-block cluster of its shared-memory size can be scheduled).
+static int g_cluster_max[64] = {0};
+
+static cudaError_t prepare_cluster_align() {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  for (auto k : {align_cluster_kernel<true>, align_cluster_kernel<false>}) {
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kAlignSmemMax);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kClusterMax);
+  cfg.blockDim = dim3(kAlignThreads);
+  cfg.dynamicSmemBytes = kAlignSmemMax;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kClusterMax;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  e = cudaOccupancyMaxActiveClusters(&n, (void*)align_cluster_kernel<true>, &cfg);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();  // a refused query leaves the portable size
+    n = 0;
+  }
+  if (dev >= 0 && dev < 64) g_cluster_max[dev] = n >= 1 ? kClusterMax : 8;
+  return cudaSuccess;
 }
 
 static int sm_count(int device) {
@@ -364,6 +587,8 @@ cudaError_t prepare_kernels() {
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(align_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kAlignSmemMax);
+  if (e != cudaSuccess) return e;
+  e = prepare_cluster_align();
   if (e != cudaSuccess) return e;
   e = prepare_stage_kernels();
   if (e != cudaSuccess) return e;
@@ -401,6 +626,27 @@ cudaError_t launch_align(const AlignPlan& plan, bool remap, const int32_t* src,
   int device = 0;
   cudaError_t e = cudaGetDevice(&device);
   if (e != cudaSuccess) return e;
+  if (plan.cluster) {
+    // blocks of 4096 pairs, up to the device's cluster size, then larger tiles
+    const int cmax = (device >= 0 && device < 64 && g_cluster_max[device]) ? g_cluster_max[device] : 8;
+    const int cl = (int)std::min<int64_t>(cmax, (plan.numel + kTileMin - 1) / kTileMin);
+    const int tile = (int)(((plan.numel + cl - 1) / cl + 255) / 256 * 256);
+    if (tile > kClusterTileMax) return cudaErrorInvalidConfiguration;
+    const int per = (plan.nb + cl - 1) / cl;
+    const size_t smem = (size_t)kAlignWarps * plan.nb_pad * 2 + (size_t)tile * 2 +
+                        (size_t)plan.nb * 4 + (size_t)per * 4;
+    if (smem > (size_t)kAlignSmemMax) return cudaErrorInvalidConfiguration;
+    if (remap)
+      return launch_pdl_cluster(align_cluster_kernel<true>, cl, dim3(kAlignThreads), smem, stream,
+                                src, lora_ids, topk, num_experts, max_loras, vtopk_out, plan.numel,
+                                num_vexperts, plan.block_m, plan.capacity, tile, plan.nb_pad,
+                                sorted_ids, expert_ids, ntpp, trig);
+    return launch_pdl_cluster(align_cluster_kernel<false>, cl, dim3(kAlignThreads), smem, stream,
+                              src, static_cast<const int32_t*>(nullptr), 1, 1, 1,
+                              static_cast<int32_t*>(nullptr), plan.numel, num_vexperts,
+                              plan.block_m, plan.capacity, tile, plan.nb_pad, sorted_ids,
+                              expert_ids, ntpp, trig);
+  }
   int* ws_hist = nullptr;
   int* ws_offs = nullptr;
   int* ws_rank = nullptr;

@@ -16,8 +16,9 @@ struct AlignPlan {
   int64_t capacity;
   int tile;        // pairs per tile block
   int tiles;       // number of tile blocks (1 = single fused block)
+  bool cluster;    // the tiles are the blocks of one cluster (sized at launch): no workspace
   size_t smem_tile;
-  size_t ws_bytes;  // workspace (0 when tiles == 1), 256-byte multiple
+  size_t ws_bytes;  // workspace (0 with one tile or one cluster), 256-byte multiple
 };
 
 AlignPlan make_align_plan(int64_t numel, int num_vexperts, int block_m);
@@ -28,6 +29,27 @@ cudaError_t prepare_kernels();
 // Launch with programmatic stream serialization: the kernel's blocks may be
 // scheduled while the previous kernel in the stream finishes; each kernel
 // guards its reads of that kernel's output with griddepcontrol.wait.
+// The same for a grid that is one thread-block cluster of `blocks` blocks.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), int blocks, dim3 block, size_t smem,
+                               cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks);
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = blocks;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                        cudaStream_t stream, Args... args) {

@@ -69,8 +69,10 @@ def test_capacity_matches_oracle(mol, numel, V, BM):
 def test_workspace_sizes(mol):
     assert mol.workspace_bytes(184, 1024, 16) == 0          # one block does the whole align
     assert mol.workspace_bytes(4096, 8191, 16) == 0
-    w = mol.workspace_bytes(65536, 4096, 64)
-    assert w >= 4 * (65536 + 4097) and w % 256 == 0
+    assert mol.workspace_bytes(65536, 4096, 64) == 0        # one cluster does the whole align
+    assert mol.workspace_bytes(131072, 8191, 16) == 0
+    w = mol.workspace_bytes(131073, 4096, 64)               # tiles, scan and scatter launches
+    assert w >= 4 * (33 * 4097 + 4097 + 131073) and w % 256 == 0
     assert mol.workspace_bytes(1 << 22, 8191, 16) <= 4 * (128 * 8192 + 8192 + (1 << 22)) + 256
     assert mol.workspace_bytes(-1, 16, 16) == 0
     assert mol.workspace_bytes(16, 8192, 16) == 0           # rejected sizes report 0
@@ -85,7 +87,7 @@ def test_validation_rejects_before_any_launch(mol):
     assert lib.mol_align_block_size(P(16), 64, 8192, 16, P(16), 4096, P(16), P(16), None, 0, None) == -3
     assert lib.mol_align_block_size(P(16), -5, 16, 16, P(16), 4096, P(16), P(16), None, 0, None) == -1
     assert lib.mol_align_block_size(P(16), 64, 16, 16, P(16), 64, P(16), P(16), None, 0, None) == -2
-    assert lib.mol_align_block_size(P(16), 70000, 16, 16, P(16), 1 << 20, P(16), P(16), None, 0, None) == -2
+    assert lib.mol_align_block_size(P(16), 200000, 16, 16, P(16), 1 << 20, P(16), P(16), None, 0, None) == -2
     assert lib.mol_align_block_size(P(16), (1 << 22) + 1, 16, 16, P(16), 1 << 30, P(16), P(16), None, 0, None) == -3
     # shrink / expand contracts
     assert lib.mol_lora_shrink(P(16), 64, 1, 60, P(16), 1, 16, P(16), P(16), P(16), 64, 16, 8, 4, P(16), 0, None, None) == -3

@@ -32,7 +32,7 @@ CASES = [
     (23, 8, 32, 4, 16, 2560, 1, 32, 6144, 0.3, 0, 0, False),     # wide: chunked jobs when rows > 1
     (40, 5, 64, 2, 64, 520, 2, 16, 200, 0.6, 16, 0, True),       # hot expert: > 16 rows, row tiles
     (40, 4, 32, 3, 32, 4104, 3, 8, 72, 0.6, 0, 24, False),       # rank 8, three slices, long K
-    (25, 6, 48, 2, 16, 264, 1, 64, 300, 0.2, 8, 8, True),        # rank 64, column tail 44
+    (25, 6, 48, 2, 16, 264, 1, 64, 296, 0.2, 8, 8, True),        # rank 64, column tail 40
     (40, 2, 16, 2, 128, 64, 2, 16, 8, 0.9, 0, 0, False),         # tiny N, one hot block of 128 slots
 ]
 

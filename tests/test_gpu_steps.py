@@ -53,6 +53,10 @@ ALIGN_CASES = [
     (65536, 4096, 64, "random"),
     (70001, 8191, 64, "random"),
     (200000, 33, 16, "random"),
+    (131072, 8191, 16, "random"),      # the largest one-cluster align
+    (131073, 8191, 16, "random"),      # the smallest tiles-scan-scatter align
+    (20000, 1, 16, "random"),          # fewer buckets than cluster blocks
+    (12289, 3, 128, "random"),
     (5000, 64, 32, "all_invalid"),
     (3000, 64, 64, "single_bucket"),
     (9000, 8191, 16, "top_bucket"),
@@ -320,7 +324,7 @@ def test_invalid_arguments_launch_nothing():
     assert lib.mol_align_block_size(P(vid), 64, 8192, 16, P(s), 4096, P(e), P(n), None, 0, st()) == mol.MOL_ERR_UNSUPPORTED
     assert lib.mol_align_block_size(P(vid), -1, 16, 16, P(s), 4096, P(e), P(n), None, 0, st()) == mol.MOL_ERR_INVALID_ARG
     assert lib.mol_align_block_size(None, 64, 16, 16, P(s), 4096, P(e), P(n), None, 0, st()) == mol.MOL_ERR_INVALID_ARG
-    big = 70000
+    big = 200000  # past the one-cluster align: a workspace is needed
     assert lib.mol_workspace_bytes(big, 100, 16) > 0
     assert lib.mol_align_block_size(P(vid), big, 100, 16, P(s), 1 << 20, P(e), P(n), None, 0, st()) in (mol.MOL_ERR_CAPACITY,)
     x = torch.zeros((8, 64), dtype=torch.bfloat16, device=dev)
