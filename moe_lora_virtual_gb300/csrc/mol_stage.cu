@@ -23,6 +23,7 @@
 // weight copies before griddepcontrol.wait, so its blocks stream weights while
 // the previous stage drains.
 //
+// Two blocks share an SM up to R = 64 (2 x 111 KB of shared memory).
 // Roles (160 threads): warp 4 is the producer -- routing words, row
 // compaction, every bulk copy (cp.async.bulk) and the stage headers. Warps 0-3
 // consume: shrink chunks on mma.sync m16n8k16 (each warp a quarter of the
@@ -53,7 +54,9 @@ constexpr int kConsumers = 4;
 constexpr int kThreads = (kConsumers + 1) * 32;
 constexpr int kJT = 8;                 // lora_a rows per shrink job (one n8 mma tile)
 constexpr int kMR = 16;                // pair rows per row tile (one m16 mma tile)
-constexpr int kStageBytes = 48 * 1024;
+// The shrink's stage size: jobs are cut along k exactly as in the separate
+// shrink, so both give bit-identical intermediates.
+constexpr int kStageBytes = 52 * 1024;
 constexpr int kStages = 2;
 constexpr int kHeader = 1024;          // barriers and stage headers
 constexpr int kCols = 256;             // output columns per expand tile
