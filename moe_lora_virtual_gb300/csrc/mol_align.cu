@@ -316,7 +316,7 @@ MOL_DEV uint32_t peer_smem(const void* p, uint32_t rank) {
 }
 MOL_DEV int ld_peer(uint32_t a) {
   int v;
-  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(a));
   return v;
 }
 MOL_DEV void st_peer(uint32_t a, int v) {
@@ -391,8 +391,12 @@ align_cluster_kernel(const int* __restrict__ src, const int* __restrict__ lora_i
   const int pad = block_m - 1, lg = __ffs(block_m) - 1;
   int local = 0;
   for (int b = c0; b < c1; ++b) {
+    int c[kClusterMax];  // every tile's count of b: independent remote loads, all in flight
+#pragma unroll
+    for (int p = 0; p < kClusterMax; ++p) c[p] = p < CL ? ld_peer(peer_smem(cnt + b, p)) : 0;
     int tot = 0;
-    for (int p = 0; p < CL; ++p) tot += ld_peer(peer_smem(cnt + b, p));
+#pragma unroll
+    for (int p = 0; p < kClusterMax; ++p) tot += c[p];
     const int pb = (tot + pad) & ~pad;
     opad[b - b0] = pb;
     local += pb;
@@ -415,12 +419,14 @@ align_cluster_kernel(const int* __restrict__ src, const int* __restrict__ lora_i
   }
   for (int b = c0; b < c1; ++b) {
     const int o = base + opad[b - b0];
+    int c[kClusterMax];  // loads first, then the stores of the running sums
+#pragma unroll
+    for (int p = 0; p < kClusterMax; ++p) c[p] = p < CL ? ld_peer(peer_smem(cnt + b, p)) : 0;
     int r = o;
-    for (int p = 0; p < CL; ++p) {
-      const uint32_t a = peer_smem(cnt + b, p);
-      const int c = ld_peer(a);
-      st_peer(a, r);
-      r += c;
+#pragma unroll
+    for (int p = 0; p < kClusterMax; ++p) {
+      if (p < CL) st_peer(peer_smem(cnt + b, p), r);
+      r += c[p];
     }
     if (b < num_vexperts) {
       const int nblk = ((r - o) + pad) >> lg;
