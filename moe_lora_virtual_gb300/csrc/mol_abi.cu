@@ -164,12 +164,13 @@ int32_t mol_take_fault_flags(uint32_t* flags) {
   if (st != MOL_OK) return st;
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cuda_fail(e);
-  unsigned a = 0, b = 0, c = 0;
+  unsigned a = 0, b = 0, c = 0, d = 0;
   e = mol::take_lora_faults(&a);
   if (e == cudaSuccess) e = mol::take_tc_faults(&b);
   if (e == cudaSuccess) e = mol::take_stage_faults(&c);
+  if (e == cudaSuccess) e = mol::take_rows_faults(&d);
   if (e != cudaSuccess) return cuda_fail(e);
-  *flags = a | b | c;
+  *flags = a | b | c | d;
   return MOL_OK;
 }
 
@@ -319,8 +320,8 @@ int32_t mol_lora_forward(const void* x, int64_t x_row_stride, int32_t x_row_div,
     if (e != cudaSuccess) return cuda_fail(e);
   }
   if (numel == 0 || capacity == 0) return MOL_OK;
-  if (mol::stage_fused_fits(numel, V, num_slices * rank, rank, K, block_m,
-                            lora_ranks != nullptr || lora_scalings != nullptr)) {
+  if (mol::stage_fused_fits(numel, V, num_slices * rank, rank, K, num_slices * slice_n, block_m,
+                            capacity, lora_ranks != nullptr || lora_scalings != nullptr)) {
     e = mol::launch_stage(x, x_row_stride, x_row_div, K, lora_a, lora_b, num_slices, rank, slice_n,
                           scale, topk_weights, sorted_token_ids, expert_ids,
                           num_tokens_post_padded, capacity, block_m, numel, V, inter, out,

@@ -414,14 +414,31 @@ lora_stage_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, i
 
 // --- host side ----------------------------------------------------------------
 
-bool stage_fused_fits(int64_t numel, int num_vexperts, int R, int r, int K, int block_m,
-                      bool adapter_arrays) {
+static int stage_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+bool stage_fused_fits(int64_t numel, int num_vexperts, int R, int r, int K, int N, int block_m,
+                      int64_t capacity, bool adapter_arrays) {
   if (adapter_arrays || numel <= 0) return false;
   if (!(r == 8 || r == 16 || r == 32 || r == 64) || R > 128) return false;
   if (shrink_tc_fits(numel, num_vexperts, R, K, block_m)) return false;
-  // few rows per virtual expert: one block per routed block keeps every SM busy
-  // only when routed blocks are about as many as the rows they hold
-  return numel < 4 * std::min<int64_t>(numel, num_vexperts);
+  // One block per routed block streams its virtual expert's weights through two
+  // stages: that is about one round trip only when every routed block has an SM
+  // of its own and a block's weights fill about two stages. Past that the
+  // persistent shrink and the separate expand keep more bytes in flight per SM
+  // and are faster.
+  const int64_t weight_bytes = 2 * ((int64_t)R * K + (int64_t)N * r);
+  return capacity / block_m <= stage_sms() && weight_bytes <= 2 * fs::kStageBytes;
 }
 
 template <int RK>

@@ -1,14 +1,16 @@
 """The fused stage (shrink then expand per routed block in one launch) against the oracle.
 
-mol_lora_forward takes the fused stage when routed blocks hold few rows (fewer
-pairs than four per touched virtual expert), the rank is 8, 16, 32 or 64,
-R <= 128 and no per-adapter arrays are given. These cases are built to land
-there and to reach its corners: a hot expert whose routed block holds more
-than 16 rows (several row tiles, the stage repeated per tile), k chunked
-shrink jobs (wide K, several rows), output widths that end inside a 256-column
-tile, padded row strides, routed weights, two and three slices, and a second
-stage that reuses the routing (its weights are read before the kernel's
-dependency wait).
+mol_lora_forward takes the fused stage for small layers: every routed block
+on an SM of its own (capacity / block_m at most the SM count), a virtual
+expert's weights within two 52 KB stages (2 (R K + N r) bytes), rank 8, 16, 32
+or 64, R <= 128, no per-adapter arrays, and not the tensor-core shrink's
+regime. These cases are built to land there (`in_fused_regime` restates the
+rule) and to reach its corners: a hot virtual expert whose routed block holds
+more than 16 rows (the stage repeated per 16-row tile), k-chunked shrink jobs
+(wide K with many rows), output widths that end inside a 256-column tile,
+padded row strides, routed weights, one to three slices, and a second stage
+that reuses the routing (its weights are read before the kernel's dependency
+wait).
 """
 
 import numpy as np
@@ -21,21 +23,27 @@ from tests.gpu_util import (bf16_host, check_inter, check_out, mol_lib, to_dev_b
 pytestmark = pytest.mark.gpu
 
 
+def in_fused_regime(numel, V, BM, K, S, r, Ns, sms=148):
+    cap = oracle.align_capacity(numel, V, BM)
+    R, N = S * r, S * Ns
+    tc = (R % 64 == 0 and K % 64 == 0 and BM in (64, 128) and numel >= 32 * min(numel, V))
+    return (r in (8, 16, 32, 64) and R <= 128 and not tc and cap // BM <= sms
+            and 2 * (R * K + N * r) <= 2 * 52 * 1024)
+
+
 def bits(a):
     return oracle.f64_to_bf16(np.asarray(a, np.float64))
 
 
 CASES = [
     # T, k, E, L, BM, K, S, r, Ns, hot, x_pad, out_pad, weights
-    (23, 8, 32, 4, 16, 2048, 2, 32, 768, 0.0, 0, 0, False),      # decode gate_up widths
-    (23, 8, 32, 4, 16, 768, 1, 32, 2048, 0.0, 8, 8, True),       # decode down widths
-    (23, 8, 32, 4, 16, 2560, 1, 32, 6144, 0.3, 0, 0, False),     # wide: chunked jobs when rows > 1
-    (40, 5, 64, 2, 64, 520, 2, 16, 200, 0.6, 16, 0, True),       # hot expert: > 16 rows, row tiles
-    (40, 4, 32, 3, 32, 4104, 3, 8, 72, 0.6, 0, 24, False),       # rank 8, three slices, long K
-    (25, 6, 48, 2, 16, 264, 1, 64, 296, 0.2, 8, 8, True),        # rank 64, column tail 40
-    (40, 2, 16, 2, 128, 64, 2, 16, 8, 0.9, 0, 0, False),         # tiny N, one hot block of 128 slots
+    (16, 2, 8, 2, 16, 256, 1, 16, 128, 0.0, 0, 0, False),       # the tiny workload's widths
+    (10, 4, 8, 2, 16, 2048, 1, 8, 64, 0.9, 8, 8, True),         # rank 8, hot block: k-chunked jobs
+    (40, 2, 4, 2, 64, 128, 2, 16, 40, 0.8, 16, 0, True),        # hot expert: > 16 rows, row tiles
+    (12, 4, 6, 2, 16, 64, 1, 64, 296, 0.2, 8, 8, True),         # rank 64, column tail 40
+    (30, 3, 5, 2, 32, 96, 3, 32, 24, 0.8, 0, 24, False),        # three slices, rank 32, hot
+    (60, 2, 3, 1, 128, 64, 2, 16, 8, 0.9, 0, 0, False),         # one hot block of 128 slots
 ]
-
 
 @pytest.mark.parametrize("case", CASES)
 def test_fused_stage_matches_oracle(case):
@@ -45,7 +53,7 @@ def test_fused_stage_matches_oracle(case):
     T, k, E, L, BM, K, S, r, Ns, hot, x_pad, out_pad, use_w = case
     rng = np.random.default_rng(sum(case[:9]))
     numel, V, R, N = T * k, E * L, S * r, S * Ns
-    assert numel < 4 * min(numel, V)  # few rows per virtual expert: the fused stage's regime
+    assert in_fused_regime(numel, V, BM, K, S, r, Ns)
     topk = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
     lora = rng.integers(-1, L, size=T).astype(np.int32)
     hot_t = rng.random(T) < hot  # a hot virtual expert: expert 0 with adapter 0
@@ -92,6 +100,7 @@ def test_fused_stage_matches_oracle(case):
 
     # a second stage on the same routing (pair-row activations), read early
     K2, r2, Ns2 = 256 + 8 * (case[0] % 5), r, 136
+    assert in_fused_regime(numel, V, BM, K2, 1, r2, Ns2)
     x2 = bits(rng.standard_normal((numel, K2)))
     A2 = bits(rng.standard_normal((V, r2, K2)) * 0.05)
     B2 = bits(rng.standard_normal((V, Ns2, r2)) * 0.05)
@@ -120,7 +129,7 @@ def test_fused_stage_small_integers_bit_exact(r):
     rng = np.random.default_rng(900 + r)
     T, k, E, L, BM, K, S, Ns = 30, 4, 24, 2, 16, 128, 2, 40
     numel, V, R, N = T * k, E * L, S * r, S * Ns
-    assert numel < 4 * min(numel, V)
+    assert in_fused_regime(numel, V, BM, K, S, r, Ns)
     topk = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
     lora = rng.integers(-1, L, size=T).astype(np.int32)
     x = bits(rng.integers(-3, 4, size=(T, K)))
