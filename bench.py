@@ -335,7 +335,7 @@ def kernel_times(torch, mol, wl, layers, cnt, ranks, steps, config):
     us = kern[name]
     achieved = nbytes / (us * 1e-6) / 1e9
     cap = None if ranks is not None else TRAFFIC.get((config, name))
-    fresh = cap is not None and cap[2] == kernel_source_digest()
+    fresh = cap is not None and cap[3] == kernel_source_digest(cap[2])
     roof = dict(kernel=name, bound="hbm", achieved=round(achieved, 1), peak=peaks["hbm_gbs"],
                 unit="GB/s", frac=round(achieved / peaks["hbm_gbs"], 4),
                 traffic=cap[0] if fresh else None,
@@ -667,24 +667,23 @@ E2E_ROUNDS = 4
 
 
 # traffic (dram bytes read + written) of one captured launch, with the algorithmic bytes of
-# that same launch (the first layer of the workload, seed 0) and the digest of the kernel
-# sources it was captured with, keyed by (workload, kernel). An entry whose digest differs
-# from the current sources is stale and reported as null. Sources: the ncu summaries under
-# profiles/.
+# that same launch (the first layer of the workload, seed 0), the source file of the kernel
+# and the digest of that file (with the shared device header) when it was captured, keyed by
+# (workload, kernel). An entry whose digest differs from the current sources is stale and
+# reported as null. Sources: the ncu summaries under profiles/.
 TRAFFIC = {
 }
 
 
-def kernel_source_digest() -> str:
-    """sha256 (first 16 hex digits) over the library's CUDA sources and headers."""
+def kernel_source_digest(src: str) -> str:
+    """sha256 (first 16 hex digits) of a kernel's source file and the shared device header."""
     import hashlib
 
     csrc = os.path.join(ROOT, "moe_lora_virtual_gb300", "csrc")
     h = hashlib.sha256()
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            h.update(f.encode())
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    for f in (src, "mol_device.cuh"):
+        h.update(f.encode())
+        h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 

@@ -12,8 +12,7 @@ CSRC = os.path.join(PKG_DIR, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_PATH = os.path.join(PKG_DIR, "libmol.so")
 
-SOURCES = ["mol_abi.cu", "mol_align.cu", "mol_lora.cu", "mol_umma.cu", "mol_stage.cu",
-           "mol_shrink_rows.cu"]
+SOURCES = ["mol_abi.cu", "mol_align.cu", "mol_lora.cu", "mol_umma.cu", "mol_stage.cu"]
 HEADERS = ["mol_device.cuh", "mol_internal.h"]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -164,13 +164,12 @@ int32_t mol_take_fault_flags(uint32_t* flags) {
   if (st != MOL_OK) return st;
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cuda_fail(e);
-  unsigned a = 0, b = 0, c = 0, d = 0;
+  unsigned a = 0, b = 0, c = 0;
   e = mol::take_lora_faults(&a);
   if (e == cudaSuccess) e = mol::take_tc_faults(&b);
   if (e == cudaSuccess) e = mol::take_stage_faults(&c);
-  if (e == cudaSuccess) e = mol::take_rows_faults(&d);
   if (e != cudaSuccess) return cuda_fail(e);
-  *flags = a | b | c | d;
+  *flags = a | b | c;
   return MOL_OK;
 }
 

@@ -147,19 +147,6 @@ cudaError_t launch_stage(const void* x, int64_t x_stride, int x_div, int K, cons
                          int64_t out_stride, bool early, cudaStream_t stream);
 cudaError_t take_stage_faults(unsigned* out);
 
-// Shrink for routed blocks of many rows (on average at least four pairs per
-// virtual expert, K <= 2048, block_m >= 32, no per-adapter ranks): one block
-// per SM walks routed blocks, keeps each tile of activation rows resident and
-// streams only lora_a. Same arithmetic as the item shrink.
-bool shrink_rows_fits(int64_t numel, int num_vexperts, int R, int K, int block_m,
-                      bool adapter_ranks);
-cudaError_t prepare_rows_kernels();
-cudaError_t launch_shrink_rows(const void* x, int64_t x_stride, int x_div, int K,
-                               const void* lora_a, int R, const int32_t* sorted_ids,
-                               const int32_t* expert_ids, const int32_t* ntpp, int64_t capacity,
-                               int block_m, int64_t numel, int num_vexperts, float* inter,
-                               bool early, cudaStream_t stream);
-cudaError_t take_rows_faults(unsigned* out);
 
 // Fault words of the pipelined kernels (bit 0: a bounded barrier or copy wait
 // ran out); read and cleared by mol_take_fault_flags.

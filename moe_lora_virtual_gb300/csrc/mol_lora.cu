@@ -845,8 +845,6 @@ static cudaError_t prepare_expand_st() {
 cudaError_t prepare_lora_kernels() {
   cudaError_t e = prepare_tc_kernels();
   if (e != cudaSuccess) return e;
-  e = prepare_rows_kernels();
-  if (e != cudaSuccess) return e;
   e = prepare_expand_st<64, true>();
   if (e != cudaSuccess) return e;
   e = prepare_expand_st<64, false>();
@@ -880,9 +878,6 @@ cudaError_t launch_shrink(const void* x, int64_t x_stride, int x_div, int K, con
   if (!lora_ranks && shrink_tc_fits(numel, num_vexperts, R, K, block_m))
     return launch_shrink_tc(x, x_stride, x_div, K, lora_a, R, sorted_ids, expert_ids, ntpp,
                             capacity, block_m, numel, num_vexperts, inter, stream);
-  if (shrink_rows_fits(numel, num_vexperts, R, K, block_m, lora_ranks != nullptr))
-    return launch_shrink_rows(x, x_stride, x_div, K, lora_a, R, sorted_ids, expert_ids, ntpp,
-                              capacity, block_m, numel, num_vexperts, inter, early, stream);
   const int n_jt = R / sp::kJT;
   const int num_loras = lora_ranks ? num_vexperts / num_experts : 0;
   const int64_t n_items = nblk * n_jt;

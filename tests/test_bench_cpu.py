@@ -65,8 +65,9 @@ def test_byte_model_matches_walked_blocks(name):
 @pytest.mark.parametrize("key", sorted(bench.TRAFFIC))
 def test_traffic_entries_belong_to_their_launch(key):
     name, kernel = key
-    traffic, launch_bytes, digest = bench.TRAFFIC[key]
+    traffic, launch_bytes, src, digest = bench.TRAFFIC[key]
     assert len(digest) == 16 and int(digest, 16) >= 0
+    assert len(bench.kernel_source_digest(src)) == 16  # the file exists
     wl, li, vt, s, e, n = _routing(name)
     kind, stage_name = kernel.split("_", 1)
     si = [st.stage.name for st in li.stages].index(stage_name)
