@@ -451,8 +451,11 @@ def run_gpu(args):
     torch.cuda.synchronize()
     cnt = [L_.counts() for L_ in layers]
     pairs_per_step = float(np.mean([c[0] for c in cnt]))
-    plan_tiles = 1 if mol.workspace_bytes(wl.numel, wl.V, wl.BM) == 0 else 3
-    launches_per_step = plan_tiles + 2 * len(wl.stages)
+    # kernels per layer, counted by the library over one eager layer
+    n0 = mol.mol_launch_count()
+    layers[0].forward(mol)
+    torch.cuda.synchronize()
+    launches_per_step = mol.mol_launch_count() - n0
 
     # A real decode step replays all MoE layers inside one graph; here one graph
     # holds the rotating layers back to back, and one more graph holds the first

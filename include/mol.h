@@ -75,6 +75,11 @@ const char* mol_status_string(int32_t status);
 /* cudaError_t of the last MOL_ERR_CUDA returned on this host thread (0 if none). */
 int32_t mol_last_cuda_error(void);
 
+/* Kernels this library has enqueued in this process so far (all threads; a
+ * launch captured into a CUDA graph counts once, when it is captured). Lets a
+ * caller see how many launches a call makes. */
+int64_t mol_launch_count(void);
+
 /*
  * Slots of sorted_token_ids needed for any routing of `numel` pairs:
  * ceil_BM(numel + min(numel, V + 1) * (block_m - 1)). The fork PR #24

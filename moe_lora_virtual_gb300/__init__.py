@@ -30,6 +30,7 @@ EXPORTS = (
     "mol_workspace_bytes", "mol_virtual_topk", "mol_align_block_size", "mol_lora_shrink",
     "mol_lora_expand", "mol_lora_forward", "mol_align_block_size_noalloc", "mol_token_lora_ids",
     "mol_take_fault_flags", "mol_debug_wait_test", "mol_forward_workspace_bytes",
+    "mol_launch_count",
 )
 
 _lib = None
@@ -43,6 +44,7 @@ _SIGS = {
     "mol_version": (_I32, []),
     "mol_status_string": (ctypes.c_char_p, [_I32]),
     "mol_last_cuda_error": (_I32, []),
+    "mol_launch_count": (_I64, []),
     "mol_align_capacity": (_I64, [_I64, _I32, _I32]),
     "mol_workspace_bytes": (_SZ, [_I64, _I32, _I32]),
     "mol_forward_workspace_bytes": (_SZ, [_I64, _I32, _I32, _I64]),
@@ -323,3 +325,8 @@ def mol_debug_wait_test(stall_producer: bool, wait_limit_ns: int = 0) -> None:
     a fault bit. Synchronizes the device."""
     _check("mol_debug_wait_test", library().mol_debug_wait_test(int(bool(stall_producer)),
                                                                 int(wait_limit_ns)))
+
+
+def mol_launch_count() -> int:
+    """Kernels the library has enqueued in this process so far."""
+    return int(library().mol_launch_count())

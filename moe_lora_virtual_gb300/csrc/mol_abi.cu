@@ -10,6 +10,12 @@
 
 
 namespace {
+std::atomic<int64_t> g_launches{0};
+}  // namespace
+
+void mol::count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+namespace {
 
 thread_local int32_t g_last_cuda_error = 0;
 
@@ -130,6 +136,8 @@ const char* mol_status_string(int32_t status) {
 }
 
 int32_t mol_last_cuda_error(void) { return g_last_cuda_error; }
+
+int64_t mol_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 int64_t mol_align_capacity(int64_t numel, int32_t num_vexperts, int32_t block_m) {
   if (numel < 0 || num_vexperts < 1 || block_m < 1) return -1;

@@ -7,6 +7,9 @@
 
 namespace mol {
 
+// Kernels this library has enqueued in this process (read by mol_launch_count).
+void count_launch();
+
 // Geometry of the align step for given sizes (host arithmetic).
 struct AlignPlan {
   int64_t numel;
@@ -47,6 +50,7 @@ cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), int blocks, dim3 block,
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
+  count_launch();
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
@@ -63,6 +67,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  count_launch();
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 

@@ -43,7 +43,7 @@ def declared_functions():
 def test_exports_every_declared_symbol(mol):
     lib = mol.library()
     names = declared_functions()
-    assert len(names) == 15
+    assert len(names) == 16
     for n in names:
         assert hasattr(lib, n), n
     assert set(names) == set(mol.EXPORTS)
@@ -56,6 +56,7 @@ def test_status_strings_and_version(mol):
     for code in (0, -1, -2, -3, -4, 7):
         assert isinstance(lib.mol_status_string(code), bytes)
     assert lib.mol_last_cuda_error() == 0
+    assert lib.mol_launch_count() >= 0
 
 
 @needs_nvcc

@@ -143,3 +143,19 @@ def test_persistent_stage_counts_left_at_zero():
     assert mol.mol_take_fault_flags() == 0
     counts = ws[align_part:align_part + 8 * nblk].view(torch.int32)
     assert int(counts.abs().sum().item()) == 0
+
+
+def test_launches_per_layer():
+    """The library's launch count: a decode-like layer is 3 launches with the persistent stage
+    (align, gate_up stage, down stage) and 5 without it (align, then a shrink and an expand per
+    stage)."""
+    torch = torch_cuda()
+    mol = mol_lib()
+    dev = torch.device("cuda:0")
+    c = _case(CASES[0])
+    numel, V, BM = c["numel"], c["V"], c["BM"]
+    for stage, want in ((True, 3), (False, 5)):
+        ws = mol.alloc_workspace(numel, V, BM, dev, stage=stage)
+        n0 = mol.mol_launch_count()
+        _layer(mol, torch, c, dev, ws)
+        assert mol.mol_launch_count() - n0 == want
