@@ -97,18 +97,6 @@ int64_t mol_align_capacity(int64_t numel, int32_t num_vexperts, int32_t block_m)
  */
 size_t mol_workspace_bytes(int64_t numel, int32_t num_vexperts, int32_t block_m);
 
-/*
- * Bytes of device workspace that let mol_lora_forward run a stage as ONE
- * persistent launch (fork PR #24 PR body "Background (measured attribution)":
- * the MoL stages are separate fused_moe launches; here the shrink items and
- * the expand items of a stage share one grid): mol_workspace_bytes(numel, V,
- * block_m) for the align, then two arrays of capacity / block_m per-block
- * counts (one for stages that compute the routing, one for stages that reuse
- * it), 256-byte rounded. capacity is the routing buffer's (a multiple of
- * block_m). Pure host arithmetic; 0 on invalid arguments.
- */
-size_t mol_forward_workspace_bytes(int64_t numel, int32_t num_vexperts, int32_t block_m,
-                                   int64_t capacity);
 
 /*
  * Step 1: virtual top-k remap (sglang PR 24171 prhub summary, "Key source
@@ -269,18 +257,6 @@ int32_t mol_lora_expand(const float* inter, const void* lora_b, int32_t num_slic
  * lets its dependents start early, before writing them). lora_ranks and
  * lora_scalings (each NULL or one entry per adapter) are those of the shrink
  * and the expand.
- * Workspace: at least mol_workspace_bytes (the align's) when compute_routing
- * = 1. With at least mol_forward_workspace_bytes, calls with few rows per
- * virtual expert (fewer than four pairs each on average; ranks 8-64; no
- * adapter arrays) run the stage as one persistent launch whose expand items
- * wait (bounded) for their routed block's shrink items through per-block
- * counts kept in the workspace. The align of a compute_routing = 1 call (and
- * mol_align_block_size given such a workspace) sets them to zero and every
- * stage leaves them at zero, so a compute_routing = 0 call must get the
- * workspace of the call (or align) that computed its routing, or a zero-filled
- * one. Calls in flight at the same time need workspaces of their own. With
- * less workspace the stage runs as a shrink launch and an expand launch
- * (the results are the same, bit for bit).
  */
 int32_t mol_lora_forward(const void* x, int64_t x_row_stride, int32_t x_row_div, int32_t K,
                          const int32_t* topk_ids, const int32_t* lora_ids, int64_t num_tokens,

@@ -29,8 +29,7 @@ EXPORTS = (
     "mol_version", "mol_status_string", "mol_last_cuda_error", "mol_align_capacity",
     "mol_workspace_bytes", "mol_virtual_topk", "mol_align_block_size", "mol_lora_shrink",
     "mol_lora_expand", "mol_lora_forward", "mol_align_block_size_noalloc", "mol_token_lora_ids",
-    "mol_take_fault_flags", "mol_debug_wait_test", "mol_forward_workspace_bytes",
-    "mol_launch_count",
+    "mol_take_fault_flags", "mol_debug_wait_test", "mol_launch_count",
 )
 
 _lib = None
@@ -47,7 +46,6 @@ _SIGS = {
     "mol_launch_count": (_I64, []),
     "mol_align_capacity": (_I64, [_I64, _I32, _I32]),
     "mol_workspace_bytes": (_SZ, [_I64, _I32, _I32]),
-    "mol_forward_workspace_bytes": (_SZ, [_I64, _I32, _I32, _I64]),
     "mol_virtual_topk": (_I32, [_P, _P, _I64, _I32, _I32, _I32, _P, _P]),
     "mol_align_block_size": (_I32, [_P, _I64, _I32, _I32, _P, _I64, _P, _P, _P, _SZ, _P]),
     "mol_align_block_size_noalloc": (_I32, [_P, _I64, _I32, _I32, _P, _I64, _P, _P, _P]),
@@ -149,20 +147,9 @@ def alloc_routing(numel: int, num_vexperts: int, block_m: int, device) -> Routin
                    block_m, numel, num_vexperts)
 
 
-def forward_workspace_bytes(numel: int, num_vexperts: int, block_m: int,
-                            capacity: Optional[int] = None) -> int:
-    cap = align_capacity(numel, num_vexperts, block_m) if capacity is None else capacity
-    return int(library().mol_forward_workspace_bytes(numel, num_vexperts, block_m, cap))
-
-
-def alloc_workspace(numel: int, num_vexperts: int, block_m: int, device,
-                    capacity: Optional[int] = None, stage: bool = True) -> Optional[torch.Tensor]:
-    """Workspace for mol_align_block_size / mol_lora_forward. With `stage` (default) it also
-    holds the persistent fused stage's per-block counts for a routing of `capacity` slots
-    (default: the tight capacity); zero-filled, as the counts must start."""
-    n = (forward_workspace_bytes(numel, num_vexperts, block_m, capacity) if stage
-         else workspace_bytes(numel, num_vexperts, block_m))
-    return torch.zeros(n, dtype=torch.uint8, device=device) if n else None
+def alloc_workspace(numel: int, num_vexperts: int, block_m: int, device) -> Optional[torch.Tensor]:
+    n = workspace_bytes(numel, num_vexperts, block_m)
+    return torch.empty(n, dtype=torch.uint8, device=device) if n else None
 
 
 def mol_virtual_topk(topk_ids: torch.Tensor, lora_ids: torch.Tensor, num_experts: int,

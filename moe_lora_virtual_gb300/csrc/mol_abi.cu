@@ -150,15 +150,6 @@ size_t mol_workspace_bytes(int64_t numel, int32_t num_vexperts, int32_t block_m)
   return mol::make_align_plan(numel, num_vexperts, block_m).ws_bytes;
 }
 
-size_t mol_forward_workspace_bytes(int64_t numel, int32_t num_vexperts, int32_t block_m,
-                                   int64_t capacity) {
-  if (check_align_args(numel, num_vexperts, block_m) != MOL_OK || capacity < 0 ||
-      capacity % block_m != 0)
-    return 0;
-  return mol::make_align_plan(numel, num_vexperts, block_m).ws_bytes +
-         mol::stage_count_bytes(capacity, block_m);
-}
-
 int32_t mol_virtual_topk(const int32_t* topk_ids, const int32_t* lora_ids, int64_t num_tokens,
                          int32_t topk, int32_t num_experts, int32_t max_loras,
                          int32_t* vtopk_ids, void* stream) {
@@ -231,15 +222,9 @@ int32_t mol_align_block_size(const int32_t* vtopk_ids, int64_t numel, int32_t nu
   if (st != MOL_OK) return st;
   mol::AlignPlan p = plan;
   p.capacity = capacity;  // fill the caller's whole buffer
-  // a workspace with room for the fused stage's counts gets them zeroed too
-  int32_t* counts = nullptr;
-  const size_t cnt = mol::stage_count_bytes(capacity, block_m);
-  if (workspace && workspace_bytes >= plan.ws_bytes + cnt && aligned16(workspace))
-    counts = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + plan.ws_bytes);
   cudaError_t e = mol::launch_align(p, false, vtopk_ids, nullptr, 1, 1, 1, nullptr, num_vexperts,
                                     sorted_token_ids, expert_ids, num_tokens_post_padded,
-                                    workspace, false, static_cast<cudaStream_t>(stream), counts,
-                                    counts ? (int)(2 * (capacity / block_m)) : 0);
+                                    workspace, false, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MOL_OK : cuda_fail(e);
 }
 
@@ -334,21 +319,11 @@ int32_t mol_lora_forward(const void* x, int64_t x_row_stride, int32_t x_row_div,
   if (st != MOL_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
-  // The persistent fused stage's per-block counts follow the align's part of
-  // the workspace: one array for stages that compute the routing, one for
-  // stages that reuse it. The align zeroes both; each stage leaves its own at
-  // zero. Without room for them the stage runs as a shrink and an expand launch.
-  const int64_t nblk = capacity / block_m;
-  int32_t* counts = nullptr;
-  if (workspace && aligned16(workspace) && nblk <= INT32_MAX / 2 &&
-      workspace_bytes >= plan.ws_bytes + mol::stage_count_bytes(capacity, block_m))
-    counts = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + plan.ws_bytes);
   if (compute_routing) {
     mol::AlignPlan p = plan;
     p.capacity = capacity;
     e = mol::launch_align(p, true, topk_ids, lora_ids, topk, num_experts, max_loras, vtopk_ids, V,
-                          sorted_token_ids, expert_ids, num_tokens_post_padded, workspace, true, s,
-                          counts, counts ? (int)(2 * nblk) : 0);
+                          sorted_token_ids, expert_ids, num_tokens_post_padded, workspace, true, s);
     if (e != cudaSuccess) return cuda_fail(e);
   }
   if (numel == 0 || capacity == 0) return MOL_OK;
@@ -358,16 +333,6 @@ int32_t mol_lora_forward(const void* x, int64_t x_row_stride, int32_t x_row_div,
                           scale, topk_weights, sorted_token_ids, expert_ids,
                           num_tokens_post_padded, capacity, block_m, numel, V, inter, out,
                           out_row_stride, compute_routing == 0, s);
-    return e == cudaSuccess ? MOL_OK : cuda_fail(e);
-  }
-  if (counts && mol::stage_persistent_fits(numel, V, num_slices * rank, rank, K, block_m,
-                                           lora_ranks != nullptr || lora_scalings != nullptr)) {
-    e = mol::launch_stage_persistent(x, x_row_stride, x_row_div, K, lora_a, lora_b, num_slices,
-                                     rank, slice_n, scale, topk_weights, sorted_token_ids,
-                                     expert_ids, num_tokens_post_padded, capacity, block_m, numel,
-                                     V, inter, out, out_row_stride,
-                                     counts + (compute_routing ? 0 : nblk), compute_routing == 0,
-                                     s);
     return e == cudaSuccess ? MOL_OK : cuda_fail(e);
   }
   e = mol::launch_shrink(x, x_row_stride, x_row_div, K, lora_a, num_slices * rank,

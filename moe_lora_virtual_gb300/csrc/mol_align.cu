@@ -214,8 +214,7 @@ align_tile_kernel(const int* __restrict__ src, const int* __restrict__ lora_ids,
                   int num_vexperts, int block_m, int64_t capacity, int tile, int tiles, int nb_pad,
                   int* __restrict__ sorted_ids, int* __restrict__ expert_ids,
                   int* __restrict__ ntpp_out, int* __restrict__ ws_hist,
-                  int* __restrict__ ws_rank, int trigger, int* __restrict__ zero_out,
-                  int zero_n) {
+                  int* __restrict__ ws_rank, int trigger) {
   extern __shared__ __align__(16) unsigned char smem[];
   __shared__ int sh_scan[kAlignWarps + 1];
   const int nb = num_vexperts + 1;
@@ -238,9 +237,6 @@ align_tile_kernel(const int* __restrict__ src, const int* __restrict__ lora_ids,
   // routing, and may start early. With several tiles the scatter kernel is the
   // last writer and plays that role.
   if (tiles > 1 || trigger) pdl_launch_dependents();
-  // the persistent stage's per-block counts (if given) start at zero
-  for (int q = (int)blockIdx.x * kAlignThreads + tid; q < zero_n; q += (int)gridDim.x * kAlignThreads)
-    zero_out[q] = 0;
 
   // Every slot starts as padding (value numel); real pairs overwrite theirs.
   for (int64_t q = (int64_t)blockIdx.x * kAlignThreads + tid; q < capacity;
@@ -342,8 +338,7 @@ align_cluster_kernel(const int* __restrict__ src, const int* __restrict__ lora_i
                      int num_experts, int max_loras, int* __restrict__ vtopk_out, int64_t numel,
                      int num_vexperts, int block_m, int64_t capacity, int tile, int nb_pad,
                      int* __restrict__ sorted_ids, int* __restrict__ expert_ids,
-                     int* __restrict__ ntpp_out, int trigger, int* __restrict__ zero_out,
-                     int zero_n) {
+                     int* __restrict__ ntpp_out, int trigger) {
   extern __shared__ __align__(16) unsigned char smem[];
   __shared__ int sh_scan[kAlignWarps + 1];
   __shared__ int rsum[kClusterMax];  // padded total of each block's share of the buckets
@@ -363,7 +358,6 @@ align_cluster_kernel(const int* __restrict__ src, const int* __restrict__ lora_i
   }
   pdl_wait();  // inputs and routing buffers belong to earlier kernels until here
   if (trigger) pdl_launch_dependents();  // see align_tile_kernel
-  for (int q = me * kAlignThreads + tid; q < zero_n; q += CL * kAlignThreads) zero_out[q] = 0;
 
   for (int64_t q = (int64_t)me * kAlignThreads + tid; q < capacity;
        q += (int64_t)CL * kAlignThreads)
@@ -633,7 +627,7 @@ cudaError_t launch_align(const AlignPlan& plan, bool remap, const int32_t* src,
                          const int32_t* lora_ids, int topk, int num_experts, int max_loras,
                          int32_t* vtopk_out, int num_vexperts, int32_t* sorted_ids,
                          int32_t* expert_ids, int32_t* ntpp, void* workspace, bool trigger_early,
-                         cudaStream_t stream, int32_t* zero_out, int zero_n) {
+                         cudaStream_t stream) {
   const int trig = trigger_early ? 1 : 0;
   int device = 0;
   cudaError_t e = cudaGetDevice(&device);
@@ -652,12 +646,12 @@ cudaError_t launch_align(const AlignPlan& plan, bool remap, const int32_t* src,
       return launch_pdl_cluster(align_cluster_kernel<true>, cl, dim3(kAlignThreads), smem, stream,
                                 src, lora_ids, topk, num_experts, max_loras, vtopk_out, plan.numel,
                                 num_vexperts, plan.block_m, plan.capacity, tile, plan.nb_pad,
-                                sorted_ids, expert_ids, ntpp, trig, zero_out, zero_n);
+                                sorted_ids, expert_ids, ntpp, trig);
     return launch_pdl_cluster(align_cluster_kernel<false>, cl, dim3(kAlignThreads), smem, stream,
                               src, static_cast<const int32_t*>(nullptr), 1, 1, 1,
                               static_cast<int32_t*>(nullptr), plan.numel, num_vexperts,
                               plan.block_m, plan.capacity, tile, plan.nb_pad, sorted_ids,
-                              expert_ids, ntpp, trig, zero_out, zero_n);
+                              expert_ids, ntpp, trig);
   }
   int* ws_hist = nullptr;
   int* ws_offs = nullptr;
@@ -674,13 +668,12 @@ cudaError_t launch_align(const AlignPlan& plan, bool remap, const int32_t* src,
     e = launch_pdl(align_tile_kernel<true>, dim3(grid), dim3(kAlignThreads), plan.smem_tile, stream,
                    src, lora_ids, topk, num_experts, max_loras, vtopk_out, plan.numel, num_vexperts,
                    plan.block_m, plan.capacity, plan.tile, plan.tiles, plan.nb_pad, sorted_ids,
-                   expert_ids, ntpp, ws_hist, ws_rank, trig, zero_out, zero_n);
+                   expert_ids, ntpp, ws_hist, ws_rank, trig);
   } else {
     e = launch_pdl(align_tile_kernel<false>, dim3(grid), dim3(kAlignThreads), plan.smem_tile, stream,
                    src, static_cast<const int32_t*>(nullptr), 1, 1, 1, static_cast<int32_t*>(nullptr),
                    plan.numel, num_vexperts, plan.block_m, plan.capacity, plan.tile, plan.tiles,
-                   plan.nb_pad, sorted_ids, expert_ids, ntpp, ws_hist, ws_rank, trig, zero_out,
-                   zero_n);
+                   plan.nb_pad, sorted_ids, expert_ids, ntpp, ws_hist, ws_rank, trig);
   }
   if (e != cudaSuccess || plan.tiles == 1) return e;
   e = launch_pdl(align_scan_kernel, dim3(1), dim3(kScanThreads), (size_t)plan.nb * 4, stream, ws_hist,

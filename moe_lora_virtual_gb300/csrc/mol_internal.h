@@ -86,13 +86,12 @@ cudaError_t launch_virtual_topk(const int32_t* topk_ids, const int32_t* lora_ids
 // trigger_early: let the next kernel start before the align exits (only when
 // that kernel reads the routing after griddepcontrol.wait, as in
 // mol_lora_forward); otherwise the next kernel starts once the routing is
-// complete and may read it early. zero_out[0, zero_n) is set to zero (the
-// persistent stage's per-block counts; NULL/0 for none).
+// complete and may read it early.
 cudaError_t launch_align(const AlignPlan& plan, bool remap, const int32_t* src,
                          const int32_t* lora_ids, int topk, int num_experts, int max_loras,
                          int32_t* vtopk_out, int num_vexperts, int32_t* sorted_ids,
                          int32_t* expert_ids, int32_t* ntpp, void* workspace, bool trigger_early,
-                         cudaStream_t stream, int32_t* zero_out = nullptr, int zero_n = 0);
+                         cudaStream_t stream);
 
 // r1: rank per slice; lora_ranks (per adapter, adapter = v / num_experts, may
 // be NULL) limit the columns computed: rank 0 writes nothing, columns past
@@ -153,24 +152,6 @@ cudaError_t launch_stage(const void* x, int64_t x_stride, int x_div, int K, cons
                          int64_t out_stride, bool early, cudaStream_t stream);
 cudaError_t take_stage_faults(unsigned* out);
 
-// Persistent fused stage: the item shrink and the staged expand in one
-// persistent grid; an expand item waits (bounded) on its routed block's count
-// of finished shrink jobs. counts: capacity / block_m ints at zero, left at zero.
-// For calls with few rows per virtual expert, ranks 8-64, no adapter arrays,
-// not the tensor-core shrink's regime.
-bool stage_persistent_fits(int64_t numel, int num_vexperts, int R, int r, int K, int block_m,
-                           bool adapter_arrays);
-// Bytes of the two count arrays (one for stages that compute the routing, one
-// for stages that reuse it), 256-byte multiple.
-size_t stage_count_bytes(int64_t capacity, int block_m);
-cudaError_t launch_stage_persistent(const void* x, int64_t x_stride, int x_div, int K,
-                                    const void* lora_a, const void* lora_b, int S, int r, int Ns,
-                                    float scale, const float* topk_weights,
-                                    const int32_t* sorted_ids, const int32_t* expert_ids,
-                                    const int32_t* ntpp, int64_t capacity, int block_m,
-                                    int64_t numel, int num_vexperts, float* inter, void* out,
-                                    int64_t out_stride, int32_t* counts, bool early,
-                                    cudaStream_t stream);
 
 
 // Fault words of the pipelined kernels (bit 0: a bounded barrier or copy wait

@@ -412,478 +412,6 @@ lora_stage_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, i
   }
 }
 
-// ---------------------------------------------------------------------------
-// Persistent fused stage: the item shrink and the expand in one grid.
-//
-// The same work as the shrink launch followed by the expand launch, in one
-// persistent grid of two blocks per SM, without a grid-wide handoff. The grid
-// walks one list of items: first every (routed block t, 8 lora_a rows) shrink
-// item, then every (routed block t, slice s, 256 output columns) expand item;
-// block b takes items b, b + G, ... . A shrink job's last chunk, once its
-// intermediate rows are stored, adds one to count[t]; the producer of an
-// expand item issues the item's lora_b tile and output rows at once, waits
-// (bounded) until count[t] shows every shrink job of block t done, and then
-// copies the tile's intermediate rows into the same stage. So the lora_b
-// stream follows the lora_a stream through the ring without a break, and an
-// expand item waits only for its own routed block. Every block's items keep the
-// item shrink's balance (8-row shrink items, 256-column expand items). The
-// last expand tile of a block sets count[t] back to zero, so the counts are
-// zero again when the launch ends (the align zeroes them before the stage of
-// a new routing). Arithmetic: the item shrink's and the staged expand's, so the
-// results are bit-identical to the two launches.
-namespace ps {
-constexpr int kConsumers = 4;
-constexpr int kThreads = (kConsumers + 1) * 32;
-constexpr int kJT = 8;                 // lora_a rows per shrink item
-constexpr int kXR = 16;                // pair rows per job (one m16 mma tile)
-constexpr int kStageBytes = 52 * 1024;  // the item shrink's stage: same k chunks
-constexpr int kStages = 2;
-constexpr int kMeta = kStages + 2;     // jobs whose meta a consumer may still read
-constexpr int kHeader = 2048;          // barriers, stage headers, job meta
-constexpr int kCols = 256;             // output columns per expand item
-constexpr int kOutPitch = kCols * 2 + 64;
-constexpr int kInterOff = kCols * 64 * 2 + kXR * kOutPitch;  // expand stage: B tile, out rows, inter rows
-constexpr size_t kSmem = kHeader + (size_t)kStages * kStageBytes;
-constexpr uint32_t kPolls = 1u << 22;
-struct Job {
-  int t, jt, cm, s, col0, ncols, total;  // block, group (shrink) / slice, columns, count total (expand)
-  int rows[kXR];
-};
-struct StageHdr {
-  int kind;   // 0 shrink chunk, 1 expand tile, -1 end of work
-  int job;    // meta slot
-  int k0, len, pitch;  // shrink chunk
-};
-static_assert(2 * kStages * 8 + kStages * (int)sizeof(StageHdr) + kMeta * (int)sizeof(Job) <= kHeader,
-              "header");
-static_assert(kInterOff + kXR * 64 * 4 <= kStageBytes, "expand stage");
-
-MOL_DEV void chunk(int K, int cm, int& len, int& pitch) {
-  const int rows = kJT + cm;
-  if (rows * K * 2 <= kStageBytes) {
-    len = K;
-    pitch = K * 2;
-    return;
-  }
-  const int lmax = (kStageBytes / rows - 64) / 2 / 64 * 64;
-  const int n = (K + lmax - 1) / lmax;
-  len = ((K + n - 1) / n + 63) / 64 * 64;
-  pitch = len * 2 + 64;
-}
-
-// Bounded wait until *p >= target (acquire at GPU scope); false on timeout.
-MOL_DEV bool wait_count(const int* p, int target) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  if (v >= target) return true;
-  const uint64_t t0 = global_ns();
-  for (uint32_t i = 0; i < kPolls; ++i) {
-    __nanosleep(32);
-    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    if (v >= target) return true;
-    if (global_ns() - t0 > kWaitLimitNs) return false;
-  }
-  return false;
-}
-// Orders the data this thread acquired (generic proxy) before its later bulk
-// copies (async proxy) that read it.
-MOL_DEV void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
-}  // namespace ps
-
-struct PsRaw {  // routing words of one item, loaded one item ahead
-  int64_t t;
-  int ntpp, e;
-  int sl[4];
-};
-
-template <int RK>
-__global__ void __launch_bounds__(ps::kThreads, 2)
-lora_stage_persistent_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, int K,
-                             const uint16_t* __restrict__ lora_a, int R,
-                             const uint16_t* __restrict__ lora_b, int S, int Ns, float scale,
-                             const float* __restrict__ topk_w, const int* __restrict__ sorted_ids,
-                             const int* __restrict__ expert_ids, const int* __restrict__ ntpp_ptr,
-                             int block_m, int64_t numel, int num_vexperts,
-                             float* __restrict__ inter, uint16_t* __restrict__ out,
-                             int64_t out_stride, int* __restrict__ count, int n_jt, int n_chunks,
-                             int64_t n_shrink, int64_t n_items, int early) {
-  using namespace ps;
-  static_assert(RK == 8 || RK == 16 || RK == 32 || RK == 64, "persistent stage: rank 8 to 64");
-  constexpr bool K16 = (RK <= 16);
-  constexpr int KB = K16 ? 1 : RK / 32;
-  extern __shared__ __align__(128) unsigned char smem[];
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-  uint64_t* empty = full + kStages;
-  StageHdr* hdr = reinterpret_cast<StageHdr*>(smem + 2 * kStages * 8);
-  Job* meta = reinterpret_cast<Job*>(smem + 2 * kStages * 8 + kStages * sizeof(StageHdr));
-  unsigned char* stages = smem + kHeader;
-  __shared__ float red[kConsumers - 1][4][32];
-  __shared__ int prow[128];
-
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid == 0) {
-    for (int st = 0; st < kStages; ++st) {
-      mbar_init(&full[st], 1);
-      mbar_init(&empty[st], kConsumers);
-    }
-    fence_mbar_init();
-  }
-  __syncthreads();
-  const int per_block_exp = S * n_chunks;
-
-  if (warp == kConsumers) {
-    // ------------------------------------------------------------ producer
-    // Routing words and lora weights are read before griddepcontrol.wait only
-    // with `early` (the routing is older than the kernel before this one);
-    // activations, output rows and the counts, after it.
-    bool waited = !early;
-    if (!early) {
-      pdl_wait();
-      pdl_launch_dependents();
-    }
-    const int64_t G = gridDim.x;
-    uint32_t q = 0, jn = 0;
-    bool fault = false;
-    auto acquire = [&](int& st) -> bool {
-      st = (int)(q % kStages);
-      const uint32_t ph = (q / kStages) & 1;
-      bool ok = true;
-      if (lane == 0) ok = mbar_wait(&empty[st], ph ^ 1, kPolls);
-      return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-    };
-    auto wait_dep = [&]() {
-      if (!waited) {
-        pdl_wait();
-        pdl_launch_dependents();
-        waited = true;
-      }
-    };
-    auto fetch = [&](int64_t it, PsRaw& r) {
-      r.t = it >= n_items ? -1 : it < n_shrink ? it / n_jt : (it - n_shrink) / per_block_exp;
-      r.ntpp = 0;
-      r.e = -1;
-#pragma unroll
-      for (int u = 0; u < 4; ++u) r.sl[u] = -1;
-      if (r.t < 0) return;
-      r.ntpp = __ldg(ntpp_ptr);
-      r.e = __ldg(expert_ids + r.t);
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int idx = u * 32 + lane;
-        if (idx < block_m) r.sl[u] = __ldg(sorted_ids + r.t * block_m + idx);
-      }
-    };
-    PsRaw nxt;
-    int64_t item = blockIdx.x;
-    fetch(item, nxt);
-    while (item < n_items && !fault) {
-      const PsRaw cr = nxt;
-      const int64_t cur = item;
-      item += G;
-      fetch(item, nxt);
-      const int v = (cr.t * block_m < cr.ntpp) ? cr.e : -1;
-      if (v < 0 || v >= num_vexperts) continue;
-      int c = 0;
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int slu = cr.sl[u];
-        const bool ok = slu >= 0 && (int64_t)slu < numel;
-        const unsigned bal = __ballot_sync(0xffffffffu, ok);
-        if (ok) prow[c + __popc(bal & lanemask_lt())] = slu;
-        c += __popc(bal);
-      }
-      __syncwarp();
-      if (c == 0) continue;
-      const int tiles_m = (c + kXR - 1) / kXR;
-      if (cur < n_shrink) {
-        // ---- shrink item: 8 lora_a rows of virtual expert v, every row tile
-        const int jt = (int)(cur % n_jt);
-        const uint16_t* wrows = lora_a + ((int64_t)v * R + jt * kJT) * K;
-        for (int m0 = 0; m0 < c && !fault; m0 += kXR) {
-          const int cm = min(kXR, c - m0);
-          int len, pitch;
-          chunk(K, cm, len, pitch);
-          const bool whole = (len == K && pitch == K * 2);
-          const int slot = (int)(jn % kMeta);
-          Job& jb = meta[slot];
-          if (lane == 0) {
-            jb.t = (int)cr.t;
-            jb.jt = jt;
-            jb.cm = cm;
-          }
-          if (lane < cm) jb.rows[lane] = prow[m0 + lane];
-          const uint16_t* xsrc =
-              (lane >= 16 && lane - 16 < cm) ? x + (int64_t)(prow[m0 + lane - 16] / x_div) * x_stride
-                                             : nullptr;
-          __syncwarp();
-          for (int k0 = 0; k0 < K; k0 += len) {
-            int st;
-            if (!acquire(st)) {
-              fault = true;
-              break;
-            }
-            const int cl = min(len, K - k0);
-            unsigned char* base = stages + (size_t)st * kStageBytes;
-            if (lane == 0) {
-              hdr[st] = StageHdr{0, slot, k0, cl, pitch};
-              mbar_arrive_expect_tx(&full[st], (uint32_t)((kJT + cm) * cl * 2));
-            }
-            __syncwarp();
-            if (whole) {
-              if (lane == 0) bulk_g2s(base, wrows, kJT * K * 2, &full[st]);
-            } else if (lane < kJT) {
-              bulk_g2s(base + lane * pitch, wrows + (int64_t)lane * K + k0, cl * 2, &full[st]);
-            }
-            wait_dep();
-            if (xsrc) bulk_g2s(base + (kJT + lane - 16) * pitch, xsrc + k0, cl * 2, &full[st]);
-            ++q;
-          }
-          ++jn;
-        }
-      } else {
-        // ---- expand item: slice s, 256 output columns, every row tile
-        const int rem = (int)((cur - n_shrink) % per_block_exp);
-        const int s = rem / n_chunks;
-        const int col0 = (rem - s * n_chunks) * kCols;
-        const int ncols = min(kCols, Ns - col0);
-        const int total = tiles_m * (n_jt + per_block_exp);
-        const uint32_t wbytes = (uint32_t)ncols * RK * 2;
-        const uint16_t* bsrc = lora_b + (((int64_t)v * S + s) * Ns + col0) * RK;
-        for (int m0 = 0; m0 < c && !fault; m0 += kXR) {
-          const int cm = min(kXR, c - m0);
-          const int slot = (int)(jn % kMeta);
-          Job& jb = meta[slot];
-          if (lane == 0) {
-            jb.t = (int)cr.t;
-            jb.cm = cm;
-            jb.s = s;
-            jb.col0 = col0;
-            jb.ncols = ncols;
-            jb.total = total;
-          }
-          if (lane < cm) jb.rows[lane] = prow[m0 + lane];
-          __syncwarp();
-          int st;
-          if (!acquire(st)) {
-            fault = true;
-            break;
-          }
-          unsigned char* base = stages + (size_t)st * kStageBytes;
-          if (lane == 0) {
-            hdr[st] = StageHdr{1, slot, 0, 0, 0};
-            mbar_arrive_expect_tx(&full[st], wbytes + (uint32_t)(cm * ncols * 2) +
-                                                 (uint32_t)(cm * RK * 4));
-            bulk_g2s(base, bsrc, wbytes, &full[st]);
-          }
-          wait_dep();
-          const int row = lane < cm ? prow[m0 + lane] : 0;
-          if (lane < cm)
-            bulk_g2s(base + wbytes + lane * kOutPitch,
-                     out + (int64_t)row * out_stride + (int64_t)s * Ns + col0, (uint32_t)ncols * 2,
-                     &full[st]);
-          // the tile's intermediate rows, once every shrink job of the block is done
-          bool ok = true;
-          if (lane == 0) ok = wait_count(count + cr.t, tiles_m * n_jt);
-          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-          if (!ok) {  // the stage never completes: its consumers give up too
-            fault = true;
-            ++q;
-            break;
-          }
-          if (lane < cm) {
-            fence_proxy_async_global();
-            bulk_g2s(base + kInterOff + lane * RK * 4, inter + (int64_t)row * R + s * RK, RK * 4,
-                     &full[st]);
-          }
-          ++q;
-          ++jn;
-        }
-      }
-    }
-    wait_dep();
-    if (!fault) {
-      int st;
-      if (acquire(st)) {
-        if (lane == 0) {
-          hdr[st].kind = -1;
-          mbar_arrive(&full[st]);
-        }
-      } else {
-        fault = true;
-      }
-    }
-    if (fault && lane == 0) {
-      atomicOr(&g_stage_fault_flags, kFaultBulkTimeout);
-      for (uint32_t u = q > (uint32_t)kStages ? q - kStages : 0; u < q; ++u)
-        mbar_wait(&full[u % kStages], (u / kStages) & 1, kPolls);
-    }
-    __syncwarp();
-    return;
-  }
-
-  // -------------------------------------------------------------- consumers
-  pdl_wait();  // they write the intermediate, the output and the counts
-  pdl_launch_dependents();
-  const int g = lane >> 2, tq = lane & 3;
-  const uint4 zero = make_uint4(0, 0, 0, 0);
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  float acc2[4] = {0.f, 0.f, 0.f, 0.f};
-  for (uint32_t q = 0;; ++q) {
-    const int st = (int)(q % kStages);
-    if (!mbar_wait(&full[st], (q / kStages) & 1, kPolls)) {
-      if (lane == 0) atomicOr(&g_stage_fault_flags, kFaultBulkTimeout);
-      return;
-    }
-    const StageHdr h = hdr[st];
-    if (h.kind < 0) break;
-    const Job& jb = meta[h.job];
-    const int cm = jb.cm;
-    const unsigned char* W = stages + (size_t)st * kStageBytes;
-    if (h.kind == 0) {
-      // ---- shrink chunk (the item shrink's consumer)
-      const int k0 = h.k0, len = h.len, pitch = h.pitch;
-      if (k0 == 0) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[e] = acc2[e] = 0.f;
-      }
-      const unsigned char* X = W + kJT * pitch;
-      const int nkb = (len + 31) >> 5;
-      const int kb0 = warp * nkb / kConsumers, kb1 = (warp + 1) * nkb / kConsumers;
-#pragma unroll 2
-      for (int kb = kb0; kb < kb1; kb += 2) {
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int kk = (kb + hh) * 32 + 8 * tq;
-          const bool kin = kb + hh < kb1 && kk < len;
-          const uint4 xa = (kin && g < cm) ? lds16(X + g * pitch + kk * 2) : zero;
-          const uint4 xb = (kin && g + 8 < cm) ? lds16(X + (g + 8) * pitch + kk * 2) : zero;
-          const uint4 a = kin ? lds16(W + g * pitch + kk * 2) : zero;
-          if (hh == 0) {
-            mma_16816(acc, xa.x, xb.x, xa.y, xb.y, a.x, a.y);
-            mma_16816(acc, xa.z, xb.z, xa.w, xb.w, a.z, a.w);
-          } else {
-            mma_16816(acc2, xa.x, xb.x, xa.y, xb.y, a.x, a.y);
-            mma_16816(acc2, xa.z, xb.z, xa.w, xb.w, a.z, a.w);
-          }
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[st]);
-      if (k0 + len >= K) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[e] += acc2[e];
-        if (warp > 0) {
-#pragma unroll
-          for (int e = 0; e < 4; ++e) red[warp - 1][e][lane] = acc[e];
-        }
-        named_sync(1, kConsumers * 32);
-        if (warp == 0) {
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-#pragma unroll
-            for (int w = 0; w < kConsumers - 1; ++w) acc[e] += red[w][e][lane];
-          const int col = jb.jt * kJT + 2 * tq;
-          if (g < cm)
-            *reinterpret_cast<float2*>(inter + (int64_t)jb.rows[g] * R + col) =
-                make_float2(acc[0], acc[1]);
-          if (g + 8 < cm)
-            *reinterpret_cast<float2*>(inter + (int64_t)jb.rows[g + 8] * R + col) =
-                make_float2(acc[2], acc[3]);
-          __syncwarp();
-          if (lane == 0) {  // publish: the job's rows are stored
-            __threadfence();
-            atomicAdd(count + jb.t, 1);
-          }
-        }
-        named_sync(1, kConsumers * 32);
-      }
-      continue;
-    }
-    // ---- expand tile (the staged expand's arithmetic)
-    const int s = jb.s, col0 = jb.col0, ncols = jb.ncols;
-    const uint16_t* wsm = reinterpret_cast<const uint16_t*>(W);
-    const unsigned char* osm = W + (size_t)ncols * RK * 2;
-    const float* ism = reinterpret_cast<const float*>(W + kInterOff);  // [cm][RK]
-    const bool kq = RK != 8 || tq < 2;
-    const int i0 = g < cm ? jb.rows[g] : -1;
-    const int i1 = g + 8 < cm ? jb.rows[g + 8] : -1;
-    const float4 zf = make_float4(0.f, 0.f, 0.f, 0.f);
-    uint32_t hf[KB][8], lf[KB][8];
-#pragma unroll
-    for (int kb = 0; kb < KB; ++kb) {
-      const int j = K16 ? 4 * tq : kb * 32 + 8 * tq;
-      const float* p0 = ism + g * RK + j;
-      const float* p1 = ism + (g + 8) * RK + j;
-      const float4 a0 = (kq && i0 >= 0) ? *reinterpret_cast<const float4*>(p0) : zf;
-      const float4 a1 = (kq && i1 >= 0) ? *reinterpret_cast<const float4*>(p1) : zf;
-      split_bf16x2(a0.x, a0.y, hf[kb][0], lf[kb][0]);
-      split_bf16x2(a1.x, a1.y, hf[kb][1], lf[kb][1]);
-      split_bf16x2(a0.z, a0.w, hf[kb][2], lf[kb][2]);
-      split_bf16x2(a1.z, a1.w, hf[kb][3], lf[kb][3]);
-      if constexpr (!K16) {
-        const float4 b0 = i0 >= 0 ? *reinterpret_cast<const float4*>(p0 + 4) : zf;
-        const float4 b1 = i1 >= 0 ? *reinterpret_cast<const float4*>(p1 + 4) : zf;
-        split_bf16x2(b0.x, b0.y, hf[kb][4], lf[kb][4]);
-        split_bf16x2(b1.x, b1.y, hf[kb][5], lf[kb][5]);
-        split_bf16x2(b0.z, b0.w, hf[kb][6], lf[kb][6]);
-        split_bf16x2(b1.z, b1.w, hf[kb][7], lf[kb][7]);
-      }
-    }
-    const float sw0 = i0 >= 0 ? (topk_w ? scale * __ldg(topk_w + i0) : scale) : 0.f;
-    const float sw1 = i1 >= 0 ? (topk_w ? scale * __ldg(topk_w + i1) : scale) : 0.f;
-#pragma unroll
-    for (int cg = 0; cg < 2; ++cg) {
-      const int nb = warp * 64 + cg * 32;
-      if (nb >= ncols) break;
-      float d[4][4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) d[u][0] = d[u][1] = d[u][2] = d[u][3] = 0.f;
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int wr = nb + 8 * (g >> 1) + 2 * u + (g & 1);
-        const bool bv = wr < ncols;
-        if constexpr (K16) {
-          const uint2 q2 = (bv && kq) ? lds8(wsm + wr * RK + 4 * tq) : make_uint2(0, 0);
-          mma_16816(d[u], hf[0][0], hf[0][1], hf[0][2], hf[0][3], q2.x, q2.y);
-          mma_16816(d[u], lf[0][0], lf[0][1], lf[0][2], lf[0][3], q2.x, q2.y);
-        } else {
-#pragma unroll
-          for (int kb = 0; kb < KB; ++kb) {
-            const uint4 w4 = bv ? lds16(wsm + wr * RK + kb * 32 + 8 * tq) : zero;
-            mma_16816(d[u], hf[kb][0], hf[kb][1], hf[kb][2], hf[kb][3], w4.x, w4.y);
-            mma_16816(d[u], lf[kb][0], lf[kb][1], lf[kb][2], lf[kb][3], w4.x, w4.y);
-            mma_16816(d[u], hf[kb][4], hf[kb][5], hf[kb][6], hf[kb][7], w4.z, w4.w);
-            mma_16816(d[u], lf[kb][4], lf[kb][5], lf[kb][6], lf[kb][7], w4.z, w4.w);
-          }
-        }
-      }
-      if (nb + 8 * tq < ncols) {
-        const int64_t oc = (int64_t)s * Ns + col0 + nb + 8 * tq;
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int i = hh ? i1 : i0;
-          if (i < 0) continue;
-          const float sw = hh ? sw1 : sw0;
-          uint4 ov = lds16(osm + (8 * hh + g) * kOutPitch + (nb + 8 * tq) * 2);
-          uint32_t* ow = reinterpret_cast<uint32_t*>(&ov);
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const float lo = fmaf(sw, d[u][2 * hh], bf16_lo(ow[u]));
-            const float hi = fmaf(sw, d[u][2 * hh + 1], bf16_hi(ow[u]));
-            ow[u] = pack_bf16x2(lo, hi);
-          }
-          *reinterpret_cast<uint4*>(out + (int64_t)i * out_stride + oc) = ov;
-        }
-      }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[st]);
-    if (warp == 0 && lane == 0) {  // the block's last item of the launch leaves its count at zero
-      if (atomicAdd(count + jb.t, 1) == jb.total - 1) atomicExch(count + jb.t, 0);
-    }
-  }
-}
-
 // --- host side ----------------------------------------------------------------
 
 static int stage_sms() {
@@ -913,30 +441,14 @@ bool stage_fused_fits(int64_t numel, int num_vexperts, int R, int r, int K, int 
   return capacity / block_m <= stage_sms() && weight_bytes <= 2 * fs::kStageBytes;
 }
 
-bool stage_persistent_fits(int64_t numel, int num_vexperts, int R, int r, int K, int block_m,
-                           bool adapter_arrays) {
-  if (adapter_arrays || numel <= 0) return false;
-  if (!(r == 8 || r == 16 || r == 32 || r == 64) || R % 8 != 0) return false;
-  if (shrink_tc_fits(numel, num_vexperts, R, K, block_m)) return false;
-  return numel < 4 * std::min<int64_t>(numel, num_vexperts);  // few rows per virtual expert
-}
-
-size_t stage_count_bytes(int64_t capacity, int block_m) {
-  const size_t n = 2 * (size_t)(capacity / block_m);
-  return (n * 4 + 255) / 256 * 256;
-}
-
 template <int RK>
 static cudaError_t prepare_stage_rk() {
   const int bytes = (int)fs::smem_bytes(128);
   cudaError_t e = cudaFuncSetAttribute(lora_stage_kernel<RK, false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(lora_stage_kernel<RK, true>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(lora_stage_persistent_kernel<RK>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ps::kSmem);
+  return cudaFuncSetAttribute(lora_stage_kernel<RK, true>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
 cudaError_t prepare_stage_kernels() {
@@ -980,48 +492,6 @@ cudaError_t launch_stage(const void* x, int64_t x_stride, int x_div, int K, cons
       return cudaErrorInvalidValue;
   }
 #undef MOL_STAGE
-}
-
-cudaError_t launch_stage_persistent(const void* x, int64_t x_stride, int x_div, int K,
-                                    const void* lora_a, const void* lora_b, int S, int r, int Ns,
-                                    float scale, const float* topk_weights,
-                                    const int32_t* sorted_ids, const int32_t* expert_ids,
-                                    const int32_t* ntpp, int64_t capacity, int block_m,
-                                    int64_t numel, int num_vexperts, float* inter, void* out,
-                                    int64_t out_stride, int32_t* counts, bool early,
-                                    cudaStream_t stream) {
-  const int64_t nblk = capacity / block_m;
-  if (numel == 0 || nblk == 0) return cudaSuccess;
-  const int R = S * r;
-  const int n_jt = R / ps::kJT;
-  const int n_chunks = (Ns + ps::kCols - 1) / ps::kCols;
-  const int64_t n_shrink = nblk * n_jt;
-  const int64_t n_items = n_shrink + nblk * S * n_chunks;
-  // every block of the grid must be resident at once (expand items wait on
-  // other blocks' shrink items): two per SM, the kernel's occupancy
-  const dim3 grid((unsigned)std::min<int64_t>(n_items, 2LL * stage_sms()));
-  const uint16_t* xp = static_cast<const uint16_t*>(x);
-  const uint16_t* a = static_cast<const uint16_t*>(lora_a);
-  const uint16_t* b = static_cast<const uint16_t*>(lora_b);
-  uint16_t* o = static_cast<uint16_t*>(out);
-#define MOL_PSTAGE(RK)                                                                         \
-  launch_pdl(lora_stage_persistent_kernel<RK>, grid, dim3(ps::kThreads), ps::kSmem, stream, xp, \
-             x_stride, x_div, K, a, R, b, S, Ns, scale, topk_weights, sorted_ids, expert_ids,    \
-             ntpp, block_m, numel, num_vexperts, inter, o, out_stride, counts, n_jt, n_chunks,  \
-             n_shrink, n_items, early ? 1 : 0)
-  switch (r) {
-    case 8:
-      return MOL_PSTAGE(8);
-    case 16:
-      return MOL_PSTAGE(16);
-    case 32:
-      return MOL_PSTAGE(32);
-    case 64:
-      return MOL_PSTAGE(64);
-    default:
-      return cudaErrorInvalidValue;
-  }
-#undef MOL_PSTAGE
 }
 
 }  // namespace mol

@@ -43,7 +43,7 @@ def declared_functions():
 def test_exports_every_declared_symbol(mol):
     lib = mol.library()
     names = declared_functions()
-    assert len(names) == 16
+    assert len(names) == 15
     for n in names:
         assert hasattr(lib, n), n
     assert set(names) == set(mol.EXPORTS)
