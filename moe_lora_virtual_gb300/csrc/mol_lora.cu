@@ -612,9 +612,11 @@ lora_expand_kernel(const float* __restrict__ inter, int R, const uint16_t* __res
 constexpr int kStCols = 256;
 constexpr int kStGroups = kStCols / (kExpandThreads / 32) / 32;  // column groups per warp
 constexpr int kStOutPitch = kStCols + 32;  // staged output row, elements (64-byte skew per row)
-// dynamic shared memory of one block: the lora_b tile, then the output row tile(s)
+// dynamic shared memory of one block: the lora_b tile, then the output row tile(s), then
+// (two staged tiles) the next tile's intermediate fragments
 constexpr size_t expand_st_smem(int rk, bool db) {
-  return (size_t)kStCols * rk * 2 + (size_t)(db ? 2 : 1) * 16 * kStOutPitch * 2;
+  return (size_t)kStCols * rk * 2 + (size_t)(db ? 2 : 1) * 16 * kStOutPitch * 2 +
+         (db ? (size_t)16 * rk * 4 : 0);
 }
 
 template <int RK, bool EARLY, bool ADAPT, bool DB>
@@ -632,6 +634,7 @@ lora_expand_st_kernel(const float* __restrict__ inter, int R, const uint16_t* __
   extern __shared__ __align__(128) unsigned char st_smem[];
   uint16_t* wsm = reinterpret_cast<uint16_t*>(st_smem);  // kStCols x RK lora_b rows
   uint16_t* osm = wsm + kStCols * RK;                     // (DB ? 2 : 1) x 16 output rows
+  float* ism = reinterpret_cast<float*>(osm + (DB ? 2 : 1) * 16 * kStOutPitch);  // DB: 16 x RK
   __shared__ uint64_t wbar;
   __shared__ int rows[128];
   __shared__ int wcnt[kExpandThreads / 32];
@@ -704,12 +707,34 @@ lora_expand_st_kernel(const float* __restrict__ inter, int R, const uint16_t* __
         if (ok && i >= 0) cp_async16_zfill(osm_at(buf, hh, col), out + (int64_t)i * out_stride + oc, 16u);
       }
     }
-    cp_async_commit();
+  };
+  // DB: this thread's intermediate fragments of rows r0 and r1 (columns of its
+  // quad in every k block), staged at ism[(8 * hh + g) * RK + column] and read
+  // back by this thread only, into registers, before it stages the next tile's
+  auto ism_at = [&](int hh, int j) { return ism + (8 * hh + g) * RK + j; };
+  auto load_inter = [&](int r0, int r1) {
+#pragma unroll
+    for (int kb = 0; kb < KB; ++kb) {
+      const int j = K16 ? 4 * tq : kb * 32 + 8 * tq;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int i = hh ? r1 : r0;
+        if (!kq || i < 0) continue;
+        const float* src = inter + (int64_t)i * R + s * RK + j;
+        cp_async16_zfill(ism_at(hh, j), src, 16u);
+        if constexpr (!K16) cp_async16_zfill(ism_at(hh, j + 4), src + 4, 16u);
+      }
+    }
   };
   load_out(0, i0, i1);
+  cp_async_commit();
   if (EARLY) {
     pdl_wait();  // the intermediate comes from the shrink that precedes this kernel
     pdl_launch_dependents();
+  }
+  if constexpr (DB) {
+    load_inter(i0, i1);
+    cp_async_commit();
   }
 
   bool landed = false;
@@ -718,42 +743,66 @@ lora_expand_st_kernel(const float* __restrict__ inter, int R, const uint16_t* __
     if (m0 > 0) {
       i0 = m0 + g < c ? rows[m0 + g] : -1;
       i1 = m0 + 8 + g < c ? rows[m0 + 8 + g] : -1;
-      if (!DB) load_out(0, i0, i1);
+      if (!DB) {
+        load_out(0, i0, i1);
+        cp_async_commit();
+      }
     }
     const bool ahead = DB && m0 + 16 < c;
-    if (ahead)  // the next tile's output rows, into the other buffer (read last in the previous tile)
-      load_out(buf ^ 1, m0 + 16 + g < c ? rows[m0 + 16 + g] : -1,
-               m0 + 24 + g < c ? rows[m0 + 24 + g] : -1);
-    // the intermediate fragments, split into bf16 head and tail, serve every column group
+    const int n0 = ahead && m0 + 16 + g < c ? rows[m0 + 16 + g] : -1;
+    const int n1 = ahead && m0 + 24 + g < c ? rows[m0 + 24 + g] : -1;
+    if (ahead) {  // the next tile's output rows, into the other buffer
+      load_out(buf ^ 1, n0, n1);
+      cp_async_commit();
+    }
+    // the intermediate fragments, split into bf16 head and tail, serve every column
+    // group: from global memory (L2) at once with one staged tile, from the staged
+    // copies (after their wait below) with two
     const int koff = s * RK + (K16 ? 4 * tq : 8 * tq);
     const float* p0 = inter + (int64_t)(i0 >= 0 ? i0 : 0) * R + koff;
     const float* p1 = inter + (int64_t)(i1 >= 0 ? i1 : 0) * R + koff;
     uint32_t h[KB][8], l[KB][8];
+    auto build = [&]() {
 #pragma unroll
-    for (int kb = 0; kb < KB; ++kb) {
-      float4 a0 = (kq && i0 >= 0) ? ld_l2_f4(p0 + kb * 32) : zf;
-      float4 a1 = (kq && i1 >= 0) ? ld_l2_f4(p1 + kb * 32) : zf;
-      if (ADAPT && rl < RK) {
-        mask_cols(a0, (K16 ? 4 * tq : kb * 32 + 8 * tq), rl);
-        mask_cols(a1, (K16 ? 4 * tq : kb * 32 + 8 * tq), rl);
-      }
-      split_bf16x2(a0.x, a0.y, h[kb][0], l[kb][0]);
-      split_bf16x2(a1.x, a1.y, h[kb][1], l[kb][1]);
-      split_bf16x2(a0.z, a0.w, h[kb][2], l[kb][2]);
-      split_bf16x2(a1.z, a1.w, h[kb][3], l[kb][3]);
-      if constexpr (!K16) {
-        float4 b0 = i0 >= 0 ? ld_l2_f4(p0 + kb * 32 + 4) : zf;
-        float4 b1 = i1 >= 0 ? ld_l2_f4(p1 + kb * 32 + 4) : zf;
-        if (ADAPT && rl < RK) {
-          mask_cols(b0, kb * 32 + 8 * tq + 4, rl);
-          mask_cols(b1, kb * 32 + 8 * tq + 4, rl);
+      for (int kb = 0; kb < KB; ++kb) {
+        const int j = K16 ? 4 * tq : kb * 32 + 8 * tq;
+        float4 a0, a1;
+        if constexpr (DB) {
+          a0 = (kq && i0 >= 0) ? *reinterpret_cast<const float4*>(ism_at(0, j)) : zf;
+          a1 = (kq && i1 >= 0) ? *reinterpret_cast<const float4*>(ism_at(1, j)) : zf;
+        } else {
+          a0 = (kq && i0 >= 0) ? ld_l2_f4(p0 + kb * 32) : zf;
+          a1 = (kq && i1 >= 0) ? ld_l2_f4(p1 + kb * 32) : zf;
         }
-        split_bf16x2(b0.x, b0.y, h[kb][4], l[kb][4]);
-        split_bf16x2(b1.x, b1.y, h[kb][5], l[kb][5]);
-        split_bf16x2(b0.z, b0.w, h[kb][6], l[kb][6]);
-        split_bf16x2(b1.z, b1.w, h[kb][7], l[kb][7]);
+        if (ADAPT && rl < RK) {
+          mask_cols(a0, j, rl);
+          mask_cols(a1, j, rl);
+        }
+        split_bf16x2(a0.x, a0.y, h[kb][0], l[kb][0]);
+        split_bf16x2(a1.x, a1.y, h[kb][1], l[kb][1]);
+        split_bf16x2(a0.z, a0.w, h[kb][2], l[kb][2]);
+        split_bf16x2(a1.z, a1.w, h[kb][3], l[kb][3]);
+        if constexpr (!K16) {
+          float4 b0, b1;
+          if constexpr (DB) {
+            b0 = i0 >= 0 ? *reinterpret_cast<const float4*>(ism_at(0, j + 4)) : zf;
+            b1 = i1 >= 0 ? *reinterpret_cast<const float4*>(ism_at(1, j + 4)) : zf;
+          } else {
+            b0 = i0 >= 0 ? ld_l2_f4(p0 + kb * 32 + 4) : zf;
+            b1 = i1 >= 0 ? ld_l2_f4(p1 + kb * 32 + 4) : zf;
+          }
+          if (ADAPT && rl < RK) {
+            mask_cols(b0, j + 4, rl);
+            mask_cols(b1, j + 4, rl);
+          }
+          split_bf16x2(b0.x, b0.y, h[kb][4], l[kb][4]);
+          split_bf16x2(b1.x, b1.y, h[kb][5], l[kb][5]);
+          split_bf16x2(b0.z, b0.w, h[kb][6], l[kb][6]);
+          split_bf16x2(b1.z, b1.w, h[kb][7], l[kb][7]);
+        }
       }
-    }
+    };
+    if (!DB) build();
     if (!landed) {  // every thread sees the weight copy land before it reads the tile
       if (!mbar_wait(&wbar, 0, kWaitPolls)) {
         atomicOr(&g_fault_flags, kFaultBulkTimeout);
@@ -763,9 +812,16 @@ lora_expand_st_kernel(const float* __restrict__ inter, int R, const uint16_t* __
       landed = true;
     }
     if (ahead)
-      cp_async_wait_group<1>();  // this tile's output pieces; the next tile's stay in flight
+      cp_async_wait_group<1>();  // this tile's pieces; the next tile's output rows stay in flight
     else
-      cp_async_wait_all();  // this thread's output pieces
+      cp_async_wait_all();  // this thread's pieces
+    if constexpr (DB) {
+      build();
+      if (ahead) {  // the staged fragments are in registers: stage the next tile's
+        load_inter(n0, n1);
+        cp_async_commit();
+      }
+    }
 #pragma unroll
     for (int cg = 0; cg < kStGroups; ++cg) {
       const int nb = wcol + cg * 32;  // the group's first column inside the item

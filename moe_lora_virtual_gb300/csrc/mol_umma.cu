@@ -7,8 +7,9 @@
 // virtual experts with N = S*r and K = the input width; code-review commit,
 // weights laid out [E, N, K]. This kernel computes, per routed block t of
 // virtual expert v and per 128 lora_a rows (mt; when R is not a multiple of
-// 128 the last tile reaches past R into the next expert's rows, or zeros past
-// the last expert: those rows are computed and not stored),
+// 128 the last tile holds the expert's last 64 rows only: a 64-row weight box
+// fills the first half of the stage's weight tile, the MMA's other 64 rows
+// read whatever the stage held before and are computed but not stored),
 //   D[j, n] = sum_k lora_a[v, mt*128 + j, k] * x[row(n), k]     (j < 128, n < BM)
 // as tcgen05.mma M=128 x N=BM x K=16 steps (bf16 in, fp32 in tensor memory),
 // and writes inter[pair(n), mt*128 + j] = D[j, n] for the block's real rows.
@@ -151,6 +152,7 @@ struct IDesc {
 template <int BN>
 __global__ void __launch_bounds__(tc::kThreads, tc::Geo<BN>::kBlocksPerSM)
 lora_shrink_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                      const __grid_constant__ CUtensorMap tmap_h,
                       const uint16_t* __restrict__ x, int64_t x_stride, int x_div, int K, int R,
                       const int* __restrict__ sorted_ids, const int* __restrict__ expert_ids,
                       const int* __restrict__ ntpp_ptr, int64_t numel, int num_vexperts,
@@ -207,14 +209,15 @@ lora_shrink_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
         int mt, v;
         if (!item(it, t, mt, v)) continue;
         const int y = v * R + mt * kM;
+        const bool half = R - mt * kM < kM;  // the expert's last 64 rows: the 64-row box
         for (int ks = 0; ks < nk; ++ks, ++q) {
           const int s = (int)(q % kStages);
           if (!mbar_wait(&empty[s], ((q / kStages) & 1) ^ 1, kPolls)) {
             fault = true;
             break;
           }
-          mbar_arrive_expect_tx(&full[s], (uint32_t)kATile);
-          tma_load_2d(stageA(q), &tmap_a, ks * kKStep, y, &full[s]);
+          mbar_arrive_expect_tx(&full[s], (uint32_t)(half ? kATile / 2 : kATile));
+          tma_load_2d(stageA(q), half ? &tmap_h : &tmap_a, ks * kKStep, y, &full[s]);
         }
       }
     }
@@ -404,19 +407,26 @@ cudaError_t launch_shrink_tc(const void* x, int64_t x_stride, int x_div, int K, 
                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  // the same tensor with a 64-row box, for the last tile when R % 128 == 64
+  CUtensorMap map_h;
+  const cuuint32_t box_h[2] = {(cuuint32_t)tc::kKStep, (cuuint32_t)(tc::kM / 2)};
+  cr = g_encode(&map_h, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(lora_a), dims,
+                strides, box_h, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
   const int mtiles = (R + tc::kM - 1) / tc::kM;
   const int64_t n_items = nblk * mtiles;
   const uint16_t* xp = static_cast<const uint16_t*>(x);
   if (block_m == 64) {
     const dim3 grid((unsigned)std::min<int64_t>(n_items, (int64_t)tc_device_sms() * 2));
     return launch_pdl(lora_shrink_tc_kernel<64>, grid, dim3(tc::kThreads), tc::Geo<64>::kSmem,
-                      stream, map, xp, x_stride, x_div, K, R, sorted_ids, expert_ids, ntpp, numel,
-                      num_vexperts, inter, n_items, mtiles);
+                      stream, map, map_h, xp, x_stride, x_div, K, R, sorted_ids, expert_ids, ntpp,
+                      numel, num_vexperts, inter, n_items, mtiles);
   }
   const dim3 grid((unsigned)std::min<int64_t>(n_items, (int64_t)tc_device_sms()));
   return launch_pdl(lora_shrink_tc_kernel<128>, grid, dim3(tc::kThreads), tc::Geo<128>::kSmem,
-                    stream, map, xp, x_stride, x_div, K, R, sorted_ids, expert_ids, ntpp, numel,
-                    num_vexperts, inter, n_items, mtiles);
+                    stream, map, map_h, xp, x_stride, x_div, K, R, sorted_ids, expert_ids, ntpp,
+                    numel, num_vexperts, inter, n_items, mtiles);
 }
 
 }  // namespace mol
