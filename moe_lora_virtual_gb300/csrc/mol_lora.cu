@@ -708,9 +708,11 @@ lora_expand_st_kernel(const float* __restrict__ inter, int R, const uint16_t* __
       }
     }
   };
-  // DB: this thread's intermediate fragments of rows r0 and r1 (columns of its
-  // quad in every k block), staged at ism[(8 * hh + g) * RK + column] and read
-  // back by this thread only, into registers, before it stages the next tile's
+  // DB: the intermediate fragments of rows r0 and r1 (columns of the quad in
+  // every k block), staged at ism[(8 * hh + g) * RK + column]; the four warps
+  // copy the same values to the same places, each thread reads back what it
+  // copied, and a block barrier separates every warp's reads of one tile from
+  // the copies of the next
   auto ism_at = [&](int hh, int j) { return ism + (8 * hh + g) * RK + j; };
   auto load_inter = [&](int r0, int r1) {
 #pragma unroll
@@ -804,7 +806,10 @@ lora_expand_st_kernel(const float* __restrict__ inter, int R, const uint16_t* __
     };
     if (!DB) build();
     if (!landed) {  // every thread sees the weight copy land before it reads the tile
-      if (!mbar_wait(&wbar, 0, kWaitPolls)) {
+      bool ok = mbar_wait(&wbar, 0, kWaitPolls);
+      // two staged tiles: a barrier follows, so the block leaves together or not at all
+      if constexpr (DB) ok = __syncthreads_and(ok ? 1 : 0) != 0;
+      if (!ok) {
         atomicOr(&g_fault_flags, kFaultBulkTimeout);
         cp_async_wait_all();
         return;
@@ -817,7 +822,8 @@ lora_expand_st_kernel(const float* __restrict__ inter, int R, const uint16_t* __
       cp_async_wait_all();  // this thread's pieces
     if constexpr (DB) {
       build();
-      if (ahead) {  // the staged fragments are in registers: stage the next tile's
+      if (ahead) {  // every warp has this tile's fragments in registers: stage the next tile's
+        named_sync(1, kExpandThreads);
         load_inter(n0, n1);
         cp_async_commit();
       }
