@@ -96,20 +96,14 @@ struct Raw {
 namespace sp {
 constexpr int kConsumers = 4;                    // consumer warps
 constexpr int kThreads = (kConsumers + 1) * 32;  // + the producer warp
+constexpr int kJT = 8;                           // weight rows per item (one 8-column mma tile)
 constexpr int kXR = 16;                          // activation rows per job (one 16-row mma tile)
+constexpr int kStageBytes = 52 * 1024;
+constexpr int kStages = 2;
 constexpr int kBlocksPerSM = 2;                  // two issuing producers per SM
+constexpr int kMeta = kStages + 2;               // jobs whose rows a consumer may still read
 constexpr int kHeader = 1024;                    // barriers, stage headers, job meta
-// Geometry per weight rows per item (JT): 8 rows (one n8 mma tile) in two
-// 52 KB stages, or 4 rows (half of it) in four 26 KB stages -- the same bytes in
-// flight in items half as large, for calls with few rows per virtual expert,
-// whose last round of items then leaves fewer blocks idle.
-template <int JT>
-struct Geo {
-  static constexpr int kStages = JT == 8 ? 2 : 4;
-  static constexpr int kStageBytes = (JT == 8 ? 52 : 26) * 1024;
-  static constexpr int kMeta = kStages + 2;  // jobs whose rows a consumer may still read
-  static constexpr size_t kSmem = kHeader + (size_t)kStages * kStageBytes;
-};
+constexpr size_t kSmem = kHeader + (size_t)kStages * kStageBytes;
 struct Job {
   int v, jt, cm, ncols;  // ncols: leading columns of the item inside the adapter's rank
   int rows[kXR];
@@ -120,17 +114,13 @@ struct StageHdr {
   int len;    // k values in the chunk
   int pitch;  // bytes between rows in the stage
 };
-static_assert(2 * Geo<4>::kStages * 8 + Geo<4>::kStages * (int)sizeof(StageHdr) +
-                      Geo<4>::kMeta * (int)sizeof(Job) <= kHeader,
+static_assert(2 * kStages * 8 + kStages * (int)sizeof(StageHdr) + kMeta * (int)sizeof(Job) <= kHeader,
               "header");
 
-// k chunk of a job with JT weight rows and cm activation rows: all of K with
-// unpadded rows when that fits a stage, else equal chunks (multiples of 64) of
-// padded rows.
-template <int JT>
+// k chunk of a job with cm activation rows: all of K with unpadded rows when
+// that fits a stage, else equal chunks (multiples of 64) of padded rows.
 MOL_DEV void job_chunk(int K, int cm, int& len, int& pitch) {
-  constexpr int kStageBytes = Geo<JT>::kStageBytes;
-  const int rows = JT + cm;
+  const int rows = kJT + cm;
   if (rows * K * 2 <= kStageBytes) {
     len = K;
     pitch = K * 2;
@@ -143,7 +133,7 @@ MOL_DEV void job_chunk(int K, int cm, int& len, int& pitch) {
 }
 }  // namespace sp
 
-template <bool RANKS, int JT>
+template <bool RANKS>
 __global__ void __launch_bounds__(sp::kThreads, sp::kBlocksPerSM)
 lora_shrink_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, int K,
                    const uint16_t* __restrict__ lora_a, int R, const int* __restrict__ sorted_ids,
@@ -152,10 +142,6 @@ lora_shrink_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, 
                    int n_jt, int64_t n_items, int early, int r1,
                    const int* __restrict__ lora_ranks, int num_experts, int num_loras) {
   using namespace sp;
-  constexpr int kStages = Geo<JT>::kStages;
-  constexpr int kStageBytes = Geo<JT>::kStageBytes;
-  constexpr int kMeta = Geo<JT>::kMeta;
-  constexpr int kJT = JT;
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + kStages;
@@ -260,9 +246,8 @@ lora_shrink_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, 
           waited = true;
         }
         const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-        constexpr int n4 = kJT / 4;  // float4 pieces of an item's columns per row
-        for (int q2 = lane; q2 < n4 * c; q2 += 32)
-          *reinterpret_cast<float4*>(inter + (int64_t)prow[q2 / n4] * R + jt * kJT + 4 * (q2 % n4)) = z;
+        for (int q2 = lane; q2 < 2 * c; q2 += 32)
+          *reinterpret_cast<float4*>(inter + (int64_t)prow[q2 >> 1] * R + jt * kJT + 4 * (q2 & 1)) = z;
         __syncwarp();
         continue;
       }
@@ -270,7 +255,7 @@ lora_shrink_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, 
       for (int m0 = 0; m0 < c && !fault; m0 += kXR) {
         const int cm = min(kXR, c - m0);
         int len, pitch;
-        job_chunk<JT>(K, cm, len, pitch);
+        job_chunk(K, cm, len, pitch);
         const bool whole = (len == K && pitch == K * 2);
         const int slot = (int)(jn % kMeta);
         Job& jb = meta[slot];
@@ -377,8 +362,7 @@ lora_shrink_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, 
         const bool kin = kb + h < kb1 && kk < len;
         const uint4 xa = (kin && g < cm) ? lds16(X + g * pitch + kk * 2) : zero;
         const uint4 xb = (kin && g + 8 < cm) ? lds16(X + (g + 8) * pitch + kk * 2) : zero;
-        // rows past the item's JT weight rows (4-row items) feed columns that are not stored
-        const uint4 a = (kin && g < kJT) ? lds16(W + g * pitch + kk * 2) : zero;
+        const uint4 a = kin ? lds16(W + g * pitch + kk * 2) : zero;
         // k step 0 <- elements 8t..8t+3, k step 1 <- 8t+4..8t+7 (same map in both operands)
         if (h == 0) {
           mma_16816(acc, xa.x, xb.x, xa.y, xb.y, a.x, a.y);
@@ -407,10 +391,10 @@ lora_shrink_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, 
         const int col = jb.jt * kJT + 2 * tq;
         // columns past the adapter's rank are zero padding: written as 0
         const bool k0v = !RANKS || 2 * tq < jb.ncols, k1v = !RANKS || 2 * tq + 1 < jb.ncols;
-        if (2 * tq < kJT && g < cm)
+        if (g < cm)
           *reinterpret_cast<float2*>(inter + (int64_t)jb.rows[g] * R + col) =
               make_float2(k0v ? acc[0] : 0.f, k1v ? acc[1] : 0.f);
-        if (2 * tq < kJT && g + 8 < cm)
+        if (g + 8 < cm)
           *reinterpret_cast<float2*>(inter + (int64_t)jb.rows[g + 8] * R + col) =
               make_float2(k0v ? acc[2] : 0.f, k1v ? acc[3] : 0.f);
       }
@@ -939,13 +923,11 @@ cudaError_t prepare_lora_kernels() {
   if (e != cudaSuccess) return e;
   e = prepare_expand_st<8, false>();
   if (e != cudaSuccess) return e;
-  for (auto k : {lora_shrink_kernel<false, 8>, lora_shrink_kernel<true, 8>})
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sp::Geo<8>::kSmem);
-  for (auto k : {lora_shrink_kernel<false, 4>, lora_shrink_kernel<true, 4>})
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sp::Geo<4>::kSmem);
-  return e;
+  e = cudaFuncSetAttribute(lora_shrink_kernel<false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sp::kSmem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(lora_shrink_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)sp::kSmem);
 }
 
 cudaError_t launch_shrink(const void* x, int64_t x_stride, int x_div, int K, const void* lora_a,
@@ -958,23 +940,16 @@ cudaError_t launch_shrink(const void* x, int64_t x_stride, int x_div, int K, con
   if (!lora_ranks && shrink_tc_fits(numel, num_vexperts, R, K, block_m))
     return launch_shrink_tc(x, x_stride, x_div, K, lora_a, R, sorted_ids, expert_ids, ntpp,
                             capacity, block_m, numel, num_vexperts, inter, stream);
-  // few rows per virtual expert (decode): 4-row items, so that the last round of
-  // items leaves fewer blocks idle; else 8-row items
-  const bool small = numel < 4 * std::min<int64_t>(numel, num_vexperts);
-  const int jt_rows = small ? 4 : 8;
-  const int n_jt = R / jt_rows;
+  const int n_jt = R / sp::kJT;
   const int num_loras = lora_ranks ? num_vexperts / num_experts : 0;
   const int64_t n_items = nblk * n_jt;
   const dim3 grid((unsigned)std::min<int64_t>(n_items, (int64_t)device_sms() * sp::kBlocksPerSM));
-#define MOL_SHRINK(RK_, JT_)                                                                      \
-  launch_pdl(lora_shrink_kernel<RK_, JT_>, grid, dim3(sp::kThreads), sp::Geo<JT_>::kSmem, stream,   \
-             static_cast<const uint16_t*>(x), x_stride, x_div, K,                                  \
-             static_cast<const uint16_t*>(lora_a), R, sorted_ids, expert_ids, ntpp, block_m, numel,  \
-             num_vexperts, inter, n_jt, n_items, early ? 1 : 0, r1, lora_ranks,                     \
-             num_experts < 1 ? 1 : num_experts, num_loras)
-  if (small) return lora_ranks ? MOL_SHRINK(true, 4) : MOL_SHRINK(false, 4);
-  return lora_ranks ? MOL_SHRINK(true, 8) : MOL_SHRINK(false, 8);
-#undef MOL_SHRINK
+  return launch_pdl(lora_ranks ? lora_shrink_kernel<true> : lora_shrink_kernel<false>, grid,
+                    dim3(sp::kThreads), sp::kSmem, stream,
+                    static_cast<const uint16_t*>(x), x_stride, x_div, K,
+                    static_cast<const uint16_t*>(lora_a), R, sorted_ids, expert_ids, ntpp, block_m,
+                    numel, num_vexperts, inter, n_jt, n_items, early ? 1 : 0, r1, lora_ranks,
+                    num_experts < 1 ? 1 : num_experts, num_loras);
 }
 
 template <int RK, bool EARLY>

@@ -54,8 +54,8 @@ constexpr int kConsumers = 4;
 constexpr int kThreads = (kConsumers + 1) * 32;
 constexpr int kJT = 8;                 // lora_a rows per shrink job (one n8 mma tile)
 constexpr int kMR = 16;                // pair rows per row tile (one m16 mma tile)
-// The 8-row item shrink's stage size: jobs are cut along k as there, so the
-// two give bit-identical intermediates on the same rows.
+// The shrink's stage size: jobs are cut along k exactly as in the separate
+// shrink, so both give bit-identical intermediates.
 constexpr int kStageBytes = 52 * 1024;
 constexpr int kStages = 2;
 constexpr int kHeader = 1024;          // barriers and stage headers
