@@ -637,7 +637,7 @@ def run_e2e(args, torch, mol, wl, layers, pairs_per_step, world, dev):
         main.wait_stream(s_out)
 
     graph = capture(torch, all_steps)
-    replays = max(1, min(args.steps, 5000) // n_steps)
+    replays = max(4, min(args.steps, 5000) // n_steps)
     ms = time_graphs(torch, [graph], replays, max(1, min(args.warmup, 50) // n_steps)) / n_steps
     steps = replays * n_steps
     # one step at a time (copy in, layer, copy out in order), graph per layer, for reference
@@ -675,6 +675,11 @@ E2E_ROUNDS = 4
 # (workload, kernel). An entry whose digest differs from the current sources is stale and
 # reported as null. Sources: the ncu summaries under profiles/.
 TRAFFIC = {
+    ("decode", "shrink_gate_up"): (35507456 + 1792, 35506176, "mol_lora.cu", "ffe4c30e860832a2"),
+    ("wide", "expand_down"): (41633280 + 29440, 43469824, "mol_lora.cu", "ffe4c30e860832a2"),
+    ("wide1k", "expand_down"): (172935680 + 7954176, 184738816, "mol_lora.cu", "ffe4c30e860832a2"),
+    ("ep", "shrink_gate_up"): (569548032 + 6291968, 572089984, "mol_lora.cu", "ffe4c30e860832a2"),
+    ("dense", "expand_down"): (344122880 + 215101952, 612368384, "mol_lora.cu", "ffe4c30e860832a2"),
 }
 
 
