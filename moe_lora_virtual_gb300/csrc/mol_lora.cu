@@ -98,19 +98,12 @@ constexpr int kConsumers = 4;                    // consumer warps
 constexpr int kThreads = (kConsumers + 1) * 32;  // + the producer warp
 constexpr int kJT = 8;                           // weight rows per item (one 8-column mma tile)
 constexpr int kXR = 16;                          // activation rows per job (one 16-row mma tile)
-constexpr int kRingBytes = 104 * 1024;           // the stages of one block
+constexpr int kStageBytes = 52 * 1024;
+constexpr int kStages = 2;
 constexpr int kBlocksPerSM = 2;                  // two issuing producers per SM
+constexpr int kMeta = kStages + 2;               // jobs whose rows a consumer may still read
 constexpr int kHeader = 1024;                    // barriers, stage headers, job meta
-// The ring as NS stages: two of 52 KB, or three of 34.7 KB for calls whose
-// jobs are cut along k anyway (many activation rows per routed block): three
-// such chunks in flight instead of two, in the same shared memory.
-template <int NS>
-struct Geo {
-  static constexpr int kStages = NS;
-  static constexpr int kStageBytes = kRingBytes / NS / 16 * 16;
-  static constexpr int kMeta = NS + 2;  // jobs whose rows a consumer may still read
-  static constexpr size_t kSmem = kHeader + (size_t)NS * kStageBytes;
-};
+constexpr size_t kSmem = kHeader + (size_t)kStages * kStageBytes;
 struct Job {
   int v, jt, cm, ncols;  // ncols: leading columns of the item inside the adapter's rank
   int rows[kXR];
@@ -121,14 +114,12 @@ struct StageHdr {
   int len;    // k values in the chunk
   int pitch;  // bytes between rows in the stage
 };
-static_assert(2 * 3 * 8 + 3 * (int)sizeof(StageHdr) + Geo<3>::kMeta * (int)sizeof(Job) <= kHeader,
+static_assert(2 * kStages * 8 + kStages * (int)sizeof(StageHdr) + kMeta * (int)sizeof(Job) <= kHeader,
               "header");
 
 // k chunk of a job with cm activation rows: all of K with unpadded rows when
 // that fits a stage, else equal chunks (multiples of 64) of padded rows.
-template <int NS>
 MOL_DEV void job_chunk(int K, int cm, int& len, int& pitch) {
-  constexpr int kStageBytes = Geo<NS>::kStageBytes;
   const int rows = kJT + cm;
   if (rows * K * 2 <= kStageBytes) {
     len = K;
@@ -142,7 +133,7 @@ MOL_DEV void job_chunk(int K, int cm, int& len, int& pitch) {
 }
 }  // namespace sp
 
-template <bool RANKS, int NS>
+template <bool RANKS>
 __global__ void __launch_bounds__(sp::kThreads, sp::kBlocksPerSM)
 lora_shrink_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, int K,
                    const uint16_t* __restrict__ lora_a, int R, const int* __restrict__ sorted_ids,
@@ -151,9 +142,6 @@ lora_shrink_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, 
                    int n_jt, int64_t n_items, int early, int r1,
                    const int* __restrict__ lora_ranks, int num_experts, int num_loras) {
   using namespace sp;
-  constexpr int kStages = Geo<NS>::kStages;
-  constexpr int kStageBytes = Geo<NS>::kStageBytes;
-  constexpr int kMeta = Geo<NS>::kMeta;
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + kStages;
@@ -267,7 +255,7 @@ lora_shrink_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, 
       for (int m0 = 0; m0 < c && !fault; m0 += kXR) {
         const int cm = min(kXR, c - m0);
         int len, pitch;
-        job_chunk<NS>(K, cm, len, pitch);
+        job_chunk(K, cm, len, pitch);
         const bool whole = (len == K && pitch == K * 2);
         const int slot = (int)(jn % kMeta);
         Job& jb = meta[slot];
@@ -935,13 +923,11 @@ cudaError_t prepare_lora_kernels() {
   if (e != cudaSuccess) return e;
   e = prepare_expand_st<8, false>();
   if (e != cudaSuccess) return e;
-  for (auto k : {lora_shrink_kernel<false, 2>, lora_shrink_kernel<true, 2>})
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sp::Geo<2>::kSmem);
-  for (auto k : {lora_shrink_kernel<false, 3>, lora_shrink_kernel<true, 3>})
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sp::Geo<3>::kSmem);
-  return e;
+  e = cudaFuncSetAttribute(lora_shrink_kernel<false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sp::kSmem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(lora_shrink_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)sp::kSmem);
 }
 
 cudaError_t launch_shrink(const void* x, int64_t x_stride, int x_div, int K, const void* lora_a,
@@ -958,20 +944,12 @@ cudaError_t launch_shrink(const void* x, int64_t x_stride, int x_div, int K, con
   const int num_loras = lora_ranks ? num_vexperts / num_experts : 0;
   const int64_t n_items = nblk * n_jt;
   const dim3 grid((unsigned)std::min<int64_t>(n_items, (int64_t)device_sms() * sp::kBlocksPerSM));
-  // many activation rows per routed block (on average at least four pairs per
-  // virtual expert) and K <= 2048: a job (8 lora_a rows + its rows) is cut
-  // along k in the two-stage ring as well, so three smaller stages hold the
-  // same chunks with one more in flight
-  const bool three = K <= 2048 && numel >= 4 * std::min<int64_t>(numel, num_vexperts);
-#define MOL_SHRINK(RK_, NS_)                                                                      \
-  launch_pdl(lora_shrink_kernel<RK_, NS_>, grid, dim3(sp::kThreads), sp::Geo<NS_>::kSmem, stream,   \
-             static_cast<const uint16_t*>(x), x_stride, x_div, K,                                  \
-             static_cast<const uint16_t*>(lora_a), R, sorted_ids, expert_ids, ntpp, block_m, numel,  \
-             num_vexperts, inter, n_jt, n_items, early ? 1 : 0, r1, lora_ranks,                     \
-             num_experts < 1 ? 1 : num_experts, num_loras)
-  if (three) return lora_ranks ? MOL_SHRINK(true, 3) : MOL_SHRINK(false, 3);
-  return lora_ranks ? MOL_SHRINK(true, 2) : MOL_SHRINK(false, 2);
-#undef MOL_SHRINK
+  return launch_pdl(lora_ranks ? lora_shrink_kernel<true> : lora_shrink_kernel<false>, grid,
+                    dim3(sp::kThreads), sp::kSmem, stream,
+                    static_cast<const uint16_t*>(x), x_stride, x_div, K,
+                    static_cast<const uint16_t*>(lora_a), R, sorted_ids, expert_ids, ntpp, block_m,
+                    numel, num_vexperts, inter, n_jt, n_items, early ? 1 : 0, r1, lora_ranks,
+                    num_experts < 1 ? 1 : num_experts, num_loras);
 }
 
 template <int RK, bool EARLY>
