@@ -26,7 +26,9 @@
  * - Arguments are validated on the host before anything is enqueued. On an
  *   error status nothing is launched and no output is touched.
  * - Bad device *data* never faults: ids outside [0, V) go to the sentinel
- *   bucket; sorted_token_ids entries outside [0, numel) are skipped.
+ *   bucket; sorted_token_ids entries outside [0, numel) are skipped, and so
+ *   are blocks whose expert id is outside [0, V) (the checked build below
+ *   records such entries).
  * - Return value: MOL_OK (0) or a negative MOL_ERR_* status;
  *   mol_status_string() names it, mol_last_cuda_error() gives the cudaError_t
  *   behind MOL_ERR_CUDA (per host thread).
@@ -322,6 +324,55 @@ int32_t mol_take_fault_flags(uint32_t* flags);
  * thread uses the library. Returns MOL_ERR_INVALID_ARG for stall_producer > 1.
  */
 int32_t mol_debug_wait_test(uint32_t stall_producer, uint64_t wait_limit_ns);
+
+/*
+ * Checked build (no counterpart on the pages). The same sources compiled with
+ * MOL_CHECKED (libmol_checked.so, built beside libmol.so) test the index
+ * arithmetic of every kernel on the device: before a guarded access a kernel
+ * checks the index against its buffer; a failed check records its site and
+ * the offending value and the access is skipped (no trap, no fault; a kernel
+ * whose pipeline a skip would stall ends its work early instead, so outputs
+ * after a failed check are undefined). Routing data passed in by the caller
+ * is checked the same way: entries that the release build silently skips
+ * (see the conventions above) are recorded as well. The release build
+ * compiles every check out.
+ *
+ * Sites (the value recorded with each):
+ */
+#define MOL_CHECK_ROUTE_EXPERT 1  /* a block below num_tokens_post_padded has an expert id
+                                     outside [-1, V); value: the block */
+#define MOL_CHECK_ROUTE_PAIR 2    /* a sorted_token_ids entry of such a block is outside
+                                     [0, numel]; value: the slot */
+#define MOL_CHECK_ROUTE_NTPP 3    /* num_tokens_post_padded is negative, above capacity or not a
+                                     multiple of block_m; value: num_tokens_post_padded */
+#define MOL_CHECK_ALIGN_SLOT 4    /* the align writes a slot outside [0, capacity); value: slot */
+#define MOL_CHECK_ALIGN_BLOCK 5   /* the align writes expert_ids outside [0, capacity / block_m);
+                                     value: the index */
+#define MOL_CHECK_ALIGN_TOTAL 6   /* the align's padded total exceeds capacity; value: total */
+#define MOL_CHECK_ALIGN_WORKSPACE 7 /* a workspace index past the tile histograms or ranks;
+                                       value: the index */
+#define MOL_CHECK_ROW 8           /* a pair row of x, inter or out outside the tensor (x:
+                                     numel / x_row_div rows); value: the row */
+#define MOL_CHECK_COLUMN 9        /* a column range of inter or out outside its row; value: the
+                                     first column */
+#define MOL_CHECK_SMEM 10         /* a copy into or a read of shared memory past its region;
+                                     value: the byte offset of its end */
+#define MOL_CHECK_TMA_COORD 11    /* a tensor copy whose inner coordinate is not a multiple of 16
+                                     bytes or lies outside the tensor; value: the coordinate */
+#define MOL_CHECK_WEIGHT_ROW 12   /* a lora_a / lora_b row outside [0, V * rows per expert);
+                                     value: the row */
+
+/* 1 for the checked build, 0 for the release build. */
+int32_t mol_checked_build(void);
+
+/*
+ * Reads and clears the check record of the current device: *count = failed
+ * checks since the last call (0 in the release build), *first = (site << 48)
+ * | (value & 0xFFFFFFFFFFFF) of the first one recorded by the earliest kernel
+ * file in the path's order (align, shrink/expand, tcgen05 shrink, fused
+ * stage), 0 if none. Synchronizes the device. Either pointer may be NULL.
+ */
+int32_t mol_take_check_record(uint64_t* first, uint64_t* count);
 
 #ifdef __cplusplus
 }

@@ -9,13 +9,14 @@ is missing, the first call raises.
 
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 from typing import NamedTuple, Optional
 
 import torch
 
-from .build import LIB_PATH
+from .build import CHECKED_LIB_PATH, LIB_PATH
 
 MOL_OK = 0
 MOL_ERR_INVALID_ARG = -1
@@ -29,8 +30,16 @@ EXPORTS = (
     "mol_version", "mol_status_string", "mol_last_cuda_error", "mol_align_capacity",
     "mol_workspace_bytes", "mol_virtual_topk", "mol_align_block_size", "mol_lora_shrink",
     "mol_lora_expand", "mol_lora_forward", "mol_align_block_size_noalloc", "mol_token_lora_ids",
-    "mol_take_fault_flags", "mol_debug_wait_test", "mol_launch_count",
+    "mol_take_fault_flags", "mol_debug_wait_test", "mol_launch_count", "mol_checked_build",
+    "mol_take_check_record",
 )
+
+# Check sites of the checked build (include/mol.h, MOL_CHECK_*).
+CHECK_SITES = {
+    1: "ROUTE_EXPERT", 2: "ROUTE_PAIR", 3: "ROUTE_NTPP", 4: "ALIGN_SLOT", 5: "ALIGN_BLOCK",
+    6: "ALIGN_TOTAL", 7: "ALIGN_WORKSPACE", 8: "ROW", 9: "COLUMN", 10: "SMEM", 11: "TMA_COORD",
+    12: "WEIGHT_ROW",
+}
 
 _lib = None
 _P = ctypes.c_void_p
@@ -59,6 +68,8 @@ _SIGS = {
     "mol_token_lora_ids": (_I32, [_P, _P, _I32, _I64, _I32, _P, _P, _P]),
     "mol_take_fault_flags": (_I32, [ctypes.POINTER(ctypes.c_uint32)]),
     "mol_debug_wait_test": (_I32, [ctypes.c_uint32, ctypes.c_uint64]),
+    "mol_checked_build": (_I32, []),
+    "mol_take_check_record": (_I32, [ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(ctypes.c_uint64)]),
 }
 
 
@@ -72,11 +83,11 @@ class MolError(RuntimeError):
         self.cuda_error = cuda
 
 
-def library(path: Optional[str] = None) -> ctypes.CDLL:
-    """Load libmol.so once and declare every export's signature."""
-    global _lib
-    if _lib is None:
-        p = path or LIB_PATH
+_loaded = {}
+
+
+def _load(p: str) -> ctypes.CDLL:
+    if p not in _loaded:
         if not os.path.exists(p):
             raise RuntimeError(f"MoL CUDA library not built ({p} missing): run "
                                "moe_lora_virtual_gb300.build.build_library() first")
@@ -85,8 +96,31 @@ def library(path: Optional[str] = None) -> ctypes.CDLL:
             fn = getattr(lib, name)
             fn.restype = res
             fn.argtypes = args
-        _lib = lib
+        _loaded[p] = lib
+    return _loaded[p]
+
+
+def library(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load libmol.so once and declare every export's signature."""
+    global _lib
+    if _lib is None:
+        _lib = _load(path or LIB_PATH)
     return _lib
+
+
+@contextlib.contextmanager
+def use_library(path: str):
+    """Route every call of this module through the library at `path` (for instance the
+    checked build, CHECKED_LIB_PATH) inside the block; the previous one is restored after.
+    Both libraries keep their own device state; do not mix their routing buffers' users
+    across a stream without a synchronisation."""
+    global _lib
+    prev = _lib
+    _lib = _load(path)
+    try:
+        yield _lib
+    finally:
+        _lib = prev
 
 
 def _check(fn: str, status: int) -> None:
@@ -305,7 +339,6 @@ def mol_take_fault_flags() -> int:
     return int(v.value)
 
 
-
 def mol_debug_wait_test(stall_producer: bool, wait_limit_ns: int = 0) -> None:
     """Test hook of the bounded waits: with stall_producer the shrink's producer warps issue
     nothing, so its consumers' waits run out (after wait_limit_ns; 0 = one second) and record
@@ -317,3 +350,35 @@ def mol_debug_wait_test(stall_producer: bool, wait_limit_ns: int = 0) -> None:
 def mol_launch_count() -> int:
     """Kernels the library has enqueued in this process so far."""
     return int(library().mol_launch_count())
+
+
+def mol_checked_build() -> bool:
+    """True when the loaded library is the checked build."""
+    return bool(library().mol_checked_build())
+
+
+class CheckRecord(NamedTuple):
+    count: int   # failed checks since the last read (0 in the release build)
+    site: int    # MOL_CHECK_* of the first one recorded, 0 if none
+    value: int   # the index or value it recorded
+
+    @property
+    def site_name(self) -> str:
+        return CHECK_SITES.get(self.site, "none" if self.site == 0 else f"site {self.site}")
+
+
+def mol_take_check_record() -> CheckRecord:
+    """Reads and clears the checked build's record of failed device-side checks;
+    synchronizes the device."""
+    first, count = ctypes.c_uint64(0), ctypes.c_uint64(0)
+    _check("mol_take_check_record",
+           library().mol_take_check_record(ctypes.byref(first), ctypes.byref(count)))
+    return decode_check_record(int(first.value), int(count.value))
+
+
+def decode_check_record(first: int, count: int) -> CheckRecord:
+    """(site << 48) | (value & 0xFFFFFFFFFFFF), with the value sign-extended from 48 bits."""
+    value = first & 0xFFFFFFFFFFFF
+    if value >= 1 << 47:
+        value -= 1 << 48
+    return CheckRecord(count, first >> 48, value)

@@ -190,6 +190,36 @@ int32_t mol_debug_wait_test(uint32_t stall_producer, uint64_t wait_limit_ns) {
   return e == cudaSuccess ? MOL_OK : cuda_fail(e);
 }
 
+int32_t mol_checked_build(void) {
+#ifdef MOL_CHECKED
+  return 1;
+#else
+  return 0;
+#endif
+}
+
+int32_t mol_take_check_record(uint64_t* first, uint64_t* count) {
+  int32_t st = ensure_device();
+  if (st != MOL_OK) return st;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e);
+  // in the path's order: align, item shrink and expands, tcgen05 shrink, fused stage
+  cudaError_t (*const take[4])(unsigned long long*, unsigned long long*) = {
+      mol::take_align_checks, mol::take_lora_checks, mol::take_tc_checks,
+      mol::take_stage_checks};
+  unsigned long long f = 0, n = 0;
+  for (auto fn : take) {
+    unsigned long long fi = 0, ni = 0;
+    e = fn(&fi, &ni);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (f == 0) f = fi;
+    n += ni;
+  }
+  if (first) *first = f;
+  if (count) *count = n;
+  return MOL_OK;
+}
+
 int32_t mol_token_lora_ids(const int32_t* weight_indices, const int32_t* seg_indptr,
                            int32_t num_reqs, int64_t num_tokens, int32_t max_loras,
                            const int32_t* lora_ranks, int32_t* lora_ids, void* stream) {

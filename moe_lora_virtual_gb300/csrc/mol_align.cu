@@ -149,7 +149,8 @@ MOL_DEV void bucket_offsets(int* counts, int nb, int num_vexperts, int block_m, 
     counts[b] = run;
     if (b < num_vexperts) {
       const int t0 = run >> lg;
-      for (int k = 0; k < (pb >> lg); ++k) expert_ids[t0 + k] = b;
+      for (int k = 0; k < (pb >> lg); ++k)
+        if (MOL_CHECK(t0 + k < (capacity >> lg), MOL_CHECK_ALIGN_BLOCK, t0 + k)) expert_ids[t0 + k] = b;
     }
     run += pb;
   }
@@ -157,7 +158,10 @@ MOL_DEV void bucket_offsets(int* counts, int nb, int num_vexperts, int block_m, 
   const int64_t nblk = capacity >> lg;
   for (int64_t t = (counts[num_vexperts] >> lg) + threadIdx.x; t < nblk; t += THREADS)
     expert_ids[t] = -1;
-  if (threadIdx.x == 0) *ntpp_out = total;
+  if (threadIdx.x == 0) {
+    MOL_CHECK(total <= capacity, MOL_CHECK_ALIGN_TOTAL, total);
+    *ntpp_out = total;
+  }
 }
 
 // Pass 1: the warp's bucket counts over its contiguous segment [s0, s1) of the
@@ -269,10 +273,11 @@ align_tile_kernel(const int* __restrict__ src, const int* __restrict__ lora_ids,
   // Column scan: warp tables become exclusive bases; the tile total per bucket
   // goes to shared memory (one tile) or to the workspace histogram.
   column_scan(tbl, nb, nb_pad, [&](int b, int n) {
+    const int64_t w = (int64_t)blockIdx.x * nb + b;
     if (fused)
       offs[b] = n;
-    else
-      ws_hist[(int64_t)blockIdx.x * nb + b] = n;
+    else if (MOL_CHECK(w < (int64_t)tiles * nb, MOL_CHECK_ALIGN_WORKSPACE, w))
+      ws_hist[w] = n;
   });
   __syncthreads();
   if (fused)
@@ -282,10 +287,12 @@ align_tile_kernel(const int* __restrict__ src, const int* __restrict__ lora_ids,
   // Pass 2: stable rank of every pair inside the tile.
   warp_rank(keys, s0, s1, mine, lane, [&](int q, int key, int lr) {
     const int64_t i = t0 + q;
-    if (fused)
-      sorted_ids[offs[key] + lr] = (int)i;
-    else
+    if (fused) {
+      const int64_t pos = (int64_t)offs[key] + lr;
+      if (MOL_CHECK(pos >= 0 && pos < capacity, MOL_CHECK_ALIGN_SLOT, pos)) sorted_ids[pos] = (int)i;
+    } else {
       ws_rank[i] = lr;
+    }
   });
 }
 
@@ -430,12 +437,17 @@ align_cluster_kernel(const int* __restrict__ src, const int* __restrict__ lora_i
     }
     if (b < num_vexperts) {
       const int nblk = ((r - o) + pad) >> lg;
-      for (int k = 0; k < nblk; ++k) expert_ids[(o >> lg) + k] = b;
+      for (int k = 0; k < nblk; ++k)
+        if (MOL_CHECK((o >> lg) + k < (capacity >> lg), MOL_CHECK_ALIGN_BLOCK, (o >> lg) + k))
+          expert_ids[(o >> lg) + k] = b;
     } else {
       s_sentinel = o;  // b == V: the last bucket
     }
   }
-  if (me == 0 && tid == 0) *ntpp_out = ntpp;
+  if (me == 0 && tid == 0) {
+    MOL_CHECK(ntpp <= capacity, MOL_CHECK_ALIGN_TOTAL, ntpp);
+    *ntpp_out = ntpp;
+  }
   __syncthreads();
   if (b0 < nb && b1 == nb) {  // the sentinel's blocks and every block past them carry -1
     for (int64_t t = (s_sentinel >> lg) + tid; t < (capacity >> lg); t += kAlignThreads)
@@ -443,8 +455,10 @@ align_cluster_kernel(const int* __restrict__ src, const int* __restrict__ lora_i
   }
   cluster_barrier();  // 3: cnt[b] is this tile's base in bucket b; the pad fill is done
 
-  warp_rank(keys, s0, s1, mine, lane,
-            [&](int q, int key, int lr) { sorted_ids[cnt[key] + lr] = (int)(t0 + q); });
+  warp_rank(keys, s0, s1, mine, lane, [&](int q, int key, int lr) {
+    const int64_t pos = (int64_t)cnt[key] + lr;
+    if (MOL_CHECK(pos >= 0 && pos < capacity, MOL_CHECK_ALIGN_SLOT, pos)) sorted_ids[pos] = (int)(t0 + q);
+  });
 }
 
 // Multi-tile: per-bucket prefix over tiles, bucket offsets, expert_ids, ntpp.
@@ -488,14 +502,15 @@ __global__ void align_scatter_kernel(const int* __restrict__ vtopk, int64_t nume
                                      int tile, const int* __restrict__ ws_hist,
                                      const int* __restrict__ ws_offs,
                                      const int* __restrict__ ws_rank, int* __restrict__ sorted_ids,
-                                     int trigger) {
+                                     int64_t capacity, int trigger) {
   pdl_wait();  // last writer of the routing: dependents start when it exits unless trigger
   if (trigger) pdl_launch_dependents();
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= numel) return;
   const int key = bucket_of(vtopk[i], num_vexperts);
   const int64_t p = i / tile;
-  sorted_ids[ws_offs[key] + ws_hist[p * (num_vexperts + 1) + key] + ws_rank[i]] = (int)i;
+  const int64_t pos = (int64_t)ws_offs[key] + ws_hist[p * (num_vexperts + 1) + key] + ws_rank[i];
+  if (MOL_CHECK(pos >= 0 && pos < capacity, MOL_CHECK_ALIGN_SLOT, pos)) sorted_ids[pos] = (int)i;
 }
 
 // ---------------------------------------------------------------------------
@@ -682,7 +697,16 @@ cudaError_t launch_align(const AlignPlan& plan, bool remap, const int32_t* src,
   const int64_t sblocks = (plan.numel + 255) / 256;
   const int32_t* vt = remap ? vtopk_out : src;
   return launch_pdl(align_scatter_kernel, dim3((unsigned)sblocks), dim3(256), 0, stream, vt,
-                    plan.numel, num_vexperts, plan.tile, ws_hist, ws_offs, ws_rank, sorted_ids, trig);
+                    plan.numel, num_vexperts, plan.tile, ws_hist, ws_offs, ws_rank, sorted_ids,
+                    plan.capacity, trig);
+}
+
+cudaError_t take_align_checks(unsigned long long* first, unsigned long long* count) {
+  CheckRecord r;
+  const cudaError_t e = take_check_record_here(&r);
+  *first = r.first;
+  *count = r.count;
+  return e;
 }
 
 }  // namespace mol

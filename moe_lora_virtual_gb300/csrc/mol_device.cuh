@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "mol.h"
+
 #define MOL_DEV __device__ __forceinline__
 
 namespace mol {
@@ -151,10 +153,73 @@ MOL_DEV void cp_async_wait_group() {
 // Error bits a kernel records instead of hanging or trapping.
 constexpr unsigned kFaultBulkTimeout = 1u;
 
+// Device-side index checks. Each translation unit owns one check record: the
+// first failed check's site and value, and the number of failed checks.
+// MOL_CHECK(cond, site, value) guards an access whose bounds hold by
+// construction: the release build compiles it to `true`; the checked build
+// (MOL_CHECKED) records a false `cond` and yields it, and the caller skips the
+// access. MOL_NOTE(cond, site, value) guards against caller data that every
+// build skips when `cond` is false: it yields `cond` in both builds and the
+// checked build also records it. `kChecked` lets a caller guard a skip that
+// only the checked build takes (`if (kChecked && !ok) return;`).
+struct CheckRecord {
+  unsigned long long first;  // (site << 48) | (value & 0xFFFFFFFFFFFF), 0 = none
+  unsigned long long count;
+};
+#ifdef MOL_CHECKED
+static __device__ CheckRecord g_check_record;
+__device__ __noinline__ static void check_record(unsigned site, long long value) {
+  const unsigned long long code =
+      ((unsigned long long)site << 48) | ((unsigned long long)value & 0xFFFFFFFFFFFFull);
+  atomicCAS(&g_check_record.first, 0ull, code);
+  atomicAdd(&g_check_record.count, 1ull);
+}
+MOL_DEV bool check_cond(bool cond, unsigned site, long long value) {
+  if (!cond) check_record(site, value);
+  return cond;
+}
+#define MOL_CHECK(cond, site, value) (::mol::check_cond((cond), (site), (long long)(value)))
+#define MOL_NOTE(cond, site, value) (::mol::check_cond((cond), (site), (long long)(value)))
+// Host: reads and clears this translation unit's record on the current device.
+static inline cudaError_t take_check_record_here(CheckRecord* out) {
+  cudaError_t e = cudaMemcpyFromSymbol(out, g_check_record, sizeof(CheckRecord));
+  if (e != cudaSuccess) return e;
+  const CheckRecord zero = {0ull, 0ull};
+  return cudaMemcpyToSymbol(g_check_record, &zero, sizeof(CheckRecord));
+}
+constexpr bool kChecked = true;
+#else
+constexpr bool kChecked = false;
+#define MOL_CHECK(cond, site, value) (true)
+#define MOL_NOTE(cond, site, value) (cond)
+static inline cudaError_t take_check_record_here(CheckRecord* out) {
+  out->first = 0ull;
+  out->count = 0ull;
+  return cudaSuccess;
+}
+#endif
+
 MOL_DEV unsigned lanemask_lt() {
   unsigned m;
   asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
   return m;
+}
+
+// Checked build: records the caller's routing words of routed block t that
+// every build skips (a bad num_tokens_post_padded, an expert id outside
+// [-1, V) below it, a slot outside [0, numel] of a block with an expert).
+// Every thread of one item of the block calls it with its slot (-1 past block_m).
+MOL_DEV void note_block_routing(int64_t t, int ntpp, int v, int slot, int block_m, int64_t numel,
+                                int num_vexperts, int64_t capacity) {
+  if (!kChecked) return;
+  const int tid = threadIdx.x;
+  const bool below = t * block_m < ntpp;
+  if (tid == 0) {
+    (void)MOL_NOTE(ntpp >= 0 && ntpp <= capacity && ntpp % block_m == 0, MOL_CHECK_ROUTE_NTPP, ntpp);
+    if (below) (void)MOL_NOTE(v >= -1 && v < num_vexperts, MOL_CHECK_ROUTE_EXPERT, t);
+  }
+  if (below && v >= 0 && v < num_vexperts && tid < block_m)
+    (void)MOL_NOTE(slot >= 0 && (int64_t)slot <= numel, MOL_CHECK_ROUTE_PAIR, t * block_m + tid);
 }
 
 // Compact the valid pair ids of one block into `rows`, keeping slot order.

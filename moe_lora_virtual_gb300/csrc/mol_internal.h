@@ -152,12 +152,17 @@ cudaError_t launch_stage(const void* x, int64_t x_stride, int x_div, int K, cons
                          int64_t out_stride, bool early, cudaStream_t stream);
 cudaError_t take_stage_faults(unsigned* out);
 
-
-
 // Fault words of the pipelined kernels (bit 0: a bounded barrier or copy wait
 // ran out); read and cleared by mol_take_fault_flags.
 cudaError_t take_lora_faults(unsigned* out);
 cudaError_t take_tc_faults(unsigned* out);
+// Check records of the checked build, per kernel file (read and cleared; zero
+// in the release build): the first failed check's (site << 48 | value) and the
+// number of failed checks.
+cudaError_t take_align_checks(unsigned long long* first, unsigned long long* count);
+cudaError_t take_lora_checks(unsigned long long* first, unsigned long long* count);
+cudaError_t take_tc_checks(unsigned long long* first, unsigned long long* count);
+cudaError_t take_stage_checks(unsigned long long* first, unsigned long long* count);
 // Test controls of the shrink's bounded waits (mol_debug_wait_test).
 cudaError_t set_wait_test(unsigned stall, unsigned long long limit_ns);
 

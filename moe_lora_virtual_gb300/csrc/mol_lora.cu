@@ -212,16 +212,34 @@ lora_shrink_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, 
       __syncwarp();
     }
     bool fault = false;
-    while (item < n_items && !fault) {
+    bool stop = false;  // checked build: a failed check ends the block's work
+    while (item < n_items && !fault && !stop) {
       const Raw cur_r = nxt;
       const int64_t cur = item;
       item += G;
       fetch(item, nxt);  // next item's routing is in flight while this one streams
-      const int v = (cur_r.t * block_m < cur_r.ntpp) ? cur_r.e : -1;
+      const int jt_c = (int)(cur % n_jt);
+      const bool below = cur_r.t * block_m < cur_r.ntpp;
+      if (kChecked && jt_c == 0 && lane == 0) {  // the caller's routing words, once per block
+        const int64_t cap = n_items / n_jt * block_m;
+        (void)MOL_NOTE(cur_r.ntpp >= 0 && cur_r.ntpp <= cap && cur_r.ntpp % block_m == 0,
+                       MOL_CHECK_ROUTE_NTPP, cur_r.ntpp);
+        if (below)
+          (void)MOL_NOTE(cur_r.e >= -1 && cur_r.e < num_vexperts, MOL_CHECK_ROUTE_EXPERT, cur_r.t);
+      }
+      const int v = below ? cur_r.e : -1;
       if (v < 0 || v >= num_vexperts) continue;
+      if (kChecked && jt_c == 0) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int idx = u * 32 + lane;
+          if (idx < block_m)
+            (void)MOL_NOTE(cur_r.sl[u] >= 0 && (int64_t)cur_r.sl[u] <= numel, MOL_CHECK_ROUTE_PAIR,
+                           cur_r.t * block_m + idx);
+        }
+      }
       // Columns of this item inside the adapter's rank: rank 0 writes nothing,
       // an item wholly past the rank writes zeros (its weights are padding).
-      const int jt_c = (int)(cur % n_jt);
       int in_rank = kJT;  // columns of the item below the rank (r1 % 8 == 0 with ranks)
       if constexpr (RANKS) {
         const int rl = (int)s_rank[v / num_experts];
@@ -252,11 +270,27 @@ lora_shrink_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, 
         continue;
       }
       const uint16_t* wrows = lora_a + ((int64_t)v * R + jt * kJT) * K;
+      if (kChecked) {
+        const int64_t wr = (int64_t)v * R + jt * kJT;
+        stop = !__all_sync(0xffffffffu, lane != 0 || MOL_CHECK(jt * kJT + kJT <= R && wr + kJT <=
+                                                                   (int64_t)num_vexperts * R,
+                                                               MOL_CHECK_WEIGHT_ROW, wr));
+        if (stop) break;
+      }
       for (int m0 = 0; m0 < c && !fault; m0 += kXR) {
         const int cm = min(kXR, c - m0);
         int len, pitch;
         job_chunk(K, cm, len, pitch);
         const bool whole = (len == K && pitch == K * 2);
+        if (kChecked) {  // the job's rows fit a stage; its activation rows exist
+          const int xr = lane >= 16 && lane - 16 < cm ? prow[m0 + lane - 16] / x_div : 0;
+          const bool ok =
+              (lane != 0 || MOL_CHECK((kJT + cm) * pitch <= kStageBytes && pitch >= 2 * min(len, K),
+                                      MOL_CHECK_SMEM, (kJT + cm) * pitch)) &&
+              MOL_CHECK(xr >= 0 && (int64_t)xr < (numel + x_div - 1) / x_div, MOL_CHECK_ROW, xr);
+          stop = !__all_sync(0xffffffffu, ok);
+          if (stop) break;
+        }
         const int slot = (int)(jn % kMeta);
         Job& jb = meta[slot];
         if (lane == 0) {
@@ -391,10 +425,14 @@ lora_shrink_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, 
         const int col = jb.jt * kJT + 2 * tq;
         // columns past the adapter's rank are zero padding: written as 0
         const bool k0v = !RANKS || 2 * tq < jb.ncols, k1v = !RANKS || 2 * tq + 1 < jb.ncols;
-        if (g < cm)
+        const bool cok = MOL_CHECK(col >= 0 && col + 2 <= R, MOL_CHECK_COLUMN, col);
+        if (g < cm && cok &&
+            MOL_CHECK(jb.rows[g] >= 0 && (int64_t)jb.rows[g] < numel, MOL_CHECK_ROW, jb.rows[g]))
           *reinterpret_cast<float2*>(inter + (int64_t)jb.rows[g] * R + col) =
               make_float2(k0v ? acc[0] : 0.f, k1v ? acc[1] : 0.f);
-        if (g + 8 < cm)
+        if (g + 8 < cm && cok &&
+            MOL_CHECK(jb.rows[g + 8] >= 0 && (int64_t)jb.rows[g + 8] < numel, MOL_CHECK_ROW,
+                      jb.rows[g + 8]))
           *reinterpret_cast<float2*>(inter + (int64_t)jb.rows[g + 8] * R + col) =
               make_float2(k0v ? acc[2] : 0.f, k1v ? acc[3] : 0.f);
       }
@@ -459,6 +497,9 @@ lora_expand_kernel(const float* __restrict__ inter, int R, const uint16_t* __res
   const int ntpp = __ldg(ntpp_ptr);
   const int v = __ldg(expert_ids + t);
   const int slot = tid < block_m ? __ldg(sorted_ids + (int64_t)t * block_m + tid) : -1;
+  if (kChecked && rem == 0)
+    note_block_routing(t, ntpp, v, slot, block_m, numel, num_vexperts,
+                       (int64_t)(gridDim.x / per_block) * block_m);
   if ((int64_t)t * block_m >= ntpp || v < 0 || v >= num_vexperts) return;
   // the adapter's rank and scaling, loaded with the weights below
   int rk_raw = RK;
@@ -501,6 +542,7 @@ lora_expand_kernel(const float* __restrict__ inter, int R, const uint16_t* __res
 
   const bool ovalid = (n_base + 8 * tq) < Ns;
   const int64_t ocol = (int64_t)s * Ns + n_base + 8 * tq;
+  if (kChecked && !MOL_CHECK(s * RK + RK <= R, MOL_CHECK_COLUMN, s * RK)) return;
   const float4 zf = make_float4(0.f, 0.f, 0.f, 0.f);
   const uint4 zu = make_uint4(0, 0, 0, 0);
   // output rows of the first row tile, fetched with the weights
@@ -579,6 +621,9 @@ lora_expand_kernel(const float* __restrict__ inter, int R, const uint16_t* __res
       for (int h = 0; h < 2; ++h) {
         const int i = h ? i1 : i0;
         if (i < 0) continue;
+        if (!MOL_CHECK((int64_t)i < numel, MOL_CHECK_ROW, i) ||
+            !MOL_CHECK(ocol + 8 <= (int64_t)S * Ns, MOL_CHECK_COLUMN, ocol))
+          continue;
         const float sw = topk_w ? scale_v * __ldg(topk_w + i) : scale_v;
         uint4 o = h ? o1 : o0;
         uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
@@ -652,6 +697,9 @@ lora_expand_st_kernel(const float* __restrict__ inter, int R, const uint16_t* __
   const int ntpp = __ldg(ntpp_ptr);
   const int v = __ldg(expert_ids + t);
   const int slot = tid < block_m ? __ldg(sorted_ids + (int64_t)t * block_m + tid) : -1;
+  if (kChecked && rem == 0)
+    note_block_routing(t, ntpp, v, slot, block_m, numel, num_vexperts,
+                       (int64_t)(gridDim.x / per_block) * block_m);
   if ((int64_t)t * block_m >= ntpp || v < 0 || v >= num_vexperts) return;
   // the adapter's rank and scaling, in flight over the row compaction
   int rk_raw = RK;
@@ -675,6 +723,16 @@ lora_expand_st_kernel(const float* __restrict__ inter, int R, const uint16_t* __
   // multiple of 8, so the copy is a multiple of 16 bytes from a 16-byte aligned row
   const int col0 = chunk * kStCols;
   const int ncols = min(kStCols, Ns - col0);
+  if (kChecked) {  // block-uniform: the whole block leaves before the copy is issued
+    const int64_t wr = (int64_t)v * S * Ns + (int64_t)s * Ns + col0;
+    const bool wok = ncols > 0 && ncols <= kStCols && wr + ncols <= (int64_t)num_vexperts * S * Ns;
+    const bool cok = s * RK + RK <= R;
+    if (tid == 0) {
+      (void)MOL_CHECK(wok, MOL_CHECK_WEIGHT_ROW, wr);
+      (void)MOL_CHECK(cok, MOL_CHECK_COLUMN, s * RK);
+    }
+    if (!wok || !cok) return;
+  }
   if (tid == 0) {
     const uint32_t bytes = (uint32_t)ncols * RK * 2;
     mbar_arrive_expect_tx(&wbar, bytes);
@@ -704,7 +762,9 @@ lora_expand_st_kernel(const float* __restrict__ inter, int R, const uint16_t* __
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         const int i = hh ? r1 : r0;
-        if (ok && i >= 0) cp_async16_zfill(osm_at(buf, hh, col), out + (int64_t)i * out_stride + oc, 16u);
+        if (ok && i >= 0 && MOL_CHECK((int64_t)i < numel, MOL_CHECK_ROW, i) &&
+            MOL_CHECK(oc + 8 <= (int64_t)S * Ns, MOL_CHECK_COLUMN, oc))
+          cp_async16_zfill(osm_at(buf, hh, col), out + (int64_t)i * out_stride + oc, 16u);
       }
     }
   };
@@ -721,7 +781,7 @@ lora_expand_st_kernel(const float* __restrict__ inter, int R, const uint16_t* __
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         const int i = hh ? r1 : r0;
-        if (!kq || i < 0) continue;
+        if (!kq || i < 0 || !MOL_CHECK((int64_t)i < numel, MOL_CHECK_ROW, i)) continue;
         const float* src = inter + (int64_t)i * R + s * RK + j;
         cp_async16_zfill(ism_at(hh, j), src, 16u);
         if constexpr (!K16) cp_async16_zfill(ism_at(hh, j + 4), src + 4, 16u);
@@ -865,6 +925,9 @@ lora_expand_st_kernel(const float* __restrict__ inter, int R, const uint16_t* __
         for (int hh = 0; hh < 2; ++hh) {
           const int i = hh ? i1 : i0;
           if (i < 0) continue;
+          if (!MOL_CHECK((int64_t)i < numel, MOL_CHECK_ROW, i) ||
+              !MOL_CHECK(oc + 8 <= (int64_t)S * Ns, MOL_CHECK_COLUMN, oc))
+            continue;
           const float sw = topk_w ? scale_v * __ldg(topk_w + i) : scale_v;
           uint4 ov = lds16(osm_at(buf, hh, nb + 8 * tq));
           uint32_t* ow = reinterpret_cast<uint32_t*>(&ov);
@@ -1025,6 +1088,14 @@ cudaError_t launch_expand(const float* inter, const void* lora_b, int S, int r, 
       return cudaErrorInvalidValue;
   }
 #undef MOL_EXPAND_CASE
+}
+
+cudaError_t take_lora_checks(unsigned long long* first, unsigned long long* count) {
+  CheckRecord r;
+  const cudaError_t e = take_check_record_here(&r);
+  *first = r.first;
+  *count = r.count;
+  return e;
 }
 
 }  // namespace mol

@@ -42,6 +42,14 @@ namespace mol {
 
 __device__ unsigned int g_stage_fault_flags;
 
+cudaError_t take_stage_checks(unsigned long long* first, unsigned long long* count) {
+  CheckRecord r;
+  const cudaError_t e = take_check_record_here(&r);
+  *first = r.first;
+  *count = r.count;
+  return e;
+}
+
 cudaError_t take_stage_faults(unsigned* out) {
   cudaError_t e = cudaMemcpyFromSymbol(out, g_stage_fault_flags, sizeof(unsigned));
   if (e != cudaSuccess) return e;
@@ -143,6 +151,19 @@ lora_stage_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, i
       sl[u] = idx < block_m ? __ldg(sorted_ids + (int64_t)t * block_m + idx) : -1;
     }
     const int v = ((int64_t)t * block_m < ntpp && e >= 0 && e < num_vexperts) ? e : -1;
+    if (kChecked) {  // the caller's routing words
+      if (lane == 0) {
+        (void)MOL_NOTE(ntpp >= 0 && ntpp <= (int64_t)gridDim.x * block_m && ntpp % block_m == 0,
+                       MOL_CHECK_ROUTE_NTPP, ntpp);
+        if ((int64_t)t * block_m < ntpp)
+          (void)MOL_NOTE(e >= -1 && e < num_vexperts, MOL_CHECK_ROUTE_EXPERT, t);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (v >= 0 && u * 32 + lane < block_m)
+          (void)MOL_NOTE(sl[u] >= 0 && (int64_t)sl[u] <= numel, MOL_CHECK_ROUTE_PAIR,
+                         (int64_t)t * block_m + u * 32 + lane);
+    }
     int c = 0;
     if (v >= 0) {
 #pragma unroll
@@ -164,7 +185,8 @@ lora_stage_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, i
       return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     };
     const int njt = R / kJT;
-    for (int m0 = 0; m0 < c && !fault; m0 += kMR) {
+    bool stop = false;  // checked build: a failed check ends the block's work
+    for (int m0 = 0; m0 < c && !fault && !stop; m0 += kMR) {
       const int cm = min(kMR, c - m0);
       const uint16_t* xsrc =
           (lane >= 16 && lane - 16 < cm) ? x + (int64_t)(prow[m0 + lane - 16] / x_div) * x_stride
@@ -172,8 +194,25 @@ lora_stage_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, i
       int len, pitch;
       chunk(K, cm, len, pitch);
       const bool whole = (len == K && pitch == K * 2);
+      if (kChecked) {  // the tile's rows fit a stage and the intermediate tile; x rows exist
+        const int xr = lane >= 16 && lane - 16 < cm ? prow[m0 + lane - 16] / x_div : 0;
+        const bool ok =
+            (lane != 0 ||
+             (MOL_CHECK((kJT + cm) * pitch <= kStageBytes && pitch >= 2 * min(len, K),
+                        MOL_CHECK_SMEM, (kJT + cm) * pitch) &&
+              MOL_CHECK(R <= 128 && R % kJT == 0, MOL_CHECK_SMEM, kMR * (R + 4) * 4))) &&
+            MOL_CHECK(xr >= 0 && (int64_t)xr < (numel + x_div - 1) / x_div, MOL_CHECK_ROW, xr);
+        stop = !__all_sync(0xffffffffu, ok);
+        if (stop) break;
+      }
       // shrink: 8 lora_a rows (and the tile's activation rows) per stage
-      for (int jt = 0; jt < njt && !fault; ++jt) {
+      for (int jt = 0; jt < njt && !fault && !stop; ++jt) {
+        if (kChecked) {
+          const int64_t wr = (int64_t)v * R + jt * kJT;
+          stop = !__all_sync(0xffffffffu, lane != 0 || MOL_CHECK(wr + kJT <= (int64_t)num_vexperts * R,
+                                                                 MOL_CHECK_WEIGHT_ROW, wr));
+          if (stop) break;
+        }
         const uint16_t* wrows = lora_a + ((int64_t)v * R + jt * kJT) * K;
         for (int k0 = 0; k0 < K; k0 += len) {
           int st;
@@ -203,14 +242,24 @@ lora_stage_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, i
         }
       }
       // expand: per slice, 256 output columns of lora_b and the rows they update
-      for (int s = 0; s < S && !fault; ++s) {
+      for (int s = 0; s < S && !fault && !stop; ++s) {
         for (int col0 = 0; col0 < Ns; col0 += kCols) {
+          const int ncols = min(kCols, Ns - col0);
+          if (kChecked) {  // lora_b rows of the tile exist; weights and output rows fit a stage
+            const int64_t wr = ((int64_t)v * S + s) * Ns + col0;
+            const bool ok =
+                lane != 0 ||
+                (MOL_CHECK(wr + ncols <= (int64_t)num_vexperts * S * Ns, MOL_CHECK_WEIGHT_ROW, wr) &&
+                 MOL_CHECK(ncols * RK * 2 + (cm - 1) * kOutPitch + ncols * 2 <= kStageBytes,
+                           MOL_CHECK_SMEM, ncols * RK * 2 + cm * kOutPitch));
+            stop = !__all_sync(0xffffffffu, ok);
+            if (stop) break;
+          }
           int st;
           if (!acquire(st)) {
             fault = true;
             break;
           }
-          const int ncols = min(kCols, Ns - col0);
           unsigned char* base = stages + (size_t)st * kStageBytes;
           const uint32_t wbytes = (uint32_t)ncols * RK * 2;
           if (lane == 0) {
@@ -314,12 +363,15 @@ lora_stage_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, i
 #pragma unroll
             for (int w = 0; w < kConsumers - 1; ++w) acc[e] += red[w][e][lane];
           const int col = h.a * kJT + 2 * tq;
-          if (g < cm) {
+          const bool cok = MOL_CHECK(col + 2 <= R, MOL_CHECK_COLUMN, col);
+          if (g < cm && cok &&
+              MOL_CHECK((int64_t)prow[m0 + g] < numel, MOL_CHECK_ROW, prow[m0 + g])) {
             const float2 v2 = make_float2(acc[0], acc[1]);
             *reinterpret_cast<float2*>(inter + (int64_t)prow[m0 + g] * R + col) = v2;
             *reinterpret_cast<float2*>(inter_s + g * ipitch + col) = v2;
           }
-          if (g + 8 < cm) {
+          if (g + 8 < cm && cok &&
+              MOL_CHECK((int64_t)prow[m0 + g + 8] < numel, MOL_CHECK_ROW, prow[m0 + g + 8])) {
             const float2 v2 = make_float2(acc[2], acc[3]);
             *reinterpret_cast<float2*>(inter + (int64_t)prow[m0 + g + 8] * R + col) = v2;
             *reinterpret_cast<float2*>(inter_s + (g + 8) * ipitch + col) = v2;
@@ -394,6 +446,9 @@ lora_stage_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, i
         for (int hh = 0; hh < 2; ++hh) {
           const int i = hh ? i1 : i0;
           if (i < 0) continue;
+          if (!MOL_CHECK((int64_t)i < numel, MOL_CHECK_ROW, i) ||
+              !MOL_CHECK(oc + 8 <= (int64_t)S * Ns, MOL_CHECK_COLUMN, oc))
+            continue;
           const float sw = hh ? sw1 : sw0;
           uint4 ov = lds16(osm + (8 * hh + g) * kOutPitch + (nb + 8 * tq) * 2);
           uint32_t* ow = reinterpret_cast<uint32_t*>(&ov);

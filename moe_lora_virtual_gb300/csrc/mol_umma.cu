@@ -207,6 +207,15 @@ lora_shrink_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
       for (int64_t it = blockIdx.x; it < n_items && !fault; it += Gs) {
         int64_t t;
         int mt, v;
+        if (kChecked && it % mtiles == 0) {  // the caller's routing words, once per block
+          const int64_t tb = it / mtiles;
+          const int64_t cap = n_items / mtiles * BN;
+          (void)MOL_NOTE(ntpp >= 0 && ntpp <= cap && ntpp % BN == 0, MOL_CHECK_ROUTE_NTPP, ntpp);
+          if (tb * BN < ntpp) {
+            const int e = __ldg(expert_ids + tb);
+            (void)MOL_NOTE(e >= -1 && e < num_vexperts, MOL_CHECK_ROUTE_EXPERT, tb);
+          }
+        }
         if (!item(it, t, mt, v)) continue;
         const int y = v * R + mt * kM;
         const bool half = R - mt * kM < kM;  // the expert's last 64 rows: the 64-row box
@@ -215,6 +224,17 @@ lora_shrink_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
           if (!mbar_wait(&empty[s], ((q / kStages) & 1) ^ 1, kPolls)) {
             fault = true;
             break;
+          }
+          // checked build: the box starts on a 16-byte boundary and lies inside the tensor;
+          // a failed check skips the copy (the stage then holds stale data)
+          const bool in_box =
+              MOL_CHECK((ks * kKStep) % 8 == 0 && ks * kKStep + kKStep <= K, MOL_CHECK_TMA_COORD,
+                        ks * kKStep) &&
+              MOL_CHECK(y >= 0 && (int64_t)y + (half ? kM / 2 : kM) <= (int64_t)num_vexperts * R,
+                        MOL_CHECK_TMA_COORD, y);
+          if (kChecked && !in_box) {
+            mbar_arrive_expect_tx(&full[s], 0u);
+            continue;
           }
           mbar_arrive_expect_tx(&full[s], (uint32_t)(half ? kATile / 2 : kATile));
           tma_load_2d(stageA(q), half ? &tmap_h : &tmap_a, ks * kKStep, y, &full[s]);
@@ -279,7 +299,12 @@ lora_shrink_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
 #pragma unroll
       for (int i = 0; i < kRowsPerThr; ++i) {
         const int pid = __ldg(sorted_ids + t * BN + r0 + kRowStep * i);
-        const bool ok = pid >= 0 && (int64_t)pid < numel;
+        if (kChecked && mt == 0 && c == 0)
+          (void)MOL_NOTE(pid >= 0 && (int64_t)pid <= numel, MOL_CHECK_ROUTE_PAIR,
+                         t * BN + r0 + kRowStep * i);
+        const bool ok = pid >= 0 && (int64_t)pid < numel &&
+                        MOL_CHECK((int64_t)(pid / x_div) < (numel + x_div - 1) / x_div,
+                                  MOL_CHECK_ROW, pid / x_div);
         src[i] = (ok ? x + (int64_t)(pid / x_div) * x_stride : x) + c * 8;
         nbytes[i] = ok ? 16u : 0u;
       }
@@ -427,6 +452,14 @@ cudaError_t launch_shrink_tc(const void* x, int64_t x_stride, int x_div, int K, 
   return launch_pdl(lora_shrink_tc_kernel<128>, grid, dim3(tc::kThreads), tc::Geo<128>::kSmem,
                     stream, map, map_h, xp, x_stride, x_div, K, R, sorted_ids, expert_ids, ntpp,
                     numel, num_vexperts, inter, n_items, mtiles);
+}
+
+cudaError_t take_tc_checks(unsigned long long* first, unsigned long long* count) {
+  CheckRecord r;
+  const cudaError_t e = take_check_record_here(&r);
+  *first = r.first;
+  *count = r.count;
+  return e;
 }
 
 }  // namespace mol

@@ -24,9 +24,9 @@ needs_nvcc = pytest.mark.skipif(not (shutil.which("nvcc") or os.path.exists("/us
 
 @pytest.fixture(scope="module")
 def mol():
-    from moe_lora_virtual_gb300.build import build_library
+    from moe_lora_virtual_gb300.build import build_all
 
-    build_library()
+    build_all()
     import moe_lora_virtual_gb300 as m
 
     m.library()
@@ -43,10 +43,37 @@ def declared_functions():
 def test_exports_every_declared_symbol(mol):
     lib = mol.library()
     names = declared_functions()
-    assert len(names) == 15
+    assert len(names) == 17
     for n in names:
         assert hasattr(lib, n), n
     assert set(names) == set(mol.EXPORTS)
+
+
+@needs_nvcc
+def test_checked_build_exports_the_same_symbols(mol):
+    """libmol_checked.so is the same library with device-side index checks compiled in."""
+    lib = mol.library()
+    with mol.use_library(mol.CHECKED_LIB_PATH) as chk:
+        for n in declared_functions():
+            assert hasattr(chk, n), n
+        assert mol.mol_checked_build() is True
+        assert chk.mol_version() == lib.mol_version()
+    assert mol.mol_checked_build() is False
+    assert mol.library() is lib
+
+
+def test_check_sites_match_header(mol):
+    src = open(HEADER).read()
+    sites = {int(v): k for k, v in re.findall(r"#define MOL_CHECK_(\w+) (\d+)", src)}
+    assert sites == mol.CHECK_SITES
+
+
+def test_check_record_decoding(mol):
+    r = mol.decode_check_record((2 << 48) | 12345, 7)
+    assert (r.count, r.site, r.value, r.site_name) == (7, 2, 12345, "ROUTE_PAIR")
+    r = mol.decode_check_record((3 << 48) | ((-5) & 0xFFFFFFFFFFFF), 1)
+    assert (r.site, r.value, r.site_name) == (3, -5, "ROUTE_NTPP")
+    assert mol.decode_check_record(0, 0).site_name == "none"
 
 
 @needs_nvcc
