@@ -7,6 +7,11 @@ reusing the routing. The workload is the bs=23 decode configuration (23
 tokens, 128 experts x 8 adapters = 1024 virtual experts, top-8, rank 32,
 gate_up 2048 -> 2x32 -> 2x768, down 768 -> 32 -> 2048), synthetic seeded data.
 
+The first stage computes the routing with compute_routing = 2 (--routing-mode):
+the top-k and adapter ids are ready before the kernel that precedes the layer,
+as when the router ran earlier in the MoE layer; the line also reports the
+layer time with mode 1 (ids that may come from the preceding kernel).
+
 Steps rotate over --layers distinct layers (own weights, routing and
 activations) so that a step never finds its weights in L2: 8 decode layers
 touch ~0.7 GB per cycle, over 5x the 129 MB L2. As in a real decode step, one
@@ -51,6 +56,10 @@ def parse_args(argv=None):
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--ranks", default=None,
                    help="per-adapter ranks, comma separated (one per adapter; scaling 16/rank)")
+    p.add_argument("--routing-mode", type=int, choices=[1, 2], default=2,
+                   help="compute_routing of each layer's first stage: 2 = the top-k and adapter "
+                        "ids are ready before the kernel preceding the layer (as after a router "
+                        "that ran earlier in the layer), 1 = they may come from that kernel")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--no-kernels", action="store_true", help="skip the per-kernel timing phase")
@@ -152,6 +161,9 @@ def shard_tokens(num_tokens: int, world: int, rank: int):
 class LayerState:
     """Device tensors of one layer: routing, workspace, per-stage inputs and outputs."""
 
+    # compute_routing of the first stage (the others reuse its routing)
+    routing_mode = 2
+
     def __init__(self, wl, li, dev, mol, torch, ranks=None):
         self.wl, self.li = wl, li
         self.ranks = None if ranks is None else np.asarray(ranks, np.int32)
@@ -176,7 +188,8 @@ class LayerState:
         for si, d in enumerate(self.stages):
             mol.mol_lora_forward(d["x"], d["st"].x_row_div, self.topk, self.lora, wl.E, wl.L,
                                  d["A"], d["B"], d["st"].stage.S, wl.scale, d["out"], self.routing,
-                                 d["inter"], compute_routing=(si == 0), workspace=self.ws,
+                                 d["inter"], compute_routing=(self.routing_mode if si == 0 else 0),
+                                 workspace=self.ws,
                                  lora_ranks=self.ranks_d, lora_scalings=self.scal_d)
 
     def counts(self):
@@ -439,6 +452,7 @@ def run_gpu(args):
     mol.library()
 
     wl = WORKLOADS[args.config]
+    LayerState.routing_mode = args.routing_mode
     ranks = None
     if args.ranks:
         ranks = [int(v) for v in args.ranks.split(",")]
@@ -495,6 +509,17 @@ def run_gpu(args):
     ms, pairs_all = combine_ranks(ms, pairs_per_step, dev if world > 1 else None)
     value = pairs_all / (ms * 1e-3)
 
+    # ---- the same layers with the other routing mode (context, not the metric) -----------
+    other_mode = 3 - args.routing_mode
+    LayerState.routing_mode = other_mode
+    g_other = capture(torch, lambda: [L_.forward(mol) for L_ in layers])
+    LayerState.routing_mode = args.routing_mode
+    for _ in range(3):
+        g_other.replay()
+    other_reps = max(1, 800 // len(layers))
+    us_other = time_graphs(torch, [g_other], other_reps, 2) * 1e3 / len(layers)
+    del g_other
+
     # ---- per-kernel timing (each kernel alone in its own graphs, same rotation) -------
     peaks = measured_peaks()
     kern, roof, shrink_tensor = {}, None, None
@@ -530,6 +555,7 @@ def run_gpu(args):
                            stages=[f"{s.name} K={s.K} R={s.R} N={s.N}" for s in wl.stages],
                            pairs_per_layer=pairs_per_step, layers_rotated=args.layers,
                            adapter_ranks=ranks,
+                           routing_mode=args.routing_mode,
                            l2="inputs larger than L2: steps rotate over distinct layers",
                            graph=f"{args.layers} layers per graph replay; the K mod {args.layers} "
                                  "remainder in one more graph of that many layers; every graph "
@@ -538,6 +564,8 @@ def run_gpu(args):
                layer_hbm=dict(bytes=int(layer_bytes),
                               achieved_gbs=round(layer_bytes / (ms * 1e-3) / 1e9, 1),
                               frac=round(layer_bytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)),
+               us_per_layer_other_routing_mode={"routing_mode": other_mode,
+                                                "us": round(us_other, 3)},
                kernels_us={k: round(v, 3) for k, v in kern.items()},
                roofline=roof, shrink_tensor=shrink_tensor, e2e=e2e,
                gpu_launches=launches_per_step * args.steps,

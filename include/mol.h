@@ -256,9 +256,15 @@ int32_t mol_lora_expand(const float* inter, const void* lora_b, int32_t num_slic
  * four calls above; numel = num_tokens * topk; V = num_experts * max_loras.
  * Routing buffers passed with compute_routing = 0 must be complete when the
  * call's first kernel starts (true unless the kernel just before the call
- * lets its dependents start early, before writing them). lora_ranks and
- * lora_scalings (each NULL or one entry per adapter) are those of the shrink
- * and the expand.
+ * lets its dependents start early, before writing them). compute_routing = 2
+ * computes the routing like 1 and declares that topk_ids and lora_ids were
+ * complete before the kernel just before the call began (in a MoE layer the
+ * router's top-k runs before the expert GEMMs that precede the LoRA stage):
+ * the shrink may then start, and ask L2 for the weight rows the ids select,
+ * while that kernel and the align still run. With 1 the ids may come from the
+ * kernel just before the call. lora_ranks and lora_scalings (each NULL or one
+ * entry per adapter) are those of the shrink and the expand.
+ * compute_routing outside {0, 1, 2} is MOL_ERR_INVALID_ARG.
  */
 int32_t mol_lora_forward(const void* x, int64_t x_row_stride, int32_t x_row_div, int32_t K,
                          const int32_t* topk_ids, const int32_t* lora_ids, int64_t num_tokens,

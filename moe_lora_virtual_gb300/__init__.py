@@ -286,12 +286,16 @@ def mol_lora_forward(x: torch.Tensor, x_row_div: int, topk_ids: Optional[torch.T
                      lora_ids: Optional[torch.Tensor], num_experts: int, max_loras: int,
                      lora_a: torch.Tensor, lora_b: torch.Tensor, num_slices: int, scale: float,
                      out: torch.Tensor, routing: Routing, inter: torch.Tensor,
-                     compute_routing: bool = True, topk_weights: Optional[torch.Tensor] = None,
+                     compute_routing: int = True, topk_weights: Optional[torch.Tensor] = None,
                      workspace: Optional[torch.Tensor] = None, num_tokens: Optional[int] = None,
                      topk: Optional[int] = None, stream=None,
                      lora_ranks: Optional[torch.Tensor] = None,
                      lora_scalings: Optional[torch.Tensor] = None) -> None:
-    """One MoL LoRA stage; with compute_routing the routing buffers are (re)computed."""
+    """One MoL LoRA stage; with compute_routing the routing buffers are (re)computed.
+
+    compute_routing: False/0 reuses the routing; True/1 computes it; 2 computes it and
+    declares that topk_ids and lora_ids were complete before the kernel preceding the call
+    began, so the stage may start reading them (and the weights they select) early."""
     _need(x, torch.bfloat16, "x")
     _adapter_arrays(lora_ranks, lora_scalings)
     if topk_ids is not None:
@@ -306,7 +310,7 @@ def mol_lora_forward(x: torch.Tensor, x_row_div: int, topk_ids: Optional[torch.T
         _ptr(x), _row_stride(x, "x"), x_row_div, K, _ptr(topk_ids), _ptr(lora_ids), num_tokens,
         topk, num_experts, max_loras, _ptr(lora_a), _ptr(lora_b), num_slices, r,
         N // num_slices, float(scale), _ptr(topk_weights), _ptr(out), _row_stride(out, "out"),
-        routing.block_m, int(bool(compute_routing)), _ptr(routing.vtopk_ids),
+        routing.block_m, int(compute_routing), _ptr(routing.vtopk_ids),
         _ptr(routing.sorted_token_ids), routing.capacity, _ptr(routing.expert_ids),
         _ptr(routing.num_tokens_post_padded), _ptr(inter), _ptr(lora_ranks), _ptr(lora_scalings),
         _ptr(workspace), wsb, _stream(stream)))

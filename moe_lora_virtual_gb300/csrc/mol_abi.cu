@@ -254,7 +254,7 @@ int32_t mol_align_block_size(const int32_t* vtopk_ids, int64_t numel, int32_t nu
   p.capacity = capacity;  // fill the caller's whole buffer
   cudaError_t e = mol::launch_align(p, false, vtopk_ids, nullptr, 1, 1, 1, nullptr, num_vexperts,
                                     sorted_token_ids, expert_ids, num_tokens_post_padded,
-                                    workspace, false, static_cast<cudaStream_t>(stream));
+                                    workspace, 0, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MOL_OK : cuda_fail(e);
 }
 
@@ -319,7 +319,7 @@ int32_t mol_lora_forward(const void* x, int64_t x_row_stride, int32_t x_row_div,
                          const int32_t* lora_ranks, const float* lora_scalings,
                          void* workspace, size_t workspace_bytes, void* stream) {
   if (num_tokens < 0 || topk < 1 || num_experts < 1 || max_loras < 1) return MOL_ERR_INVALID_ARG;
-  if (compute_routing != 0 && compute_routing != 1) return MOL_ERR_INVALID_ARG;
+  if (compute_routing < 0 || compute_routing > 2) return MOL_ERR_INVALID_ARG;
   const int64_t V64 = (int64_t)num_experts * max_loras;
   if (V64 + 1 > MOL_MAX_BUCKETS) return MOL_ERR_UNSUPPORTED;
   const int32_t V = (int32_t)V64;
@@ -353,7 +353,8 @@ int32_t mol_lora_forward(const void* x, int64_t x_row_stride, int32_t x_row_div,
     mol::AlignPlan p = plan;
     p.capacity = capacity;
     e = mol::launch_align(p, true, topk_ids, lora_ids, topk, num_experts, max_loras, vtopk_ids, V,
-                          sorted_token_ids, expert_ids, num_tokens_post_padded, workspace, true, s);
+                          sorted_token_ids, expert_ids, num_tokens_post_padded, workspace,
+                          compute_routing == 2 ? 2 : 1, s);
     if (e != cudaSuccess) return cuda_fail(e);
   }
   if (numel == 0 || capacity == 0) return MOL_OK;
@@ -365,9 +366,13 @@ int32_t mol_lora_forward(const void* x, int64_t x_row_stride, int32_t x_row_div,
                           out_row_stride, compute_routing == 0, s);
     return e == cudaSuccess ? MOL_OK : cuda_fail(e);
   }
+  // ids declared ready early: the shrink asks L2 for its weight rows while the align runs
+  const mol::RoutingIds ids{topk_ids, lora_ids, (int)numel, topk, num_experts, max_loras,
+                            compute_routing == 2};
   e = mol::launch_shrink(x, x_row_stride, x_row_div, K, lora_a, num_slices * rank,
                          sorted_token_ids, expert_ids, num_tokens_post_padded, capacity, block_m,
-                         numel, V, inter, compute_routing == 0, s, rank, lora_ranks, num_experts);
+                         numel, V, inter, compute_routing == 0, s, rank, lora_ranks, num_experts,
+                         compute_routing ? &ids : nullptr);
   if (e != cudaSuccess) return cuda_fail(e);
   e = mol::launch_expand(inter, lora_b, num_slices, rank, slice_n, scale, topk_weights,
                          sorted_token_ids, expert_ids, num_tokens_post_padded, capacity, block_m,
@@ -443,6 +448,6 @@ extern "C" int32_t mol_align_block_size_noalloc(const int32_t* vtopk_ids, int64_
   p.capacity = capacity;
   cudaError_t e = mol::launch_align(p, false, vtopk_ids, nullptr, 1, 1, 1, nullptr, num_vexperts,
                                     sorted_token_ids, expert_ids, num_tokens_post_padded, scratch,
-                                    false, static_cast<cudaStream_t>(stream));
+                                    0, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MOL_OK : cuda_fail(e);
 }

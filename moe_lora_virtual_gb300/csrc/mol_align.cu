@@ -46,12 +46,6 @@ constexpr int kClusterTileMax = 16384;  // pairs per block of the cluster align
 constexpr int kClusterMax = 16;         // blocks in one cluster (above 8 where the device allows)
 constexpr int64_t kClusterPairs = 8LL * kClusterTileMax;  // largest numel of the cluster align
 
-MOL_DEV int remap_one(int base, int lora, int num_experts, int max_loras) {
-  if (base < 0) return base;
-  if (lora < 0 || lora >= max_loras || base >= num_experts) return -1;
-  return base + lora * num_experts;
-}
-
 MOL_DEV int bucket_of(int vid, int num_vexperts) {
   return (vid >= 0 && vid < num_vexperts) ? vid : num_vexperts;
 }
@@ -99,44 +93,11 @@ __global__ void token_lora_ids_kernel(const int* __restrict__ weight_indices,
   }
 }
 
-// Exclusive scan of one int per thread over the block; `total` = sum of all.
+// counts[b] -> exclusive offsets of the BM-padded buckets (in place); returns
+// the padded total. block_m is a power of two (validated on the host): padding
+// and block indices are masks and shifts.
 template <int THREADS>
-MOL_DEV int block_exclusive_scan(int v, int* sh, int& total) {
-  constexpr int NW = THREADS / 32;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int incl = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int n = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += n;
-  }
-  if (lane == 31) sh[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    const int w = lane < NW ? sh[lane] : 0;
-    int wi = w;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int n = __shfl_up_sync(0xffffffffu, wi, o);
-      if (lane >= o) wi += n;
-    }
-    if (lane < NW) sh[lane] = wi - w;
-    if (lane == NW - 1) sh[NW] = wi;
-  }
-  __syncthreads();
-  const int res = sh[warp] + incl - v;
-  total = sh[NW];
-  __syncthreads();
-  return res;
-}
-
-// counts[b] -> exclusive offsets of the BM-padded buckets (in place), then
-// expert_ids of every block and num_tokens_post_padded. block_m is a power of
-// two (validated on the host): padding and block indices are masks and shifts.
-template <int THREADS>
-MOL_DEV void bucket_offsets(int* counts, int nb, int num_vexperts, int block_m, int64_t capacity,
-                            int* __restrict__ expert_ids, int* __restrict__ ntpp_out, int* sh) {
-  const int lg = __ffs(block_m) - 1;
+MOL_DEV int bucket_scan(int* counts, int nb, int block_m, int* sh) {
   const int pad = block_m - 1;
   const int per = (nb + THREADS - 1) / THREADS;
   const int b0 = min((int)threadIdx.x * per, nb), b1 = min(b0 + per, nb);
@@ -147,21 +108,40 @@ MOL_DEV void bucket_offsets(int* counts, int nb, int num_vexperts, int block_m, 
   for (int b = b0; b < b1; ++b) {
     const int pb = (counts[b] + pad) & ~pad;
     counts[b] = run;
-    if (b < num_vexperts) {
-      const int t0 = run >> lg;
-      for (int k = 0; k < (pb >> lg); ++k)
-        if (MOL_CHECK(t0 + k < (capacity >> lg), MOL_CHECK_ALIGN_BLOCK, t0 + k)) expert_ids[t0 + k] = b;
-    }
     run += pb;
   }
-  __syncthreads();
+  return total;
+}
+
+// expert_ids of every block and num_tokens_post_padded from the offsets of
+// bucket_scan (every thread of the block, after a barrier that follows it).
+template <int THREADS>
+MOL_DEV void write_blocks(const int* offs, int nb, int num_vexperts, int block_m, int64_t capacity,
+                          int total, int* __restrict__ expert_ids, int* __restrict__ ntpp_out) {
+  const int lg = __ffs(block_m) - 1;
+  const int per = (nb + THREADS - 1) / THREADS;
+  const int b0 = min((int)threadIdx.x * per, nb), b1 = min(b0 + per, num_vexperts);
+  for (int b = b0; b < b1; ++b) {
+    const int t0 = offs[b] >> lg, t1 = (b + 1 < nb ? offs[b + 1] : total) >> lg;
+    for (int t = t0; t < t1; ++t)
+      if (MOL_CHECK(t < (capacity >> lg), MOL_CHECK_ALIGN_BLOCK, t)) expert_ids[t] = b;
+  }
   const int64_t nblk = capacity >> lg;
-  for (int64_t t = (counts[num_vexperts] >> lg) + threadIdx.x; t < nblk; t += THREADS)
+  for (int64_t t = (offs[num_vexperts] >> lg) + threadIdx.x; t < nblk; t += THREADS)
     expert_ids[t] = -1;
   if (threadIdx.x == 0) {
     MOL_CHECK(total <= capacity, MOL_CHECK_ALIGN_TOTAL, total);
     *ntpp_out = total;
   }
+}
+
+// Both: offsets in place, then expert_ids and num_tokens_post_padded.
+template <int THREADS>
+MOL_DEV void bucket_offsets(int* counts, int nb, int num_vexperts, int block_m, int64_t capacity,
+                            int* __restrict__ expert_ids, int* __restrict__ ntpp_out, int* sh) {
+  const int total = bucket_scan<THREADS>(counts, nb, block_m, sh);
+  __syncthreads();
+  write_blocks<THREADS>(counts, nb, num_vexperts, block_m, capacity, total, expert_ids, ntpp_out);
 }
 
 // Pass 1: the warp's bucket counts over its contiguous segment [s0, s1) of the
@@ -233,14 +213,59 @@ align_tile_kernel(const int* __restrict__ src, const int* __restrict__ lora_ids,
     const int n4 = kAlignWarps * nb_pad / 8;
     for (int q = tid; q < n4; q += kAlignThreads) t4[q] = make_uint4(0, 0, 0, 0);
   }
+  // The single-block align writes the final routing. Called on its own
+  // (trigger = 0) it lets its dependents start only when it exits, so a kernel
+  // that follows it may read the routing before its own griddepcontrol.wait.
+  // Inside mol_lora_forward the next kernel waits before reading the routing:
+  // it may start once this kernel has waited for the previous one (trigger = 1),
+  // or at once when the caller's ids were complete before the previous kernel
+  // began (trigger = 2: the next kernel reads the ids early). With several
+  // tiles the scatter kernel is the last writer and plays that role.
+  if (trigger == 2) pdl_launch_dependents();
+  const int64_t t0 = (int64_t)blockIdx.x * tile;
+  const int tlen = (int)max((int64_t)0, min((int64_t)tile, numel - t0));
+  const int seg = tile / kAlignWarps;
+  const int s0 = warp * seg, s1 = min(s0 + seg, tlen);
+  uint16_t* mine = tbl + warp * nb_pad;
+  // Keys, per-warp counts, the tile's bucket counts and (one tile) the bucket
+  // offsets: in shared memory only, from the ids.
+  auto count_tile = [&](bool write_vtopk) {
+    for (int q = tid; q < tlen; q += kAlignThreads) {
+      const int64_t i = t0 + q;
+      int vid;
+      if (REMAP) {
+        vid = remap_one(src[i], lora_ids[i / topk], num_experts, max_loras);
+        if (write_vtopk) vtopk_out[i] = vid;
+      } else {
+        vid = src[i];
+      }
+      keys[q] = (uint16_t)bucket_of(vid, num_vexperts);
+    }
+    __syncthreads();
+    warp_count(keys, s0, s1, mine, lane);  // pass 1: per-warp counts over the warp's segment
+    __syncthreads();
+    // column scan: warp tables become exclusive bases; the tile total per bucket
+    // goes to shared memory (one tile) or to the workspace histogram
+    column_scan(tbl, nb, nb_pad, [&](int b, int n) {
+      const int64_t w = (int64_t)blockIdx.x * nb + b;
+      if (fused)
+        offs[b] = n;
+      else if (MOL_CHECK(w < (int64_t)tiles * nb, MOL_CHECK_ALIGN_WORKSPACE, w))
+        ws_hist[w] = n;
+    });
+    __syncthreads();
+  };
+  // trigger = 2, one tile: the ids are older than the previous kernel, so all of
+  // that runs before the wait; only the writes wait.
+  const bool ids_early = trigger == 2 && fused;
+  int total = 0;
+  if (ids_early) {
+    count_tile(false);
+    total = bucket_scan<kAlignThreads>(offs, nb, block_m, sh_scan);
+    __syncthreads();  // every bucket's offset is in place
+  }
   pdl_wait();  // inputs and the routing buffers belong to earlier kernels until here
-  // The single-block align writes the final routing. Called on its own it lets
-  // its dependents start only when it exits, so a kernel that follows it may
-  // read the routing before its own griddepcontrol.wait. Inside
-  // mol_lora_forward (trigger = 1) the next kernel waits before reading the
-  // routing, and may start early. With several tiles the scatter kernel is the
-  // last writer and plays that role.
-  if (tiles > 1 || trigger) pdl_launch_dependents();
+  if (trigger == 1 || (trigger == 0 && tiles > 1)) pdl_launch_dependents();
 
   // Every slot starts as padding (value numel); real pairs overwrite theirs.
   for (int64_t q = (int64_t)blockIdx.x * kAlignThreads + tid; q < capacity;
@@ -248,41 +273,21 @@ align_tile_kernel(const int* __restrict__ src, const int* __restrict__ lora_ids,
     sorted_ids[q] = (int)numel;
   if ((int)blockIdx.x >= tiles) return;  // fill-only block
 
-  const int64_t t0 = (int64_t)blockIdx.x * tile;
-  const int tlen = (int)min((int64_t)tile, numel - t0);
-  for (int q = tid; q < tlen; q += kAlignThreads) {
-    const int64_t i = t0 + q;
-    int vid;
-    if (REMAP) {
-      vid = remap_one(src[i], lora_ids[i / topk], num_experts, max_loras);
-      vtopk_out[i] = vid;
-    } else {
-      vid = src[i];
-    }
-    keys[q] = (uint16_t)bucket_of(vid, num_vexperts);
-  }
-  __syncthreads();
-
-  // Pass 1: per-warp bucket counts over the warp's contiguous segment.
-  const int seg = tile / kAlignWarps;
-  const int s0 = warp * seg, s1 = min(s0 + seg, tlen);
-  uint16_t* mine = tbl + warp * nb_pad;
-  warp_count(keys, s0, s1, mine, lane);
-  __syncthreads();
-
-  // Column scan: warp tables become exclusive bases; the tile total per bucket
-  // goes to shared memory (one tile) or to the workspace histogram.
-  column_scan(tbl, nb, nb_pad, [&](int b, int n) {
-    const int64_t w = (int64_t)blockIdx.x * nb + b;
+  if (ids_early) {
+    if (REMAP)
+      for (int q = tid; q < tlen; q += kAlignThreads) {
+        const int64_t i = t0 + q;
+        vtopk_out[i] = remap_one(src[i], lora_ids[i / topk], num_experts, max_loras);
+      }
+    write_blocks<kAlignThreads>(offs, nb, num_vexperts, block_m, capacity, total, expert_ids,
+                                ntpp_out);
+    __syncthreads();  // the padding fill lands before the scatter overwrites it
+  } else {
+    count_tile(true);
     if (fused)
-      offs[b] = n;
-    else if (MOL_CHECK(w < (int64_t)tiles * nb, MOL_CHECK_ALIGN_WORKSPACE, w))
-      ws_hist[w] = n;
-  });
-  __syncthreads();
-  if (fused)
-    bucket_offsets<kAlignThreads>(offs, nb, num_vexperts, block_m, capacity, expert_ids, ntpp_out,
-                                  sh_scan);
+      bucket_offsets<kAlignThreads>(offs, nb, num_vexperts, block_m, capacity, expert_ids,
+                                    ntpp_out, sh_scan);
+  }
 
   // Pass 2: stable rank of every pair inside the tile.
   warp_rank(keys, s0, s1, mine, lane, [&](int q, int key, int lr) {
@@ -363,8 +368,9 @@ align_cluster_kernel(const int* __restrict__ src, const int* __restrict__ lora_i
     const int n4 = kAlignWarps * nb_pad / 8;
     for (int q = tid; q < n4; q += kAlignThreads) t4[q] = make_uint4(0, 0, 0, 0);
   }
+  if (trigger == 2) pdl_launch_dependents();  // see align_tile_kernel
   pdl_wait();  // inputs and routing buffers belong to earlier kernels until here
-  if (trigger) pdl_launch_dependents();  // see align_tile_kernel
+  if (trigger == 1) pdl_launch_dependents();
 
   for (int64_t q = (int64_t)me * kAlignThreads + tid; q < capacity;
        q += (int64_t)CL * kAlignThreads)
@@ -503,8 +509,11 @@ __global__ void align_scatter_kernel(const int* __restrict__ vtopk, int64_t nume
                                      const int* __restrict__ ws_offs,
                                      const int* __restrict__ ws_rank, int* __restrict__ sorted_ids,
                                      int64_t capacity, int trigger) {
-  pdl_wait();  // last writer of the routing: dependents start when it exits unless trigger
-  if (trigger) pdl_launch_dependents();
+  // last writer of the routing: dependents start when it exits unless trigger (see
+  // align_tile_kernel)
+  if (trigger == 2) pdl_launch_dependents();
+  pdl_wait();
+  if (trigger == 1) pdl_launch_dependents();
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= numel) return;
   const int key = bucket_of(vtopk[i], num_vexperts);
@@ -641,9 +650,9 @@ cudaError_t launch_virtual_topk(const int32_t* topk_ids, const int32_t* lora_ids
 cudaError_t launch_align(const AlignPlan& plan, bool remap, const int32_t* src,
                          const int32_t* lora_ids, int topk, int num_experts, int max_loras,
                          int32_t* vtopk_out, int num_vexperts, int32_t* sorted_ids,
-                         int32_t* expert_ids, int32_t* ntpp, void* workspace, bool trigger_early,
+                         int32_t* expert_ids, int32_t* ntpp, void* workspace, int trigger,
                          cudaStream_t stream) {
-  const int trig = trigger_early ? 1 : 0;
+  const int trig = trigger;
   int device = 0;
   cudaError_t e = cudaGetDevice(&device);
   if (e != cudaSuccess) return e;

@@ -140,6 +140,29 @@ MOL_DEV void cp_async16_zfill(void* dst, const void* src, uint32_t src_bytes) {
                "r"(src_bytes)
                : "memory");
 }
+// Virtual id of one (token, slot) pair: negative ids stay as they are; a token
+// without a valid adapter, or an expert id past the experts, gives -1; else
+// base + lora * E.
+MOL_DEV int remap_one(int base, int lora, int num_experts, int max_loras) {
+  if (base < 0) return base;
+  if (lora < 0 || lora >= max_loras || base >= num_experts) return -1;
+  return base + lora * num_experts;
+}
+// 32-bit load from L2 (no L1 allocation, so no stale L1 line is read).
+MOL_DEV int ld_cg_i32(const int* p) {
+  int v;
+  asm volatile("ld.global.cg.s32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+// Asks L2 to load `bytes` (a multiple of 16) from 16-byte aligned global memory,
+// asynchronously, in 32 KB requests; nothing waits for it.
+MOL_DEV void prefetch_l2(const void* p, int64_t bytes) {
+  const char* c = static_cast<const char*>(p);
+  for (int64_t o = 0; o < bytes; o += 32768) {
+    const uint32_t n = (uint32_t)(bytes - o < 32768 ? bytes - o : 32768);
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(c + o), "r"(n) : "memory");
+  }
+}
 // Waits until every cp.async this thread issued has landed.
 MOL_DEV void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 // Closes this thread's current group of cp.async copies.
@@ -203,6 +226,37 @@ MOL_DEV unsigned lanemask_lt() {
   unsigned m;
   asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
   return m;
+}
+
+// Exclusive scan of one int per thread over the block; `total` = sum of all.
+template <int THREADS>
+MOL_DEV int block_exclusive_scan(int v, int* sh, int& total) {
+  constexpr int NW = THREADS / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) sh[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int w = lane < NW ? sh[lane] : 0;
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += n;
+    }
+    if (lane < NW) sh[lane] = wi - w;
+    if (lane == NW - 1) sh[NW] = wi;
+  }
+  __syncthreads();
+  const int res = sh[warp] + incl - v;
+  total = sh[NW];
+  __syncthreads();
+  return res;
 }
 
 // Checked build: records the caller's routing words of routed block t that

@@ -83,14 +83,16 @@ cudaError_t launch_virtual_topk(const int32_t* topk_ids, const int32_t* lora_ids
 
 // remap != 0: `src` is topk_ids and the remap is fused (vtopk written);
 // remap == 0: `src` is vtopk_ids.
-// trigger_early: let the next kernel start before the align exits (only when
-// that kernel reads the routing after griddepcontrol.wait, as in
-// mol_lora_forward); otherwise the next kernel starts once the routing is
-// complete and may read it early.
+// trigger: when the align's dependents may start. 0: when it exits (called on
+// its own: a following kernel may read the routing early); 1: once it has waited
+// for the previous kernel (the next kernel reads the routing after its own
+// griddepcontrol.wait, as in mol_lora_forward); 2: at once, and with one tile the
+// align counts and scans before its own wait (the caller's ids were complete
+// before the previous kernel began; the next kernel may read them early).
 cudaError_t launch_align(const AlignPlan& plan, bool remap, const int32_t* src,
                          const int32_t* lora_ids, int topk, int num_experts, int max_loras,
                          int32_t* vtopk_out, int num_vexperts, int32_t* sorted_ids,
-                         int32_t* expert_ids, int32_t* ntpp, void* workspace, bool trigger_early,
+                         int32_t* expert_ids, int32_t* ntpp, void* workspace, int trigger,
                          cudaStream_t stream);
 
 // r1: rank per slice; lora_ranks (per adapter, adapter = v / num_experts, may
@@ -102,11 +104,27 @@ cudaError_t launch_align(const AlignPlan& plan, bool remap, const int32_t* src,
 // the activations after it. The routing is then older than the kernel that
 // precedes the call (or was written by a standalone align, which lets its
 // dependents start only once it has exited).
+// The top-k ids and adapter ids the routing of a mol_lora_forward call is computed
+// from. With ready_early (compute_routing = 2: the ids were complete before the
+// previous kernel began) the shrink that follows the align asks L2 for the lora_a
+// rows of every virtual expert with pairs while the align still runs (see
+// launch_shrink).
+struct RoutingIds {
+  const int32_t* topk_ids;  // [numel]
+  const int32_t* lora_ids;  // [numel / topk]
+  int numel, topk, num_experts, max_loras;
+  bool ready_early;
+};
+// Most pairs, and most bytes of weight rows, for which the shrink prefetches.
+constexpr int kPrefetchPairsMax = 4096;
+constexpr int64_t kPrefetchBudget = 64ll << 20;
+
 cudaError_t launch_shrink(const void* x, int64_t x_stride, int x_div, int K, const void* lora_a,
                           int R, const int32_t* sorted_ids, const int32_t* expert_ids,
                           const int32_t* ntpp, int64_t capacity, int block_m, int64_t numel,
                           int num_vexperts, float* inter, bool early, cudaStream_t stream,
-                          int r1, const int32_t* lora_ranks, int num_experts);
+                          int r1, const int32_t* lora_ranks, int num_experts,
+                          const RoutingIds* prefetch = nullptr);
 
 // early = true only when the preceding kernel is this library's shrink of the
 // same stage (mol_lora_forward): routing, weights and output rows are then read

@@ -140,7 +140,8 @@ lora_shrink_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, 
                    const int* __restrict__ expert_ids, const int* __restrict__ ntpp_ptr,
                    int block_m, int64_t numel, int num_vexperts, float* __restrict__ inter,
                    int n_jt, int64_t n_items, int early, int r1,
-                   const int* __restrict__ lora_ranks, int num_experts, int num_loras) {
+                   const int* __restrict__ lora_ranks, int num_experts, int num_loras,
+                   RoutingIds pf) {
   using namespace sp;
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
@@ -162,6 +163,25 @@ lora_shrink_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, 
   }
   __syncthreads();
   const uint64_t wlim = g_wait_limit_ns;
+  const int64_t G = gridDim.x;
+  // L2 prefetch (pf.topk_ids set: this shrink follows the align of the same call,
+  // whose caller declared the ids complete before the kernel preceding the call
+  // began, so they may be read before any wait). Block b asks L2 for the lora_a
+  // rows of the virtual experts v = b + j * G (j < 32) that have pairs, so the
+  // weight stream from HBM starts while the align still runs and is spread over
+  // every SM's copy engine (one SM's engine alone is far too slow for it).
+  if (pf.topk_ids != nullptr && warp == kConsumers) {
+    const int b = (int)blockIdx.x;
+    unsigned own = 0;
+    for (int i = lane; i < pf.numel; i += 32) {
+      const int v = remap_one(ld_cg_i32(pf.topk_ids + i), ld_cg_i32(pf.lora_ids + i / pf.topk),
+                              pf.num_experts, pf.max_loras);
+      if (v >= 0 && v < num_vexperts && v % G == b) own |= 1u << (v / G);
+    }
+    own = __reduce_or_sync(0xffffffffu, own);
+    if ((own >> lane) & 1u)
+      prefetch_l2(lora_a + (int64_t)(b + lane * G) * R * K, (int64_t)R * K * 2);
+  }
   // The activations may come from the kernel right before this one: only the
   // producer reads global memory, and it reads them after griddepcontrol.wait.
   // With `early` (inside mol_lora_forward, routing reused) routing words and
@@ -175,7 +195,6 @@ lora_shrink_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, 
   if (warp == kConsumers) {
     // ------------------------------------------------------------ producer
     if (g_test_stall & 1u) return;  // test control: nothing is issued, the consumers' waits run out
-    const int64_t G = gridDim.x;
     uint32_t q = 0;   // stage uses issued
     uint32_t jn = 0;  // jobs issued
     bool waited = !early;
@@ -997,7 +1016,8 @@ cudaError_t launch_shrink(const void* x, int64_t x_stride, int x_div, int K, con
                           int R, const int32_t* sorted_ids, const int32_t* expert_ids,
                           const int32_t* ntpp, int64_t capacity, int block_m, int64_t numel,
                           int num_vexperts, float* inter, bool early, cudaStream_t stream,
-                          int r1, const int32_t* lora_ranks, int num_experts) {
+                          int r1, const int32_t* lora_ranks, int num_experts,
+                          const RoutingIds* prefetch) {
   const int64_t nblk = capacity / block_m;
   if (numel == 0 || nblk == 0) return cudaSuccess;
   if (!lora_ranks && shrink_tc_fits(numel, num_vexperts, R, K, block_m))
@@ -1006,13 +1026,21 @@ cudaError_t launch_shrink(const void* x, int64_t x_stride, int x_div, int K, con
   const int n_jt = R / sp::kJT;
   const int num_loras = lora_ranks ? num_vexperts / num_experts : 0;
   const int64_t n_items = nblk * n_jt;
-  const dim3 grid((unsigned)std::min<int64_t>(n_items, (int64_t)device_sms() * sp::kBlocksPerSM));
-  return launch_pdl(lora_ranks ? lora_shrink_kernel<true> : lora_shrink_kernel<false>, grid,
-                    dim3(sp::kThreads), sp::kSmem, stream,
+  const int64_t G = std::min<int64_t>(n_items, (int64_t)device_sms() * sp::kBlocksPerSM);
+  // the L2 prefetch (ids declared ready early): few pairs, every virtual expert owned by one
+  // of 32 slots of a block, and the lora_a rows of as many virtual experts as there can be
+  // pairs within the budget
+  RoutingIds pf{nullptr, nullptr, 0, 1, 1, 1, false};
+  if (prefetch && prefetch->ready_early && prefetch->numel <= kPrefetchPairsMax &&
+      num_vexperts <= 32 * G &&
+      std::min<int64_t>(numel, num_vexperts) * R * K * 2 <= kPrefetchBudget)
+    pf = *prefetch;
+  return launch_pdl(lora_ranks ? lora_shrink_kernel<true> : lora_shrink_kernel<false>,
+                    dim3((unsigned)G), dim3(sp::kThreads), sp::kSmem, stream,
                     static_cast<const uint16_t*>(x), x_stride, x_div, K,
                     static_cast<const uint16_t*>(lora_a), R, sorted_ids, expert_ids, ntpp, block_m,
                     numel, num_vexperts, inter, n_jt, n_items, early ? 1 : 0, r1, lora_ranks,
-                    num_experts < 1 ? 1 : num_experts, num_loras);
+                    num_experts < 1 ? 1 : num_experts, num_loras, pf);
 }
 
 template <int RK, bool EARLY>

@@ -151,6 +151,11 @@ def test_validation_rejects_before_any_launch(mol):
     assert lib.mol_lora_forward(P(16), 64, 1, 64, P(16), P(16), 4, 2, 4096, 2, P(16), P(16), 1, 16, 16,
                                 1.0, None, P(16), 16, 16, 1, P(16), P(16), 4096, P(16), P(16), P(16),
                                 None, None, None, 0, None) == -3
+    # forward: compute_routing outside {0, 1, 2}
+    for mode in (-1, 3):
+        assert lib.mol_lora_forward(P(16), 64, 1, 64, P(16), P(16), 4, 2, 8, 2, P(16), P(16), 1, 16,
+                                    16, 1.0, None, P(16), 16, 16, mode, P(16), P(16), 4096, P(16),
+                                    P(16), P(16), None, None, None, 0, None) == -1
 
 
 def test_binding_fails_loudly_without_library(tmp_path):

@@ -87,7 +87,7 @@ FORWARD_SHAPES = [
 ]
 
 
-def _forward_case(mol, case, dev, routing_override=None):
+def _forward_case(mol, case, dev, routing_override=None, mode=1):
     """Random inputs of one shape; returns (gpu inter, gpu out, oracle inter, oracle out, pairs)."""
     import torch
 
@@ -128,7 +128,7 @@ def _forward_case(mol, case, dev, routing_override=None):
         ws = mol.alloc_workspace(numel, V, BM, dev)
         mol.mol_lora_forward(xd, xdiv, to_dev_i32(topk, dev), to_dev_i32(lora, dev), E, L, Ad, Bd,
                              S, 0.5, out, routing, inter, workspace=ws, lora_ranks=rk_d,
-                             lora_scalings=sc_d)
+                             lora_scalings=sc_d, compute_routing=mode)
     else:
         # the caller's routing: the stage runs on it as given (no align)
         routing = mol.Routing(to_dev_i32(vt, dev), to_dev_i32(s, dev), to_dev_i32(e, dev),
@@ -141,9 +141,11 @@ def _forward_case(mol, case, dev, routing_override=None):
 
 
 @pytest.mark.parametrize("case", FORWARD_SHAPES)
-def test_forward_shapes_pass_every_check(checked, case):
+@pytest.mark.parametrize("mode", [1, 2])
+def test_forward_shapes_pass_every_check(checked, case, mode):
     torch = torch_cuda()
-    g_inter, g_out, ref_inter, ref_out, pairs, _ = _forward_case(checked, case, torch.device("cuda:0"))
+    g_inter, g_out, ref_inter, ref_out, pairs, _ = _forward_case(checked, case, torch.device("cuda:0"),
+                                                                  mode=mode)
     assert_clean(checked)
     check_inter(g_inter, ref_inter, pairs)
     check_out(g_out, ref_out, pairs)

@@ -31,7 +31,8 @@ CASES = [
 
 @pytest.mark.parametrize("case", CASES)
 @pytest.mark.parametrize("use_ws", [True, False])
-def test_forward_paths(case, use_ws):
+@pytest.mark.parametrize("mode", [1, 2])
+def test_forward_paths(case, use_ws, mode):
     torch = torch_cuda()
     mol = mol_lib()
     dev = torch.device("cuda:0")
@@ -65,7 +66,7 @@ def test_forward_paths(case, use_ws):
         out = to_dev_bf16(out0, dev)
         inter = torch.full((numel, R), float("nan"), dtype=torch.float32, device=dev)
         mol.mol_lora_forward(xd, xdiv, to_dev_i32(topk, dev), to_dev_i32(lora, dev), E, L, Ad, Bd, S,
-                             0.5, out, routing, inter, compute_routing=True, topk_weights=wd,
+                             0.5, out, routing, inter, compute_routing=mode, topk_weights=wd,
                              workspace=ws)
         torch.cuda.synchronize()
         assert np.array_equal(routing.sorted_token_ids.cpu().numpy(), s)

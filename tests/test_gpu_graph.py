@@ -14,7 +14,8 @@ from tests.gpu_util import bf16_host, check_out, mol_lib, to_dev_i32, torch_cuda
 pytestmark = pytest.mark.gpu
 
 
-def test_layer_graph_replay_matches_eager():
+@pytest.mark.parametrize("mode", [1, 2])
+def test_layer_graph_replay_matches_eager(mode):
     torch = torch_cuda()
     mol = mol_lib()
     dev = torch.device("cuda:0")
@@ -36,7 +37,7 @@ def test_layer_graph_replay_matches_eager():
             d["out"].copy_(d["out0"])
             mol.mol_lora_forward(d["x"], d["st"].x_row_div, topk, lora, wl.E, wl.L, d["A"], d["B"],
                                  d["st"].stage.S, wl.scale, d["out"], routing, d["inter"],
-                                 compute_routing=(si == 0), workspace=ws)
+                                 compute_routing=(mode if si == 0 else 0), workspace=ws)
 
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())

@@ -19,8 +19,9 @@ from tests.gpu_util import (bf16_host, check_inter, check_out, mol_lib, to_dev_i
 pytestmark = pytest.mark.gpu
 
 
-def run_layer_gpu(wl, li, dev):
-    """All stages of one layer through mol_lora_forward (routing computed by the first stage)."""
+def run_layer_gpu(wl, li, dev, mode=1):
+    """All stages of one layer through mol_lora_forward (routing computed by the first stage,
+    with compute_routing = mode)."""
     import torch
 
     mol = mol_lib()
@@ -36,7 +37,8 @@ def run_layer_gpu(wl, li, dev):
         out = st.out0.to_device(dev)
         inter = torch.full((wl.numel, st.stage.R), float("nan"), dtype=torch.float32, device=dev)
         mol.mol_lora_forward(x, st.x_row_div, topk, lora, wl.E, wl.L, A, B, st.stage.S, wl.scale,
-                             out, routing, inter, compute_routing=(si == 0), workspace=ws)
+                             out, routing, inter, compute_routing=(mode if si == 0 else 0),
+                             workspace=ws)
         torch.cuda.synchronize()
         res.append((inter.cpu().numpy(), bf16_host(out)))
         del x, A, B, out, inter
@@ -58,12 +60,15 @@ def check_routing(wl, li, rt):
 
 @pytest.mark.parametrize("name", ["tiny", "decode", "wide", "wide1k"])
 @pytest.mark.parametrize("seed", [0, 1, 2, 3, 4])
-def test_full_parity_small(name, seed):
+@pytest.mark.parametrize("mode", [1, 2])
+def test_full_parity_small(name, seed, mode):
+    """mode 2: the ids are declared ready early; at these sizes the shrink computes its own
+    items' routing from them (the align still writes the routing the other kernels read)."""
     torch = torch_cuda()
     dev = torch.device("cuda:0")
     wl = WORKLOADS[name]
     li = make_layer(wl, seed)
-    rt, res = run_layer_gpu(wl, li, dev)
+    rt, res = run_layer_gpu(wl, li, dev, mode)
     s, e, n = check_routing(wl, li, rt)
     pairs = valid_pairs(s, e, n, wl.BM, wl.numel)
     others = np.setdiff1d(np.arange(wl.numel), pairs)
