@@ -258,12 +258,14 @@ int32_t mol_lora_expand(const float* inter, const void* lora_b, int32_t num_slic
  * call's first kernel starts (true unless the kernel just before the call
  * lets its dependents start early, before writing them). compute_routing = 2
  * computes the routing like 1 and declares that topk_ids and lora_ids were
- * complete before the kernel just before the call began (in a MoE layer the
- * router's top-k runs before the expert GEMMs that precede the LoRA stage):
- * the shrink may then start, and ask L2 for the weight rows the ids select,
- * while that kernel and the align still run. With 1 the ids may come from the
- * kernel just before the call. lora_ranks and lora_scalings (each NULL or one
- * entry per adapter) are those of the shrink and the expand.
+ * complete before the kernel just before the call on `stream` began, or that
+ * the call is ordered after their writer by an event or a copy on `stream` (in
+ * a MoE layer the router's top-k runs before the expert GEMMs that precede the
+ * LoRA stage): the align then counts the pairs, and the shrink starts and asks
+ * L2 for the weight rows the ids select, while that kernel still runs. With 1
+ * the ids may come from the kernel just before the call; both give the same
+ * results. lora_ranks and lora_scalings (each NULL or one entry per adapter)
+ * are those of the shrink and the expand.
  * compute_routing outside {0, 1, 2} is MOL_ERR_INVALID_ARG.
  */
 int32_t mol_lora_forward(const void* x, int64_t x_row_stride, int32_t x_row_div, int32_t K,
