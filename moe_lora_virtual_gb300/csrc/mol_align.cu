@@ -229,18 +229,7 @@ align_tile_kernel(const int* __restrict__ src, const int* __restrict__ lora_ids,
   uint16_t* mine = tbl + warp * nb_pad;
   // Keys, per-warp counts, the tile's bucket counts and (one tile) the bucket
   // offsets: in shared memory only, from the ids.
-  auto count_tile = [&](bool write_vtopk) {
-    for (int q = tid; q < tlen; q += kAlignThreads) {
-      const int64_t i = t0 + q;
-      int vid;
-      if (REMAP) {
-        vid = remap_one(src[i], lora_ids[i / topk], num_experts, max_loras);
-        if (write_vtopk) vtopk_out[i] = vid;
-      } else {
-        vid = src[i];
-      }
-      keys[q] = (uint16_t)bucket_of(vid, num_vexperts);
-    }
+  auto count_keys = [&]() {
     __syncthreads();
     warp_count(keys, s0, s1, mine, lane);  // pass 1: per-warp counts over the warp's segment
     __syncthreads();
@@ -256,11 +245,23 @@ align_tile_kernel(const int* __restrict__ src, const int* __restrict__ lora_ids,
     __syncthreads();
   };
   // trigger = 2, one tile: the ids are older than the previous kernel, so all of
-  // that runs before the wait; only the writes wait.
+  // that runs before the wait; only the writes wait (the virtual ids stay in
+  // registers until then: one tile holds at most kTileMin pairs).
   const bool ids_early = trigger == 2 && fused;
   int total = 0;
+  int vkeep[kTileMin / kAlignThreads];
   if (ids_early) {
-    count_tile(false);
+#pragma unroll
+    for (int j = 0; j < kTileMin / kAlignThreads; ++j) {
+      const int q = tid + j * kAlignThreads;
+      vkeep[j] = 0;
+      if (q < tlen) {
+        const int64_t i = t0 + q;
+        vkeep[j] = REMAP ? remap_one(src[i], lora_ids[i / topk], num_experts, max_loras) : src[i];
+        keys[q] = (uint16_t)bucket_of(vkeep[j], num_vexperts);
+      }
+    }
+    count_keys();
     total = bucket_scan<kAlignThreads>(offs, nb, block_m, sh_scan);
     __syncthreads();  // every bucket's offset is in place
   }
@@ -274,16 +275,29 @@ align_tile_kernel(const int* __restrict__ src, const int* __restrict__ lora_ids,
   if ((int)blockIdx.x >= tiles) return;  // fill-only block
 
   if (ids_early) {
-    if (REMAP)
-      for (int q = tid; q < tlen; q += kAlignThreads) {
-        const int64_t i = t0 + q;
-        vtopk_out[i] = remap_one(src[i], lora_ids[i / topk], num_experts, max_loras);
+    if (REMAP) {
+#pragma unroll
+      for (int j = 0; j < kTileMin / kAlignThreads; ++j) {
+        const int q = tid + j * kAlignThreads;
+        if (q < tlen) vtopk_out[t0 + q] = vkeep[j];
       }
+    }
     write_blocks<kAlignThreads>(offs, nb, num_vexperts, block_m, capacity, total, expert_ids,
                                 ntpp_out);
     __syncthreads();  // the padding fill lands before the scatter overwrites it
   } else {
-    count_tile(true);
+    for (int q = tid; q < tlen; q += kAlignThreads) {
+      const int64_t i = t0 + q;
+      int vid;
+      if (REMAP) {
+        vid = remap_one(src[i], lora_ids[i / topk], num_experts, max_loras);
+        vtopk_out[i] = vid;
+      } else {
+        vid = src[i];
+      }
+      keys[q] = (uint16_t)bucket_of(vid, num_vexperts);
+    }
+    count_keys();
     if (fused)
       bucket_offsets<kAlignThreads>(offs, nb, num_vexperts, block_m, capacity, expert_ids,
                                     ntpp_out, sh_scan);
