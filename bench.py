@@ -7,10 +7,10 @@ reusing the routing. The workload is the bs=23 decode configuration (23
 tokens, 128 experts x 8 adapters = 1024 virtual experts, top-8, rank 32,
 gate_up 2048 -> 2x32 -> 2x768, down 768 -> 32 -> 2048), synthetic seeded data.
 
-The first stage computes the routing with compute_routing = 2 (--routing-mode):
-the top-k and adapter ids are ready before the kernel that precedes the layer,
-as when the router ran earlier in the MoE layer; the line also reports the
-layer time with mode 1 (ids that may come from the preceding kernel).
+The first stage computes the routing with compute_routing = 1 (--routing-mode):
+the top-k and adapter ids may come from the kernel that precedes the layer; the
+line also reports the layer time with mode 2 (ids declared ready before that
+kernel, as when the router ran earlier in the MoE layer).
 
 Steps rotate over --layers distinct layers (own weights, routing and
 activations) so that a step never finds its weights in L2: 8 decode layers
@@ -56,10 +56,10 @@ def parse_args(argv=None):
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--ranks", default=None,
                    help="per-adapter ranks, comma separated (one per adapter; scaling 16/rank)")
-    p.add_argument("--routing-mode", type=int, choices=[1, 2], default=2,
-                   help="compute_routing of each layer's first stage: 2 = the top-k and adapter "
-                        "ids are ready before the kernel preceding the layer (as after a router "
-                        "that ran earlier in the layer), 1 = they may come from that kernel")
+    p.add_argument("--routing-mode", type=int, choices=[1, 2], default=1,
+                   help="compute_routing of each layer's first stage: 1 = the top-k and adapter "
+                        "ids may come from the kernel preceding the layer, 2 = they are ready "
+                        "before it (as after a router that ran earlier in the layer)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--no-kernels", action="store_true", help="skip the per-kernel timing phase")
@@ -162,7 +162,7 @@ class LayerState:
     """Device tensors of one layer: routing, workspace, per-stage inputs and outputs."""
 
     # compute_routing of the first stage (the others reuse its routing)
-    routing_mode = 2
+    routing_mode = 1
 
     def __init__(self, wl, li, dev, mol, torch, ranks=None):
         self.wl, self.li = wl, li
