@@ -15,7 +15,7 @@ LIB_PATH = os.path.join(PKG_DIR, "libmol.so")
 CHECKED_LIB_PATH = os.path.join(PKG_DIR, "libmol_checked.so")
 
 SOURCES = ["mol_abi.cu", "mol_align.cu", "mol_lora.cu", "mol_umma.cu", "mol_stage.cu"]
-HEADERS = ["mol_device.cuh", "mol_internal.h"]
+HEADERS = ["mol_device.cuh", "mol_internal.h", "mol_tc.cuh"]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -36,14 +36,12 @@
 // MMAs. Every wait is bounded: a timeout sets a fault bit, the roles leave
 // their loops, and the tensor memory is freed before the block exits.
 
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
 #include <algorithm>
 #include <mutex>
 
 #include "mol_device.cuh"
 #include "mol_internal.h"
+#include "mol_tc.cuh"
 
 namespace mol {
 
@@ -74,80 +72,6 @@ cudaError_t take_tc_faults(unsigned* out) {
   const unsigned zero = 0;
   return cudaMemcpyToSymbol(g_tc_fault_flags, &zero, sizeof(unsigned));
 }
-
-// --- tcgen05 / TMA helpers (inline PTX) ------------------------------------
-
-// Shared-memory matrix descriptor: K-major operand in 8-row groups of 128-byte
-// rows with the 128-byte swizzle, groups 1024 bytes apart.
-MOL_DEV uint64_t sw128_desc(uint32_t saddr) {
-  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);  // start address, 16-byte units
-  d |= (uint64_t)1 << 16;                            // leading byte offset (unused when swizzled)
-  d |= (uint64_t)(1024 >> 4) << 32;                  // stride byte offset: next 8-row group
-  d |= (uint64_t)1 << 46;                            // descriptor version of tcgen05
-  d |= (uint64_t)2 << 61;                            // 128-byte swizzle
-  return d;
-}
-MOL_DEV void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
-      : "memory");
-}
-// Arrives on `bar` once every cp.async this thread issued so far has landed
-// (the barrier's expected count includes this arrival).
-MOL_DEV void cp_async_arrive_noinc(uint64_t* bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
-}
-MOL_DEV void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-MOL_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-MOL_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-MOL_DEV void tmem_alloc(uint32_t* slot, uint32_t ncols) {  // whole warp
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                   smem_u32(slot)),
-               "r"(ncols)
-               : "memory");
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-MOL_DEV void tmem_dealloc(uint32_t taddr, uint32_t ncols) {  // whole warp
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-               : "memory");
-}
-MOL_DEV void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                       uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-MOL_DEV void umma_commit(uint64_t* bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          smem_u32(bar))
-      : "memory");
-}
-MOL_DEV void tmem_ld8(uint32_t taddr, float (&v)[8]) {
-  uint32_t r[8];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7])
-      : "r"(taddr)
-      : "memory");
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// Instruction descriptor of kind::f16: fp32 D, bf16 A and B, both K-major,
-// N = BN, M = 128.
-template <int BN>
-struct IDesc {
-  static constexpr uint32_t kValue = (1u << 4) | (1u << 7) | (1u << 10) |
-                                     ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(tc::kM >> 4) << 24);
-};
 
 template <int BN>
 __global__ void __launch_bounds__(tc::kThreads, tc::Geo<BN>::kBlocksPerSM)
@@ -244,7 +168,7 @@ lora_shrink_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = IDesc<BN>::kValue;
+      constexpr uint32_t idesc = IDesc<tc::kM, BN>::kValue;
       uint32_t q = 0, n = 0;
       for (int64_t it = blockIdx.x; it < n_items && !fault; it += Gs) {
         int64_t t;
