@@ -14,7 +14,8 @@ LIB_PATH = os.path.join(PKG_DIR, "libmol.so")
 # The same sources with device-side index checks (MOL_CHECKED): a diagnostic build.
 CHECKED_LIB_PATH = os.path.join(PKG_DIR, "libmol_checked.so")
 
-SOURCES = ["mol_abi.cu", "mol_align.cu", "mol_lora.cu", "mol_umma.cu", "mol_stage.cu"]
+SOURCES = ["mol_abi.cu", "mol_align.cu", "mol_lora.cu", "mol_umma.cu", "mol_stage.cu",
+           "mol_expand_tc.cu"]
 HEADERS = ["mol_device.cuh", "mol_internal.h", "mol_tc.cuh"]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -172,12 +172,13 @@ int32_t mol_take_fault_flags(uint32_t* flags) {
   if (st != MOL_OK) return st;
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cuda_fail(e);
-  unsigned a = 0, b = 0, c = 0;
+  unsigned a = 0, b = 0, c = 0, d = 0;
   e = mol::take_lora_faults(&a);
   if (e == cudaSuccess) e = mol::take_tc_faults(&b);
   if (e == cudaSuccess) e = mol::take_stage_faults(&c);
+  if (e == cudaSuccess) e = mol::take_expand_tc_faults(&d);
   if (e != cudaSuccess) return cuda_fail(e);
-  *flags = a | b | c;
+  *flags = a | b | c | d;
   return MOL_OK;
 }
 
@@ -203,10 +204,11 @@ int32_t mol_take_check_record(uint64_t* first, uint64_t* count) {
   if (st != MOL_OK) return st;
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cuda_fail(e);
-  // in the path's order: align, item shrink and expands, tcgen05 shrink, fused stage
-  cudaError_t (*const take[4])(unsigned long long*, unsigned long long*) = {
+  // in the path's order: align, item shrink and expands, tcgen05 shrink, fused stage,
+  // tcgen05 expand
+  cudaError_t (*const take[5])(unsigned long long*, unsigned long long*) = {
       mol::take_align_checks, mol::take_lora_checks, mol::take_tc_checks,
-      mol::take_stage_checks};
+      mol::take_stage_checks, mol::take_expand_tc_checks};
   unsigned long long f = 0, n = 0;
   for (auto fn : take) {
     unsigned long long fi = 0, ni = 0;

@@ -131,6 +131,18 @@ MOL_DEV void mbar_arrive(uint64_t* bar) {
 MOL_DEV void named_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
+// Barrier `id` among `threads` threads that also ANDs a predicate over them:
+// every participant returns true only if every participant passed true.
+MOL_DEV bool named_sync_and(int id, int threads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, %2, %3, p;\n"
+      " selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(threads)
+      : "memory");
+  return r != 0;
+}
 MOL_DEV uint4 lds16(const void* p) { return *reinterpret_cast<const uint4*>(p); }
 MOL_DEV uint2 lds8(const void* p) { return *reinterpret_cast<const uint2*>(p); }
 // 16-byte copy global -> shared through L2 (cp.async): src_bytes of 16 are

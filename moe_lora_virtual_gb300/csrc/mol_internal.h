@@ -152,6 +152,17 @@ cudaError_t launch_shrink_tc(const void* x, int64_t x_stride, int x_div, int K, 
                              const int32_t* ntpp, int64_t capacity, int block_m, int64_t numel,
                              int num_vexperts, float* inter, cudaStream_t stream);
 
+// The expand of full routed blocks of rank 64 on tcgen05 (many rows per virtual
+// expert, no adapter arrays, Ns a multiple of 128, BLOCK_M 64 or 128).
+bool expand_tc_fits(int64_t numel, int num_vexperts, int r, int Ns, int block_m,
+                    int64_t out_stride, bool adapter_arrays);
+cudaError_t prepare_expand_tc_kernels();
+cudaError_t launch_expand_tc(const float* inter, const void* lora_b, int S, int Ns, float scale,
+                             const float* topk_weights, const int32_t* sorted_ids,
+                             const int32_t* expert_ids, const int32_t* ntpp, int64_t capacity,
+                             int block_m, int64_t numel, int num_vexperts, void* out,
+                             int64_t out_stride, cudaStream_t stream);
+
 // One stage fused into one launch (shrink then expand per routed block, the
 // block's intermediate kept in shared memory and also stored): for small
 // layers (every routed block on an SM of its own, a virtual expert's weights
@@ -174,6 +185,7 @@ cudaError_t take_stage_faults(unsigned* out);
 // ran out); read and cleared by mol_take_fault_flags.
 cudaError_t take_lora_faults(unsigned* out);
 cudaError_t take_tc_faults(unsigned* out);
+cudaError_t take_expand_tc_faults(unsigned* out);
 // Check records of the checked build, per kernel file (read and cleared; zero
 // in the release build): the first failed check's (site << 48 | value) and the
 // number of failed checks.
@@ -181,6 +193,7 @@ cudaError_t take_align_checks(unsigned long long* first, unsigned long long* cou
 cudaError_t take_lora_checks(unsigned long long* first, unsigned long long* count);
 cudaError_t take_tc_checks(unsigned long long* first, unsigned long long* count);
 cudaError_t take_stage_checks(unsigned long long* first, unsigned long long* count);
+cudaError_t take_expand_tc_checks(unsigned long long* first, unsigned long long* count);
 // Test controls of the shrink's bounded waits (mol_debug_wait_test).
 cudaError_t set_wait_test(unsigned stall, unsigned long long limit_ns);
 

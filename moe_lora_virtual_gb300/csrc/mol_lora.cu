@@ -989,6 +989,8 @@ static cudaError_t prepare_expand_st() {
 cudaError_t prepare_lora_kernels() {
   cudaError_t e = prepare_tc_kernels();
   if (e != cudaSuccess) return e;
+  e = prepare_expand_tc_kernels();
+  if (e != cudaSuccess) return e;
   e = prepare_expand_st<64, true>();
   if (e != cudaSuccess) return e;
   e = prepare_expand_st<64, false>();
@@ -1068,6 +1070,10 @@ cudaError_t launch_expand(const float* inter, const void* lora_b, int S, int r, 
   const int R = S * r;
   const uint16_t* b = static_cast<const uint16_t*>(lora_b);
   uint16_t* o = static_cast<uint16_t*>(out);
+  if (expand_tc_fits(numel, num_vexperts, r, Ns, block_m, out_stride,
+                     lora_ranks != nullptr || lora_scalings != nullptr))
+    return launch_expand_tc(inter, lora_b, S, Ns, scale, topk_weights, sorted_ids, expert_ids, ntpp,
+                            capacity, block_m, numel, num_vexperts, out, out_stride, stream);
   if (r == 8 || r == 16 || r == 32 || r == 64) {
     const int cps_st = (Ns + kStCols - 1) / kStCols;
     if (nblk * S * cps_st > INT32_MAX) return cudaErrorInvalidConfiguration;
