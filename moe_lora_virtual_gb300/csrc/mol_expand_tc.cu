@@ -59,13 +59,14 @@ constexpr int kMGroup = 8;     // m-tiles per item
 constexpr int kBTile = kM * kRank * 2;        // 16 KB lora_b tile
 constexpr int kATile = kRows * kRank * 2;     // 16 KB head (or tail) operand
 constexpr int kConverters = 128;              // warps 2-5
-constexpr int kCopiers = 64;                  // warps 6-7
-constexpr int kEpiWarps = 8;                  // warps 8-15
-constexpr int kThreads = (8 + kEpiWarps) * 32;
+constexpr int kCopiers = 128;                 // warps 6-9
+constexpr int kEpiWarps = 8;                  // warps 10-17
+constexpr int kThreads = (10 + kEpiWarps) * 32;
 constexpr uint32_t kPolls = 1u << 22;
 constexpr int kOutPitch = kM * 2 + 16;  // staged output row: 256 bytes + a 16-byte skew
 constexpr int round1k(int b) { return (b + 1023) / 1024 * 1024; }
 constexpr int kBStages = 3;  // lora_b tiles in flight
+constexpr int kAccs = 2;     // accumulators in tensor memory (256 of the 512 columns)
 template <int BN>
 struct Geo {
   static constexpr int kOStages = BN == 64 ? 6 : 3;  // staged output-row tiles in flight
@@ -73,7 +74,7 @@ struct Geo {
   static constexpr int kABytes = 2 * kATile;  // head + tail
   static constexpr size_t kSmem = 1024 + (size_t)kBStages * kBTile + (size_t)kOStages * kOTile +
                                   2 * (size_t)kABytes;
-  static constexpr uint32_t kTmemCols = 2 * kM;
+  static constexpr uint32_t kTmemCols = kAccs * kM;
 };
 }  // namespace xt
 
@@ -100,8 +101,8 @@ lora_expand_tc_kernel(const __grid_constant__ CUtensorMap tmap_b, const float* _
   extern __shared__ unsigned char smem_raw[];
   // lora_b ring (TMA -> MMA), output-row ring (copiers -> epilogue), accumulators,
   // operand buffers
-  __shared__ uint64_t wfull[NB], wempty[NB], ofull[NO], oempty[NO], accf[2], acce[2], bfull[2],
-      bempty[2];
+  __shared__ uint64_t wfull[NB], wempty[NB], ofull[NO], oempty[NO], accf[kAccs], acce[kAccs],
+      bfull[2], bempty[2];
   __shared__ uint32_t tmem_slot;
   __shared__ int m_pid[2][BN];  // per operand buffer: pair of each row, -1 for padding
   __shared__ float m_w[2][BN];  // and its scale * routed weight
@@ -121,9 +122,11 @@ lora_expand_tc_kernel(const __grid_constant__ CUtensorMap tmap_b, const float* _
       mbar_init(&ofull[s], kCopiers);   // every copier thread
       mbar_init(&oempty[s], kEpiWarps);  // every epilogue warp
     }
-    for (int a = 0; a < 2; ++a) {
+    for (int a = 0; a < kAccs; ++a) {
       mbar_init(&accf[a], 1);
       mbar_init(&acce[a], kEpiWarps);
+    }
+    for (int a = 0; a < 2; ++a) {
       mbar_init(&bfull[a], kConverters);
       mbar_init(&bempty[a], 1 + kEpiWarps);  // MMA commit + every epilogue warp
     }
@@ -210,8 +213,8 @@ lora_expand_tc_kernel(const __grid_constant__ CUtensorMap tmap_b, const float* _
         }
         for (int m = m0; m < m1; ++m, ++q, ++n) {
           const int st = (int)(q % NB);
-          const int a = (int)(n & 1);
-          if (!mbar_wait(&acce[a], ((n >> 1) & 1) ^ 1, kPolls) ||
+          const int a = (int)(n % kAccs);
+          if (!mbar_wait(&acce[a], ((n / kAccs) & 1) ^ 1, kPolls) ||
               !mbar_wait(&wfull[st], (q / NB) & 1, kPolls)) {
             fault = true;
             break;
@@ -284,9 +287,13 @@ lora_expand_tc_kernel(const __grid_constant__ CUtensorMap tmap_b, const float* _
       fence_proxy_async_smem();  // generic writes, read next through the async proxy
       mbar_arrive(&bfull[j]);
     }
-  } else if (warp < 8) {
+  } else if (warp < 10) {
     // ------------------------------------------------------------ copiers
     const int l = tid - 192;  // 0 .. kCopiers-1
+    // a copier always moves 16-byte chunk c of rows r0, r0 + kRowStep, ... of an m-tile
+    constexpr int kRowStep = kCopiers / 16, kMine = BN / kRowStep;
+    const int c = l & 15, r0 = l >> 4;
+    const uint16_t* src[kMine];  // per run: the rows' first output column of the slice
     uint32_t q = 0, rn = 0;
     int64_t key = -1;
     int j = 0;
@@ -302,6 +309,11 @@ lora_expand_tc_kernel(const __grid_constant__ CUtensorMap tmap_b, const float* _
           break;
         }
         ++rn;
+#pragma unroll
+        for (int i = 0; i < kMine; ++i) {
+          const int pid = m_pid[j][r0 + i * kRowStep];
+          src[i] = pid >= 0 ? out + (int64_t)pid * out_stride + (int64_t)s * Ns + c * 8 : nullptr;
+        }
       }
       // output rows of each m-tile: BN rows x 256 bytes, 16 chunks of 16 bytes per row
       for (int m = m0; m < m1 && !fault; ++m, ++q) {
@@ -310,15 +322,11 @@ lora_expand_tc_kernel(const __grid_constant__ CUtensorMap tmap_b, const float* _
           fault = true;
           break;
         }
-        unsigned char* ot = otile(q);
-        const int64_t col = (int64_t)s * Ns + (int64_t)m * kM;
-#pragma unroll 4
-        for (int k = l; k < BN * 16; k += kCopiers) {
-          const int r = k >> 4, c = k & 15;
-          const int pid = m_pid[j][r];
-          const uint16_t* src = out + (pid >= 0 ? (int64_t)pid * out_stride : 0) + col + c * 8;
-          cp_async16_zfill(ot + r * kOutPitch + c * 16, src, pid >= 0 ? 16u : 0u);
-        }
+        unsigned char* ot = otile(q) + r0 * kOutPitch + c * 16;
+#pragma unroll
+        for (int i = 0; i < kMine; ++i)
+          cp_async16_zfill(ot + i * kRowStep * kOutPitch, src[i] ? src[i] + m * kM : out,
+                           src[i] ? 16u : 0u);
         cp_async_arrive_noinc(&ofull[st]);
       }
     }
@@ -326,7 +334,7 @@ lora_expand_tc_kernel(const __grid_constant__ CUtensorMap tmap_b, const float* _
   } else {
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;             // tensor-memory lanes 32*quarter .. +31 = rows
-    const int half = (warp - 8) >> 2;         // output columns [64 * half, 64 * half + 64)
+    const int half = (warp - 10) >> 2;        // output columns [64 * half, 64 * half + 64)
     const int r = quarter * 32 + lane;        // this thread's row of the block
     const bool has_rows = quarter * 32 < BN;  // BLOCK_M 64: two quarters hold no row
     uint32_t q = 0, n = 0, rn = 0;
@@ -351,9 +359,9 @@ lora_expand_tc_kernel(const __grid_constant__ CUtensorMap tmap_b, const float* _
       }
       for (int m = m0; m < m1; ++m, ++q, ++n) {
         const int st = (int)(q % NO);
-        const int a = (int)(n & 1);
+        const int a = (int)(n % kAccs);
         // tcgen05.ld is warp-collective: the lanes agree on the outcome of the waits
-        if (!__all_sync(0xffffffffu, mbar_wait(&accf[a], (n >> 1) & 1, kPolls) &&
+        if (!__all_sync(0xffffffffu, mbar_wait(&accf[a], (n / kAccs) & 1, kPolls) &&
                                          mbar_wait(&ofull[st], (q / NO) & 1, kPolls))) {
           fault = true;
           break;
