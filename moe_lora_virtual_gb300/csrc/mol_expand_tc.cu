@@ -67,15 +67,12 @@ constexpr int kOutPitch = kM * 2 + 16;  // staged output row: 256 bytes + a 16-b
 constexpr int round1k(int b) { return (b + 1023) / 1024 * 1024; }
 constexpr int kBStages = 3;  // lora_b tiles in flight
 constexpr int kAccs = 2;     // accumulators in tensor memory (256 of the 512 columns)
-template <int BN>
-struct Geo {
-  static constexpr int kOStages = BN == 64 ? 6 : 3;  // staged output-row tiles in flight
-  static constexpr int kOTile = round1k(BN * kOutPitch);
-  static constexpr int kABytes = 2 * kATile;  // head + tail
-  static constexpr size_t kSmem = 1024 + (size_t)kBStages * kBTile + (size_t)kOStages * kOTile +
-                                  2 * (size_t)kABytes;
-  static constexpr uint32_t kTmemCols = kAccs * kM;
-};
+constexpr int kOStages = 3;                        // staged output-row tiles in flight
+constexpr int kOTile = round1k(kRows * kOutPitch);
+constexpr int kABytes = 2 * kATile;  // head + tail
+constexpr size_t kSmem =
+    1024 + (size_t)kBStages * kBTile + (size_t)kOStages * kOTile + 2 * (size_t)kABytes;
+constexpr uint32_t kTmemCols = kAccs * kM;
 }  // namespace xt
 
 __device__ unsigned int g_xt_fault_flags;
@@ -93,24 +90,23 @@ lora_expand_tc_kernel(const __grid_constant__ CUtensorMap tmap_b, const float* _
                       int R, int S, int Ns, float scale, const float* __restrict__ topk_w,
                       const int* __restrict__ sorted_ids, const int* __restrict__ expert_ids,
                       const int* __restrict__ ntpp_ptr, int64_t numel, int num_vexperts,
-                      uint16_t* __restrict__ out, int64_t out_stride, int64_t n_items, int mgroups,
+                      uint16_t* __restrict__ out, int64_t out_stride, int64_t nblk, int mgroups,
                       int mtiles) {
   using namespace xt;
-  using G = Geo<BN>;
-  constexpr int NB = kBStages, NO = G::kOStages;
+  constexpr int NB = kBStages, NO = kOStages;
   extern __shared__ unsigned char smem_raw[];
   // lora_b ring (TMA -> MMA), output-row ring (copiers -> epilogue), accumulators,
   // operand buffers
   __shared__ uint64_t wfull[NB], wempty[NB], ofull[NO], oempty[NO], accf[kAccs], acce[kAccs],
       bfull[2], bempty[2];
   __shared__ uint32_t tmem_slot;
-  __shared__ int m_pid[2][BN];  // per operand buffer: pair of each row, -1 for padding
-  __shared__ float m_w[2][BN];  // and its scale * routed weight
+  __shared__ int m_pid[2][kRows];  // per operand buffer: pair of each row, -1 for none
+  __shared__ float m_w[2][kRows];  // and its scale * routed weight
   unsigned char* smem =
       smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // 1024-byte aligned
   unsigned char* wbuf = smem;                                  // lora_b tiles
   unsigned char* obuf = wbuf + (size_t)NB * kBTile;             // staged output rows
-  unsigned char* abuf = obuf + (size_t)NO * G::kOTile;          // two head + tail buffers
+  unsigned char* abuf = obuf + (size_t)NO * kOTile;             // two head + tail buffers
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
   if (tid == 0) {
@@ -132,7 +128,7 @@ lora_expand_tc_kernel(const __grid_constant__ CUtensorMap tmap_b, const float* _
     }
     fence_mbar_init();
   }
-  if (warp == 1) tmem_alloc(&tmem_slot, G::kTmemCols);
+  if (warp == 1) tmem_alloc(&tmem_slot, kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -142,33 +138,63 @@ lora_expand_tc_kernel(const __grid_constant__ CUtensorMap tmap_b, const float* _
 
   const int ntpp = __ldg(ntpp_ptr);
   const int per = S * mgroups;
-  // block b takes a contiguous range of the items of the routed blocks below ntpp, so
-  // consecutive items share their routed block and slice (one conversion for them all)
-  const int64_t n_eff = min(n_items, (int64_t)((max(ntpp, 0) + BN - 1) / BN) * per);
-  const int64_t it0 = n_eff * blockIdx.x / gridDim.x, it1 = n_eff * (blockIdx.x + 1) / gridDim.x;
-  // item -> routed block, slice, m-tiles [m0, m1); false when the block has no expert
-  auto item = [&](int64_t it, int64_t& t, int& s, int& m0, int& m1, int& v) -> bool {
-    t = it / per;
-    const int rem = (int)(it - t * per);
+  // Units: routed blocks (BLOCK_M 128) or pairs of routed blocks (BLOCK_M 64). A unit
+  // is one 128-row sub-unit (a block, or a pair whose two blocks have the same
+  // virtual expert) or two 64-row ones (the blocks of a pair on their own). Block b
+  // of the grid takes a contiguous range of the units (times slices and m-tile
+  // groups) below ntpp, so consecutive items share their rows and slice: one
+  // conversion of the intermediate serves them all.
+  constexpr int kPer = kRows / BN;  // routed blocks per unit
+  const int64_t nunits = (nblk + kPer - 1) / kPer;
+  const int64_t ueff = min(nunits, (int64_t)((max(ntpp, 0) + kRows - 1) / kRows));
+  const int64_t it0 = ueff * per * blockIdx.x / gridDim.x,
+                it1 = ueff * per * (blockIdx.x + 1) / gridDim.x;
+  // work x (2 per item: item x / 2, sub-unit x % 2) -> its first routing slot, slice,
+  // m-tiles [m0, m1), rows and virtual expert; false when there is no such sub-unit
+  auto work = [&](int64_t x, int64_t& slot0, int& s, int& m0, int& m1, int& nrows,
+                  int& v) -> bool {
+    const int64_t it = x >> 1;
+    const int k = (int)(x & 1);
+    const int64_t u = it / per;
+    const int rem = (int)(it - u * per);
     s = rem / mgroups;
     m0 = (rem - s * mgroups) * kMGroup;
     m1 = min(m0 + kMGroup, mtiles);
-    if (t * BN >= ntpp) return false;
-    v = __ldg(expert_ids + t);
-    return v >= 0 && v < num_vexperts;
+    auto block = [&](int64_t t) -> int {  // expert of routed block t, -1 if none
+      if (t >= nblk || t * BN >= ntpp) return -1;
+      const int e = __ldg(expert_ids + t);
+      return e >= 0 && e < num_vexperts ? e : -1;
+    };
+    if (kPer == 1) {
+      v = block(u);
+      slot0 = u * BN;
+      nrows = BN;
+      return k == 0 && v >= 0;
+    }
+    const int e0 = block(2 * u), e1 = block(2 * u + 1);
+    if (e0 >= 0 && e0 == e1) {  // one 128-row sub-unit
+      v = e0;
+      slot0 = 2 * u * BN;
+      nrows = 2 * BN;
+      return k == 0;
+    }
+    v = k ? e1 : e0;
+    slot0 = (2 * u + k) * BN;
+    nrows = BN;
+    return v >= 0;
   };
   auto wtile = [&](uint32_t q) { return wbuf + (size_t)(q % NB) * kBTile; };
-  auto otile = [&](uint32_t q) { return obuf + (size_t)(q % NO) * G::kOTile; };
+  auto otile = [&](uint32_t q) { return obuf + (size_t)(q % NO) * kOTile; };
   bool fault = false;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       uint32_t q = 0;
-      for (int64_t it = it0; it < it1 && !fault; ++it) {
-        int64_t t;
-        int s, m0, m1, v;
-        if (!item(it, t, s, m0, m1, v)) continue;
+      for (int64_t x = 2 * it0; x < 2 * it1 && !fault; ++x) {
+        int64_t slot0;
+        int s, m0, m1, nrows, v;
+        if (!work(x, slot0, s, m0, m1, nrows, v)) continue;
         for (int m = m0; m < m1; ++m, ++q) {
           const int st = (int)(q % NB);
           if (!mbar_wait(&wempty[st], ((q / NB) & 1) ^ 1, kPolls)) {
@@ -195,20 +221,20 @@ lora_expand_tc_kernel(const __grid_constant__ CUtensorMap tmap_b, const float* _
       int64_t key = -1;
       int j = 0;
       uint32_t ah = 0, at = 0;
-      for (int64_t it = it0; it < it1 && !fault; ++it) {
-        int64_t t;
-        int s, m0, m1, v;
-        if (!item(it, t, s, m0, m1, v)) continue;
-        if (t * S + s != key) {  // a new run: its operand buffer
+      for (int64_t x = 2 * it0; x < 2 * it1 && !fault; ++x) {
+        int64_t slot0;
+        int s, m0, m1, nrows, v;
+        if (!work(x, slot0, s, m0, m1, nrows, v)) continue;
+        if (slot0 * S + s != key) {  // a new run: its operand buffer
           if (key >= 0) umma_commit(&bempty[j]);  // the last run's buffer, once its MMAs are done
-          key = t * S + s;
+          key = slot0 * S + s;
           j = (int)(rn & 1);
           if (!mbar_wait(&bfull[j], (rn >> 1) & 1, kPolls)) {
             fault = true;
             break;
           }
           ++rn;
-          ah = smem_u32(abuf + (size_t)j * G::kABytes);
+          ah = smem_u32(abuf + (size_t)j * kABytes);
           at = ah + kATile;
         }
         for (int m = m0; m < m1; ++m, ++q, ++n) {
@@ -242,12 +268,12 @@ lora_expand_tc_kernel(const __grid_constant__ CUtensorMap tmap_b, const float* _
     const int l = tid - 64;  // 0 .. kConverters-1
     uint32_t rn = 0;
     int64_t key = -1;
-    for (int64_t it = it0; it < it1 && !fault; ++it) {
-      int64_t t;
-      int s, m0, m1, v;
-      if (!item(it, t, s, m0, m1, v)) continue;
-      if (t * S + s == key) continue;  // the run's operands are in place already
-      key = t * S + s;
+    for (int64_t x = 2 * it0; x < 2 * it1 && !fault; ++x) {
+      int64_t slot0;
+      int s, m0, m1, nrows, v;
+      if (!work(x, slot0, s, m0, m1, nrows, v)) continue;
+      if (slot0 * S + s == key) continue;  // the run's operands are in place already
+      key = slot0 * S + s;
       const int j = (int)(rn & 1);
       // the converters take every wait's outcome together (they meet at named barriers)
       if (!named_sync_and(2, kConverters, mbar_wait(&bempty[j], ((rn >> 1) & 1) ^ 1, kPolls))) {
@@ -255,20 +281,20 @@ lora_expand_tc_kernel(const __grid_constant__ CUtensorMap tmap_b, const float* _
         break;
       }
       ++rn;
-      // pair ids and weights of the block's rows
-      for (int r = l; r < BN; r += kConverters) {
-        const int pid = __ldg(sorted_ids + t * BN + r);
+      // pair ids and weights of the sub-unit's rows
+      for (int r = l; r < kRows; r += kConverters) {
+        const int pid = r < nrows ? __ldg(sorted_ids + slot0 + r) : -1;
         const bool ok = pid >= 0 && (int64_t)pid < numel;
         m_pid[j][r] = ok ? pid : -1;
         m_w[j][r] = ok && topk_w ? scale * __ldg(topk_w + pid) : scale;
       }
-      named_sync(2, kConverters);  // every converter sees the block's pair ids
+      named_sync(2, kConverters);  // every converter sees the sub-unit's pair ids
       // intermediate rows (slice s) as bf16 head and tail, 128-byte swizzled:
       // 16-byte chunk c (8 values) of row r at r * 128 + ((c ^ (r & 7)) << 4)
-      unsigned char* ah = abuf + (size_t)j * G::kABytes;
+      unsigned char* ah = abuf + (size_t)j * kABytes;
       unsigned char* at = ah + kATile;
 #pragma unroll 4
-      for (int k = l; k < BN * 8; k += kConverters) {
+      for (int k = l; k < nrows * 8; k += kConverters) {
         const int r = k >> 3, c = k & 7;
         const int pid = m_pid[j][r];
         uint4 h = make_uint4(0, 0, 0, 0), tl = make_uint4(0, 0, 0, 0);
@@ -291,18 +317,18 @@ lora_expand_tc_kernel(const __grid_constant__ CUtensorMap tmap_b, const float* _
     // ------------------------------------------------------------ copiers
     const int l = tid - 192;  // 0 .. kCopiers-1
     // a copier always moves 16-byte chunk c of rows r0, r0 + kRowStep, ... of an m-tile
-    constexpr int kRowStep = kCopiers / 16, kMine = BN / kRowStep;
+    constexpr int kRowStep = kCopiers / 16, kMine = kRows / kRowStep;
     const int c = l & 15, r0 = l >> 4;
     const uint16_t* src[kMine];  // per run: the rows' first output column of the slice
     uint32_t q = 0, rn = 0;
     int64_t key = -1;
     int j = 0;
-    for (int64_t it = it0; it < it1 && !fault; ++it) {
-      int64_t t;
-      int s, m0, m1, v;
-      if (!item(it, t, s, m0, m1, v)) continue;
-      if (t * S + s != key) {  // a new run: its pair ids (the copiers meet at named barriers)
-        key = t * S + s;
+    for (int64_t x = 2 * it0; x < 2 * it1 && !fault; ++x) {
+      int64_t slot0;
+      int s, m0, m1, nrows, v;
+      if (!work(x, slot0, s, m0, m1, nrows, v)) continue;
+      if (slot0 * S + s != key) {  // a new run: its pair ids (the copiers meet at named barriers)
+        key = slot0 * S + s;
         j = (int)(rn & 1);
         if (!named_sync_and(3, kCopiers, mbar_wait(&bfull[j], (rn >> 1) & 1, kPolls))) {
           fault = true;
@@ -315,7 +341,7 @@ lora_expand_tc_kernel(const __grid_constant__ CUtensorMap tmap_b, const float* _
           src[i] = pid >= 0 ? out + (int64_t)pid * out_stride + (int64_t)s * Ns + c * 8 : nullptr;
         }
       }
-      // output rows of each m-tile: BN rows x 256 bytes, 16 chunks of 16 bytes per row
+      // output rows of each m-tile: 256 bytes per real row, 16 chunks of 16 bytes
       for (int m = m0; m < m1 && !fault; ++m, ++q) {
         const int st = (int)(q % NO);
         if (!named_sync_and(3, kCopiers, mbar_wait(&oempty[st], ((q / NO) & 1) ^ 1, kPolls))) {
@@ -325,8 +351,7 @@ lora_expand_tc_kernel(const __grid_constant__ CUtensorMap tmap_b, const float* _
         unsigned char* ot = otile(q) + r0 * kOutPitch + c * 16;
 #pragma unroll
         for (int i = 0; i < kMine; ++i)
-          cp_async16_zfill(ot + i * kRowStep * kOutPitch, src[i] ? src[i] + m * kM : out,
-                           src[i] ? 16u : 0u);
+          if (src[i]) cp_async16_zfill(ot + i * kRowStep * kOutPitch, src[i] + m * kM, 16u);
         cp_async_arrive_noinc(&ofull[st]);
       }
     }
@@ -335,19 +360,19 @@ lora_expand_tc_kernel(const __grid_constant__ CUtensorMap tmap_b, const float* _
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;             // tensor-memory lanes 32*quarter .. +31 = rows
     const int half = (warp - 10) >> 2;        // output columns [64 * half, 64 * half + 64)
-    const int r = quarter * 32 + lane;        // this thread's row of the block
-    const bool has_rows = quarter * 32 < BN;  // BLOCK_M 64: two quarters hold no row
+    const int r = quarter * 32 + lane;        // this thread's row of the sub-unit
+    bool has_rows = false;                    // a 64-row sub-unit: two quarters hold no row
     uint32_t q = 0, n = 0, rn = 0;
     int64_t key = -1;
     int j = 0;
     float w = 0.f;
-    for (int64_t it = it0; it < it1 && !fault; ++it) {
-      int64_t t;
-      int s, m0, m1, v;
-      if (!item(it, t, s, m0, m1, v)) continue;
-      if (t * S + s != key) {  // a new run
+    for (int64_t x = 2 * it0; x < 2 * it1 && !fault; ++x) {
+      int64_t slot0;
+      int s, m0, m1, nrows, v;
+      if (!work(x, slot0, s, m0, m1, nrows, v)) continue;
+      if (slot0 * S + s != key) {  // a new run
         if (key >= 0 && lane == 0) mbar_arrive(&bempty[j]);  // done with the last run's buffer
-        key = t * S + s;
+        key = slot0 * S + s;
         j = (int)(rn & 1);
         // the block's pair ids and weights (written before the buffer's "full" arrival)
         if (!__all_sync(0xffffffffu, mbar_wait(&bfull[j], (rn >> 1) & 1, kPolls))) {
@@ -355,6 +380,7 @@ lora_expand_tc_kernel(const __grid_constant__ CUtensorMap tmap_b, const float* _
           break;
         }
         ++rn;
+        has_rows = quarter * 32 < nrows;
         w = has_rows ? m_w[j][r] : 0.f;
       }
       for (int m = m0; m < m1; ++m, ++q, ++n) {
@@ -421,7 +447,7 @@ lora_expand_tc_kernel(const __grid_constant__ CUtensorMap tmap_b, const float* _
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, G::kTmemCols);
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
 // --- host side ----------------------------------------------------------------
@@ -452,11 +478,11 @@ bool expand_tc_fits(int64_t numel, int num_vexperts, int r, int Ns, int block_m,
 cudaError_t prepare_expand_tc_kernels() {
   cudaError_t e = cudaFuncSetAttribute(lora_expand_tc_kernel<64>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)xt::Geo<64>::kSmem);
+                                       (int)xt::kSmem);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(lora_expand_tc_kernel<128>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)xt::Geo<128>::kSmem);
+                              (int)xt::kSmem);
 }
 
 cudaError_t launch_expand_tc(const float* inter, const void* lora_b, int S, int Ns, float scale,
@@ -489,17 +515,17 @@ cudaError_t launch_expand_tc(const float* inter, const void* lora_b, int S, int 
   if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
   const int mtiles = Ns / xt::kM;
   const int mgroups = (mtiles + xt::kMGroup - 1) / xt::kMGroup;
-  const int64_t n_items = nblk * S * mgroups;
+  const int64_t n_items = (nblk * block_m + xt::kRows - 1) / xt::kRows * S * mgroups;
   const dim3 grid((unsigned)std::min<int64_t>(n_items, (int64_t)xt_device_sms()));
   const int R = S * xt::kRank;
   uint16_t* o = static_cast<uint16_t*>(out);
   if (block_m == 64)
-    return launch_pdl(lora_expand_tc_kernel<64>, grid, dim3(xt::kThreads), xt::Geo<64>::kSmem,
+    return launch_pdl(lora_expand_tc_kernel<64>, grid, dim3(xt::kThreads), xt::kSmem,
                       stream, map, inter, R, S, Ns, scale, topk_weights, sorted_ids, expert_ids,
-                      ntpp, numel, num_vexperts, o, out_stride, n_items, mgroups, mtiles);
-  return launch_pdl(lora_expand_tc_kernel<128>, grid, dim3(xt::kThreads), xt::Geo<128>::kSmem,
+                      ntpp, numel, num_vexperts, o, out_stride, nblk, mgroups, mtiles);
+  return launch_pdl(lora_expand_tc_kernel<128>, grid, dim3(xt::kThreads), xt::kSmem,
                     stream, map, inter, R, S, Ns, scale, topk_weights, sorted_ids, expert_ids, ntpp,
-                    numel, num_vexperts, o, out_stride, n_items, mgroups, mtiles);
+                    numel, num_vexperts, o, out_stride, nblk, mgroups, mtiles);
 }
 
 cudaError_t take_expand_tc_checks(unsigned long long* first, unsigned long long* count) {
