@@ -707,17 +707,19 @@ TRAFFIC = {
     ("wide", "expand_down"): (41633024 + 37888, 43469824, "mol_lora.cu", "ca808f2911072fbb"),
     ("wide1k", "expand_down"): (172935424 + 7966464, 184738816, "mol_lora.cu", "ca808f2911072fbb"),
     ("ep", "shrink_gate_up"): (569524736 + 6288128, 572089984, "mol_lora.cu", "ca808f2911072fbb"),
-    ("dense", "expand_down"): (344127744 + 215144192, 612368384, "mol_lora.cu", "ca808f2911072fbb"),
+    ("dense", "expand_down"): (344967168 + 210716928, 612368384, "mol_expand_tc.cu", "fbaeb08d75e03155"),
 }
 
 
 def kernel_source_digest(src: str) -> str:
-    """sha256 (first 16 hex digits) of a kernel's source file and the shared device header."""
+    """sha256 (first 16 hex digits) of a kernel's source file and the shared device headers
+    it includes (the tcgen05 helpers for the tensor-core kernels)."""
     import hashlib
 
     csrc = os.path.join(ROOT, "moe_lora_virtual_gb300", "csrc")
     h = hashlib.sha256()
-    for f in (src, "mol_device.cuh"):
+    tc = ("mol_tc.cuh",) if src in ("mol_umma.cu", "mol_expand_tc.cu") else ()
+    for f in (src, "mol_device.cuh") + tc:
         h.update(f.encode())
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]

@@ -21,24 +21,29 @@
 // contiguous columns of one row.
 //
 // Layout. A persistent grid (one block per SM); block b walks items
-// (t, s, group of up to eight m-tiles) b, b+G, ...; sixteen warps:
+// (unit of 128 rows, slice s, group of up to eight m-tiles) b, b+G, ..., so the
+// blocks that run at the same time hold neighbouring units and load each lora_b
+// tile from DRAM once between them; eighteen warps:
 //   warp 0     TMA producer: per m-tile, one cp.async.bulk.tensor for the
 //              128 x 64 lora_b tile (128-byte swizzle);
 //   warp 1     allocates the tensor memory (two accumulators of 128 columns);
 //              one lane issues each m-tile's eight MMAs and commits them to
-//              the stage's "empty" barrier, the accumulator's "full" barrier
-//              and, after an item's last m-tile, to its operand buffer's
-//              "empty" barrier;
-//   warps 2-5  converters: per item, the block's pair ids and row weights and
-//              the intermediate rows as head / tail operands (128-byte
-//              swizzle) in one of two buffers, up to two items ahead;
-//   warps 6-7  copiers: per m-tile, the output rows (16-byte cp.async into
-//              the stage), arriving on the stage's "full" barrier as they land;
-//   warps 8-15 epilogue: a thread reads 32 columns of its row at a time
+//              the lora_b tile's "empty" barrier, the accumulator's "full"
+//              barrier and, after a run's last m-tile, to its operand
+//              buffer's "empty" barrier;
+//   warps 2-5  converters: per run of items with the same rows and slice, the
+//              rows' pair ids and weights and the intermediate rows as head /
+//              tail operands (128-byte swizzle) in one of two buffers, one run
+//              ahead;
+//   warps 6-9  copiers: per m-tile, the output rows (16-byte cp.async into a
+//              staged tile of their own ring), arriving on its "full" barrier
+//              as they land;
+//   warps 10-17 epilogue: a thread reads 32 columns of its row at a time
 //              (tensor-memory lane = row; two warps per 32-lane quarter, one
 //              per half of the columns), adds them to the staged output row
-//              and stores the bf16 sums with 16-byte stores; then the stage
-//              and the accumulator are released.
+//              and the warp stores its rows' bf16 sums, 128 bytes of a row per
+//              eight lanes; then the staged tile and the accumulator are
+//              released.
 // Every wait is bounded: a timeout sets a fault bit, the roles leave their
 // loops, and the tensor memory is freed before the block exits.
 
@@ -55,7 +60,7 @@ namespace xt {
 constexpr int kM = 128;        // output columns per m-tile (MMA N)
 constexpr int kRows = 128;     // MMA M: rows of the operand buffers
 constexpr int kRank = 64;      // rank: one 128-byte swizzled row of k
-constexpr int kMGroup = 8;     // m-tiles per item
+constexpr int kMGroup = 8;     // most m-tiles per item
 constexpr int kBTile = kM * kRank * 2;        // 16 KB lora_b tile
 constexpr int kATile = kRows * kRank * 2;     // 16 KB head (or tail) operand
 constexpr int kConverters = 128;              // warps 2-5
@@ -140,15 +145,14 @@ lora_expand_tc_kernel(const __grid_constant__ CUtensorMap tmap_b, const float* _
   const int per = S * mgroups;
   // Units: routed blocks (BLOCK_M 128) or pairs of routed blocks (BLOCK_M 64). A unit
   // is one 128-row sub-unit (a block, or a pair whose two blocks have the same
-  // virtual expert) or two 64-row ones (the blocks of a pair on their own). Block b
-  // of the grid takes a contiguous range of the units (times slices and m-tile
-  // groups) below ntpp, so consecutive items share their rows and slice: one
-  // conversion of the intermediate serves them all.
+  // virtual expert) or two 64-row ones (the blocks of a pair on their own). An item is
+  // a unit, a slice and a group of its m-tiles; the items cover the units below ntpp.
   constexpr int kPer = kRows / BN;  // routed blocks per unit
   const int64_t nunits = (nblk + kPer - 1) / kPer;
   const int64_t ueff = min(nunits, (int64_t)((max(ntpp, 0) + kRows - 1) / kRows));
-  const int64_t it0 = ueff * per * blockIdx.x / gridDim.x,
-                it1 = ueff * per * (blockIdx.x + 1) / gridDim.x;
+  // items b, b + G, ... of the grid: blocks that run at the same time hold neighbouring
+  // items, so the units of one virtual expert load the same lora_b tiles together
+  const int64_t nitems = ueff * per, G = gridDim.x;
   // work x (2 per item: item x / 2, sub-unit x % 2) -> its first routing slot, slice,
   // m-tiles [m0, m1), rows and virtual expert; false when there is no such sub-unit
   auto work = [&](int64_t x, int64_t& slot0, int& s, int& m0, int& m1, int& nrows,
@@ -158,8 +162,9 @@ lora_expand_tc_kernel(const __grid_constant__ CUtensorMap tmap_b, const float* _
     const int64_t u = it / per;
     const int rem = (int)(it - u * per);
     s = rem / mgroups;
-    m0 = (rem - s * mgroups) * kMGroup;
-    m1 = min(m0 + kMGroup, mtiles);
+    const int g = rem - s * mgroups;  // the slice's m-tiles in mgroups equal groups
+    m0 = g * mtiles / mgroups;
+    m1 = (g + 1) * mtiles / mgroups;
     auto block = [&](int64_t t) -> int {  // expert of routed block t, -1 if none
       if (t >= nblk || t * BN >= ntpp) return -1;
       const int e = __ldg(expert_ids + t);
@@ -191,7 +196,7 @@ lora_expand_tc_kernel(const __grid_constant__ CUtensorMap tmap_b, const float* _
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       uint32_t q = 0;
-      for (int64_t x = 2 * it0; x < 2 * it1 && !fault; ++x) {
+      for (int64_t x = 2 * blockIdx.x; x < 2 * nitems && !fault; x += (x & 1) ? 2 * G - 1 : 1) {
         int64_t slot0;
         int s, m0, m1, nrows, v;
         if (!work(x, slot0, s, m0, m1, nrows, v)) continue;
@@ -221,7 +226,7 @@ lora_expand_tc_kernel(const __grid_constant__ CUtensorMap tmap_b, const float* _
       int64_t key = -1;
       int j = 0;
       uint32_t ah = 0, at = 0;
-      for (int64_t x = 2 * it0; x < 2 * it1 && !fault; ++x) {
+      for (int64_t x = 2 * blockIdx.x; x < 2 * nitems && !fault; x += (x & 1) ? 2 * G - 1 : 1) {
         int64_t slot0;
         int s, m0, m1, nrows, v;
         if (!work(x, slot0, s, m0, m1, nrows, v)) continue;
@@ -268,7 +273,7 @@ lora_expand_tc_kernel(const __grid_constant__ CUtensorMap tmap_b, const float* _
     const int l = tid - 64;  // 0 .. kConverters-1
     uint32_t rn = 0;
     int64_t key = -1;
-    for (int64_t x = 2 * it0; x < 2 * it1 && !fault; ++x) {
+    for (int64_t x = 2 * blockIdx.x; x < 2 * nitems && !fault; x += (x & 1) ? 2 * G - 1 : 1) {
       int64_t slot0;
       int s, m0, m1, nrows, v;
       if (!work(x, slot0, s, m0, m1, nrows, v)) continue;
@@ -293,8 +298,9 @@ lora_expand_tc_kernel(const __grid_constant__ CUtensorMap tmap_b, const float* _
       // 16-byte chunk c (8 values) of row r at r * 128 + ((c ^ (r & 7)) << 4)
       unsigned char* ah = abuf + (size_t)j * kABytes;
       unsigned char* at = ah + kATile;
-#pragma unroll 4
-      for (int k = l; k < nrows * 8; k += kConverters) {
+#pragma unroll
+      for (int k = l; k < kRows * 8; k += kConverters) {
+        if (k >= nrows * 8) break;
         const int r = k >> 3, c = k & 7;
         const int pid = m_pid[j][r];
         uint4 h = make_uint4(0, 0, 0, 0), tl = make_uint4(0, 0, 0, 0);
@@ -323,7 +329,7 @@ lora_expand_tc_kernel(const __grid_constant__ CUtensorMap tmap_b, const float* _
     uint32_t q = 0, rn = 0;
     int64_t key = -1;
     int j = 0;
-    for (int64_t x = 2 * it0; x < 2 * it1 && !fault; ++x) {
+    for (int64_t x = 2 * blockIdx.x; x < 2 * nitems && !fault; x += (x & 1) ? 2 * G - 1 : 1) {
       int64_t slot0;
       int s, m0, m1, nrows, v;
       if (!work(x, slot0, s, m0, m1, nrows, v)) continue;
@@ -366,7 +372,7 @@ lora_expand_tc_kernel(const __grid_constant__ CUtensorMap tmap_b, const float* _
     int64_t key = -1;
     int j = 0;
     float w = 0.f;
-    for (int64_t x = 2 * it0; x < 2 * it1 && !fault; ++x) {
+    for (int64_t x = 2 * blockIdx.x; x < 2 * nitems && !fault; x += (x & 1) ? 2 * G - 1 : 1) {
       int64_t slot0;
       int s, m0, m1, nrows, v;
       if (!work(x, slot0, s, m0, m1, nrows, v)) continue;
