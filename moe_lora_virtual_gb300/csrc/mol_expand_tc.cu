@@ -217,6 +217,11 @@ lora_expand_tc_kernel(const __grid_constant__ CUtensorMap tmap_b, const float* _
           tma_load_2d(wtile(q), &tmap_b, 0, (int)row, &wfull[st]);
         }
       }
+      // after a timeout, let the last copies into each tile land (bounded) before the
+      // block's shared memory is released
+      if (fault)
+        for (uint32_t u = q > (uint32_t)NB ? q - NB : 0; u < q; ++u)
+          mbar_wait(&wfull[u % NB], (u / NB) & 1, kPolls);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
