@@ -313,12 +313,11 @@ int32_t mol_token_lora_ids(const int32_t* weight_indices, const int32_t* seg_ind
  * out) and clears them. It synchronizes, so it belongs in checks and tests,
  * not in a captured or timed sequence.
  * After a wait ran out, the outputs of the call that recorded it are undefined
- * (rows may be missing or partial). The shrink's producer and the tensor-core
- * expand's weight producer wait, bounded, for the copies they issued before
- * their block exits, and the copy threads of both tensor-core kernels wait for
- * their own row copies; the tensor-core shrink cannot observe its weight
- * copies apart from the row copies that share their barrier, so a block of it
- * that gives up may exit with a weight copy in flight.
+ * (rows may be missing or partial). Before a block exits after a timeout, the
+ * producers wait, bounded, for the copies they issued, and the threads that
+ * copy rows with cp.async wait for their own; if one of those waits runs out
+ * too (the tensor-core shrink's stage barriers also count the gathered rows),
+ * the block may exit with a copy in flight.
  * (No counterpart on the pages: the pages' kernels have no bounded waits.)
  */
 int32_t mol_take_fault_flags(uint32_t* flags);

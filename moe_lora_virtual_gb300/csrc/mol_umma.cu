@@ -164,6 +164,12 @@ lora_shrink_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
           tma_load_2d(stageA(q), half ? &tmap_h : &tmap_a, ks * kKStep, y, &full[s]);
         }
       }
+      // after a timeout, wait (bounded) for the last uses of each stage to complete: their
+      // barriers also count the gather's row copies, so a stage whose rows never came
+      // costs one more bounded wait
+      if (fault)
+        for (uint32_t u = q > (uint32_t)kStages ? q - kStages : 0; u < q; ++u)
+          mbar_wait(&full[u % kStages], (u / kStages) & 1, kPolls);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
