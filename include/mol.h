@@ -326,10 +326,11 @@ int32_t mol_take_fault_flags(uint32_t* flags);
  * Test hook of the bounded waits (no counterpart on the pages). With
  * stall_producer = 1 the producer warp of every block of mol_lora_shrink (and
  * of the shrink inside mol_lora_forward, on the mma path) leaves before it
- * issues any copy, so the consumers' waits run out with nothing in flight and
- * record bit 0 of mol_take_fault_flags; 0 restores normal operation.
- * wait_limit_ns bounds every wait of that shrink (0 = the default, one
- * second). Synchronizes the device; for tests only, never while another
+ * issues any copy, and so does the weight producer of the tensor-core expand
+ * (full routed blocks of rank 64), so the other roles' waits run out with
+ * nothing in flight and record bit 0 of mol_take_fault_flags; 0 restores
+ * normal operation. wait_limit_ns bounds every wait of those two kernels (0 =
+ * the default, one second). Synchronizes the device; for tests only, never while another
  * thread uses the library. Returns MOL_ERR_INVALID_ARG for stall_producer > 1.
  */
 int32_t mol_debug_wait_test(uint32_t stall_producer, uint64_t wait_limit_ns);

@@ -81,6 +81,17 @@ constexpr uint32_t kTmemCols = kAccs * kM;
 }  // namespace xt
 
 __device__ unsigned int g_xt_fault_flags;
+// Test controls of the bounded waits, set only through mol_debug_wait_test: bit 0
+// of g_xt_test_stall makes the weight producer issue no copy (so every other
+// role's waits run out), g_xt_wait_limit_ns is the wall-clock limit of every wait.
+__device__ unsigned int g_xt_test_stall;
+__device__ unsigned long long g_xt_wait_limit_ns = kWaitLimitNs;
+
+cudaError_t set_expand_tc_wait_test(unsigned stall, unsigned long long limit_ns) {
+  cudaError_t e = cudaMemcpyToSymbol(g_xt_test_stall, &stall, sizeof(unsigned));
+  if (e != cudaSuccess) return e;
+  return cudaMemcpyToSymbol(g_xt_wait_limit_ns, &limit_ns, sizeof(unsigned long long));
+}
 
 cudaError_t take_expand_tc_faults(unsigned* out) {
   cudaError_t e = cudaMemcpyFromSymbol(out, g_xt_fault_flags, sizeof(unsigned));
@@ -138,6 +149,7 @@ lora_expand_tc_kernel(const __grid_constant__ CUtensorMap tmap_b, const float* _
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
+  const uint64_t wlim = g_xt_wait_limit_ns;
   pdl_wait();  // routing, intermediate and output rows come from earlier kernels
   pdl_launch_dependents();
 
@@ -194,7 +206,7 @@ lora_expand_tc_kernel(const __grid_constant__ CUtensorMap tmap_b, const float* _
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
+    if (lane == 0 && !(g_xt_test_stall & 1u)) {  // test control: no copy, every wait runs out
       uint32_t q = 0;
       for (int64_t x = 2 * blockIdx.x; x < 2 * nitems && !fault; x += (x & 1) ? 2 * G - 1 : 1) {
         int64_t slot0;
@@ -202,7 +214,7 @@ lora_expand_tc_kernel(const __grid_constant__ CUtensorMap tmap_b, const float* _
         if (!work(x, slot0, s, m0, m1, nrows, v)) continue;
         for (int m = m0; m < m1; ++m, ++q) {
           const int st = (int)(q % NB);
-          if (!mbar_wait(&wempty[st], ((q / NB) & 1) ^ 1, kPolls)) {
+          if (!mbar_wait(&wempty[st], ((q / NB) & 1) ^ 1, kPolls, wlim)) {
             fault = true;
             break;
           }
@@ -221,7 +233,7 @@ lora_expand_tc_kernel(const __grid_constant__ CUtensorMap tmap_b, const float* _
       // block's shared memory is released
       if (fault)
         for (uint32_t u = q > (uint32_t)NB ? q - NB : 0; u < q; ++u)
-          mbar_wait(&wfull[u % NB], (u / NB) & 1, kPolls);
+          mbar_wait(&wfull[u % NB], (u / NB) & 1, kPolls, wlim);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -239,7 +251,7 @@ lora_expand_tc_kernel(const __grid_constant__ CUtensorMap tmap_b, const float* _
           if (key >= 0) umma_commit(&bempty[j]);  // the last run's buffer, once its MMAs are done
           key = slot0 * S + s;
           j = (int)(rn & 1);
-          if (!mbar_wait(&bfull[j], (rn >> 1) & 1, kPolls)) {
+          if (!mbar_wait(&bfull[j], (rn >> 1) & 1, kPolls, wlim)) {
             fault = true;
             break;
           }
@@ -250,8 +262,8 @@ lora_expand_tc_kernel(const __grid_constant__ CUtensorMap tmap_b, const float* _
         for (int m = m0; m < m1; ++m, ++q, ++n) {
           const int st = (int)(q % NB);
           const int a = (int)(n % kAccs);
-          if (!mbar_wait(&acce[a], ((n / kAccs) & 1) ^ 1, kPolls) ||
-              !mbar_wait(&wfull[st], (q / NB) & 1, kPolls)) {
+          if (!mbar_wait(&acce[a], ((n / kAccs) & 1) ^ 1, kPolls, wlim) ||
+              !mbar_wait(&wfull[st], (q / NB) & 1, kPolls, wlim)) {
             fault = true;
             break;
           }
@@ -286,7 +298,7 @@ lora_expand_tc_kernel(const __grid_constant__ CUtensorMap tmap_b, const float* _
       key = slot0 * S + s;
       const int j = (int)(rn & 1);
       // the converters take every wait's outcome together (they meet at named barriers)
-      if (!named_sync_and(2, kConverters, mbar_wait(&bempty[j], ((rn >> 1) & 1) ^ 1, kPolls))) {
+      if (!named_sync_and(2, kConverters, mbar_wait(&bempty[j], ((rn >> 1) & 1) ^ 1, kPolls, wlim))) {
         fault = true;
         break;
       }
@@ -341,7 +353,7 @@ lora_expand_tc_kernel(const __grid_constant__ CUtensorMap tmap_b, const float* _
       if (slot0 * S + s != key) {  // a new run: its pair ids (the copiers meet at named barriers)
         key = slot0 * S + s;
         j = (int)(rn & 1);
-        if (!named_sync_and(3, kCopiers, mbar_wait(&bfull[j], (rn >> 1) & 1, kPolls))) {
+        if (!named_sync_and(3, kCopiers, mbar_wait(&bfull[j], (rn >> 1) & 1, kPolls, wlim))) {
           fault = true;
           break;
         }
@@ -355,7 +367,7 @@ lora_expand_tc_kernel(const __grid_constant__ CUtensorMap tmap_b, const float* _
       // output rows of each m-tile: 256 bytes per real row, 16 chunks of 16 bytes
       for (int m = m0; m < m1 && !fault; ++m, ++q) {
         const int st = (int)(q % NO);
-        if (!named_sync_and(3, kCopiers, mbar_wait(&oempty[st], ((q / NO) & 1) ^ 1, kPolls))) {
+        if (!named_sync_and(3, kCopiers, mbar_wait(&oempty[st], ((q / NO) & 1) ^ 1, kPolls, wlim))) {
           fault = true;
           break;
         }
@@ -386,7 +398,7 @@ lora_expand_tc_kernel(const __grid_constant__ CUtensorMap tmap_b, const float* _
         key = slot0 * S + s;
         j = (int)(rn & 1);
         // the block's pair ids and weights (written before the buffer's "full" arrival)
-        if (!__all_sync(0xffffffffu, mbar_wait(&bfull[j], (rn >> 1) & 1, kPolls))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&bfull[j], (rn >> 1) & 1, kPolls, wlim))) {
           fault = true;
           break;
         }
@@ -398,8 +410,8 @@ lora_expand_tc_kernel(const __grid_constant__ CUtensorMap tmap_b, const float* _
         const int st = (int)(q % NO);
         const int a = (int)(n % kAccs);
         // tcgen05.ld is warp-collective: the lanes agree on the outcome of the waits
-        if (!__all_sync(0xffffffffu, mbar_wait(&accf[a], (n / kAccs) & 1, kPolls) &&
-                                         mbar_wait(&ofull[st], (q / NO) & 1, kPolls))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&accf[a], (n / kAccs) & 1, kPolls, wlim) &&
+                                         mbar_wait(&ofull[st], (q / NO) & 1, kPolls, wlim))) {
           fault = true;
           break;
         }

@@ -194,8 +194,10 @@ cudaError_t take_lora_checks(unsigned long long* first, unsigned long long* coun
 cudaError_t take_tc_checks(unsigned long long* first, unsigned long long* count);
 cudaError_t take_stage_checks(unsigned long long* first, unsigned long long* count);
 cudaError_t take_expand_tc_checks(unsigned long long* first, unsigned long long* count);
-// Test controls of the shrink's bounded waits (mol_debug_wait_test).
+// Test controls of the bounded waits (mol_debug_wait_test): the item shrink's and
+// the tcgen05 expand's producers.
 cudaError_t set_wait_test(unsigned stall, unsigned long long limit_ns);
+cudaError_t set_expand_tc_wait_test(unsigned stall, unsigned long long limit_ns);
 
 // Largest contraction width accepted by the shrink (it streams K in chunks).
 constexpr int kShrinkMaxK = 1 << 16;

@@ -57,11 +57,13 @@ cudaError_t take_lora_faults(unsigned* out) {
 }
 
 cudaError_t set_wait_test(unsigned stall, unsigned long long limit_ns) {
-  cudaError_t e = cudaDeviceSynchronize();  // no shrink may be running while they change
+  cudaError_t e = cudaDeviceSynchronize();  // no kernel may be running while they change
   if (e != cudaSuccess) return e;
   e = cudaMemcpyToSymbol(g_test_stall, &stall, sizeof(unsigned));
   if (e != cudaSuccess) return e;
-  return cudaMemcpyToSymbol(g_wait_limit_ns, &limit_ns, sizeof(unsigned long long));
+  e = cudaMemcpyToSymbol(g_wait_limit_ns, &limit_ns, sizeof(unsigned long long));
+  if (e != cudaSuccess) return e;
+  return set_expand_tc_wait_test(stall, limit_ns);
 }
 
 // Routing words of one work item as loaded: a producer fetches them one item

@@ -1,4 +1,4 @@
-"""A bounded wait that runs out: the shrink records a fault bit, leaves, and the device stays usable.
+"""A bounded wait that runs out: the kernel records a fault bit, leaves, and the device stays usable.
 
 mol_debug_wait_test makes the shrink's producer warps leave before they issue
 any copy, so every consumer's wait on a stage finds nothing arriving and gives
@@ -95,3 +95,41 @@ def test_wait_limit_restored_by_default():
     ref = oracle.lora_shrink(c["x"], c["k"], c["A"], s, e, n, BM, numel,
                              np.full((numel, R), np.nan, np.float32))
     check_inter(inter.cpu().numpy(), ref, valid_pairs(s, e, n, BM, numel))
+
+
+def test_tc_expand_wait_runs_out_sets_flag_then_device_recovers():
+    """The tensor-core expand (full routed blocks of rank 64): with its weight producer issuing
+    nothing, the MMA, epilogue, copier and converter waits all run out; the call returns, bit 0
+    is reported, no output row changed, and a normal expand right after matches the oracle."""
+    torch = torch_cuda()
+    mol = mol_lib()
+    dev = torch.device("cuda:0")
+    rng = np.random.default_rng(7)
+    T, k, E, BM, S, Ns, r = 256, 2, 4, 64, 2, 256, 64
+    numel, V, N = T * k, E, S * Ns
+    topk = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    vid = oracle.virtual_topk(topk, np.zeros(T, np.int32), E, 1).reshape(-1)
+    s, e, n = oracle.align_block_size(vid, V, BM)
+    inter = (rng.standard_normal((numel, S * r))).astype(np.float32)
+    B = bits(rng.standard_normal((V, N, r)) * 0.05)
+    out0 = bits(rng.standard_normal((numel, N)))
+    routing = mol.Routing(to_dev_i32(vid, dev), to_dev_i32(s, dev), to_dev_i32(e, dev),
+                          torch.tensor([n], dtype=torch.int32, device=dev), BM, numel, V)
+    inter_d, B_d = torch.from_numpy(inter).to(dev), to_dev_bf16(B, dev)
+    mol.mol_take_fault_flags()
+    out = to_dev_bf16(out0, dev)
+    try:
+        mol.mol_debug_wait_test(True, 2_000_000)  # waits give up after 2 ms
+        mol.mol_lora_expand(inter_d, B_d, S, 0.5, routing, out)
+        flags = mol.mol_take_fault_flags()
+    finally:
+        mol.mol_debug_wait_test(False, 0)
+    assert flags == 1
+    assert np.array_equal(bf16_host(out), out0), "no product ran, so no output row changed"
+
+    out = to_dev_bf16(out0, dev)
+    mol.mol_lora_expand(inter_d, B_d, S, 0.5, routing, out)
+    torch.cuda.synchronize()
+    assert mol.mol_take_fault_flags() == 0
+    ref = oracle.lora_expand(inter, B, S, r, Ns, 0.5, None, s, e, n, BM, numel, out0)
+    check_out(bf16_host(out), ref, valid_pairs(s, e, n, BM, numel))
