@@ -167,8 +167,8 @@ lora_expand_tc_kernel(const __grid_constant__ CUtensorMap tmap_b, const float* _
   const int64_t nitems = ueff * per, G = gridDim.x;
   // work x (2 per item: item x / 2, sub-unit x % 2) -> its first routing slot, slice,
   // m-tiles [m0, m1), rows and virtual expert; false when there is no such sub-unit
-  auto work = [&](int64_t x, int64_t& slot0, int& s, int& m0, int& m1, int& nrows,
-                  int& v) -> bool {
+  auto work = [&](int64_t x, int64_t& slot0, int& s, int& m0, int& m1, int& nrows, int& v,
+                  bool note = false) -> bool {
     const int64_t it = x >> 1;
     const int k = (int)(x & 1);
     const int64_t u = it / per;
@@ -180,6 +180,8 @@ lora_expand_tc_kernel(const __grid_constant__ CUtensorMap tmap_b, const float* _
     auto block = [&](int64_t t) -> int {  // expert of routed block t, -1 if none
       if (t >= nblk || t * BN >= ntpp) return -1;
       const int e = __ldg(expert_ids + t);
+      if (kChecked && note && s == 0 && m0 == 0)  // the caller's expert ids, once per block
+        (void)MOL_NOTE(e >= -1 && e < num_vexperts, MOL_CHECK_ROUTE_EXPERT, t);
       return e >= 0 && e < num_vexperts ? e : -1;
     };
     if (kPer == 1) {
@@ -207,11 +209,13 @@ lora_expand_tc_kernel(const __grid_constant__ CUtensorMap tmap_b, const float* _
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && !(g_xt_test_stall & 1u)) {  // test control: no copy, every wait runs out
+      if (kChecked && blockIdx.x == 0)  // the caller's post-padded count
+        (void)MOL_NOTE(ntpp >= 0 && ntpp <= nblk * BN && ntpp % BN == 0, MOL_CHECK_ROUTE_NTPP, ntpp);
       uint32_t q = 0;
       for (int64_t x = 2 * blockIdx.x; x < 2 * nitems && !fault; x += (x & 1) ? 2 * G - 1 : 1) {
         int64_t slot0;
         int s, m0, m1, nrows, v;
-        if (!work(x, slot0, s, m0, m1, nrows, v)) continue;
+        if (!work(x, slot0, s, m0, m1, nrows, v, true)) continue;
         for (int m = m0; m < m1; ++m, ++q) {
           const int st = (int)(q % NB);
           if (!mbar_wait(&wempty[st], ((q / NB) & 1) ^ 1, kPolls, wlim)) {
@@ -306,6 +310,8 @@ lora_expand_tc_kernel(const __grid_constant__ CUtensorMap tmap_b, const float* _
       // pair ids and weights of the sub-unit's rows
       for (int r = l; r < kRows; r += kConverters) {
         const int pid = r < nrows ? __ldg(sorted_ids + slot0 + r) : -1;
+        if (kChecked && r < nrows)  // the caller's slots
+          (void)MOL_NOTE(pid >= 0 && (int64_t)pid <= numel, MOL_CHECK_ROUTE_PAIR, slot0 + r);
         const bool ok = pid >= 0 && (int64_t)pid < numel;
         m_pid[j][r] = ok ? pid : -1;
         m_w[j][r] = ok && topk_w ? scale * __ldg(topk_w + pid) : scale;

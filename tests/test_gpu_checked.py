@@ -8,7 +8,8 @@ instead of touching memory. These tests run the checked build
 
 - on the workloads and on shapes that reach every kernel variant (single-block,
   cluster and multi-tile align; item shrink with and without adapter ranks;
-  tcgen05 shrink; register, staged and two-tile expands; the fused stage) and
+  tcgen05 shrink; register, staged, two-tile and tcgen05 expands; the fused
+  stage) and
   on adversarial routings of the align, and assert that no check failed and
   that the results still match the oracle;
 - on routing data passed in by the caller with entries that every build skips
@@ -84,6 +85,7 @@ FORWARD_SHAPES = [
     (40, 8, 6, 2, 32, 4096, 2, 32, 96, True, 0.1, True),      # item shrink with ranks, k chunks
     (30, 4, 5, 2, 16, 320, 1, 8, 200, True, 0.1, True),       # rank 8 with ranks and scalings
     (700, 8, 64, 2, 16, 128, 1, 16, 64, True, 0.1, False),    # cluster align (5600 pairs)
+    (256, 2, 4, 1, 64, 256, 2, 64, 384, True, 0.05, False),   # tcgen05 shrink and expand
 ]
 
 
@@ -208,7 +210,7 @@ CORRUPTIONS = ["expert_past_v", "negative_slot", "slot_past_numel", "ntpp_past_c
 
 
 @pytest.mark.parametrize("case", [FORWARD_SHAPES[1], FORWARD_SHAPES[2], FORWARD_SHAPES[4],
-                                  FORWARD_SHAPES[0], FORWARD_SHAPES[3]])
+                                  FORWARD_SHAPES[0], FORWARD_SHAPES[3], FORWARD_SHAPES[9]])
 @pytest.mark.parametrize("corruption", CORRUPTIONS)
 def test_bad_caller_routing_is_recorded_and_skipped(checked, case, corruption):
     """Entries that every build skips are recorded by the checked build, site and value;
