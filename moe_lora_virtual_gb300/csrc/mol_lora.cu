@@ -98,7 +98,6 @@ struct Raw {
 namespace sp {
 constexpr int kConsumers = 4;                    // consumer warps
 constexpr int kThreads = (kConsumers + 1) * 32;  // + the producer warp
-constexpr int kJT = 8;                           // weight rows per item (one 8-column mma tile)
 constexpr int kXR = 16;                          // activation rows per job (one 16-row mma tile)
 constexpr int kStageBytes = 52 * 1024;
 constexpr int kStages = 2;
@@ -119,10 +118,12 @@ struct StageHdr {
 static_assert(2 * kStages * 8 + kStages * (int)sizeof(StageHdr) + kMeta * (int)sizeof(Job) <= kHeader,
               "header");
 
-// k chunk of a job with cm activation rows: all of K with unpadded rows when
-// that fits a stage, else equal chunks (multiples of 64) of padded rows.
+// k chunk of a job of JT weight rows and cm activation rows: all of K with
+// unpadded rows when that fits a stage, else equal chunks (multiples of 64) of
+// padded rows.
+template <int JT>
 MOL_DEV void job_chunk(int K, int cm, int& len, int& pitch) {
-  const int rows = kJT + cm;
+  const int rows = JT + cm;
   if (rows * K * 2 <= kStageBytes) {
     len = K;
     pitch = K * 2;
@@ -135,7 +136,8 @@ MOL_DEV void job_chunk(int K, int cm, int& len, int& pitch) {
 }
 }  // namespace sp
 
-template <bool RANKS>
+// JT: weight rows per item, one (8) or two (16) 8-column mma tiles.
+template <bool RANKS, int JT>
 __global__ void __launch_bounds__(sp::kThreads, sp::kBlocksPerSM)
 lora_shrink_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, int K,
                    const uint16_t* __restrict__ lora_a, int R, const int* __restrict__ sorted_ids,
@@ -261,11 +263,11 @@ lora_shrink_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, 
       }
       // Columns of this item inside the adapter's rank: rank 0 writes nothing,
       // an item wholly past the rank writes zeros (its weights are padding).
-      int in_rank = kJT;  // columns of the item below the rank (r1 % 8 == 0 with ranks)
+      int in_rank = JT;  // columns of the item below the rank (r1 % JT == 0 with ranks)
       if constexpr (RANKS) {
         const int rl = (int)s_rank[v / num_experts];
         if (rl == 0) continue;
-        in_rank = rl - (jt_c * kJT) % r1;
+        in_rank = rl - (jt_c * JT) % r1;
       }
       int c = 0;
 #pragma unroll
@@ -285,15 +287,16 @@ lora_shrink_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, 
           waited = true;
         }
         const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int q2 = lane; q2 < 2 * c; q2 += 32)
-          *reinterpret_cast<float4*>(inter + (int64_t)prow[q2 >> 1] * R + jt * kJT + 4 * (q2 & 1)) = z;
+        constexpr int kQ = JT / 4;  // float4 pieces of the item's columns per row
+        for (int q2 = lane; q2 < kQ * c; q2 += 32)
+          *reinterpret_cast<float4*>(inter + (int64_t)prow[q2 / kQ] * R + jt * JT + 4 * (q2 % kQ)) = z;
         __syncwarp();
         continue;
       }
-      const uint16_t* wrows = lora_a + ((int64_t)v * R + jt * kJT) * K;
+      const uint16_t* wrows = lora_a + ((int64_t)v * R + jt * JT) * K;
       if (kChecked) {
-        const int64_t wr = (int64_t)v * R + jt * kJT;
-        stop = !__all_sync(0xffffffffu, lane != 0 || MOL_CHECK(jt * kJT + kJT <= R && wr + kJT <=
+        const int64_t wr = (int64_t)v * R + jt * JT;
+        stop = !__all_sync(0xffffffffu, lane != 0 || MOL_CHECK(jt * JT + JT <= R && wr + JT <=
                                                                    (int64_t)num_vexperts * R,
                                                                MOL_CHECK_WEIGHT_ROW, wr));
         if (stop) break;
@@ -301,13 +304,13 @@ lora_shrink_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, 
       for (int m0 = 0; m0 < c && !fault; m0 += kXR) {
         const int cm = min(kXR, c - m0);
         int len, pitch;
-        job_chunk(K, cm, len, pitch);
+        job_chunk<JT>(K, cm, len, pitch);
         const bool whole = (len == K && pitch == K * 2);
         if (kChecked) {  // the job's rows fit a stage; its activation rows exist
           const int xr = lane >= 16 && lane - 16 < cm ? prow[m0 + lane - 16] / x_div : 0;
           const bool ok =
-              (lane != 0 || MOL_CHECK((kJT + cm) * pitch <= kStageBytes && pitch >= 2 * min(len, K),
-                                      MOL_CHECK_SMEM, (kJT + cm) * pitch)) &&
+              (lane != 0 || MOL_CHECK((JT + cm) * pitch <= kStageBytes && pitch >= 2 * min(len, K),
+                                      MOL_CHECK_SMEM, (JT + cm) * pitch)) &&
               MOL_CHECK(xr >= 0 && (int64_t)xr < (numel + x_div - 1) / x_div, MOL_CHECK_ROW, xr);
           stop = !__all_sync(0xffffffffu, ok);
           if (stop) break;
@@ -318,7 +321,7 @@ lora_shrink_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, 
           jb.v = v;
           jb.jt = jt;
           jb.cm = cm;
-          jb.ncols = in_rank < kJT ? in_rank : kJT;
+          jb.ncols = in_rank < JT ? in_rank : JT;
         }
         if (lane < cm) jb.rows[lane] = prow[m0 + lane];
         const uint16_t* xsrc =
@@ -338,12 +341,12 @@ lora_shrink_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, 
             hdr[st].k0 = k0;
             hdr[st].len = cl;
             hdr[st].pitch = pitch;
-            mbar_arrive_expect_tx(&full[st], (uint32_t)((kJT + cm) * cl * 2));
+            mbar_arrive_expect_tx(&full[st], (uint32_t)((JT + cm) * cl * 2));
           }
           __syncwarp();
           if (whole) {
-            if (lane == 0) bulk_g2s(base, wrows, kJT * K * 2, &full[st]);
-          } else if (lane < kJT) {
+            if (lane == 0) bulk_g2s(base, wrows, JT * K * 2, &full[st]);
+          } else if (lane < JT) {
             bulk_g2s(base + lane * pitch, wrows + (int64_t)lane * K + k0, cl * 2, &full[st]);
           }
           if (!waited) {  // the weight copy is on its way; activations wait for the producer kernel
@@ -352,7 +355,7 @@ lora_shrink_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, 
             waited = true;
           }
           if (xsrc)
-            bulk_g2s(base + (kJT + lane - 16) * pitch, xsrc + k0, cl * 2, &full[st]);
+            bulk_g2s(base + (JT + lane - 16) * pitch, xsrc + k0, cl * 2, &full[st]);
           ++q;
         }
         ++jn;
@@ -388,8 +391,9 @@ lora_shrink_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, 
   // -------------------------------------------------------------- consumers
   const int g = lane >> 2, tq = lane & 3;
   const uint4 zero = make_uint4(0, 0, 0, 0);
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  float acc2[4] = {0.f, 0.f, 0.f, 0.f};  // odd k blocks: a second, independent mma chain
+  constexpr int NT = JT / 8;  // 8-column mma tiles per item
+  float acc[NT][4] = {};
+  float acc2[NT][4] = {};  // odd k blocks: a second, independent mma chain
   for (uint32_t q = 0;; ++q) {
     const int st = (int)(q % kStages);
     if (!mbar_wait(&full[st], (q / kStages) & 1, kWaitPolls, wlim)) {
@@ -403,10 +407,12 @@ lora_shrink_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, 
     const int cm = jb.cm;
     if (k0 == 0) {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) acc[e] = acc2[e] = 0.f;
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[nt][e] = acc2[nt][e] = 0.f;
     }
     const unsigned char* W = stages + (size_t)st * kStageBytes;
-    const unsigned char* X = W + kJT * pitch;
+    const unsigned char* X = W + JT * pitch;
     const int nkb = (len + 31) >> 5;
     const int kb0 = warp * nkb / kConsumers, kb1 = (warp + 1) * nkb / kConsumers;
 #pragma unroll 2
@@ -417,14 +423,17 @@ lora_shrink_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, 
         const bool kin = kb + h < kb1 && kk < len;
         const uint4 xa = (kin && g < cm) ? lds16(X + g * pitch + kk * 2) : zero;
         const uint4 xb = (kin && g + 8 < cm) ? lds16(X + (g + 8) * pitch + kk * 2) : zero;
-        const uint4 a = kin ? lds16(W + g * pitch + kk * 2) : zero;
-        // k step 0 <- elements 8t..8t+3, k step 1 <- 8t+4..8t+7 (same map in both operands)
-        if (h == 0) {
-          mma_16816(acc, xa.x, xb.x, xa.y, xb.y, a.x, a.y);
-          mma_16816(acc, xa.z, xb.z, xa.w, xb.w, a.z, a.w);
-        } else {
-          mma_16816(acc2, xa.x, xb.x, xa.y, xb.y, a.x, a.y);
-          mma_16816(acc2, xa.z, xb.z, xa.w, xb.w, a.z, a.w);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {  // weight row nt * 8 + g
+          const uint4 a = kin ? lds16(W + (nt * 8 + g) * pitch + kk * 2) : zero;
+          // k step 0 <- elements 8t..8t+3, k step 1 <- 8t+4..8t+7 (same map in both operands)
+          if (h == 0) {
+            mma_16816(acc[nt], xa.x, xb.x, xa.y, xb.y, a.x, a.y);
+            mma_16816(acc[nt], xa.z, xb.z, xa.w, xb.w, a.z, a.w);
+          } else {
+            mma_16816(acc2[nt], xa.x, xb.x, xa.y, xb.y, a.x, a.y);
+            mma_16816(acc2[nt], xa.z, xb.z, xa.w, xb.w, a.z, a.w);
+          }
         }
       }
     }
@@ -432,32 +441,36 @@ lora_shrink_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, 
     if (lane == 0) mbar_arrive(&empty[st]);
     if (k0 + len >= K) {  // last chunk of the job: add the four partials, store
 #pragma unroll
-      for (int e = 0; e < 4; ++e) acc[e] += acc2[e];
-      if (warp > 0) {
+      for (int nt = 0; nt < NT; ++nt) {  // one 8-column tile at a time through `red`
 #pragma unroll
-        for (int e = 0; e < 4; ++e) red[warp - 1][e][lane] = acc[e];
+        for (int e = 0; e < 4; ++e) acc[nt][e] += acc2[nt][e];
+        if (warp > 0) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) red[warp - 1][e][lane] = acc[nt][e];
+        }
+        named_sync(1, kConsumers * 32);
+        if (warp == 0) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+#pragma unroll
+            for (int w = 0; w < kConsumers - 1; ++w) acc[nt][e] += red[w][e][lane];
+          const int cin = nt * 8 + 2 * tq;  // column inside the item
+          const int col = jb.jt * JT + cin;
+          // columns past the adapter's rank are zero padding: written as 0
+          const bool k0v = !RANKS || cin < jb.ncols, k1v = !RANKS || cin + 1 < jb.ncols;
+          const bool cok = MOL_CHECK(col >= 0 && col + 2 <= R, MOL_CHECK_COLUMN, col);
+          if (g < cm && cok &&
+              MOL_CHECK(jb.rows[g] >= 0 && (int64_t)jb.rows[g] < numel, MOL_CHECK_ROW, jb.rows[g]))
+            *reinterpret_cast<float2*>(inter + (int64_t)jb.rows[g] * R + col) =
+                make_float2(k0v ? acc[nt][0] : 0.f, k1v ? acc[nt][1] : 0.f);
+          if (g + 8 < cm && cok &&
+              MOL_CHECK(jb.rows[g + 8] >= 0 && (int64_t)jb.rows[g + 8] < numel, MOL_CHECK_ROW,
+                        jb.rows[g + 8]))
+            *reinterpret_cast<float2*>(inter + (int64_t)jb.rows[g + 8] * R + col) =
+                make_float2(k0v ? acc[nt][2] : 0.f, k1v ? acc[nt][3] : 0.f);
+        }
+        named_sync(1, kConsumers * 32);
       }
-      named_sync(1, kConsumers * 32);
-      if (warp == 0) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-#pragma unroll
-          for (int w = 0; w < kConsumers - 1; ++w) acc[e] += red[w][e][lane];
-        const int col = jb.jt * kJT + 2 * tq;
-        // columns past the adapter's rank are zero padding: written as 0
-        const bool k0v = !RANKS || 2 * tq < jb.ncols, k1v = !RANKS || 2 * tq + 1 < jb.ncols;
-        const bool cok = MOL_CHECK(col >= 0 && col + 2 <= R, MOL_CHECK_COLUMN, col);
-        if (g < cm && cok &&
-            MOL_CHECK(jb.rows[g] >= 0 && (int64_t)jb.rows[g] < numel, MOL_CHECK_ROW, jb.rows[g]))
-          *reinterpret_cast<float2*>(inter + (int64_t)jb.rows[g] * R + col) =
-              make_float2(k0v ? acc[0] : 0.f, k1v ? acc[1] : 0.f);
-        if (g + 8 < cm && cok &&
-            MOL_CHECK(jb.rows[g + 8] >= 0 && (int64_t)jb.rows[g + 8] < numel, MOL_CHECK_ROW,
-                      jb.rows[g + 8]))
-          *reinterpret_cast<float2*>(inter + (int64_t)jb.rows[g + 8] * R + col) =
-              make_float2(k0v ? acc[2] : 0.f, k1v ? acc[3] : 0.f);
-      }
-      named_sync(1, kConsumers * 32);
     }
   }
 }
@@ -1009,11 +1022,10 @@ cudaError_t prepare_lora_kernels() {
   if (e != cudaSuccess) return e;
   e = prepare_expand_st<8, false>();
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(lora_shrink_kernel<false>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sp::kSmem);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(lora_shrink_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)sp::kSmem);
+  for (auto k : {lora_shrink_kernel<false, 8>, lora_shrink_kernel<true, 8>,
+                 lora_shrink_kernel<false, 16>, lora_shrink_kernel<true, 16>})
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sp::kSmem);
+  return e;
 }
 
 cudaError_t launch_shrink(const void* x, int64_t x_stride, int x_div, int K, const void* lora_a,
@@ -1027,7 +1039,11 @@ cudaError_t launch_shrink(const void* x, int64_t x_stride, int x_div, int K, con
   if (!lora_ranks && shrink_tc_fits(numel, num_vexperts, R, K, block_m))
     return launch_shrink_tc(x, x_stride, x_div, K, lora_a, R, sorted_ids, expert_ids, ntpp,
                             capacity, block_m, numel, num_vexperts, inter, stream);
-  const int n_jt = R / sp::kJT;
+  // many activation rows per routed block (at least four pairs per virtual expert on
+  // average): items of 16 weight rows, so each item's rows are copied once for twice
+  // the weight bytes; otherwise items of 8 weight rows keep the blocks' shares even
+  const int JT = (r1 % 16 == 0 && numel >= 4 * std::min<int64_t>(numel, num_vexperts)) ? 16 : 8;
+  const int n_jt = R / JT;
   const int num_loras = lora_ranks ? num_vexperts / num_experts : 0;
   const int64_t n_items = nblk * n_jt;
   const int64_t G = std::min<int64_t>(n_items, (int64_t)device_sms() * sp::kBlocksPerSM);
@@ -1039,7 +1055,9 @@ cudaError_t launch_shrink(const void* x, int64_t x_stride, int x_div, int K, con
       num_vexperts <= 32 * G &&
       std::min<int64_t>(numel, num_vexperts) * R * K * 2 <= kPrefetchBudget)
     pf = *prefetch;
-  return launch_pdl(lora_ranks ? lora_shrink_kernel<true> : lora_shrink_kernel<false>,
+  auto kernel = JT == 16 ? (lora_ranks ? lora_shrink_kernel<true, 16> : lora_shrink_kernel<false, 16>)
+                         : (lora_ranks ? lora_shrink_kernel<true, 8> : lora_shrink_kernel<false, 8>);
+  return launch_pdl(kernel,
                     dim3((unsigned)G), dim3(sp::kThreads), sp::kSmem, stream,
                     static_cast<const uint16_t*>(x), x_stride, x_div, K,
                     static_cast<const uint16_t*>(lora_a), R, sorted_ids, expert_ids, ntpp, block_m,
