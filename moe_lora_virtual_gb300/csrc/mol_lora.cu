@@ -673,12 +673,12 @@ lora_expand_kernel(const float* __restrict__ inter, int R, const uint16_t* __res
   }
 }
 
-// Staged expand, rank 8, 16, 32 or 64. One item = (routed block t, slice s, 256
-// output columns). One thread copies the item's lora_b rows (256 x RK bf16,
-// contiguous in [V, N, r]) into shared memory with a bulk copy, and every
-// thread copies its pieces of the output rows to update with cp.async, so
-// neither takes registers while in flight; each warp covers 64 columns (two
-// 32-column groups) with the intermediate it loads once. At rank 32, 64
+// Staged expand, rank 8, 16, 32 or 64. One item = (routed block t, slice s, COLS
+// output columns, 256 or 512). One thread copies the item's lora_b rows (COLS x
+// RK bf16, contiguous in [V, N, r]) into shared memory with a bulk copy, and
+// every thread copies its pieces of the output rows to update with cp.async, so
+// neither takes registers while in flight; each warp covers COLS / 4 columns
+// (32-column groups) with the intermediate it loads once. At rank 32, 64
 // registers and 26 KB let eight blocks share an SM, enough to run the decode
 // expands in about one wave. Fragment layout, MMA order per accumulator,
 // rounding and the handling of adapter arrays (ADAPT: rank 0 writes nothing;
@@ -688,18 +688,17 @@ lora_expand_kernel(const float* __restrict__ inter, int R, const uint16_t* __res
 // output rows are copied while the current one computes. Rank 8 runs the
 // rank-16 step (k = 16) with the upper eight k columns zero in both operands:
 // quads tq = 2, 3 of a warp, which would hold them, load nothing.
-constexpr int kStCols = 256;
-constexpr int kStGroups = kStCols / (kExpandThreads / 32) / 32;  // column groups per warp
-constexpr int kStOutPitch = kStCols + 32;  // staged output row, elements (64-byte skew per row)
+// COLS: output columns per item, 256, or 512 (ranks 8 and 16 with one staged tile)
+__host__ __device__ constexpr int st_out_pitch(int cols) { return cols + 32; }  // elements (64-byte skew per row)
 // dynamic shared memory of one block: the lora_b tile, then the output row tile(s), then
 // (two staged tiles) the next tile's intermediate fragments
-constexpr size_t expand_st_smem(int rk, bool db) {
-  return (size_t)kStCols * rk * 2 + (size_t)(db ? 2 : 1) * 16 * kStOutPitch * 2 +
+constexpr size_t expand_st_smem(int rk, bool db, int cols) {
+  return (size_t)cols * rk * 2 + (size_t)(db ? 2 : 1) * 16 * st_out_pitch(cols) * 2 +
          (db ? (size_t)16 * rk * 4 : 0);
 }
 
-template <int RK, bool EARLY, bool ADAPT, bool DB>
-__global__ void __launch_bounds__(kExpandThreads, RK == 64 ? (DB ? 4 : 5) : (DB ? 6 : 8))
+template <int RK, bool EARLY, bool ADAPT, bool DB, int COLS>
+__global__ void __launch_bounds__(kExpandThreads, RK == 64 ? (DB ? 4 : 5) : COLS == 512 ? 6 : (DB ? 6 : 8))
 lora_expand_st_kernel(const float* __restrict__ inter, int R, const uint16_t* __restrict__ lora_b,
                       int S, int Ns, float scale, const float* __restrict__ topk_w,
                       const int* __restrict__ sorted_ids, const int* __restrict__ expert_ids,
@@ -708,6 +707,10 @@ lora_expand_st_kernel(const float* __restrict__ inter, int R, const uint16_t* __
                       int chunks_per_slice, const int* __restrict__ lora_ranks,
                       const float* __restrict__ lora_scalings, int num_experts) {
   static_assert(RK == 8 || RK == 16 || RK == 32 || RK == 64, "staged expand: rank 8, 16, 32 or 64");
+  static_assert(COLS == 256 || COLS == 512, "staged expand: 256 or 512 columns per item");
+  constexpr int kStCols = COLS;
+  constexpr int kStGroups = kStCols / (kExpandThreads / 32) / 32;  // column groups per warp
+  constexpr int kStOutPitch = st_out_pitch(kStCols);
   constexpr bool K16 = (RK <= 16);
   constexpr int KB = K16 ? 1 : RK / 32;  // k blocks (32 wide, or one 16-wide block)
   extern __shared__ __align__(128) unsigned char st_smem[];
@@ -991,12 +994,12 @@ static int device_sms() {
 }
 
 // Opts the staged expand instances above 48 KB of dynamic shared memory in.
-template <int RK, bool DB>
+template <int RK, bool DB, int COLS = 256>
 static cudaError_t prepare_expand_st() {
-  const int bytes = (int)expand_st_smem(RK, DB);
+  const int bytes = (int)expand_st_smem(RK, DB, COLS);
   cudaError_t e = cudaSuccess;
-  for (auto k : {lora_expand_st_kernel<RK, false, false, DB>, lora_expand_st_kernel<RK, false, true, DB>,
-                 lora_expand_st_kernel<RK, true, false, DB>, lora_expand_st_kernel<RK, true, true, DB>})
+  for (auto k : {lora_expand_st_kernel<RK, false, false, DB, COLS>, lora_expand_st_kernel<RK, false, true, DB, COLS>,
+                 lora_expand_st_kernel<RK, true, false, DB, COLS>, lora_expand_st_kernel<RK, true, true, DB, COLS>})
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   return e;
 }
@@ -1021,6 +1024,10 @@ cudaError_t prepare_lora_kernels() {
   e = prepare_expand_st<8, true>();
   if (e != cudaSuccess) return e;
   e = prepare_expand_st<8, false>();
+  if (e != cudaSuccess) return e;
+  e = prepare_expand_st<16, false, 512>();
+  if (e != cudaSuccess) return e;
+  e = prepare_expand_st<8, false, 512>();
   if (e != cudaSuccess) return e;
   for (auto k : {lora_shrink_kernel<false, 8>, lora_shrink_kernel<true, 8>,
                  lora_shrink_kernel<false, 16>, lora_shrink_kernel<true, 16>})
@@ -1095,28 +1102,35 @@ cudaError_t launch_expand(const float* inter, const void* lora_b, int S, int r, 
     return launch_expand_tc(inter, lora_b, S, Ns, scale, topk_weights, sorted_ids, expert_ids, ntpp,
                             capacity, block_m, numel, num_vexperts, out, out_stride, stream);
   if (r == 8 || r == 16 || r == 32 || r == 64) {
-    const int cps_st = (Ns + kStCols - 1) / kStCols;
+    // many rows per virtual expert (on average at least 32 pairs each): blocks hold
+    // several row tiles, so the output rows of the next one are prefetched
+    const bool db = numel >= 32 * std::min<int64_t>(numel, num_vexperts);
+    // ranks 8 and 16 with at least four pairs per virtual expert on average: items of
+    // 512 columns, so a block moves about as many bytes as a rank-32 item of 256 and
+    // the grid has half the blocks (each pays the routing reads and the row compaction)
+    const bool wide = r <= 16 && !db && numel >= 4 * std::min<int64_t>(numel, num_vexperts);
+    const int cols = wide ? 512 : 256;
+    const int cps_st = (Ns + cols - 1) / cols;
     if (nblk * S * cps_st > INT32_MAX) return cudaErrorInvalidConfiguration;
     const dim3 grid_st((unsigned)(nblk * S * cps_st));
     const bool adapt = lora_ranks != nullptr || lora_scalings != nullptr;
     const int ne = num_experts < 1 ? 1 : num_experts;
-    // many rows per virtual expert (on average at least 32 pairs each): blocks hold
-    // several row tiles, so the output rows of the next one are prefetched
-    const bool db = numel >= 32 * std::min<int64_t>(numel, num_vexperts);
-#define MOL_EXPAND_ST(RK, E, A, D)                                                            \
-  launch_pdl(lora_expand_st_kernel<RK, E, A, D>, grid_st, dim3(kExpandThreads),               \
-             expand_st_smem(RK, D), stream, inter, R, b, S, Ns, scale, topk_weights, sorted_ids, \
-             expert_ids, ntpp, block_m, numel, num_vexperts, o, out_stride, cps_st, lora_ranks, \
+#define MOL_EXPAND_ST(RK, E, A, D, C)                                                            \
+  launch_pdl(lora_expand_st_kernel<RK, E, A, D, C>, grid_st, dim3(kExpandThreads),               \
+             expand_st_smem(RK, D, C), stream, inter, R, b, S, Ns, scale, topk_weights, sorted_ids, \
+             expert_ids, ntpp, block_m, numel, num_vexperts, o, out_stride, cps_st, lora_ranks,    \
              lora_scalings, ne)
-#define MOL_EXPAND_ST_A(RK, E, A) (db ? MOL_EXPAND_ST(RK, E, A, true) : MOL_EXPAND_ST(RK, E, A, false))
-#define MOL_EXPAND_ST_RK(RK)                                                              \
-  return early ? (adapt ? MOL_EXPAND_ST_A(RK, true, true) : MOL_EXPAND_ST_A(RK, true, false)) \
-               : (adapt ? MOL_EXPAND_ST_A(RK, false, true) : MOL_EXPAND_ST_A(RK, false, false))
-    if (r == 8) MOL_EXPAND_ST_RK(8);
-    if (r == 16) MOL_EXPAND_ST_RK(16);
-    if (r == 32) MOL_EXPAND_ST_RK(32);
-    MOL_EXPAND_ST_RK(64);
+#define MOL_EXPAND_ST_A(RK, E, A) (db ? MOL_EXPAND_ST(RK, E, A, true, 256) : MOL_EXPAND_ST(RK, E, A, false, 256))
+#define MOL_EXPAND_ST_W(RK, E, A) (wide ? MOL_EXPAND_ST(RK, E, A, false, 512) : MOL_EXPAND_ST_A(RK, E, A))
+#define MOL_EXPAND_ST_RK(RK, M)                                                  \
+  return early ? (adapt ? M(RK, true, true) : M(RK, true, false))                \
+               : (adapt ? M(RK, false, true) : M(RK, false, false))
+    if (r == 8) MOL_EXPAND_ST_RK(8, MOL_EXPAND_ST_W);
+    if (r == 16) MOL_EXPAND_ST_RK(16, MOL_EXPAND_ST_W);
+    if (r == 32) MOL_EXPAND_ST_RK(32, MOL_EXPAND_ST_A);
+    MOL_EXPAND_ST_RK(64, MOL_EXPAND_ST_A);
 #undef MOL_EXPAND_ST_RK
+#undef MOL_EXPAND_ST_W
 #undef MOL_EXPAND_ST_A
 #undef MOL_EXPAND_ST
   }

@@ -128,6 +128,10 @@ SHAPES = [
     (20, 2, 2, 1, 32, 64, 8, 128, 16, False, 0, 8, False, 0.0),    # largest R = 8 x 128
     (30, 4, 5, 2, 16, 320, 1, 8, 200, True, 8, 8, True, 0.1),      # rank 8, one slice (R = 8)
     (25, 2, 3, 2, 32, 128, 2, 8, 48, False, 0, 0, False, 0.2),     # rank 8, two slices
+    # four to 32 pairs per virtual expert: 16-row shrink items, 512-column expand items
+    # with a ragged last item
+    (120, 8, 16, 4, 32, 256, 2, 16, 1288, True, 0, 8, True, 0.1),
+    (100, 6, 12, 3, 16, 136, 1, 8, 1096, False, 8, 0, False, 0.2),
 ]
 
 
