@@ -71,6 +71,22 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// A launch in plain stream order: it starts once the previous kernel has finished
+// (for grids of resident blocks with a fixed share of work each, which would
+// otherwise start one by one as the previous kernel's blocks leave).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_ordered(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                           cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.numAttrs = 0;
+  count_launch();
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Per-token adapter ids from per-request slots (seg_indptr non-decreasing).
 cudaError_t launch_token_lora_ids(const int32_t* weight_indices, const int32_t* seg_indptr,
                                   int num_reqs, int64_t num_tokens, int max_loras,

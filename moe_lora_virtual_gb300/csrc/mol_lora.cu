@@ -250,7 +250,8 @@ lora_shrink_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, 
         if (below)
           (void)MOL_NOTE(cur_r.e >= -1 && cur_r.e < num_vexperts, MOL_CHECK_ROUTE_EXPERT, cur_r.t);
       }
-      const int v = below ? cur_r.e : -1;
+      if (!below) break;  // the block's later items lie further past the routed blocks
+      const int v = cur_r.e;
       if (v < 0 || v >= num_vexperts) continue;
       if (kChecked && jt_c == 0) {
 #pragma unroll
@@ -697,15 +698,22 @@ constexpr size_t expand_st_smem(int rk, bool db, int cols) {
          (db ? (size_t)16 * rk * 4 : 0);
 }
 
-template <int RK, bool EARLY, bool ADAPT, bool DB, int COLS>
-__global__ void __launch_bounds__(kExpandThreads, RK == 64 ? (DB ? 4 : 5) : COLS == 512 ? 6 : (DB ? 6 : 8))
-lora_expand_st_kernel(const float* __restrict__ inter, int R, const uint16_t* __restrict__ lora_b,
-                      int S, int Ns, float scale, const float* __restrict__ topk_w,
-                      const int* __restrict__ sorted_ids, const int* __restrict__ expert_ids,
-                      const int* __restrict__ ntpp_ptr, int block_m, int64_t numel,
-                      int num_vexperts, uint16_t* __restrict__ out, int64_t out_stride,
-                      int chunks_per_slice, const int* __restrict__ lora_ranks,
-                      const float* __restrict__ lora_scalings, int num_experts) {
+// Outcome of one staged expand item: skipped (nothing copied), done (its weight tile
+// consumed one phase of the weight barrier), past the routed blocks, or the block leaves
+// (a wait ran out or a check failed).
+enum StItem : int { kStSkip = 0, kStDone = 1, kStPast = 2, kStLeave = 3 };
+
+// Item `it` of the staged expand (lora_expand_st_kernel). Every return is block-uniform.
+template <int RK, bool EARLY, bool ADAPT, bool DB, int COLS, bool LOOP>
+MOL_DEV int expand_st_item(int it, uint32_t wphase, bool& waited, unsigned char* st_smem,
+                           uint64_t* wbar, int* rows, int* wcnt, const float* __restrict__ inter,
+                           int R, const uint16_t* __restrict__ lora_b, int S, int Ns, float scale,
+                           const float* __restrict__ topk_w, const int* __restrict__ sorted_ids,
+                           const int* __restrict__ expert_ids, const int* __restrict__ ntpp_ptr,
+                           int block_m, int64_t numel, int num_vexperts,
+                           uint16_t* __restrict__ out, int64_t out_stride, int chunks_per_slice,
+                           int n_items, const int* __restrict__ lora_ranks,
+                           const float* __restrict__ lora_scalings, int num_experts) {
   static_assert(RK == 8 || RK == 16 || RK == 32 || RK == 64, "staged expand: rank 8, 16, 32 or 64");
   static_assert(COLS == 256 || COLS == 512, "staged expand: 256 or 512 columns per item");
   constexpr int kStCols = COLS;
@@ -713,31 +721,23 @@ lora_expand_st_kernel(const float* __restrict__ inter, int R, const uint16_t* __
   constexpr int kStOutPitch = st_out_pitch(kStCols);
   constexpr bool K16 = (RK <= 16);
   constexpr int KB = K16 ? 1 : RK / 32;  // k blocks (32 wide, or one 16-wide block)
-  extern __shared__ __align__(128) unsigned char st_smem[];
   uint16_t* wsm = reinterpret_cast<uint16_t*>(st_smem);  // kStCols x RK lora_b rows
   uint16_t* osm = wsm + kStCols * RK;                     // (DB ? 2 : 1) x 16 output rows
   float* ism = reinterpret_cast<float*>(osm + (DB ? 2 : 1) * 16 * kStOutPitch);  // DB: 16 x RK
-  __shared__ uint64_t wbar;
-  __shared__ int rows[128];
-  __shared__ int wcnt[kExpandThreads / 32];
-
   const int tid = threadIdx.x;
   const int per_block = S * chunks_per_slice;
-  const int t = blockIdx.x / per_block;
-  const int rem = blockIdx.x - t * per_block;
+  const int t = it / per_block;
+  const int rem = it - t * per_block;
   const int s = rem / chunks_per_slice;
   const int chunk = rem - s * chunks_per_slice;
-  if (!EARLY) {
-    pdl_wait();
-    pdl_launch_dependents();
-  }
   const int ntpp = __ldg(ntpp_ptr);
   const int v = __ldg(expert_ids + t);
   const int slot = tid < block_m ? __ldg(sorted_ids + (int64_t)t * block_m + tid) : -1;
   if (kChecked && rem == 0)
     note_block_routing(t, ntpp, v, slot, block_m, numel, num_vexperts,
-                       (int64_t)(gridDim.x / per_block) * block_m);
-  if ((int64_t)t * block_m >= ntpp || v < 0 || v >= num_vexperts) return;
+                       (int64_t)(n_items / per_block) * block_m);
+  if ((int64_t)t * block_m >= ntpp) return kStPast;
+  if (v < 0 || v >= num_vexperts) return kStSkip;
   // the adapter's rank and scaling, in flight over the row compaction
   int rk_raw = RK;
   float scl = 1.f;
@@ -745,16 +745,12 @@ lora_expand_st_kernel(const float* __restrict__ inter, int R, const uint16_t* __
     if (lora_ranks) rk_raw = __ldg(lora_ranks + v / num_experts);
     if (lora_scalings) scl = __ldg(lora_scalings + v / num_experts);
   }
-  if (tid == 0) {
-    mbar_init(&wbar, 1);
-    fence_mbar_init();
-  }
-  const int c = compact_block_rows(slot, numel, rows, wcnt);  // its barriers publish the init
-  if (c == 0) return;
+  const int c = compact_block_rows(slot, numel, rows, wcnt);
+  if (c == 0) return kStSkip;
   // rank 0: the adapter writes no delta (nothing is copied); past rank rl the
   // intermediate and the weight columns are padding and take no part
   const int rl = rk_raw < 0 ? 0 : (rk_raw > RK ? RK : rk_raw);
-  if (ADAPT && rl == 0) return;
+  if (ADAPT && rl == 0) return kStSkip;
   const float scale_v = ADAPT ? scale * scl : scale;
   // columns [col0, col0 + ncols) of the slice; ncols > 0 (chunk < ceil(Ns / kStCols)) and a
   // multiple of 8, so the copy is a multiple of 16 bytes from a 16-byte aligned row
@@ -768,12 +764,12 @@ lora_expand_st_kernel(const float* __restrict__ inter, int R, const uint16_t* __
       (void)MOL_CHECK(wok, MOL_CHECK_WEIGHT_ROW, wr);
       (void)MOL_CHECK(cok, MOL_CHECK_COLUMN, s * RK);
     }
-    if (!wok || !cok) return;
+    if (!wok || !cok) return kStLeave;
   }
   if (tid == 0) {
     const uint32_t bytes = (uint32_t)ncols * RK * 2;
-    mbar_arrive_expect_tx(&wbar, bytes);
-    bulk_g2s(wsm, lora_b + ((int64_t)v * S * Ns + (int64_t)s * Ns + col0) * RK, bytes, &wbar);
+    mbar_arrive_expect_tx(wbar, bytes);
+    bulk_g2s(wsm, lora_b + ((int64_t)v * S * Ns + (int64_t)s * Ns + col0) * RK, bytes, wbar);
   }
 
   const int lane = tid & 31, warp = tid >> 5, g = lane >> 2, tq = lane & 3;
@@ -827,9 +823,10 @@ lora_expand_st_kernel(const float* __restrict__ inter, int R, const uint16_t* __
   };
   load_out(0, i0, i1);
   cp_async_commit();
-  if (EARLY) {
+  if (!waited) {
     pdl_wait();  // the intermediate comes from the shrink that precedes this kernel
     pdl_launch_dependents();
+    waited = true;
   }
   if constexpr (DB) {
     load_inter(i0, i1);
@@ -903,13 +900,14 @@ lora_expand_st_kernel(const float* __restrict__ inter, int R, const uint16_t* __
     };
     if (!DB) build();
     if (!landed) {  // every thread sees the weight copy land before it reads the tile
-      bool ok = mbar_wait(&wbar, 0, kWaitPolls);
-      // two staged tiles: a barrier follows, so the block leaves together or not at all
-      if constexpr (DB) ok = __syncthreads_and(ok ? 1 : 0) != 0;
+      bool ok = mbar_wait(wbar, wphase, kWaitPolls);
+      // two staged tiles, or more items to come: barriers follow, so the block leaves
+      // together or not at all (one item: each thread may leave alone)
+      if constexpr (DB || LOOP) ok = __syncthreads_and(ok ? 1 : 0) != 0;
       if (!ok) {
         atomicOr(&g_fault_flags, kFaultBulkTimeout);
         cp_async_wait_all();
-        return;
+        return kStLeave;
       }
       landed = true;
     }
@@ -979,6 +977,51 @@ lora_expand_st_kernel(const float* __restrict__ inter, int R, const uint16_t* __
       }
     }
   }
+  return kStDone;
+}
+
+// LOOP (more than four items per resident block): a wave of resident blocks, block b
+// taking items b + j * gridDim.x in order of the routed block t, so once t lies past the
+// routed blocks so do all later ones and the block leaves; the row compaction's first
+// barrier comes after every thread has finished the previous item (its rows, its weight
+// tile, its weight barrier phase). Otherwise one block per item.
+template <int RK, bool EARLY, bool ADAPT, bool DB, int COLS, bool LOOP>
+__global__ void __launch_bounds__(kExpandThreads, RK == 64 ? (DB ? 4 : 5) : COLS == 512 ? 6 : (DB ? 6 : 8))
+lora_expand_st_kernel(const float* __restrict__ inter, int R, const uint16_t* __restrict__ lora_b,
+                      int S, int Ns, float scale, const float* __restrict__ topk_w,
+                      const int* __restrict__ sorted_ids, const int* __restrict__ expert_ids,
+                      const int* __restrict__ ntpp_ptr, int block_m, int64_t numel,
+                      int num_vexperts, uint16_t* __restrict__ out, int64_t out_stride,
+                      int chunks_per_slice, int n_items, const int* __restrict__ lora_ranks,
+                      const float* __restrict__ lora_scalings, int num_experts) {
+  extern __shared__ __align__(128) unsigned char st_smem[];
+  __shared__ uint64_t wbar;
+  __shared__ int rows[128];
+  __shared__ int wcnt[kExpandThreads / 32];
+  if (threadIdx.x == 0) {
+    mbar_init(&wbar, 1);
+    fence_mbar_init();  // the first row compaction's barriers publish the init
+  }
+  if (!EARLY) {
+    pdl_wait();
+    pdl_launch_dependents();
+  }
+  bool waited = !EARLY;
+#define MOL_ST_ITEM_ARGS                                                                       \
+  st_smem, &wbar, rows, wcnt, inter, R, lora_b, S, Ns, scale, topk_w, sorted_ids, expert_ids, \
+      ntpp_ptr, block_m, numel, num_vexperts, out, out_stride, chunks_per_slice, n_items,      \
+      lora_ranks, lora_scalings, num_experts
+  if constexpr (!LOOP) {
+    (void)expand_st_item<RK, EARLY, ADAPT, DB, COLS, false>(blockIdx.x, 0u, waited, MOL_ST_ITEM_ARGS);
+  } else {
+    uint32_t wphase = 0;  // parity of the weight barrier's next phase
+    for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+      const int r = expand_st_item<RK, EARLY, ADAPT, DB, COLS, true>(it, wphase, waited, MOL_ST_ITEM_ARGS);
+      if (r == kStPast || r == kStLeave) break;
+      if (r == kStDone) wphase ^= 1;
+    }
+  }
+#undef MOL_ST_ITEM_ARGS
 }
 
 static int device_sms() {
@@ -993,13 +1036,35 @@ static int device_sms() {
   return cache[dev];
 }
 
-// Opts the staged expand instances above 48 KB of dynamic shared memory in.
+// Blocks of `kernel` (kExpandThreads threads, `smem` dynamic bytes) resident on the
+// device at once: its SM count times its occupancy, cached per kernel and device.
+template <typename Kernel>
+static int64_t resident_blocks(Kernel kernel, size_t smem) {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kExpandThreads, smem) != cudaSuccess ||
+        n <= 0)
+      n = 1;
+    cache[dev] = n;
+  }
+  return (int64_t)device_sms() * cache[dev];
+}
+
+// Opts the staged expand instances above 48 KB of dynamic shared memory in (the looping
+// ones exist for one staged tile and without early reads).
 template <int RK, bool DB, int COLS = 256>
 static cudaError_t prepare_expand_st() {
   const int bytes = (int)expand_st_smem(RK, DB, COLS);
   cudaError_t e = cudaSuccess;
-  for (auto k : {lora_expand_st_kernel<RK, false, false, DB, COLS>, lora_expand_st_kernel<RK, false, true, DB, COLS>,
-                 lora_expand_st_kernel<RK, true, false, DB, COLS>, lora_expand_st_kernel<RK, true, true, DB, COLS>})
+  for (auto k : {lora_expand_st_kernel<RK, false, false, DB, COLS, false>,
+                 lora_expand_st_kernel<RK, false, true, DB, COLS, false>,
+                 lora_expand_st_kernel<RK, true, false, DB, COLS, false>,
+                 lora_expand_st_kernel<RK, true, true, DB, COLS, false>,
+                 lora_expand_st_kernel<RK, false, false, false, COLS, true>,
+                 lora_expand_st_kernel<RK, false, true, false, COLS, true>})
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   return e;
 }
@@ -1072,6 +1137,32 @@ cudaError_t launch_shrink(const void* x, int64_t x_stride, int x_div, int K, con
                     num_experts < 1 ? 1 : num_experts, num_loras, pf);
 }
 
+// One staged expand instance over n_items items. One staged tile and more than four
+// items per resident block: one wave of resident blocks, each looping over items (no block
+// launch, barrier set-up and routing read per item; the blocks past the routed ones leave
+// at their first item there); otherwise one block per item, which the hardware deals to
+// the SMs as they free up (measured faster with few items per block).
+template <int RK, bool E, bool A, bool D, int C>
+static cudaError_t launch_expand_st(cudaStream_t stream, int64_t n_items, const float* inter, int R,
+                                    const uint16_t* b, int S, int Ns, float scale, const float* w,
+                                    const int32_t* sorted_ids, const int32_t* expert_ids,
+                                    const int32_t* ntpp, int block_m, int64_t numel,
+                                    int num_vexperts, uint16_t* o, int64_t out_stride, int cps,
+                                    const int32_t* ranks, const float* scalings, int ne) {
+  const size_t smem = expand_st_smem(RK, D, C);
+  const int64_t resident = resident_blocks(lora_expand_st_kernel<RK, E, A, D, C, false>, smem);
+  // every block starts at once, after the previous kernel (no early launch, so no early reads)
+  if (!D && n_items > 4 * resident)
+    return launch_ordered(lora_expand_st_kernel<RK, false, A, false, C, true>, dim3((unsigned)resident),
+                          dim3(kExpandThreads), smem, stream, inter, R, b, S, Ns, scale, w,
+                          sorted_ids, expert_ids, ntpp, block_m, numel, num_vexperts, o,
+                          out_stride, cps, (int)n_items, ranks, scalings, ne);
+  return launch_pdl(lora_expand_st_kernel<RK, E, A, D, C, false>, dim3((unsigned)n_items),
+                    dim3(kExpandThreads), smem, stream, inter, R, b, S, Ns, scale, w, sorted_ids,
+                    expert_ids, ntpp, block_m, numel, num_vexperts, o, out_stride, cps,
+                    (int)n_items, ranks, scalings, ne);
+}
+
 template <int RK, bool EARLY>
 static cudaError_t expand_rk(dim3 grid, cudaStream_t stream, const float* inter, int R,
                              const uint16_t* b, int S, int Ns, float scale, const float* w,
@@ -1111,17 +1202,18 @@ cudaError_t launch_expand(const float* inter, const void* lora_b, int S, int r, 
     const bool wide = r <= 16 && !db && numel >= 4 * std::min<int64_t>(numel, num_vexperts);
     const int cols = wide ? 512 : 256;
     const int cps_st = (Ns + cols - 1) / cols;
-    if (nblk * S * cps_st > INT32_MAX) return cudaErrorInvalidConfiguration;
-    const dim3 grid_st((unsigned)(nblk * S * cps_st));
+    const int64_t n_items = nblk * S * cps_st;
+    if (n_items > INT32_MAX) return cudaErrorInvalidConfiguration;
     const bool adapt = lora_ranks != nullptr || lora_scalings != nullptr;
     const int ne = num_experts < 1 ? 1 : num_experts;
 #define MOL_EXPAND_ST(RK, E, A, D, C)                                                            \
-  launch_pdl(lora_expand_st_kernel<RK, E, A, D, C>, grid_st, dim3(kExpandThreads),               \
-             expand_st_smem(RK, D, C), stream, inter, R, b, S, Ns, scale, topk_weights, sorted_ids, \
-             expert_ids, ntpp, block_m, numel, num_vexperts, o, out_stride, cps_st, lora_ranks,    \
-             lora_scalings, ne)
-#define MOL_EXPAND_ST_A(RK, E, A) (db ? MOL_EXPAND_ST(RK, E, A, true, 256) : MOL_EXPAND_ST(RK, E, A, false, 256))
-#define MOL_EXPAND_ST_W(RK, E, A) (wide ? MOL_EXPAND_ST(RK, E, A, false, 512) : MOL_EXPAND_ST_A(RK, E, A))
+  launch_expand_st<RK, E, A, D, C>(stream, n_items, inter, R, b, S, Ns, scale, topk_weights,     \
+                                   sorted_ids, expert_ids, ntpp, block_m, numel, num_vexperts, o, \
+                                   out_stride, cps_st, lora_ranks, lora_scalings, ne)
+#define MOL_EXPAND_ST_A(RK, E, A) \
+  (db ? MOL_EXPAND_ST(RK, E, A, true, 256) : MOL_EXPAND_ST(RK, E, A, false, 256))
+#define MOL_EXPAND_ST_W(RK, E, A) \
+  (wide ? MOL_EXPAND_ST(RK, E, A, false, 512) : MOL_EXPAND_ST_A(RK, E, A))
 #define MOL_EXPAND_ST_RK(RK, M)                                                  \
   return early ? (adapt ? M(RK, true, true) : M(RK, true, false))                \
                : (adapt ? M(RK, false, true) : M(RK, false, false))

@@ -72,6 +72,10 @@ CASES = [
     (40, 8, 8, 4, 16, 1032, 2, 32, 104, True, [5, 32, 19, 1]),
     (24, 4, 6, 3, 32, 776, 1, 16, 64, False, [3, 13, 16]),
     (16, 8, 8, 2, 64, 1544, 2, 64, 40, True, [33, 61]),
+    # more than four expand items per resident block: blocks loop over items (rank 16:
+    # 512-column items; rank 64: 256-column items), adapters of rank 0 skipped in the loop
+    (600, 8, 64, 4, 16, 256, 2, 16, 2048, True, [16, 0, 8, 12]),
+    (400, 8, 32, 4, 16, 128, 1, 64, 4096, False, [64, 0, 40, 17]),
 ]
 
 
