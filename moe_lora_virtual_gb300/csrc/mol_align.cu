@@ -176,12 +176,12 @@ MOL_DEV void warp_rank(const uint16_t* keys, int s0, int s1, uint16_t* mine, int
 
 // Column scan: the warp tables become exclusive per-warp bases inside the tile;
 // total(b, n) receives the tile's count of bucket b.
-template <typename F>
+template <int WARPS, typename F>
 MOL_DEV void column_scan(uint16_t* tbl, int nb, int nb_pad, F&& total) {
-  for (int b = threadIdx.x; b < nb; b += kAlignThreads) {
+  for (int b = threadIdx.x; b < nb; b += WARPS * 32) {
     int run = 0;
 #pragma unroll
-    for (int w = 0; w < kAlignWarps; ++w) {
+    for (int w = 0; w < WARPS; ++w) {
       uint16_t* p = tbl + w * nb_pad + b;
       const int c = *p;
       *p = (uint16_t)run;
@@ -235,7 +235,7 @@ align_tile_kernel(const int* __restrict__ src, const int* __restrict__ lora_ids,
     __syncthreads();
     // column scan: warp tables become exclusive bases; the tile total per bucket
     // goes to shared memory (one tile) or to the workspace histogram
-    column_scan(tbl, nb, nb_pad, [&](int b, int n) {
+    column_scan<kAlignWarps>(tbl, nb, nb_pad, [&](int b, int n) {
       const int64_t w = (int64_t)blockIdx.x * nb + b;
       if (fused)
         offs[b] = n;
@@ -358,62 +358,71 @@ MOL_DEV void st_peer(uint32_t a, int v) {
 // barrier every block scatters its pairs: cnt[key] + the pair's stable rank in
 // the tile. Every block reaches every barrier (no early exit, no data-dependent
 // wait), and no block reads or writes another's shared memory after the last.
-template <bool REMAP>
-__global__ void __launch_bounds__(kAlignThreads, 1)
+template <bool REMAP, int WARPS>
+__global__ void __launch_bounds__(WARPS * 32, 1)
 align_cluster_kernel(const int* __restrict__ src, const int* __restrict__ lora_ids, int topk,
                      int num_experts, int max_loras, int* __restrict__ vtopk_out, int64_t numel,
                      int num_vexperts, int block_m, int64_t capacity, int tile, int nb_pad,
                      int* __restrict__ sorted_ids, int* __restrict__ expert_ids,
                      int* __restrict__ ntpp_out, int trigger) {
+  constexpr int THREADS = WARPS * 32;
   extern __shared__ __align__(16) unsigned char smem[];
-  __shared__ int sh_scan[kAlignWarps + 1];
+  __shared__ int sh_scan[WARPS + 1];
   __shared__ int rsum[kClusterMax];  // padded total of each block's share of the buckets
   __shared__ int s_sentinel;         // offset of the sentinel bucket (in the block that holds it)
   const int nb = num_vexperts + 1;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int CL = (int)cluster_blocks(), me = (int)cluster_rank();
-  uint16_t* tbl = reinterpret_cast<uint16_t*>(smem);  // [kAlignWarps][nb_pad]
-  uint16_t* keys = tbl + kAlignWarps * nb_pad;        // [tile]
+  uint16_t* tbl = reinterpret_cast<uint16_t*>(smem);  // [WARPS][nb_pad]
+  uint16_t* keys = tbl + WARPS * nb_pad;              // [tile]
   int* cnt = reinterpret_cast<int*>(keys + tile);     // [nb]: counts, then this tile's bases
   int* opad = cnt + nb;                               // [per]: offsets inside this block's share
 
   {
     uint4* t4 = reinterpret_cast<uint4*>(tbl);
-    const int n4 = kAlignWarps * nb_pad / 8;
-    for (int q = tid; q < n4; q += kAlignThreads) t4[q] = make_uint4(0, 0, 0, 0);
+    const int n4 = WARPS * nb_pad / 8;
+    for (int q = tid; q < n4; q += THREADS) t4[q] = make_uint4(0, 0, 0, 0);
   }
   if (trigger == 2) pdl_launch_dependents();  // see align_tile_kernel
   pdl_wait();  // inputs and routing buffers belong to earlier kernels until here
   if (trigger == 1) pdl_launch_dependents();
 
-  for (int64_t q = (int64_t)me * kAlignThreads + tid; q < capacity;
-       q += (int64_t)CL * kAlignThreads)
-    sorted_ids[q] = (int)numel;
   const int64_t t0 = (int64_t)me * tile;
   const int tlen = (int)max((int64_t)0, min((int64_t)tile, numel - t0));
-  for (int q = tid; q < tlen; q += kAlignThreads) {
-    const int64_t i = t0 + q;
-    int vid;
-    if (REMAP) {
-      vid = remap_one(src[i], lora_ids[i / topk], num_experts, max_loras);
-      vtopk_out[i] = vid;
-    } else {
-      vid = src[i];
+  // the tile's ids, kLd per thread in flight at once, then its keys
+  constexpr int kLd = 8;
+  for (int q0 = 0; q0 < tlen; q0 += kLd * THREADS) {
+    int sv[kLd], lv[kLd];
+#pragma unroll
+    for (int j = 0; j < kLd; ++j) {
+      const int q = q0 + j * THREADS + tid;
+      sv[j] = q < tlen ? src[t0 + q] : -1;
+      lv[j] = (REMAP && q < tlen) ? lora_ids[(t0 + q) / topk] : -1;
     }
-    keys[q] = (uint16_t)bucket_of(vid, num_vexperts);
+#pragma unroll
+    for (int j = 0; j < kLd; ++j) {
+      const int q = q0 + j * THREADS + tid;
+      if (q < tlen) {
+        const int vid = REMAP ? remap_one(sv[j], lv[j], num_experts, max_loras) : sv[j];
+        if (REMAP) vtopk_out[t0 + q] = vid;
+        keys[q] = (uint16_t)bucket_of(vid, num_vexperts);
+      }
+    }
   }
+  for (int64_t q = (int64_t)me * THREADS + tid; q < capacity; q += (int64_t)CL * THREADS)
+    sorted_ids[q] = (int)numel;
   __syncthreads();
-  const int seg = tile / kAlignWarps;
+  const int seg = tile / WARPS;
   const int s0 = warp * seg, s1 = min(s0 + seg, tlen);
   uint16_t* mine = tbl + warp * nb_pad;
   warp_count(keys, s0, s1, mine, lane);
   __syncthreads();
-  column_scan(tbl, nb, nb_pad, [&](int b, int n) { cnt[b] = n; });
+  column_scan<WARPS>(tbl, nb, nb_pad, [&](int b, int n) { cnt[b] = n; });
   cluster_barrier();  // 1: every tile's counts are in its block's shared memory
 
   const int per = (nb + CL - 1) / CL;
   const int b0 = min(me * per, nb), b1 = min(b0 + per, nb);
-  const int ppt = (per + kAlignThreads - 1) / kAlignThreads;
+  const int ppt = (per + THREADS - 1) / THREADS;
   const int c0 = min(b0 + tid * ppt, b1), c1 = min(c0 + ppt, b1);
   const int pad = block_m - 1, lg = __ffs(block_m) - 1;
   int local = 0;
@@ -429,7 +438,7 @@ align_cluster_kernel(const int* __restrict__ src, const int* __restrict__ lora_i
     local += pb;
   }
   int share_total;
-  int run = block_exclusive_scan<kAlignThreads>(local, sh_scan, share_total);
+  int run = block_exclusive_scan<THREADS>(local, sh_scan, share_total);
   for (int b = c0; b < c1; ++b) {
     const int pb = opad[b - b0];
     opad[b - b0] = run;
@@ -470,7 +479,7 @@ align_cluster_kernel(const int* __restrict__ src, const int* __restrict__ lora_i
   }
   __syncthreads();
   if (b0 < nb && b1 == nb) {  // the sentinel's blocks and every block past them carry -1
-    for (int64_t t = (s_sentinel >> lg) + tid; t < (capacity >> lg); t += kAlignThreads)
+    for (int64_t t = (s_sentinel >> lg) + tid; t < (capacity >> lg); t += THREADS)
       expert_ids[t] = -1;
   }
   cluster_barrier();  // 3: cnt[b] is this tile's base in bucket b; the pad fill is done
@@ -582,7 +591,8 @@ static cudaError_t prepare_cluster_align() {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  for (auto k : {align_cluster_kernel<true>, align_cluster_kernel<false>}) {
+  for (auto k : {align_cluster_kernel<true, 8>, align_cluster_kernel<false, 8>,
+                 align_cluster_kernel<true, 16>, align_cluster_kernel<false, 16>}) {
     e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kAlignSmemMax);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
@@ -599,7 +609,7 @@ static cudaError_t prepare_cluster_align() {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  e = cudaOccupancyMaxActiveClusters(&n, (void*)align_cluster_kernel<true>, &cfg);
+  e = cudaOccupancyMaxActiveClusters(&n, (void*)align_cluster_kernel<true, 8>, &cfg);
   if (e != cudaSuccess) {
     (void)cudaGetLastError();  // a refused query leaves the portable size
     n = 0;
@@ -677,19 +687,24 @@ cudaError_t launch_align(const AlignPlan& plan, bool remap, const int32_t* src,
     const int tile = (int)(((plan.numel + cl - 1) / cl + 255) / 256 * 256);
     if (tile > kClusterTileMax) return cudaErrorInvalidConfiguration;
     const int per = (plan.nb + cl - 1) / cl;
-    const size_t smem = (size_t)kAlignWarps * plan.nb_pad * 2 + (size_t)tile * 2 +
-                        (size_t)plan.nb * 4 + (size_t)per * 4;
+    // shared memory of a block with `warps` warp tables
+    auto smem_of = [&](int warps) {
+      return (size_t)warps * plan.nb_pad * 2 + (size_t)tile * 2 + (size_t)plan.nb * 4 + (size_t)per * 4;
+    };
+    // sixteen warps where their tables fit (half the match rounds per warp), else eight
+    const bool w16 = smem_of(16) <= (size_t)kAlignSmemMax;
+    const size_t smem = smem_of(w16 ? 16 : 8);
     if (smem > (size_t)kAlignSmemMax) return cudaErrorInvalidConfiguration;
-    if (remap)
-      return launch_pdl_cluster(align_cluster_kernel<true>, cl, dim3(kAlignThreads), smem, stream,
-                                src, lora_ids, topk, num_experts, max_loras, vtopk_out, plan.numel,
-                                num_vexperts, plan.block_m, plan.capacity, tile, plan.nb_pad,
-                                sorted_ids, expert_ids, ntpp, trig);
-    return launch_pdl_cluster(align_cluster_kernel<false>, cl, dim3(kAlignThreads), smem, stream,
-                              src, static_cast<const int32_t*>(nullptr), 1, 1, 1,
-                              static_cast<int32_t*>(nullptr), plan.numel, num_vexperts,
-                              plan.block_m, plan.capacity, tile, plan.nb_pad, sorted_ids,
-                              expert_ids, ntpp, trig);
+    const int32_t* lids = remap ? lora_ids : nullptr;
+    int32_t* vout = remap ? vtopk_out : nullptr;
+    const int tk = remap ? topk : 1, ne = remap ? num_experts : 1, ml = remap ? max_loras : 1;
+#define MOL_ALIGN_CLUSTER(R, W)                                                                 \
+  launch_pdl_cluster(align_cluster_kernel<R, W>, cl, dim3(W * 32), smem, stream, src, lids, tk, \
+                     ne, ml, vout, plan.numel, num_vexperts, plan.block_m, plan.capacity, tile,  \
+                     plan.nb_pad, sorted_ids, expert_ids, ntpp, trig)
+    if (remap) return w16 ? MOL_ALIGN_CLUSTER(true, 16) : MOL_ALIGN_CLUSTER(true, 8);
+    return w16 ? MOL_ALIGN_CLUSTER(false, 16) : MOL_ALIGN_CLUSTER(false, 8);
+#undef MOL_ALIGN_CLUSTER
   }
   int* ws_hist = nullptr;
   int* ws_offs = nullptr;
