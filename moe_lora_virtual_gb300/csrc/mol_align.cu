@@ -12,21 +12,22 @@
 //
 // Design. The order inside a bucket is ascending flat index, so the scatter
 // is a stable counting sort. Pairs are cut into tiles (one thread block each);
-// a tile is cut into 8 contiguous warp segments; a warp walks its segment in
-// rounds of 32 pairs in order. Inside a round, __match_any_sync gives each
-// lane the lanes holding the same bucket; a per-warp shared-memory table of
-// 16-bit counters (one per bucket) carries the running count across rounds.
-// Pass 1 counts, a column scan over the 8 warp tables turns counts into
-// per-warp bases, pass 2 recomputes each pair's stable rank inside the tile.
+// a tile is cut into 8 (or 16) contiguous warp segments; a warp walks its
+// segment in rounds of 32 pairs in order. Inside a round, __match_any_sync
+// gives each lane the lanes holding the same bucket; a per-warp shared-memory
+// table of 16-bit counters (one per bucket) carries the running count across
+// rounds. Pass 1 counts, a column
+// scan over the warp tables turns counts into per-warp bases, pass 2
+// recomputes each pair's stable rank inside the tile.
 // Everything is ordered by construction (tile < warp < round < lane), so the
 // result is bit-reproducible with no atomics. With one tile the same block
 // finishes the job (bucket scan, expert_ids, scatter): one launch. Up to
 // 131072 pairs the tiles are the thread blocks of one cluster (up to 16) and
 // the cross-tile steps go through distributed shared memory: each block sums
 // the tiles' counts of its share of the buckets, the shares' padded totals
-// are exchanged, and each block writes back, into every tile's shared memory,
-// that tile's base in each of its buckets -- one launch, no workspace, three
-// cluster barriers. Beyond that, per-tile histograms go to the workspace, one
+// are exchanged together with each tile's base in each bucket relative to its
+// share (written into every tile's shared memory) -- one launch, no
+// workspace, two cluster barriers. Beyond that, per-tile histograms go to the workspace, one
 // block scans them, and a third launch scatters.
 
 #include <algorithm>
@@ -176,18 +177,27 @@ MOL_DEV void warp_rank(const uint16_t* keys, int s0, int s1, uint16_t* mine, int
 
 // Column scan: the warp tables become exclusive per-warp bases inside the tile;
 // total(b, n) receives the tile's count of bucket b.
+// Two buckets per thread and access (32-bit words of two 16-bit counters, rows
+// of nb_pad, a multiple of 8, counters: 16-byte aligned rows), every warp's
+// word loaded first: the scan moves the tables through shared memory at full
+// width.
 template <int WARPS, typename F>
 MOL_DEV void column_scan(uint16_t* tbl, int nb, int nb_pad, F&& total) {
-  for (int b = threadIdx.x; b < nb; b += WARPS * 32) {
-    int run = 0;
+  uint32_t* t32 = reinterpret_cast<uint32_t*>(tbl);
+  const int row = nb_pad / 2;
+  for (int j = threadIdx.x; 2 * j < nb; j += WARPS * 32) {
+    uint32_t c[WARPS];
+#pragma unroll
+    for (int w = 0; w < WARPS; ++w) c[w] = t32[w * row + j];
+    uint32_t lo = 0, hi = 0;  // running sums of bucket 2j and 2j + 1
 #pragma unroll
     for (int w = 0; w < WARPS; ++w) {
-      uint16_t* p = tbl + w * nb_pad + b;
-      const int c = *p;
-      *p = (uint16_t)run;
-      run += c;
+      t32[w * row + j] = lo | (hi << 16);
+      lo += c[w] & 0xFFFFu;
+      hi += c[w] >> 16;
     }
-    total(b, run);
+    total(2 * j, (int)lo);
+    if (2 * j + 1 < nb) total(2 * j + 1, (int)hi);
   }
 }
 
@@ -351,13 +361,16 @@ MOL_DEV void st_peer(uint32_t a, int v) {
 
 // Block p of the cluster holds tile p (`tile` pairs from p * tile). After the
 // tile's counts (cnt[b]), block c takes buckets [c * per, (c + 1) * per):
-// it sums the tiles' counts of each (remote reads), pads, scans its share and
-// sends the share's padded total to every block. Then, with the offset o_b of
-// each of its buckets, it writes o_b + (counts of the tiles before p) into
-// block p's cnt[b] (remote writes), and the bucket's expert_ids. After the third
-// barrier every block scatters its pairs: cnt[key] + the pair's stable rank in
-// the tile. Every block reaches every barrier (no early exit, no data-dependent
-// wait), and no block reads or writes another's shared memory after the last.
+// it sums the tiles' counts of each (remote reads), pads and scans its share;
+// with the offset o_b of each of its buckets inside the share it writes
+// o_b + (counts of the tiles before p) into block p's cnt[b] (remote writes),
+// and it sends the share's padded total to every block. After the second
+// barrier every block knows where each share starts: it writes its buckets'
+// expert_ids and scatters its pairs to cnt[key] + the start of key's share +
+// the pair's stable rank in the tile (the padding fill of every slot comes
+// before the second barrier). Every block reaches every barrier (no
+// early exit, no data-dependent wait), and no block reads or writes another's
+// shared memory after the last.
 template <bool REMAP, int WARPS>
 __global__ void __launch_bounds__(WARPS * 32, 1)
 align_cluster_kernel(const int* __restrict__ src, const int* __restrict__ lora_ids, int topk,
@@ -370,6 +383,7 @@ align_cluster_kernel(const int* __restrict__ src, const int* __restrict__ lora_i
   __shared__ int sh_scan[WARPS + 1];
   __shared__ int rsum[kClusterMax];  // padded total of each block's share of the buckets
   __shared__ int s_sentinel;         // offset of the sentinel bucket (in the block that holds it)
+  __shared__ int sbase[kClusterMax];  // where each block's share of the buckets starts
   const int nb = num_vexperts + 1;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int CL = (int)cluster_blocks(), me = (int)cluster_rank();
@@ -409,8 +423,6 @@ align_cluster_kernel(const int* __restrict__ src, const int* __restrict__ lora_i
       }
     }
   }
-  for (int64_t q = (int64_t)me * THREADS + tid; q < capacity; q += (int64_t)CL * THREADS)
-    sorted_ids[q] = (int)numel;
   __syncthreads();
   const int seg = tile / WARPS;
   const int s0 = warp * seg, s1 = min(s0 + seg, tlen);
@@ -419,12 +431,17 @@ align_cluster_kernel(const int* __restrict__ src, const int* __restrict__ lora_i
   __syncthreads();
   column_scan<WARPS>(tbl, nb, nb_pad, [&](int b, int n) { cnt[b] = n; });
   cluster_barrier();  // 1: every tile's counts are in its block's shared memory
+  // every slot starts as padding (the pairs overwrite theirs after barrier 2, which
+  // orders these stores before them)
+  for (int64_t q = (int64_t)me * THREADS + tid; q < capacity; q += (int64_t)CL * THREADS)
+    sorted_ids[q] = (int)numel;
 
   const int per = (nb + CL - 1) / CL;
   const int b0 = min(me * per, nb), b1 = min(b0 + per, nb);
   const int ppt = (per + THREADS - 1) / THREADS;
   const int c0 = min(b0 + tid * ppt, b1), c1 = min(c0 + ppt, b1);
   const int pad = block_m - 1, lg = __ffs(block_m) - 1;
+  int ck[kClusterMax];  // one bucket per thread: its tiles' counts stay in registers
   int local = 0;
   for (int b = c0; b < c1; ++b) {
     int c[kClusterMax];  // every tile's count of b: independent remote loads, all in flight
@@ -432,7 +449,10 @@ align_cluster_kernel(const int* __restrict__ src, const int* __restrict__ lora_i
     for (int p = 0; p < kClusterMax; ++p) c[p] = p < CL ? ld_peer(peer_smem(cnt + b, p)) : 0;
     int tot = 0;
 #pragma unroll
-    for (int p = 0; p < kClusterMax; ++p) tot += c[p];
+    for (int p = 0; p < kClusterMax; ++p) {
+      tot += c[p];
+      ck[p] = c[p];
+    }
     const int pb = (tot + pad) & ~pad;
     opad[b - b0] = pb;
     local += pb;
@@ -440,12 +460,22 @@ align_cluster_kernel(const int* __restrict__ src, const int* __restrict__ lora_i
   int share_total;
   int run = block_exclusive_scan<THREADS>(local, sh_scan, share_total);
   for (int b = c0; b < c1; ++b) {
-    const int pb = opad[b - b0];
-    opad[b - b0] = run;
-    run += pb;
+    const int o = run;  // the bucket's offset inside the share
+    run += opad[b - b0];
+    opad[b - b0] = o;
+    int c[kClusterMax];
+#pragma unroll
+    for (int p = 0; p < kClusterMax; ++p)
+      c[p] = ppt == 1 ? ck[p] : (p < CL ? ld_peer(peer_smem(cnt + b, p)) : 0);
+    int r = o;  // tile p's base in b, relative to the share's start
+#pragma unroll
+    for (int p = 0; p < kClusterMax; ++p) {
+      if (p < CL) st_peer(peer_smem(cnt + b, p), r);
+      r += c[p];
+    }
   }
   if (tid < CL) st_peer(peer_smem(rsum + me, tid), share_total);
-  cluster_barrier();  // 2: every share's padded total is in every block
+  cluster_barrier();  // 2: every tile's relative bases and every share's padded total are in place
 
   int base = 0, ntpp = 0;
   for (int c = 0; c < CL; ++c) {
@@ -453,19 +483,16 @@ align_cluster_kernel(const int* __restrict__ src, const int* __restrict__ lora_i
     base += c < me ? v : 0;
     ntpp += v;
   }
+  if (tid < CL) {  // where each share starts
+    int a = 0;
+    for (int c = 0; c < tid; ++c) a += rsum[c];
+    sbase[tid] = a;
+  }
   for (int b = c0; b < c1; ++b) {
     const int o = base + opad[b - b0];
-    int c[kClusterMax];  // loads first, then the stores of the running sums
-#pragma unroll
-    for (int p = 0; p < kClusterMax; ++p) c[p] = p < CL ? ld_peer(peer_smem(cnt + b, p)) : 0;
-    int r = o;
-#pragma unroll
-    for (int p = 0; p < kClusterMax; ++p) {
-      if (p < CL) st_peer(peer_smem(cnt + b, p), r);
-      r += c[p];
-    }
+    const int pb = (b + 1 < b1 ? opad[b + 1 - b0] : share_total) - opad[b - b0];
     if (b < num_vexperts) {
-      const int nblk = ((r - o) + pad) >> lg;
+      const int nblk = pb >> lg;
       for (int k = 0; k < nblk; ++k)
         if (MOL_CHECK((o >> lg) + k < (capacity >> lg), MOL_CHECK_ALIGN_BLOCK, (o >> lg) + k))
           expert_ids[(o >> lg) + k] = b;
@@ -477,15 +504,14 @@ align_cluster_kernel(const int* __restrict__ src, const int* __restrict__ lora_i
     MOL_CHECK(ntpp <= capacity, MOL_CHECK_ALIGN_TOTAL, ntpp);
     *ntpp_out = ntpp;
   }
-  __syncthreads();
+  __syncthreads();  // s_sentinel and sbase
   if (b0 < nb && b1 == nb) {  // the sentinel's blocks and every block past them carry -1
     for (int64_t t = (s_sentinel >> lg) + tid; t < (capacity >> lg); t += THREADS)
       expert_ids[t] = -1;
   }
-  cluster_barrier();  // 3: cnt[b] is this tile's base in bucket b; the pad fill is done
 
   warp_rank(keys, s0, s1, mine, lane, [&](int q, int key, int lr) {
-    const int64_t pos = (int64_t)cnt[key] + lr;
+    const int64_t pos = (int64_t)cnt[key] + sbase[key / per] + lr;
     if (MOL_CHECK(pos >= 0 && pos < capacity, MOL_CHECK_ALIGN_SLOT, pos)) sorted_ids[pos] = (int)(t0 + q);
   });
 }
