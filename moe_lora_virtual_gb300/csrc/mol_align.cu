@@ -16,18 +16,17 @@
 // segment in rounds of 32 pairs in order. Inside a round, __match_any_sync
 // gives each lane the lanes holding the same bucket; a per-warp shared-memory
 // table of 16-bit counters (one per bucket) carries the running count across
-// rounds. Pass 1 counts, a column
-// scan over the warp tables turns counts into per-warp bases, pass 2
-// recomputes each pair's stable rank inside the tile.
+// rounds. Pass 1 counts, a column scan over the warp tables turns counts into
+// per-warp bases, pass 2 recomputes each pair's stable rank inside the tile.
 // Everything is ordered by construction (tile < warp < round < lane), so the
 // result is bit-reproducible with no atomics. With one tile the same block
 // finishes the job (bucket scan, expert_ids, scatter): one launch. Up to
 // 131072 pairs the tiles are the thread blocks of one cluster (up to 16) and
 // the cross-tile steps go through distributed shared memory: each block sums
-// the tiles' counts of its share of the buckets, the shares' padded totals
-// are exchanged together with each tile's base in each bucket relative to its
-// share (written into every tile's shared memory) -- one launch, no
-// workspace, two cluster barriers. Beyond that, per-tile histograms go to the workspace, one
+// the tiles' counts of its share of the buckets and writes, into every tile's
+// shared memory, that tile's base in each bucket relative to the share, and
+// the shares' padded totals are exchanged -- one launch, no workspace, two
+// cluster barriers. Beyond that, per-tile histograms go to the workspace, one
 // block scans them, and a third launch scatters.
 
 #include <algorithm>
