@@ -703,10 +703,10 @@ E2E_ROUNDS = 4
 # (workload, kernel). An entry whose digest differs from the current sources is stale and
 # reported as null. Sources: the ncu summaries under profiles/.
 TRAFFIC = {
-    ("decode", "shrink_gate_up"): (35516160 + 256, 35506176, "mol_lora.cu", "694d4a080a3d0398"),
-    ("wide", "expand_down"): (41633024 + 37376, 43469824, "mol_lora.cu", "694d4a080a3d0398"),
-    ("wide1k", "expand_down"): (172935424 + 7999744, 184738816, "mol_lora.cu", "694d4a080a3d0398"),
-    ("ep", "shrink_gate_up"): (569530880 + 6263808, 572089984, "mol_lora.cu", "694d4a080a3d0398"),
+    ("decode", "shrink_gate_up"): (35516672 + 256, 35506176, "mol_lora.cu", "6a01e8d891db5ba6"),
+    ("wide", "expand_down"): (41627648 + 42240, 43469824, "mol_lora.cu", "6a01e8d891db5ba6"),
+    ("wide1k", "expand_down"): (172901376 + 7652352, 184738816, "mol_lora.cu", "6a01e8d891db5ba6"),
+    ("ep", "shrink_gate_up"): (569618944 + 6196480, 572089984, "mol_lora.cu", "6a01e8d891db5ba6"),
     ("dense", "expand_down"): (344967168 + 210716928, 612368384, "mol_expand_tc.cu", "fbaeb08d75e03155"),
 }
 
