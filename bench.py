@@ -707,7 +707,7 @@ TRAFFIC = {
     ("wide", "expand_down"): (41627648 + 42240, 43469824, "mol_lora.cu", "6a01e8d891db5ba6"),
     ("wide1k", "expand_down"): (172901376 + 7652352, 184738816, "mol_lora.cu", "6a01e8d891db5ba6"),
     ("ep", "shrink_gate_up"): (569618944 + 6196480, 572089984, "mol_lora.cu", "6a01e8d891db5ba6"),
-    ("dense", "expand_down"): (344967168 + 210716928, 612368384, "mol_expand_tc.cu", "fbaeb08d75e03155"),
+    ("dense", "expand_down"): (344987904 + 210557696, 612368384, "mol_expand_tc.cu", "250f63fa3e035bd5"),
 }
 
 
