@@ -1036,16 +1036,16 @@ static int device_sms() {
   return cache[dev];
 }
 
-// Blocks of `kernel` (kExpandThreads threads, `smem` dynamic bytes) resident on the
+// Blocks of kernel K (kExpandThreads threads, `smem` dynamic bytes) resident on the
 // device at once: its SM count times its occupancy, cached per kernel and device.
-template <typename Kernel>
-static int64_t resident_blocks(Kernel kernel, size_t smem) {
+template <auto K>
+static int64_t resident_blocks(size_t smem) {
   static int cache[64] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
   if (cache[dev] == 0) {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kExpandThreads, smem) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, K, kExpandThreads, smem) != cudaSuccess ||
         n <= 0)
       n = 1;
     cache[dev] = n;
@@ -1150,7 +1150,8 @@ static cudaError_t launch_expand_st(cudaStream_t stream, int64_t n_items, const 
                                     int num_vexperts, uint16_t* o, int64_t out_stride, int cps,
                                     const int32_t* ranks, const float* scalings, int ne) {
   const size_t smem = expand_st_smem(RK, D, C);
-  const int64_t resident = resident_blocks(lora_expand_st_kernel<RK, E, A, D, C, false>, smem);
+  const int64_t resident =
+      D ? 0 : resident_blocks<lora_expand_st_kernel<RK, false, A, false, C, true>>(smem);
   // every block starts at once, after the previous kernel (no early launch, so no early reads)
   if (!D && n_items > 4 * resident)
     return launch_ordered(lora_expand_st_kernel<RK, false, A, false, C, true>, dim3((unsigned)resident),
