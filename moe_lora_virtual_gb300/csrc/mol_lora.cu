@@ -478,11 +478,11 @@ lora_shrink_kernel(const uint16_t* __restrict__ x, int64_t x_stride, int x_div, 
 
 // Expand with the weight fragments in registers (rank 128; ranks 16-64 take
 // the staged expand below). One item = (routed block t, slice s, 128 output
-// columns), 4 warps x 32 columns. Round 1 loads the routing words together,
-// round 2 the weight fragments and the output rows to update, round 3 the
+// columns), 4 warps x 32 columns. Three waves of loads: the routing words
+// together, then the weight fragments and the output rows to update, then the
 // intermediate. With EARLY (inside mol_lora_forward, right after this stage's
-// shrink) rounds 1-2 run before griddepcontrol.wait, overlapping the shrink's
-// tail.
+// shrink) the first two run before griddepcontrol.wait, overlapping the
+// shrink's tail.
 constexpr int kExpandThreads = 128;
 constexpr int kExpandCols = 128;
 
