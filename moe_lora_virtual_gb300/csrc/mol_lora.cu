@@ -675,7 +675,7 @@ lora_expand_kernel(const float* __restrict__ inter, int R, const uint16_t* __res
 }
 
 // Staged expand, rank 8, 16, 32 or 64. One item = (routed block t, slice s, COLS
-// output columns, 256 or 512). One thread copies the item's lora_b rows (COLS x
+// output columns: 256, 512 or 768). One thread copies the item's lora_b rows (COLS x
 // RK bf16, contiguous in [V, N, r]) into shared memory with a bulk copy, and
 // every thread copies its pieces of the output rows to update with cp.async, so
 // neither takes registers while in flight; each warp covers COLS / 4 columns
@@ -689,7 +689,7 @@ lora_expand_kernel(const float* __restrict__ inter, int R, const uint16_t* __res
 // output rows are copied while the current one computes. Rank 8 runs the
 // rank-16 step (k = 16) with the upper eight k columns zero in both operands:
 // quads tq = 2, 3 of a warp, which would hold them, load nothing.
-// COLS: output columns per item, 256, or 512 (ranks 8 and 16 with one staged tile)
+// COLS: output columns per item, 256, or 512 or 768 (ranks 8 and 16, one staged tile)
 __host__ __device__ constexpr int st_out_pitch(int cols) { return cols + 32; }  // elements (64-byte skew per row)
 // dynamic shared memory of one block: the lora_b tile, then the output row tile(s), then
 // (two staged tiles) the next tile's intermediate fragments
@@ -715,7 +715,8 @@ MOL_DEV int expand_st_item(int it, uint32_t wphase, bool& waited, unsigned char*
                            int n_items, const int* __restrict__ lora_ranks,
                            const float* __restrict__ lora_scalings, int num_experts) {
   static_assert(RK == 8 || RK == 16 || RK == 32 || RK == 64, "staged expand: rank 8, 16, 32 or 64");
-  static_assert(COLS == 256 || COLS == 512, "staged expand: 256 or 512 columns per item");
+  static_assert(COLS == 256 || COLS == 512 || COLS == 768,
+                "staged expand: 256, 512 or 768 columns per item");
   constexpr int kStCols = COLS;
   constexpr int kStGroups = kStCols / (kExpandThreads / 32) / 32;  // column groups per warp
   constexpr int kStOutPitch = st_out_pitch(kStCols);
@@ -986,7 +987,8 @@ MOL_DEV int expand_st_item(int it, uint32_t wphase, bool& waited, unsigned char*
 // barrier comes after every thread has finished the previous item (its rows, its weight
 // tile, its weight barrier phase). Otherwise one block per item.
 template <int RK, bool EARLY, bool ADAPT, bool DB, int COLS, bool LOOP>
-__global__ void __launch_bounds__(kExpandThreads, RK == 64 ? (DB ? 4 : 5) : COLS == 512 ? 6 : (DB ? 6 : 8))
+__global__ void __launch_bounds__(kExpandThreads, RK == 64 ? (DB ? 4 : 5)
+                                                  : COLS == 768 ? 4 : COLS == 512 ? 6 : (DB ? 6 : 8))
 lora_expand_st_kernel(const float* __restrict__ inter, int R, const uint16_t* __restrict__ lora_b,
                       int S, int Ns, float scale, const float* __restrict__ topk_w,
                       const int* __restrict__ sorted_ids, const int* __restrict__ expert_ids,
@@ -1091,8 +1093,9 @@ cudaError_t prepare_lora_kernels() {
   e = prepare_expand_st<8, false>();
   if (e != cudaSuccess) return e;
   e = prepare_expand_st<16, false, 512>();
-  if (e != cudaSuccess) return e;
-  e = prepare_expand_st<8, false, 512>();
+  if (e == cudaSuccess) e = prepare_expand_st<16, false, 768>();
+  if (e == cudaSuccess) e = prepare_expand_st<8, false, 512>();
+  if (e == cudaSuccess) e = prepare_expand_st<8, false, 768>();
   if (e != cudaSuccess) return e;
   for (auto k : {lora_shrink_kernel<false, 8>, lora_shrink_kernel<true, 8>,
                  lora_shrink_kernel<false, 16>, lora_shrink_kernel<true, 16>})
@@ -1197,11 +1200,13 @@ cudaError_t launch_expand(const float* inter, const void* lora_b, int S, int r, 
     // many rows per virtual expert (on average at least 32 pairs each): blocks hold
     // several row tiles, so the output rows of the next one are prefetched
     const bool db = numel >= 32 * std::min<int64_t>(numel, num_vexperts);
-    // ranks 8 and 16 with at least four pairs per virtual expert on average: items of
-    // 512 columns, so a block moves about as many bytes as a rank-32 item of 256 and
-    // the grid has half the blocks (each pays the routing reads and the row compaction)
+    // ranks 8 and 16 with at least four pairs per virtual expert on average: items of 768
+    // columns where they tile the slice, else 512, so a block moves at least as many
+    // bytes as a rank-32 item of 256 and the grid has fewer items (each pays the routing
+    // reads and the row compaction); measured: 768 where a slice is 768 wide beats 512,
+    // 1024 on a 2048-wide slice loses to 512 (three blocks per SM instead of six)
     const bool wide = r <= 16 && !db && numel >= 4 * std::min<int64_t>(numel, num_vexperts);
-    const int cols = wide ? 512 : 256;
+    const int cols = wide ? (Ns % 768 == 0 ? 768 : 512) : 256;
     const int cps_st = (Ns + cols - 1) / cols;
     const int64_t n_items = nblk * S * cps_st;
     if (n_items > INT32_MAX) return cudaErrorInvalidConfiguration;
@@ -1213,8 +1218,9 @@ cudaError_t launch_expand(const float* inter, const void* lora_b, int S, int r, 
                                    out_stride, cps_st, lora_ranks, lora_scalings, ne)
 #define MOL_EXPAND_ST_A(RK, E, A) \
   (db ? MOL_EXPAND_ST(RK, E, A, true, 256) : MOL_EXPAND_ST(RK, E, A, false, 256))
-#define MOL_EXPAND_ST_W(RK, E, A) \
-  (wide ? MOL_EXPAND_ST(RK, E, A, false, 512) : MOL_EXPAND_ST_A(RK, E, A))
+#define MOL_EXPAND_ST_W(RK, E, A)                                                     \
+  (cols == 768 ? MOL_EXPAND_ST(RK, E, A, false, 768)                                 \
+   : cols == 512 ? MOL_EXPAND_ST(RK, E, A, false, 512) : MOL_EXPAND_ST_A(RK, E, A))
 #define MOL_EXPAND_ST_RK(RK, M)                                                  \
   return early ? (adapt ? M(RK, true, true) : M(RK, true, false))                \
                : (adapt ? M(RK, false, true) : M(RK, false, false))

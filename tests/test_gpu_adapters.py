@@ -76,6 +76,7 @@ CASES = [
     # 512-column items; rank 64: 256-column items), adapters of rank 0 skipped in the loop
     (600, 8, 64, 4, 16, 256, 2, 16, 2048, True, [16, 0, 8, 12]),
     (400, 8, 32, 4, 16, 128, 1, 64, 4096, False, [64, 0, 40, 17]),
+    (1200, 8, 128, 4, 16, 128, 1, 8, 3072, True, [8, 0, 5, 3]),  # rank 8, 768-column items
 ]
 
 

@@ -132,6 +132,7 @@ SHAPES = [
     # with a ragged last item
     (120, 8, 16, 4, 32, 256, 2, 16, 1288, True, 0, 8, True, 0.1),
     (100, 6, 12, 3, 16, 136, 1, 8, 1096, False, 8, 0, False, 0.2),
+    (90, 8, 12, 2, 16, 200, 2, 16, 768, True, 0, 8, True, 0.1),    # 768-column items
 ]
 
 
