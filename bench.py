@@ -703,10 +703,10 @@ E2E_ROUNDS = 4
 # (workload, kernel). An entry whose digest differs from the current sources is stale and
 # reported as null. Sources: the ncu summaries under profiles/.
 TRAFFIC = {
-    ("decode", "shrink_gate_up"): (35516416 + 0, 35506176, "mol_lora.cu", "3b0963741b21fb5d"),
-    ("wide", "expand_down"): (41627904 + 50432, 43469824, "mol_lora.cu", "3b0963741b21fb5d"),
-    ("wide1k", "expand_down"): (172923136 + 8281344, 184738816, "mol_lora.cu", "3b0963741b21fb5d"),
-    ("ep", "shrink_gate_up"): (569593088 + 6186496, 572089984, "mol_lora.cu", "3b0963741b21fb5d"),
+    ("decode", "shrink_gate_up"): (35517696 + 0, 35506176, "mol_lora.cu", "478d2ea81be6ce8a"),
+    ("wide", "expand_down"): (41628160 + 37376, 43469824, "mol_lora.cu", "478d2ea81be6ce8a"),
+    ("wide1k", "expand_down"): (172902144 + 7868928, 184738816, "mol_lora.cu", "478d2ea81be6ce8a"),
+    ("ep", "shrink_gate_up"): (569587456 + 6216448, 572089984, "mol_lora.cu", "478d2ea81be6ce8a"),
     ("dense", "expand_down"): (344987904 + 210557696, 612368384, "mol_expand_tc.cu", "250f63fa3e035bd5"),
 }
 
