@@ -174,6 +174,14 @@ MOL_DEV void warp_rank(const uint16_t* keys, int s0, int s1, uint16_t* mine, int
   }
 }
 
+// Pass 1 that also keeps each pair's stable rank inside its warp's segment
+// (lrank[q]), so that no second pass of matches is needed: with the column-
+// scanned tables, a pair's rank inside the tile is tbl[warp][key] + lrank[q].
+MOL_DEV void warp_count_rank(const uint16_t* keys, int s0, int s1, uint16_t* mine, int lane,
+                             uint16_t* lrank) {
+  warp_rank(keys, s0, s1, mine, lane, [&](int q, int, int lr) { lrank[q] = (uint16_t)lr; });
+}
+
 // Column scan: the warp tables become exclusive per-warp bases inside the tile;
 // total(b, n) receives the tile's count of bucket b.
 // Two buckets per thread and access (32-bit words of two 16-bit counters, rows
@@ -370,7 +378,7 @@ MOL_DEV void st_peer(uint32_t a, int v) {
 // before the second barrier). Every block reaches every barrier (no
 // early exit, no data-dependent wait), and no block reads or writes another's
 // shared memory after the last.
-template <bool REMAP, int WARPS>
+template <bool REMAP, int WARPS, bool ONEPASS>
 __global__ void __launch_bounds__(WARPS * 32, 1)
 align_cluster_kernel(const int* __restrict__ src, const int* __restrict__ lora_ids, int topk,
                      int num_experts, int max_loras, int* __restrict__ vtopk_out, int64_t numel,
@@ -388,7 +396,8 @@ align_cluster_kernel(const int* __restrict__ src, const int* __restrict__ lora_i
   const int CL = (int)cluster_blocks(), me = (int)cluster_rank();
   uint16_t* tbl = reinterpret_cast<uint16_t*>(smem);  // [WARPS][nb_pad]
   uint16_t* keys = tbl + WARPS * nb_pad;              // [tile]
-  int* cnt = reinterpret_cast<int*>(keys + tile);     // [nb]: counts, then this tile's bases
+  uint16_t* lrank = keys + tile;                      // ONEPASS: [tile] ranks inside warp segments
+  int* cnt = reinterpret_cast<int*>(keys + (ONEPASS ? 2 : 1) * tile);  // [nb]: counts, then bases
   int* opad = cnt + nb;                               // [per]: offsets inside this block's share
 
   {
@@ -426,7 +435,10 @@ align_cluster_kernel(const int* __restrict__ src, const int* __restrict__ lora_i
   const int seg = tile / WARPS;
   const int s0 = warp * seg, s1 = min(s0 + seg, tlen);
   uint16_t* mine = tbl + warp * nb_pad;
-  warp_count(keys, s0, s1, mine, lane);
+  if constexpr (ONEPASS)
+    warp_count_rank(keys, s0, s1, mine, lane, lrank);
+  else
+    warp_count(keys, s0, s1, mine, lane);
   __syncthreads();
   column_scan<WARPS>(tbl, nb, nb_pad, [&](int b, int n) { cnt[b] = n; });
   cluster_barrier();  // 1: every tile's counts are in its block's shared memory
@@ -509,10 +521,18 @@ align_cluster_kernel(const int* __restrict__ src, const int* __restrict__ lora_i
       expert_ids[t] = -1;
   }
 
-  warp_rank(keys, s0, s1, mine, lane, [&](int q, int key, int lr) {
+  auto scatter = [&](int q, int key, int lr) {
     const int64_t pos = (int64_t)cnt[key] + sbase[key / per] + lr;
     if (MOL_CHECK(pos >= 0 && pos < capacity, MOL_CHECK_ALIGN_SLOT, pos)) sorted_ids[pos] = (int)(t0 + q);
-  });
+  };
+  if constexpr (ONEPASS) {  // every thread any pair: the ranks are in shared memory
+    for (int q = tid; q < tlen; q += THREADS) {
+      const int key = keys[q];
+      scatter(q, key, (int)tbl[(q / seg) * nb_pad + key] + (int)lrank[q]);
+    }
+  } else {
+    warp_rank(keys, s0, s1, mine, lane, scatter);
+  }
 }
 
 // Multi-tile: per-bucket prefix over tiles, bucket offsets, expert_ids, ntpp.
@@ -616,8 +636,10 @@ static cudaError_t prepare_cluster_align() {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  for (auto k : {align_cluster_kernel<true, 8>, align_cluster_kernel<false, 8>,
-                 align_cluster_kernel<true, 16>, align_cluster_kernel<false, 16>}) {
+  for (auto k : {align_cluster_kernel<true, 8, false>, align_cluster_kernel<false, 8, false>,
+                 align_cluster_kernel<true, 16, false>, align_cluster_kernel<false, 16, false>,
+                 align_cluster_kernel<true, 8, true>, align_cluster_kernel<false, 8, true>,
+                 align_cluster_kernel<true, 16, true>, align_cluster_kernel<false, 16, true>}) {
     e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kAlignSmemMax);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
@@ -634,7 +656,7 @@ static cudaError_t prepare_cluster_align() {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  e = cudaOccupancyMaxActiveClusters(&n, (void*)align_cluster_kernel<true, 8>, &cfg);
+  e = cudaOccupancyMaxActiveClusters(&n, (void*)align_cluster_kernel<true, 8, false>, &cfg);
   if (e != cudaSuccess) {
     (void)cudaGetLastError();  // a refused query leaves the portable size
     n = 0;
@@ -712,23 +734,29 @@ cudaError_t launch_align(const AlignPlan& plan, bool remap, const int32_t* src,
     const int tile = (int)(((plan.numel + cl - 1) / cl + 255) / 256 * 256);
     if (tile > kClusterTileMax) return cudaErrorInvalidConfiguration;
     const int per = (plan.nb + cl - 1) / cl;
-    // shared memory of a block with `warps` warp tables
-    auto smem_of = [&](int warps) {
-      return (size_t)warps * plan.nb_pad * 2 + (size_t)tile * 2 + (size_t)plan.nb * 4 + (size_t)per * 4;
+    // shared memory of a block with `warps` warp tables (and, one pass, the pairs' ranks)
+    auto smem_of = [&](int warps, bool one) {
+      return (size_t)warps * plan.nb_pad * 2 + (size_t)tile * (one ? 4 : 2) + (size_t)plan.nb * 4 +
+             (size_t)per * 4;
     };
-    // sixteen warps where their tables fit (half the match rounds per warp), else eight
-    const bool w16 = smem_of(16) <= (size_t)kAlignSmemMax;
-    const size_t smem = smem_of(w16 ? 16 : 8);
+    // sixteen warps where their tables fit (half the match rounds per warp), else eight;
+    // one pass of matches where the pairs' ranks fit too
+    const bool w16 = smem_of(16, false) <= (size_t)kAlignSmemMax;
+    const int warps = w16 ? 16 : 8;
+    const bool one = smem_of(warps, true) <= (size_t)kAlignSmemMax;
+    const size_t smem = smem_of(warps, one);
     if (smem > (size_t)kAlignSmemMax) return cudaErrorInvalidConfiguration;
     const int32_t* lids = remap ? lora_ids : nullptr;
     int32_t* vout = remap ? vtopk_out : nullptr;
     const int tk = remap ? topk : 1, ne = remap ? num_experts : 1, ml = remap ? max_loras : 1;
-#define MOL_ALIGN_CLUSTER(R, W)                                                                 \
-  launch_pdl_cluster(align_cluster_kernel<R, W>, cl, dim3(W * 32), smem, stream, src, lids, tk, \
-                     ne, ml, vout, plan.numel, num_vexperts, plan.block_m, plan.capacity, tile,  \
+#define MOL_ALIGN_CLUSTER(R, W, O)                                                                 \
+  launch_pdl_cluster(align_cluster_kernel<R, W, O>, cl, dim3(W * 32), smem, stream, src, lids, tk, \
+                     ne, ml, vout, plan.numel, num_vexperts, plan.block_m, plan.capacity, tile,     \
                      plan.nb_pad, sorted_ids, expert_ids, ntpp, trig)
-    if (remap) return w16 ? MOL_ALIGN_CLUSTER(true, 16) : MOL_ALIGN_CLUSTER(true, 8);
-    return w16 ? MOL_ALIGN_CLUSTER(false, 16) : MOL_ALIGN_CLUSTER(false, 8);
+#define MOL_ALIGN_CLUSTER_W(R, O) (w16 ? MOL_ALIGN_CLUSTER(R, 16, O) : MOL_ALIGN_CLUSTER(R, 8, O))
+    if (remap) return one ? MOL_ALIGN_CLUSTER_W(true, true) : MOL_ALIGN_CLUSTER_W(true, false);
+    return one ? MOL_ALIGN_CLUSTER_W(false, true) : MOL_ALIGN_CLUSTER_W(false, false);
+#undef MOL_ALIGN_CLUSTER_W
 #undef MOL_ALIGN_CLUSTER
   }
   int* ws_hist = nullptr;
