@@ -208,7 +208,9 @@ MOL_DEV void column_scan(uint16_t* tbl, int nb, int nb_pad, F&& total) {
   }
 }
 
-template <bool REMAP>
+// ONE: pass 1 keeps each pair's rank inside its warp's segment (lrank, in
+// shared memory after the keys), and pass 2 needs no matches.
+template <bool REMAP, bool ONE>
 __global__ void __launch_bounds__(kAlignThreads, 1)
 align_tile_kernel(const int* __restrict__ src, const int* __restrict__ lora_ids, int topk,
                   int num_experts, int max_loras, int* __restrict__ vtopk_out, int64_t numel,
@@ -222,7 +224,8 @@ align_tile_kernel(const int* __restrict__ src, const int* __restrict__ lora_ids,
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint16_t* tbl = reinterpret_cast<uint16_t*>(smem);   // [kAlignWarps][nb_pad]
   uint16_t* keys = tbl + kAlignWarps * nb_pad;         // [tile]
-  int* offs = reinterpret_cast<int*>(keys + tile);     // [nb], single-tile only
+  uint16_t* lrank = keys + tile;                       // ONE: [tile]
+  int* offs = reinterpret_cast<int*>(keys + (ONE ? 2 : 1) * tile);  // [nb], single-tile only
   const bool fused = (tiles == 1);
 
   if ((int)blockIdx.x < tiles) {  // shared memory only: may overlap the previous kernel
@@ -248,7 +251,10 @@ align_tile_kernel(const int* __restrict__ src, const int* __restrict__ lora_ids,
   // offsets: in shared memory only, from the ids.
   auto count_keys = [&]() {
     __syncthreads();
-    warp_count(keys, s0, s1, mine, lane);  // pass 1: per-warp counts over the warp's segment
+    if constexpr (ONE)  // pass 1: per-warp counts over the warp's segment (and the ranks)
+      warp_count_rank(keys, s0, s1, mine, lane, lrank);
+    else
+      warp_count(keys, s0, s1, mine, lane);
     __syncthreads();
     // column scan: warp tables become exclusive bases; the tile total per bucket
     // goes to shared memory (one tile) or to the workspace histogram
@@ -321,7 +327,7 @@ align_tile_kernel(const int* __restrict__ src, const int* __restrict__ lora_ids,
   }
 
   // Pass 2: stable rank of every pair inside the tile.
-  warp_rank(keys, s0, s1, mine, lane, [&](int q, int key, int lr) {
+  auto emit = [&](int q, int key, int lr) {
     const int64_t i = t0 + q;
     if (fused) {
       const int64_t pos = (int64_t)offs[key] + lr;
@@ -329,7 +335,15 @@ align_tile_kernel(const int* __restrict__ src, const int* __restrict__ lora_ids,
     } else {
       ws_rank[i] = lr;
     }
-  });
+  };
+  if constexpr (ONE) {  // every thread any pair: the ranks are in shared memory
+    for (int q = tid; q < tlen; q += kAlignThreads) {
+      const int key = keys[q];
+      emit(q, key, (int)tbl[(q / seg) * nb_pad + key] + (int)lrank[q]);
+    }
+  } else {
+    warp_rank(keys, s0, s1, mine, lane, emit);
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -608,6 +622,7 @@ AlignPlan make_align_plan(int64_t numel, int num_vexperts, int block_m) {
     p.cluster = true;  // tile and block count are chosen at launch for the device
     p.tile = 0;
     p.tiles = 0;
+    p.one_pass = false;  // chosen at launch too
     p.smem_tile = 0;
     p.ws_bytes = 0;
     return p;
@@ -618,6 +633,9 @@ AlignPlan make_align_plan(int64_t numel, int num_vexperts, int block_m) {
   }
   size_t smem = (size_t)kAlignWarps * p.nb_pad * 2 + (size_t)p.tile * 2;
   if (p.tiles == 1) smem += (size_t)p.nb * 4;
+  // one pass of matches where the pairs' ranks fit beside the tables
+  p.one_pass = smem + (size_t)p.tile * 2 <= (size_t)kAlignSmemMax;
+  if (p.one_pass) smem += (size_t)p.tile * 2;
   p.smem_tile = (smem + 15) / 16 * 16;
   if (p.tiles == 1) {
     p.ws_bytes = 0;
@@ -680,11 +698,10 @@ static int sm_count(int device) {
 cudaError_t prepare_lora_kernels();
 
 cudaError_t prepare_kernels() {
-  cudaError_t e = cudaFuncSetAttribute(align_tile_kernel<true>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kAlignSmemMax);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(align_tile_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kAlignSmemMax);
+  cudaError_t e = cudaSuccess;
+  for (auto k : {align_tile_kernel<true, false>, align_tile_kernel<false, false>,
+                 align_tile_kernel<true, true>, align_tile_kernel<false, true>})
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kAlignSmemMax);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(align_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kAlignSmemMax);
@@ -770,16 +787,20 @@ cudaError_t launch_align(const AlignPlan& plan, bool remap, const int32_t* src,
     const int64_t fill_blocks = (plan.capacity + 16383) / 16384;
     grid = (unsigned)std::max<int64_t>(plan.tiles, std::min<int64_t>(sm_count(device), fill_blocks));
   }
-  if (remap) {
-    e = launch_pdl(align_tile_kernel<true>, dim3(grid), dim3(kAlignThreads), plan.smem_tile, stream,
-                   src, lora_ids, topk, num_experts, max_loras, vtopk_out, plan.numel, num_vexperts,
-                   plan.block_m, plan.capacity, plan.tile, plan.tiles, plan.nb_pad, sorted_ids,
-                   expert_ids, ntpp, ws_hist, ws_rank, trig);
-  } else {
-    e = launch_pdl(align_tile_kernel<false>, dim3(grid), dim3(kAlignThreads), plan.smem_tile, stream,
-                   src, static_cast<const int32_t*>(nullptr), 1, 1, 1, static_cast<int32_t*>(nullptr),
-                   plan.numel, num_vexperts, plan.block_m, plan.capacity, plan.tile, plan.tiles,
-                   plan.nb_pad, sorted_ids, expert_ids, ntpp, ws_hist, ws_rank, trig);
+  {
+    const int32_t* lids = remap ? lora_ids : nullptr;
+    int32_t* vout = remap ? vtopk_out : nullptr;
+    const int tk = remap ? topk : 1, ne = remap ? num_experts : 1, ml = remap ? max_loras : 1;
+#define MOL_ALIGN_TILE(R, O)                                                                      \
+  launch_pdl(align_tile_kernel<R, O>, dim3(grid), dim3(kAlignThreads), plan.smem_tile, stream, src, \
+             lids, tk, ne, ml, vout, plan.numel, num_vexperts, plan.block_m, plan.capacity,        \
+             plan.tile, plan.tiles, plan.nb_pad, sorted_ids, expert_ids, ntpp, ws_hist, ws_rank,   \
+             trig)
+    if (remap)
+      e = plan.one_pass ? MOL_ALIGN_TILE(true, true) : MOL_ALIGN_TILE(true, false);
+    else
+      e = plan.one_pass ? MOL_ALIGN_TILE(false, true) : MOL_ALIGN_TILE(false, false);
+#undef MOL_ALIGN_TILE
   }
   if (e != cudaSuccess || plan.tiles == 1) return e;
   e = launch_pdl(align_scan_kernel, dim3(1), dim3(kScanThreads), (size_t)plan.nb * 4, stream, ws_hist,

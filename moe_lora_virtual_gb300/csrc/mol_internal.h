@@ -20,6 +20,7 @@ struct AlignPlan {
   int tile;        // pairs per tile block
   int tiles;       // number of tile blocks (1 = single fused block)
   bool cluster;    // the tiles are the blocks of one cluster (sized at launch): no workspace
+  bool one_pass;   // tile kernel: the pairs' ranks kept in shared memory, one pass of matches
   size_t smem_tile;
   size_t ws_bytes;  // workspace (0 with one tile or one cluster), 256-byte multiple
 };
