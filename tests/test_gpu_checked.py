@@ -86,6 +86,9 @@ FORWARD_SHAPES = [
     (30, 4, 5, 2, 16, 320, 1, 8, 200, True, 0.1, True),       # rank 8 with ranks and scalings
     (700, 8, 64, 2, 16, 128, 1, 16, 64, True, 0.1, False),    # cluster align (5600 pairs)
     (256, 2, 4, 1, 64, 256, 2, 64, 384, True, 0.05, False),   # tcgen05 shrink and expand
+    # 16-row shrink items, 768-column expand items in a looping grid, one-pass cluster align
+    (1200, 8, 128, 4, 16, 256, 2, 16, 1536, True, 0.3, False),
+    (1200, 8, 128, 4, 16, 256, 2, 16, 1536, True, 0.3, True),  # the same with adapter arrays
 ]
 
 
