@@ -291,6 +291,19 @@ align_tile_kernel(const int* __restrict__ src, const int* __restrict__ lora_ids,
   pdl_wait();  // inputs and the routing buffers belong to earlier kernels until here
   if (trigger == 1 || (trigger == 0 && tiles > 1)) pdl_launch_dependents();
 
+  // One tile, ids read after the wait: they are loaded before the padding fill, so that
+  // their latency overlaps it (raw ids and adapter ids in registers).
+  const bool ids_first = fused && !ids_early;
+  int lkeep[kTileMin / kAlignThreads];
+  if (ids_first) {
+#pragma unroll
+    for (int j = 0; j < kTileMin / kAlignThreads; ++j) {
+      const int q = tid + j * kAlignThreads;
+      vkeep[j] = q < tlen ? src[t0 + q] : -1;
+      lkeep[j] = (REMAP && q < tlen) ? lora_ids[(t0 + q) / topk] : -1;
+    }
+  }
+
   // Every slot starts as padding (value numel); real pairs overwrite theirs.
   for (int64_t q = (int64_t)blockIdx.x * kAlignThreads + tid; q < capacity;
        q += (int64_t)gridDim.x * kAlignThreads)
@@ -309,16 +322,28 @@ align_tile_kernel(const int* __restrict__ src, const int* __restrict__ lora_ids,
                                 ntpp_out);
     __syncthreads();  // the padding fill lands before the scatter overwrites it
   } else {
-    for (int q = tid; q < tlen; q += kAlignThreads) {
-      const int64_t i = t0 + q;
-      int vid;
-      if (REMAP) {
-        vid = remap_one(src[i], lora_ids[i / topk], num_experts, max_loras);
-        vtopk_out[i] = vid;
-      } else {
-        vid = src[i];
+    if (ids_first) {
+#pragma unroll
+      for (int j = 0; j < kTileMin / kAlignThreads; ++j) {
+        const int q = tid + j * kAlignThreads;
+        if (q < tlen) {
+          const int vid = REMAP ? remap_one(vkeep[j], lkeep[j], num_experts, max_loras) : vkeep[j];
+          if (REMAP) vtopk_out[t0 + q] = vid;
+          keys[q] = (uint16_t)bucket_of(vid, num_vexperts);
+        }
       }
-      keys[q] = (uint16_t)bucket_of(vid, num_vexperts);
+    } else {
+      for (int q = tid; q < tlen; q += kAlignThreads) {
+        const int64_t i = t0 + q;
+        int vid;
+        if (REMAP) {
+          vid = remap_one(src[i], lora_ids[i / topk], num_experts, max_loras);
+          vtopk_out[i] = vid;
+        } else {
+          vid = src[i];
+        }
+        keys[q] = (uint16_t)bucket_of(vid, num_vexperts);
+      }
     }
     count_keys();
     if (fused)
