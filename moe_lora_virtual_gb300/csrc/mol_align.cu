@@ -770,9 +770,10 @@ cudaError_t launch_align(const AlignPlan& plan, bool remap, const int32_t* src,
   cudaError_t e = cudaGetDevice(&device);
   if (e != cudaSuccess) return e;
   if (plan.cluster) {
-    // blocks of 4096 pairs, up to the device's cluster size, then larger tiles
+    // blocks of 2048 pairs, up to the device's cluster size, then larger tiles (the tile
+    // passes, rounds of 32 pairs per warp, are the longest steps: more blocks, fewer rounds)
     const int cmax = (device >= 0 && device < 64 && g_cluster_max[device]) ? g_cluster_max[device] : 8;
-    const int cl = (int)std::min<int64_t>(cmax, (plan.numel + kTileMin - 1) / kTileMin);
+    const int cl = (int)std::min<int64_t>(cmax, (plan.numel + kTileMin / 2 - 1) / (kTileMin / 2));
     const int tile = (int)(((plan.numel + cl - 1) / cl + 255) / 256 * 256);
     if (tile > kClusterTileMax) return cudaErrorInvalidConfiguration;
     const int per = (plan.nb + cl - 1) / cl;
