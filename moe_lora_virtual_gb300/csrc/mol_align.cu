@@ -130,7 +130,7 @@ MOL_DEV void write_blocks(const int* offs, int nb, int num_vexperts, int block_m
   for (int64_t t = (offs[num_vexperts] >> lg) + threadIdx.x; t < nblk; t += THREADS)
     expert_ids[t] = -1;
   if (threadIdx.x == 0) {
-    MOL_CHECK(total <= capacity, MOL_CHECK_ALIGN_TOTAL, total);
+    (void)MOL_CHECK(total <= capacity, MOL_CHECK_ALIGN_TOTAL, total);
     *ntpp_out = total;
   }
 }
@@ -551,7 +551,7 @@ align_cluster_kernel(const int* __restrict__ src, const int* __restrict__ lora_i
     }
   }
   if (me == 0 && tid == 0) {
-    MOL_CHECK(ntpp <= capacity, MOL_CHECK_ALIGN_TOTAL, ntpp);
+    (void)MOL_CHECK(ntpp <= capacity, MOL_CHECK_ALIGN_TOTAL, ntpp);
     *ntpp_out = ntpp;
   }
   __syncthreads();  // s_sentinel and sbase

@@ -225,8 +225,9 @@ static inline cudaError_t take_check_record_here(CheckRecord* out) {
 constexpr bool kChecked = true;
 #else
 constexpr bool kChecked = false;
-#define MOL_CHECK(cond, site, value) (true)
-#define MOL_NOTE(cond, site, value) (cond)
+// (the operands stay unevaluated: sizeof only marks them used)
+#define MOL_CHECK(cond, site, value) ((void)sizeof(cond), (void)sizeof(value), true)
+#define MOL_NOTE(cond, site, value) ((void)sizeof(value), (cond))
 static inline cudaError_t take_check_record_here(CheckRecord* out) {
   out->first = 0ull;
   out->count = 0ull;
