@@ -694,7 +694,7 @@ def run_e2e(args, torch, mol, wl, layers, pairs_per_step, world, dev):
 
 
 # rotations of the layers inside the end-to-end graph
-E2E_ROUNDS = 4
+E2E_ROUNDS = 16
 
 
 # traffic (dram bytes read + written) of one captured launch, with the algorithmic bytes of
