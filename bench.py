@@ -627,16 +627,20 @@ def run_e2e(args, torch, mol, wl, layers, pairs_per_step, world, dev):
         host_out.copy_(dev_buf[out_lo:], non_blocking=True)
 
     # The rotating layers, E2E_ROUNDS times over, in one graph on three streams:
-    # step k's inputs are copied in on s_in, its layer runs on the capturing
-    # stream once they have landed, and its outputs go back on s_out once it is
-    # done, so the copies of neighbouring steps overlap a step's compute
-    # (whole-job throughput). A layer's buffers are reused by the step one
-    # rotation later, whose copy-in waits for this step's copy-out. More steps
-    # per graph spread the first copy-in and the last copy-out over more steps,
-    # as a graph of a whole model's layers would.
+    # the inputs of a group of E2E_GROUP steps are copied in on s_in, the group's
+    # layers run on the capturing stream once they have landed (one wait per group,
+    # so the launches inside a group stay one chain of programmatic dependent
+    # launches), and each step's outputs go back on s_out once its layer is done; the
+    # copies of neighbouring steps and groups overlap the layers (whole-job
+    # throughput). A layer's buffers are reused by the step one rotation later, whose
+    # copy-in waits for this step's copy-out (a group is shorter than a rotation, so
+    # no copy-in waits on a layer of its own group). More steps per graph spread the
+    # first copy-in and the last copy-out over more steps, as a graph of a whole
+    # model's layers would.
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
     nl = len(layers)
     n_steps = E2E_ROUNDS * nl
+    group = max(1, min(E2E_GROUP, nl))
 
     def all_steps():
         main = torch.cuda.current_stream()
@@ -645,22 +649,27 @@ def run_e2e(args, torch, mol, wl, layers, pairs_per_step, world, dev):
         s_in.wait_event(start)
         s_out.wait_event(start)
         copied_out = []
-        for k in range(n_steps):
-            L_, (dev_buf, host_in, host_out, out_lo) = layers[k % nl], packs[k % nl]
-            landed, done, back = torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event()
+        for k0 in range(0, n_steps, group):
+            ks = range(k0, min(k0 + group, n_steps))
+            landed = torch.cuda.Event()
             with torch.cuda.stream(s_in):
-                if k >= nl:
-                    s_in.wait_event(copied_out[k - nl])
-                dev_buf.copy_(host_in, non_blocking=True)
+                for k in ks:
+                    dev_buf, host_in = packs[k % nl][0], packs[k % nl][1]
+                    if k >= nl:
+                        s_in.wait_event(copied_out[k - nl])
+                    dev_buf.copy_(host_in, non_blocking=True)
                 landed.record(s_in)
             main.wait_event(landed)
-            L_.forward(mol)
-            done.record(main)
-            s_out.wait_event(done)
-            with torch.cuda.stream(s_out):
-                host_out.copy_(dev_buf[out_lo:], non_blocking=True)
-                back.record(s_out)
-            copied_out.append(back)
+            for k in ks:
+                L_, (dev_buf, host_in, host_out, out_lo) = layers[k % nl], packs[k % nl]
+                done, back = torch.cuda.Event(), torch.cuda.Event()
+                L_.forward(mol)
+                done.record(main)
+                s_out.wait_event(done)
+                with torch.cuda.stream(s_out):
+                    host_out.copy_(dev_buf[out_lo:], non_blocking=True)
+                    back.record(s_out)
+                copied_out.append(back)
         main.wait_stream(s_in)
         main.wait_stream(s_out)
 
@@ -686,7 +695,8 @@ def run_e2e(args, torch, mol, wl, layers, pairs_per_step, world, dev):
                 mode=f"graph replay of {n_steps} steps ({E2E_ROUNDS} rotations of the layers): per "
                      "step one pinned-host copy of the packed inputs, the mol_lora_forward calls, "
                      "one copy of the outputs back; copies on their own streams overlap "
-                     "neighbouring steps' compute",
+                     f"neighbouring steps' compute; the layers wait for their inputs in groups of "
+                     f"{group} steps",
                 serial_value=round(pairs_per_step * world / (ms_serial * 1e-3), 1),
                 serial_ms_per_step=round(ms_serial, 6),
                 eager_value=round(pairs_per_step * world / (ms_eager * 1e-3), 1),
@@ -695,6 +705,8 @@ def run_e2e(args, torch, mol, wl, layers, pairs_per_step, world, dev):
 
 # rotations of the layers inside the end-to-end graph
 E2E_ROUNDS = 16
+# steps whose inputs the layers wait for together (at most one rotation)
+E2E_GROUP = 4
 
 
 # traffic (dram bytes read + written) of one captured launch, with the algorithmic bytes of
