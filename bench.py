@@ -262,14 +262,17 @@ def capture(torch, fn):
 
 
 def layer_steps_timer(torch, mol, layers, steps):
-    """Graphs that run exactly `steps` layer steps: the rotating layers back to back in one
-    graph (replayed steps // len(layers) times) and, for the remainder, one graph of the first
-    steps % len(layers) layers. Returns (run, warm): run() enqueues the K steps; warm(w) replays
-    every graph the timed region uses at least twice and covers at least w warm-up steps."""
+    """Graphs that run exactly `steps` layer steps, step i on layer i % len(layers): graphs of
+    GRAPH_ROTATIONS rotations of the layers back to back (replayed steps // that many times)
+    and, for the remainder, one graph of the next steps (one graph for up to that many steps,
+    as a model's layers captured together would run). Returns (run, warm): run() enqueues the
+    K steps; warm(w) replays every graph the timed region uses at least twice and covers at
+    least w warm-up steps."""
     nl = len(layers)
-    full, rest = divmod(steps, nl)
-    multi = capture(torch, lambda: [L_.forward(mol) for L_ in layers]) if full else None
-    tail = capture(torch, lambda: [L_.forward(mol) for L_ in layers[:rest]]) if rest else None
+    cap = nl * GRAPH_ROTATIONS
+    full, rest = divmod(steps, cap)
+    multi = capture(torch, lambda: [layers[i % nl].forward(mol) for i in range(cap)]) if full else None
+    tail = capture(torch, lambda: [layers[i % nl].forward(mol) for i in range(rest)]) if rest else None
 
     def run():
         for _ in range(full):
@@ -279,7 +282,7 @@ def layer_steps_timer(torch, mol, layers, steps):
 
     def warm(w):
         done = 0
-        for g, n in ((multi, nl), (tail, rest)):
+        for g, n in ((multi, cap), (tail, rest)):
             if g is None:
                 continue
             for _ in range(2):
@@ -287,10 +290,14 @@ def layer_steps_timer(torch, mol, layers, steps):
                 done += n
         while done < w:
             (multi or tail).replay()
-            done += nl if multi else rest
+            done += cap if multi else rest
         torch.cuda.synchronize()
 
     return run, warm
+
+
+# rotations of the layers in one graph of the timed loop (the remainder: one more graph)
+GRAPH_ROTATIONS = 64
 
 
 def kernel_times(torch, mol, wl, layers, cnt, ranks, steps, config):
@@ -557,8 +564,9 @@ def run_gpu(args):
                            adapter_ranks=ranks,
                            routing_mode=args.routing_mode,
                            l2="inputs larger than L2: steps rotate over distinct layers",
-                           graph=f"{args.layers} layers per graph replay; the K mod {args.layers} "
-                                 "remainder in one more graph of that many layers; every graph "
+                           graph=f"graphs of {GRAPH_ROTATIONS * args.layers} layer steps "
+                                 f"({GRAPH_ROTATIONS} rotations of the {args.layers} layers), "
+                                 "the K mod that remainder in one more graph; every graph "
                                  "replayed at least twice before the timed region",
                            parallelism=f"replicas{world}"),
                layer_hbm=dict(bytes=int(layer_bytes),

@@ -107,7 +107,8 @@ def test_timed_steps_are_exact_and_every_graph_is_warmed(monkeypatch):
     monkeypatch.setattr(bench, "capture", fake_capture)
     torch = SimpleNamespace(cuda=SimpleNamespace(synchronize=lambda: None))
     layers = [L(i) for i in range(8)]
-    for steps in (20, 16, 5, 1):
+    cap = 8 * bench.GRAPH_ROTATIONS
+    for steps in (20, 16, 5, 1, cap, 2 * cap + 13):
         graphs.clear()
         run, warm = bench.layer_steps_timer(torch, None, layers, steps)
         replayed = set()
@@ -121,5 +122,5 @@ def test_timed_steps_are_exact_and_every_graph_is_warmed(monkeypatch):
         log.clear()
         run()
         assert len(log) == steps
-        assert log == [i % 8 for i in range(8 * (steps // 8))] + list(range(steps % 8))
-        assert len(graphs) == (steps >= 8) + (steps % 8 != 0)
+        assert log == [i % 8 for i in range(steps)]   # step i on layer i % 8
+        assert len(graphs) == (steps >= cap) + (steps % cap != 0)
