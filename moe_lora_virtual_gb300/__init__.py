@@ -146,7 +146,11 @@ def _need(t: torch.Tensor, dtype: torch.dtype, name: str) -> None:
 
 
 def _row_stride(t: torch.Tensor, name: str) -> int:
-    if t.dim() != 2 or t.stride(1) != 1:
+    if t.dim() != 2:
+        raise ValueError(f"{name}: expected a 2-D tensor with unit column stride")
+    if t.numel() == 0:  # no elements: its strides mean nothing (an empty array's may be 0)
+        return max(int(t.shape[1]), 1)
+    if t.stride(1) != 1:
         raise ValueError(f"{name}: expected a 2-D tensor with unit column stride")
     return t.stride(0)
 

@@ -168,3 +168,19 @@ def test_binding_fails_loudly_without_library(tmp_path):
             m.library(str(tmp_path / "missing.so"))
     finally:
         m._lib = saved
+
+
+def test_row_stride_of_binding_tensors(mol):
+    """The binding's row stride: a 2-D tensor with unit column stride gives its row stride; a
+    tensor with no elements (an empty batch, whose strides may be 0) is accepted; others are
+    rejected before any call."""
+    import torch
+
+    x = torch.zeros(6, 40)[:, :32]
+    assert mol._row_stride(x, "x") == 40
+    empty = torch.from_numpy(np.zeros((0, 40), np.float32))[:, :32]  # strides (0, 0)
+    assert mol._row_stride(empty, "x") == 32
+    with pytest.raises(ValueError):
+        mol._row_stride(torch.zeros(6, 40)[:, ::2], "x")
+    with pytest.raises(ValueError):
+        mol._row_stride(torch.zeros(6), "x")

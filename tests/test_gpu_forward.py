@@ -79,3 +79,36 @@ def test_forward_paths(case, use_ws, mode):
         check_out(g_out, ref_out, pairs)
         assert np.all(np.isnan(g_inter[others]))
         assert np.array_equal(g_out[others], out0[others])
+
+
+@pytest.mark.parametrize("token_rows", [True, False])
+def test_empty_batch(token_rows):
+    """No tokens: inputs built from empty arrays (whose strides may be 0) are accepted; the
+    stage computing the routing launches only the align, which writes an empty routing
+    (num_tokens_post_padded = 0); the stage reusing it launches nothing; no fault."""
+    torch = torch_cuda()
+    mol = mol_lib()
+    dev = torch.device("cuda:0")
+    T, k, E, L, BM, K, S, r, Ns = 0, 8, 16, 4, 16, 256, 2, 32, 96
+    V, R, N = E * L, S * r, S * Ns
+    x = to_dev_bf16(bits(np.zeros((0, K + 8))), dev)[:, :K]
+    topk = to_dev_i32(np.zeros((0, k), np.int32), dev)
+    lora = to_dev_i32(np.zeros(0, np.int32), dev)
+    A = to_dev_bf16(bits(np.ones((V, R, K)) * 0.01), dev)
+    B = to_dev_bf16(bits(np.ones((V, N, r)) * 0.01), dev)
+    out = to_dev_bf16(bits(np.zeros((0, N))), dev)
+    inter = torch.zeros((0, R), dtype=torch.float32, device=dev)
+    routing = mol.alloc_routing(0, V, BM, dev)
+    routing.num_tokens_post_padded.fill_(-7)
+    xdiv = k if token_rows else 1
+    before = mol.mol_launch_count()
+    mol.mol_lora_forward(x, xdiv, topk, lora, E, L, A, B, S, 0.5, out, routing, inter,
+                         compute_routing=True, workspace=mol.alloc_workspace(0, V, BM, dev))
+    torch.cuda.synchronize()
+    assert mol.mol_launch_count() == before + 1
+    assert int(routing.num_tokens_post_padded.cpu().item()) == 0
+    mol.mol_lora_forward(x, xdiv, None, None, E, L, A, B, S, 0.5, out, routing, inter,
+                         compute_routing=False, num_tokens=0, topk=k)
+    torch.cuda.synchronize()
+    assert mol.mol_launch_count() == before + 1
+    assert mol.mol_take_fault_flags() == 0
