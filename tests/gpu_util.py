@@ -7,7 +7,10 @@ import pytest
 
 import oracle
 
-INTER_RTOL = 1e-3   # |gpu - ref| <= 1e-3 * (|ref| + rms(ref row)) on fp32 intermediates
+# |gpu - ref| <= 1e-3 * (|ref| + max(rms(ref row), rms(ref, every checked row))) on fp32
+# intermediates: 1e-3 relative to the scale of the intermediate, not of an element or row that
+# cancellation (or an adapter rank of one or two columns) has made small
+INTER_RTOL = 1e-3
 OUT_RTOL = 1e-2     # |gpu - ref| <= 1e-2 * (1 + |ref|) on bf16 outputs
 
 
@@ -54,8 +57,9 @@ def check_inter(gpu: np.ndarray, ref: np.ndarray, rows) -> None:
     r = ref[rows].astype(np.float64)
     assert np.all(np.isfinite(g)), "non-finite intermediate on a valid row"
     rms = np.sqrt(np.mean(r * r, axis=1, keepdims=True))
+    rms_all = np.sqrt(np.mean(r * r))
     err = np.abs(g - r)
-    bound = INTER_RTOL * (np.abs(r) + rms)
+    bound = INTER_RTOL * (np.abs(r) + np.maximum(rms, rms_all))
     bad = err > bound
     assert not bad.any(), f"inter mismatch at {np.argwhere(bad)[:5].tolist()}, max err {err.max():.3e}"
 
